@@ -1,0 +1,439 @@
+"""Plain, slow float64 CPU oracle for Grouped Cross-Attention (GCA) with causal chunk
+retrieval.
+
+TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the benchmark's
+CPU-baseline leg may import this module. It shares no code with the CUDA library and
+imports nothing from it; the two meet only through the seeded inputs.
+
+Citations name the source page and section:
+  "Notes"    = the Paper-Notes reading page "Efficient Length-Generalizable Attention
+               via Causal Retrieval for Long-Context Language Modeling" (zhaoyang97),
+               sections 整体框架 (framework), 关键设计 (key design, items "Grouped
+               Cross-Attention", "Causal retrieval", "Gumbel Top-k"), 损失函数/训练策略
+               (training strategy), 亮点与洞察 (insights).
+  "Abstract" = the abstract on the OpenReview forum page of the same paper.
+
+What is computed (the definition, written out directly):
+  * chunks of S = 64 tokens (Notes, framework);
+  * retrieval: query landmark i scores every earlier chunk landmark j < i + offset with
+    a relevance score, here the scaled dot product <q_i, k_j>/sqrt(D), keeps the top-k
+    (Notes, key design / causal retrieval; Abstract); in training the selection key gets Gumbel noise first (Notes, key design
+    / Gumbel top-k), the scores themselves stay clean;
+  * fusion: every token of the next chunk attends to each retrieved chunk with its own
+    softmax, and the k results are summed with softmax(retrieval scores) weights, so the
+    scores receive gradient (Notes, key design / GCA; insights);
+  * backward: the chain rule of that definition (dQ, dK, dV, dscores), and the
+    gradient of the scaled dot-product scores into both landmark sets.
+
+Readings where the pages are silent (each also listed in the design notes):
+  * the next-chunk rule is a shift: query chunk c uses retrieval row c - shift
+    (shift = 1 in training, 0 at decode); chunks with no row get O = 0;
+  * rows with fewer than k candidates use all of them; the remaining slots hold
+    idx = -1, score = -inf and weight 0; a row with no valid slot yields O = 0;
+  * ties in the selection key go to the lower chunk index;
+  * the top-k decision is taken on float32 keys (the kernels' precision): the exact
+    score and the exact noise are each rounded to float32 and added in float32;
+  * Gumbel noise: U from the splitmix64 generator (Steele, Lea & Flood, 2014) at the
+    counter of (seed, group, b, i, j); U = ((h >> 41) + 0.5) / 2^23; g = -log(-log U);
+  * attention inside a retrieved chunk is not causal (the chunk lies wholly in the
+    past) and is scaled by dh^-1/2.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+CHUNK = 64
+
+# ---------------------------------------------------------------------------
+# splitmix64 counter-based generator and the Gumbel noise built on it
+# ---------------------------------------------------------------------------
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def splitmix64_output(seed, n):
+    """The n-th output (n = 1, 2, ...) of splitmix64 started from state `seed`:
+    state_n = seed + n * 0x9E3779B97F4A7C15 (mod 2^64), then the published mixing
+    function (xor-shift 30, multiply, xor-shift 27, multiply, xor-shift 31)."""
+    n = np.asarray(n, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed) + n * _GAMMA
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def noise_counter(group, b, i, j):
+    """64-bit counter of a (group, batch, row, candidate) pair:
+    group in bits 56-63, b in 48-55, i in 24-47, j in 0-23."""
+    g = np.uint64(group) << np.uint64(56)
+    bb = np.uint64(b) << np.uint64(48)
+    ii = np.uint64(i) << np.uint64(24)
+    jj = np.asarray(j, dtype=np.uint64)
+    return g | bb | ii | jj
+
+
+def gumbel_uniform(seed, group, b, i, j):
+    """U in (0, 1), exactly representable in float32: ((h >> 41) + 0.5) / 2^23 where h is
+    the splitmix64 output at position counter + 1."""
+    h = splitmix64_output(seed, noise_counter(group, b, i, j) + np.uint64(1))
+    return ((h >> np.uint64(41)).astype(np.float64) + 0.5) / float(1 << 23)
+
+
+def gumbel_noise(seed, group, b, i, j):
+    """Standard Gumbel(0, 1) sample g = -log(-log U) (Notes, key design / Gumbel top-k)."""
+    u = gumbel_uniform(seed, group, b, i, j)
+    return -np.log(-np.log(u))
+
+
+# ---------------------------------------------------------------------------
+# Retrieval: causal landmark scoring + top-k
+# ---------------------------------------------------------------------------
+
+def retrieve_row(q_row, k_lmk_b, topk, n_cand, use_gumbel=False, seed=0, group=0, b=0, i=0):
+    """Top-k retrieval for one query landmark over candidates j = 0 .. n_cand-1.
+
+    Returns (idx[topk] int32, scores[topk] float64, keys64 of the chosen + next entry).
+    The score is the scaled dot product <q, k_j> / sqrt(D) in float64.  The selection
+    key is float32(score) + float32(g) evaluated in float32; candidates are ordered by
+    descending key, ties to the lower j.
+    """
+    D = q_row.shape[0]
+    idx = np.full(topk, -1, dtype=np.int32)
+    scores = np.full(topk, -np.inf, dtype=np.float64)
+    if n_cand <= 0:
+        return idx, scores, np.zeros(0)
+    j = np.arange(n_cand)
+    s = (k_lmk_b[:n_cand] @ q_row) / math.sqrt(D)
+    if use_gumbel:
+        g = gumbel_noise(seed, group, b, i, j)
+    else:
+        g = np.zeros(n_cand)
+    key32 = (s.astype(np.float32) + g.astype(np.float32)).astype(np.float32)
+    order = np.lexsort((j, -key32.astype(np.float64)))  # primary: -key, then j
+    take = min(topk, n_cand)
+    sel = order[:take]
+    idx[:take] = sel
+    scores[:take] = s[sel]
+    keys64 = (s + g)[order[: min(topk + 1, n_cand)]]
+    return idx, scores, keys64
+
+
+def retrieve_topk(q_lmk, k_lmk, topk, causal_offset=0, use_gumbel=False, seed=0, group=0,
+                  rows=None):
+    """Causal top-k retrieval for every query landmark (Notes, key design / causal
+    retrieval and Gumbel top-k).
+
+    q_lmk [B, nQ, D], k_lmk [B, nC, D] (float64 values).  Row i may retrieve chunks
+    j < min(nC, i + causal_offset).  Returns idx [B, nQ, topk] int32, scores
+    [B, nQ, topk] float64 (clean scores at the chosen chunks) and `margin`
+    [B, nQ] float64: the smallest gap between adjacent keys among the best
+    min(topk + 1, #candidates) float64 keys (inf when there is at most one
+    candidate).  `rows` optionally restricts the work to a list of (b, i) pairs.
+    """
+    B, nQ, D = q_lmk.shape
+    nC = k_lmk.shape[1]
+    idx = np.full((B, nQ, topk), -1, dtype=np.int32)
+    scores = np.full((B, nQ, topk), -np.inf)
+    margin = np.full((B, nQ), np.inf)
+    pairs = rows if rows is not None else [(b, i) for b in range(B) for i in range(nQ)]
+    for b, i in pairs:
+        n_cand = max(0, min(nC, i + causal_offset))
+        ii, ss, kk = retrieve_row(q_lmk[b, i], k_lmk[b], topk, n_cand, use_gumbel, seed,
+                                  group, b, i)
+        idx[b, i], scores[b, i] = ii, ss
+        if kk.size > 1:
+            margin[b, i] = np.min(kk[:-1] - kk[1:])
+    return idx, scores, margin
+
+
+def retrieval_weights(scores_row, idx_row):
+    """Softmax of the retrieval scores over the valid slots (idx >= 0), temperature 1
+    (Notes, key design / GCA: the scores are normalised by a softmax).  Invalid slots get
+    weight 0; a row without valid slots gets all zeros."""
+    valid = idx_row >= 0
+    w = np.zeros(scores_row.shape[0])
+    if not valid.any():
+        return w
+    s = scores_row[valid]
+    e = np.exp(s - s.max())
+    w[valid] = e / e.sum()
+    return w
+
+
+# ---------------------------------------------------------------------------
+# GCA forward
+# ---------------------------------------------------------------------------
+
+def _softmax_rows(S):
+    """Two-pass textbook softmax over the last axis; returns (P, logsumexp)."""
+    mx = S.max(axis=-1, keepdims=True)
+    e = np.exp(S - mx)
+    l = e.sum(axis=-1, keepdims=True)
+    return e / l, (mx + np.log(l))[..., 0]
+
+
+def gca_chunk_forward(qc, kv_k, kv_v, idx_row, scores_row, chunk=CHUNK):
+    """GCA for one query chunk (Notes, key design / GCA).
+
+    qc [S, H, dh]: the chunk's queries; kv_k, kv_v [nC*S, H, dh]: one sequence's keys
+    and values; idx_row/scores_row [k]: its retrieval row.
+    For each valid slot m (chunk j = idx[m]) and head h:
+        A_m = softmax(Q K_j^T / sqrt(dh)) V_j   (own softmax per retrieved chunk)
+    and O = sum_m w_m A_m with w = softmax over valid slots of the scores.
+    Returns O [S, H, dh], LSE [H, k, S] (-inf for invalid slots), A [k, S, H, dh].
+    """
+    S_, H, dh = qc.shape
+    k = idx_row.shape[0]
+    w = retrieval_weights(scores_row, idx_row)
+    o = np.zeros((S_, H, dh))
+    lse = np.full((H, k, S_), -np.inf)
+    A = np.zeros((k, S_, H, dh))
+    Qh = qc.transpose(1, 0, 2)  # [H, S, dh], one matrix per head
+    for m in range(k):
+        j = int(idx_row[m])
+        if j < 0:
+            continue
+        Kh = kv_k[j * chunk:(j + 1) * chunk].transpose(1, 0, 2)  # [H, S, dh]
+        Vh = kv_v[j * chunk:(j + 1) * chunk].transpose(1, 0, 2)
+        Sm = Qh @ Kh.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S(query), S(key)]
+        P, l = _softmax_rows(Sm)
+        A[m] = (P @ Vh).transpose(1, 0, 2)
+        lse[:, m] = l
+        o += w[m] * A[m]
+    return o, lse, A
+
+
+def gca_forward(q, kv_k, kv_v, idx, scores, shift=1, chunk=CHUNK, chunks=None):
+    """GCA forward over all query chunks.
+
+    q [B, nQ*S, H, dh]; kv_k, kv_v [B, nC*S, H, dh]; idx, scores [B, nQ, k].
+    Query chunk c uses retrieval row r = c - shift (the next-chunk rule); chunks with
+    r < 0 get O = 0 and LSE = -inf.
+    Returns O like q and LSE [B, nQ, H, k, S].  `chunks` optionally restricts the work
+    to a list of (b, c) pairs (other entries stay zero / -inf).
+    """
+    B, L, H, dh = q.shape
+    nQ = L // chunk
+    k = idx.shape[2]
+    o = np.zeros_like(q, dtype=np.float64)
+    lse = np.full((B, nQ, H, k, chunk), -np.inf)
+    pairs = chunks if chunks is not None else [(b, c) for b in range(B) for c in range(nQ)]
+    for b, c in pairs:
+        r = c - shift
+        if r < 0:
+            continue
+        oc, lc, _ = gca_chunk_forward(q[b, c * chunk:(c + 1) * chunk], kv_k[b], kv_v[b],
+                                      idx[b, r], scores[b, r], chunk)
+        o[b, c * chunk:(c + 1) * chunk] = oc
+        lse[b, c] = lc
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# GCA backward (chain rule of the forward, computed directly)
+# ---------------------------------------------------------------------------
+
+def gca_chunk_backward(qc, kv_k, kv_v, idx_row, scores_row, doc, chunk=CHUNK):
+    """Backward of gca_chunk_forward for one query chunk.
+
+    With O = sum_m w_m A_m, A_m = P_m V_j, P_m = softmax(Q K_j^T / sqrt(dh)):
+      dA_m   = w_m dO
+      dw_m   = <dO, A_m>   (summed over the chunk's tokens and all heads)
+      dscore = w * (dw - <w, dw>)   (Jacobian of the softmax weights)
+      dV_j  += P_m^T dA_m
+      dP_m   = dA_m V_j^T
+      dS_m   = P_m * (dP_m - rowsum(dP_m * P_m))
+      dQ    += dS_m K_j / sqrt(dh)
+      dK_j  += dS_m^T Q / sqrt(dh)
+    Returns dq [S, H, dh], per-slot dK, dV contributions [k, S, H, dh], dscores [k].
+    """
+    S_, H, dh = qc.shape
+    k = idx_row.shape[0]
+    w = retrieval_weights(scores_row, idx_row)
+    dq = np.zeros((H, S_, dh))
+    dk = np.zeros((k, S_, H, dh))
+    dv = np.zeros((k, S_, H, dh))
+    dw = np.zeros(k)
+    Qh = qc.transpose(1, 0, 2)    # [H, S, dh]
+    dOh = doc.transpose(1, 0, 2)  # [H, S, dh]
+    for m in range(k):
+        j = int(idx_row[m])
+        if j < 0:
+            continue
+        Kh = kv_k[j * chunk:(j + 1) * chunk].transpose(1, 0, 2)
+        Vh = kv_v[j * chunk:(j + 1) * chunk].transpose(1, 0, 2)
+        Sm = Qh @ Kh.transpose(0, 2, 1) / math.sqrt(dh)
+        P, _ = _softmax_rows(Sm)                      # [H, S, S]
+        A = P @ Vh                                    # [H, S, dh]
+        dw[m] = np.sum(dOh * A)
+        dA = w[m] * dOh
+        dv[m] = (P.transpose(0, 2, 1) @ dA).transpose(1, 0, 2)
+        dP = dA @ Vh.transpose(0, 2, 1)
+        dS = P * (dP - np.sum(dP * P, axis=2, keepdims=True))
+        dq += dS @ Kh / math.sqrt(dh)
+        dk[m] = (dS.transpose(0, 2, 1) @ Qh / math.sqrt(dh)).transpose(1, 0, 2)
+    dq = dq.transpose(1, 0, 2)
+    valid = idx_row >= 0
+    ds = np.zeros(k)
+    if valid.any():
+        ds[valid] = w[valid] * (dw[valid] - np.sum(w * dw))
+    return dq, dk, dv, ds
+
+
+def gca_backward(q, kv_k, kv_v, idx, scores, do, shift=1, chunk=CHUNK):
+    """Full backward: dq like q, dk/dv like kv_k (summed over every query chunk that
+    retrieved the chunk), dscores [B, nQ, k] aligned with the retrieval rows (rows
+    that no query chunk uses get 0)."""
+    B, L, H, dh = q.shape
+    nQ = L // chunk
+    k = idx.shape[2]
+    dq = np.zeros_like(q, dtype=np.float64)
+    dk = np.zeros_like(kv_k, dtype=np.float64)
+    dv = np.zeros_like(kv_v, dtype=np.float64)
+    dscores = np.zeros((B, nQ, k))
+    for b in range(B):
+        for c in range(nQ):
+            r = c - shift
+            if r < 0:
+                continue
+            sl = slice(c * chunk, (c + 1) * chunk)
+            dqc, dkc, dvc, ds = gca_chunk_backward(q[b, sl], kv_k[b], kv_v[b], idx[b, r],
+                                                    scores[b, r], do[b, sl], chunk)
+            dq[b, sl] = dqc
+            dscores[b, r] = ds
+            for m in range(k):
+                j = int(idx[b, r, m])
+                if j >= 0:
+                    dk[b, j * chunk:(j + 1) * chunk] += dkc[m]
+                    dv[b, j * chunk:(j + 1) * chunk] += dvc[m]
+    return dq, dk, dv, dscores
+
+
+def gca_backward_chunks(q, kv_k, kv_v, idx, scores, do, b, key_chunks, shift=1, chunk=CHUNK):
+    """dK, dV of selected key chunks of sequence b only (for sampled checks at full
+    size): sums the contributions of every query chunk whose row retrieved them."""
+    L = q.shape[1]
+    nQ = L // chunk
+    want = set(int(j) for j in key_chunks)
+    out_k = {j: np.zeros((chunk,) + q.shape[2:]) for j in want}
+    out_v = {j: np.zeros((chunk,) + q.shape[2:]) for j in want}
+    for c in range(nQ):
+        r = c - shift
+        if r < 0:
+            continue
+        hit = [m for m in range(idx.shape[2]) if int(idx[b, r, m]) in want]
+        if not hit:
+            continue
+        sl = slice(c * chunk, (c + 1) * chunk)
+        _, dkc, dvc, _ = gca_chunk_backward(q[b, sl], kv_k[b], kv_v[b], idx[b, r],
+                                            scores[b, r], do[b, sl], chunk)
+        for m in hit:
+            j = int(idx[b, r, m])
+            out_k[j] += dkc[m]
+            out_v[j] += dvc[m]
+    return out_k, out_v
+
+
+# ---------------------------------------------------------------------------
+# Retrieval-score gradient into the landmarks
+# ---------------------------------------------------------------------------
+
+def scores_backward(q_lmk, k_lmk, idx, dscores):
+    """Gradient of s[b,i,m] = <q_lmk[b,i], k_lmk[b,idx[b,i,m]]> / sqrt(D) (the scores
+    that receive gradient through the fusion weights; Notes, key design / GCA):
+      dq_lmk[b,i] = sum_m ds[b,i,m] k_lmk[b, idx[b,i,m]] / sqrt(D)
+      dk_lmk[b,j] = sum_{(i,m): idx[b,i,m] = j} ds[b,i,m] q_lmk[b,i] / sqrt(D)
+    The Gumbel noise only picks the slots and carries no gradient."""
+    B, nQ, D = q_lmk.shape
+    dq = np.zeros_like(q_lmk, dtype=np.float64)
+    dk = np.zeros_like(k_lmk, dtype=np.float64)
+    for b in range(B):
+        for i in range(nQ):
+            for m in range(idx.shape[2]):
+                j = int(idx[b, i, m])
+                if j < 0:
+                    continue
+                dq[b, i] += dscores[b, i, m] * k_lmk[b, j] / math.sqrt(D)
+                dk[b, j] += dscores[b, i, m] * q_lmk[b, i] / math.sqrt(D)
+    return dq, dk
+
+
+# ---------------------------------------------------------------------------
+# Two retrieval groups (multi-hop): group 2's query landmark = group 1's output
+# ---------------------------------------------------------------------------
+
+def landmark_rows(o, chunk=CHUNK):
+    """The output at the last token of every chunk, flattened over heads:
+    [B, nQ*S, H, dh] -> [B, nQ, H*dh]."""
+    B, L, H, dh = o.shape
+    return o[:, chunk - 1::chunk].reshape(B, L // chunk, H * dh)
+
+
+def two_group_forward(p, topk, seed, use_gumbel=True, idx1=None, idx2=None, chunk=CHUNK,
+                      q2_round=None):
+    """Two retrieval groups (Notes, framework and key design / causal retrieval: upper
+    layers split into G groups, a higher group building on the previous group's result).
+
+    p holds q1, q2 [B, L, H, dh] (each group's queries), k, v (shared K/V: the KV
+    transform is shared across layers, Notes key design / GCA), q1_lmk [B, nC, D],
+    k1_lmk, k2_lmk [B, nC, D] with D = H*dh.  Group 2's query landmarks are group 1's
+    outputs at the last token of each chunk.  idx1/idx2 may be given to hold the
+    discrete selection fixed (finite-difference checks); `q2_round` optionally rounds
+    group 2's query landmarks to the storage dtype before retrieval.
+    """
+    out = {}
+    if idx1 is None:
+        idx1, s1, m1 = retrieve_topk(p["q1_lmk"], p["k1_lmk"], topk, 0, use_gumbel, seed, 0)
+        out["margin1"] = m1
+    s1 = _scores_at(p["q1_lmk"], p["k1_lmk"], idx1)
+    o1, lse1 = gca_forward(p["q1"], p["k"], p["v"], idx1, s1, 1, chunk)
+    q2_lmk = landmark_rows(o1, chunk)
+    if q2_round is not None:
+        q2_lmk = q2_round(q2_lmk)
+    if idx2 is None:
+        idx2, _, m2 = retrieve_topk(q2_lmk, p["k2_lmk"], topk, 0, use_gumbel, seed, 1)
+        out["margin2"] = m2
+    s2 = _scores_at(q2_lmk, p["k2_lmk"], idx2)
+    o2, lse2 = gca_forward(p["q2"], p["k"], p["v"], idx2, s2, 1, chunk)
+    out.update(idx1=idx1, s1=s1, o1=o1, lse1=lse1, q2_lmk=q2_lmk, idx2=idx2, s2=s2, o2=o2,
+               lse2=lse2)
+    return out
+
+
+def two_group_backward(p, fwd, do1, do2, chunk=CHUNK):
+    """Backward through both groups.  Group 2 first; the gradient of its query
+    landmarks flows back into group 1's output gradient at each chunk's last token."""
+    B, L, H, dh = p["q1"].shape
+    dq2, dk_b, dv_b, ds2 = gca_backward(p["q2"], p["k"], p["v"], fwd["idx2"], fwd["s2"],
+                                        do2, 1, chunk)
+    dq2_lmk, dk2_lmk = scores_backward(fwd["q2_lmk"], p["k2_lmk"], fwd["idx2"], ds2)
+    do1_total = np.array(do1, dtype=np.float64, copy=True)
+    do1_total[:, chunk - 1::chunk] += dq2_lmk.reshape(B, L // chunk, H, dh)
+    dq1, dk_a, dv_a, ds1 = gca_backward(p["q1"], p["k"], p["v"], fwd["idx1"], fwd["s1"],
+                                        do1_total, 1, chunk)
+    dq1_lmk, dk1_lmk = scores_backward(p["q1_lmk"], p["k1_lmk"], fwd["idx1"], ds1)
+    return dict(dq1=dq1, dq2=dq2, dk=dk_a + dk_b, dv=dv_a + dv_b, ds1=ds1, ds2=ds2,
+                dq1_lmk=dq1_lmk, dk1_lmk=dk1_lmk, dk2_lmk=dk2_lmk, dq2_lmk=dq2_lmk,
+                do1_total=do1_total)
+
+
+def _scores_at(q_lmk, k_lmk, idx):
+    """Clean scaled dot-product scores at fixed retrieved chunks (-inf where idx < 0)."""
+    B, nQ, D = q_lmk.shape
+    s = np.full(idx.shape, -np.inf)
+    for b in range(B):
+        for i in range(nQ):
+            for m in range(idx.shape[2]):
+                j = int(idx[b, i, m])
+                if j >= 0:
+                    s[b, i, m] = q_lmk[b, i] @ k_lmk[b, j] / math.sqrt(D)
+    return s
+
+
+scores_at = _scores_at

@@ -1,0 +1,68 @@
+"""CPU tests: the float64 oracle against its pins, and broken copies of the oracle
+against the same pins (a pin suite that lets a plausible mistake through is useless)."""
+import importlib.util
+import os
+import sys
+import types
+
+import pytest
+
+import oracle.gca_oracle as orc
+from tests import oracle_pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                          "oracle", "gca_oracle.py")
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(orc)
+
+
+# Each mutation plants one plausible mistake in a private copy of the oracle source.
+MUTATIONS = {
+    "attention_scale_1_over_dh": ("Qh @ Kh.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S(query), S(key)]",
+                                  "Qh @ Kh.transpose(0, 2, 1) / dh  # [H, S(query), S(key)]"),
+    "dropped_softmax_rowsum_term": ("dS = P * (dP - np.sum(dP * P, axis=2, keepdims=True))",
+                                    "dS = P * dP"),
+    "transposed_dk": ("dk[m] = (dS.transpose(0, 2, 1) @ Qh / math.sqrt(dh))",
+                      "dk[m] = (dS @ Qh / math.sqrt(dh))"),
+    "dv_without_weight": ("dv[m] = (P.transpose(0, 2, 1) @ dA)",
+                          "dv[m] = (P.transpose(0, 2, 1) @ dOh)"),
+    "dscores_sign": ("ds[valid] = w[valid] * (dw[valid] - np.sum(w * dw))",
+                     "ds[valid] = w[valid] * (np.sum(w * dw) - dw[valid])"),
+    "tie_to_higher_index": ("order = np.lexsort((j, -key32.astype(np.float64)))",
+                            "order = np.lexsort((-j, -key32.astype(np.float64)))"),
+    "causal_off_by_one": ("n_cand = max(0, min(nC, i + causal_offset))",
+                          "n_cand = max(0, min(nC, i + causal_offset + 1))"),
+    "gumbel_sign": ("return -np.log(-np.log(u))", "return np.log(-np.log(u))"),
+    "landmark_scale_missing": ("s = (k_lmk_b[:n_cand] @ q_row) / math.sqrt(D)",
+                               "s = (k_lmk_b[:n_cand] @ q_row)"),
+    "dq_lmk_wrong_operand": ("dq[b, i] += dscores[b, i, m] * k_lmk[b, j] / math.sqrt(D)",
+                             "dq[b, i] += dscores[b, i, m] * q_lmk[b, i] / math.sqrt(D)"),
+    "weights_not_softmax": ("e = np.exp(s - s.max())", "e = np.ones_like(s)"),
+    "splitmix_shift": ("z = (z ^ (z >> np.uint64(27))) * _M2", "z = (z ^ (z >> np.uint64(28))) * _M2"),
+    "chain_wrong_token": ("do1_total[:, chunk - 1::chunk] += dq2_lmk", "do1_total[:, 0::chunk] += dq2_lmk"),
+}
+
+
+def _mutant(name, old, new):
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, f"mutation {name}: pattern not found exactly once"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutant_is_caught(name):
+    mod = _mutant(name, *MUTATIONS[name])
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mod)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except Exception as e:  # a crash also counts as caught
+            failed.append(f"{pin.__name__}:{type(e).__name__}")
+    assert failed, f"no pin catches mutation {name}"
