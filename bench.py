@@ -1,0 +1,422 @@
+"""Benchmark of the GCA hot path on GB300.
+
+Headline: one training step of the 128M-model workload (B=4 sequences of L=16384 tokens
+= 256 chunks of 64, 12 heads x 64, landmark dim 768, k=8, Gumbel noise): causal
+landmark retrieval, GCA forward, GCA backward (dQ, dK, dV, dscores) and the
+landmark-score backward, all in this library's kernels, timed with CUDA events.
+Secondary (same JSON line, key "decode"): decode-time retrieval at 16M context,
+B=16 sequences x 262144 past chunk landmarks of dim 768, plus the GCA forward over the
+8 retrieved chunks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own replica on its
+own seed (the path shards by sequence; no collective on the data path) and rank 0
+prints the job-wide throughput over the slowest rank's time.
+`--impl reference` times the float64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import resource
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+METRIC = "GCA fwd+bwd tokens/s at L=16K; landmark top-k GB/s at 16M ctx (1 GB300)"
+B, NC, H, DH, D, K = 4, 256, 12, 64, 768, 8
+L = NC * 64
+WORKLOAD = (f"GCA training step, 128M-model shape: B={B}, L={L} ({NC} chunks of 64), H={H} x dh={DH}, "
+            f"landmark dim {D}, top-k {K}, Gumbel noise; retrieval + fwd + bwd + landmark grads")
+DEC_B, DEC_NC = 16, 262144
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(os.path.dirname(os.path.abspath(__file__)), "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks"}
+
+    def __init__(self, torch):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self.max_mhz = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            prop = torch.cuda.get_device_properties(torch.cuda.current_device())
+            bus = f"{getattr(prop, 'pci_domain_id', 0):08X}:{prop.pci_bus_id:02X}:{prop.pci_device_id:02X}.0"
+            self.h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.nv, self.ok = nv, True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop:
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.02)
+
+    def __enter__(self):
+        self.stop = False
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self.stop = True
+        if self.ok:
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "note": "NVML unavailable" if not self.ok else "no sample in window"}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- flop model
+def valid_slots(nC, k):
+    """Valid (row, slot) pairs of one sequence in training: row r = c - 1 has min(k, r)
+    candidates, for query chunks c = 1 .. nC-1."""
+    return sum(min(k, r) for r in range(nC - 1))
+
+
+def algorithmic_flops(B_, nC, H_, dh, k):
+    """Per kernel launch.  Per valid (slot, head) unit: forward 4*64*64*dh (S = QK^T and
+    PV); query-side backward 6*64*64*dh (S recompute, dPo = dO V^T, dQ); key-side
+    backward 4*64*64*dh (dK, dV; its S/dPo recompute is not counted).  Whole step:
+    14*64*64*dh per unit (forward + 2.5x forward)."""
+    units = B_ * H_ * valid_slots(nC, k)
+    u = 64 * 64 * dh
+    return {"gca_fwd": 4 * u * units, "gca_bwd_q": 6 * u * units, "gca_bwd_kv": 4 * u * units,
+            "step": 14 * u * units, "units": units}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import retrieval_sparse_attention_causal_gb300 as gca
+    from retrieval_sparse_attention_causal_gb300 import synth
+
+    seed = args.seed + 1000 * rank
+    bf = torch.bfloat16
+    q = synth.device_normal(seed, synth.S_Q, (B, L, H, DH), 1 / 8, bf)
+    k = synth.device_normal(seed, synth.S_K, (B, L, H, DH), 1 / 8, bf)
+    v = synth.device_normal(seed, synth.S_V, (B, L, H, DH), 1 / 8, bf)
+    do = synth.device_normal(seed, synth.S_DO, (B, L, H, DH), 1 / 8, bf)
+    ql = synth.device_normal(seed, synth.S_QL, (B, NC, D), 1.0, bf)
+    kl = synth.device_normal(seed, synth.S_KL, (B, NC, D), 1.0, bf)
+    ws = gca.Workspace()
+    out = dict(
+        idx=torch.empty((B, NC, K), dtype=torch.int32, device="cuda"),
+        sc=torch.empty((B, NC, K), dtype=torch.float32, device="cuda"),
+        o=torch.empty_like(q), lse=torch.empty((B, NC, H, K, 64), dtype=torch.float32, device="cuda"),
+        dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+        ds=torch.empty((B, NC, K), dtype=torch.float32, device="cuda"),
+        dql=torch.empty((B, NC, D), dtype=torch.float32, device="cuda"),
+        dkl=torch.empty((B, NC, D), dtype=torch.float32, device="cuda"))
+
+    def step(i, q=q, k=k, v=v, do=do, ql=ql, kl=kl):
+        gca.retrieve_topk(ql, kl, K, 0, True, seed + i, 0, ws=ws, idx=out["idx"], scores=out["sc"])
+        gca.gca_forward(q, k, v, out["idx"], out["sc"], shift=1, ws=ws, out=out["o"], lse=out["lse"])
+        gca.gca_backward(q, k, v, out["idx"], out["sc"], do, out["lse"], shift=1, ws=ws, dq=out["dq"],
+                         dk=out["dk"], dv=out["dv"], dscores=out["ds"])
+        gca.scores_backward(ql, kl, out["idx"], out["ds"], ws=ws, dq_out=out["dql"], dk_lmk=out["dkl"])
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def timed(fn, n):
+        s = torch.cuda.current_stream()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for i in range(n):
+            fn(i)
+        e1.record(s)
+        torch.cuda.synchronize()
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    for i in range(args.warmup):
+        step(i)
+    ws.check()
+    n0 = gca.launch_count()
+    with ClockSampler(torch) as clk:
+        ms = timed(step, args.steps)
+    launches = gca.launch_count() - n0
+    ms_step = ms / args.steps
+    tokens = B * L
+    value = tokens * world / (ms_step / 1e3)
+
+    # Per-kernel durations: the same loop again with event brackets around each launch.
+    gca.profile_begin()
+    timed(step, args.steps)
+    prof = gca.profile_end()
+    fl = algorithmic_flops(B, NC, H, DH, K)
+    pk, src = peaks()
+    kern = {n: {"launches": c, "avg_ms": t / c} for n, (c, t) in prof.items()}
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    dom_flops = fl.get(dom)
+    roof = None
+    if dom_flops:
+        avg_s = kern[dom]["avg_ms"] / 1e3
+        ach = dom_flops / avg_s / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
+                "peak_source": f"{src} bf16 dense (burst)", "flops_per_launch": dom_flops}
+    step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
+
+    # End to end through the public API from pinned host buffers.
+    e2e = None
+    if not args.no_e2e:
+        hin = {n: t.cpu().pin_memory() for n, t in dict(q=q, k=k, v=v, do=do, ql=ql, kl=kl).items()}
+        din = {n: torch.empty_like(t) for n, t in dict(q=q, k=k, v=v, do=do, ql=ql, kl=kl).items()}
+        res = ["dq", "dk", "dv", "dql", "dkl", "idx", "sc", "ds"]
+        hout = {n: torch.empty(out[n].shape, dtype=out[n].dtype, pin_memory=True) for n in res}
+
+        def e2e_step(i):
+            for n in hin:
+                din[n].copy_(hin[n], non_blocking=True)
+            step(i, **din)
+            for n in res:
+                hout[n].copy_(out[n], non_blocking=True)
+
+        for i in range(max(1, args.warmup // 2)):
+            e2e_step(i)
+        ms_e = timed(e2e_step, args.steps) / args.steps
+        e2e = {"value": tokens * world / (ms_e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout.values())}
+        del hin, din, hout
+
+    dec = None if args.no_decode else decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(args.seed, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)/8 Q/K/V/dO, N(0,1) landmarks)",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": L, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (Q, K, V, dO: 4 x 100.7 MB per step)"},
+            "step_tflops_algorithmic": round(step_tflops, 2),
+            "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary(),
+            "kernels": {n: round(x["avg_ms"], 5) for n, x in kern.items()},
+            "e2e": e2e, "decode": dec, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
+    """Decode at 16M context: retrieval over 262144 landmarks per sequence (HBM-bound)
+    and the GCA forward over the retrieved chunks; one K/V store shared by the batch."""
+    bf = torch.bfloat16
+    nb = args.decode_batch
+    ql = synth.device_normal(seed, synth.S_QL, (nb, 1, D), 1.0, bf)
+    kl = synth.device_normal(seed, synth.S_KL, (nb, DEC_NC, D), 1.0, bf)
+    g = torch.Generator().manual_seed(seed)
+    jstar = torch.randint(0, DEC_NC, (nb,), generator=g)
+    for b in range(nb):
+        kl[b, int(jstar[b])] = ql[b, 0]
+    # K/V store of 262144 chunks x 64 tokens x 12 x 64 (25.8 GB each): a seeded 1 GiB
+    # block tiled across the store.
+    blk = synth.device_normal(seed, synth.S_K, (1 << 29,), 1 / 8, bf)
+    kst = torch.empty((DEC_NC * 64, H, DH), dtype=bf, device="cuda")
+    vst = torch.empty_like(kst)
+    for t in (kst, vst):
+        f = t.view(-1)
+        for s in range(0, f.numel(), blk.numel()):
+            n = min(blk.numel(), f.numel() - s)
+            f[s:s + n].copy_(blk[:n])
+    del blk
+    qn = synth.device_normal(seed, synth.S_Q, (nb, 64, H, DH), 1 / 8, bf)
+    ws = gca.Workspace()
+    idx = torch.empty((nb, 1, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((nb, 1, K), dtype=torch.float32, device="cuda")
+    o = torch.empty_like(qn)
+    lse = torch.empty((nb, 1, H, K, 64), dtype=torch.float32, device="cuda")
+
+    def retr(i):
+        gca.retrieve_topk(ql, kl, K, DEC_NC, False, ws=ws, idx=idx, scores=sc)
+
+    def full(i):
+        retr(i)
+        gca.gca_forward(qn, kst, vst, idx, sc, shift=0, kv_shared=True, ws=ws, out=o, lse=lse)
+
+    for i in range(args.warmup):
+        full(i)
+    ws.check()
+    ok = bool((idx[:, 0, 0].cpu() == jstar.to(torch.int32)).all())
+    s = torch.cuda.current_stream()
+
+    def time_loop(fn, n):
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for i in range(n):
+            fn(i)
+        e1.record(s)
+        torch.cuda.synchronize()
+        barrier()
+        return e0.elapsed_time(e1) / n
+
+    ms_r = time_loop(retr, args.steps)
+    ms_f = time_loop(full, args.steps)
+    gca.profile_begin()
+    time_loop(retr, args.steps)
+    prof = gca.profile_end()
+    nbytes = nb * DEC_NC * D * 2
+    rows_ms = prof["retrieve_rows"][1] / prof["retrieve_rows"][0]
+    ach = nbytes / (rows_ms / 1e3) / 1e9
+    del kst, vst
+    return {"metric": "landmark top-k GB/s at 16M ctx", "value": round(nbytes * world / (ms_r / 1e3) / 1e9, 1),
+            "unit": "GB/s", "batch": nb, "past_chunks": DEC_NC, "landmark_dim": D, "ms_per_retrieval": round(ms_r, 4),
+            "ms_per_decode_chunk": round(ms_f, 4), "planted_chunk_found": ok,
+            "roofline": {"kernel": "retrieve_rows", "bound": "hbm", "achieved": round(ach, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+                         "traffic": None, "peak_source": f"{src} copy bandwidth", "bytes_per_launch": nbytes},
+            "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def cpu_sample(seed, rows, budget_s=None):
+    """The oracle on one sequence of the benchmarked workload, for query chunks
+    1..rows (retrieval of their rows, GCA forward and backward, landmark gradients).
+    Returns (tokens processed, seconds, cpu seconds)."""
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    import oracle.gca_oracle as orc
+    from retrieval_sparse_attention_causal_gb300 import synth
+
+    x = synth.gca_inputs(seed, 1, NC, NC, H, DH, 1 / 8, "bf16")
+    lm = synth.landmark_inputs(seed, 1, NC, NC, D, "bf16")
+    r0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    idx, sc, _ = orc.retrieve_topk(lm["q_lmk"], lm["k_lmk"], K, 0, True, seed, rows=[(0, i) for i in range(rows)])
+    ds_all = np.zeros((1, NC, K))
+    done = 0
+    for c in range(1, rows + 1):
+        sl = slice(c * 64, (c + 1) * 64)
+        orc.gca_chunk_forward(x["q"][0, sl], x["k"][0], x["v"][0], idx[0, c - 1], sc[0, c - 1])
+        _, _, _, ds = orc.gca_chunk_backward(x["q"][0, sl], x["k"][0], x["v"][0], idx[0, c - 1], sc[0, c - 1],
+                                             x["do"][0, sl])
+        ds_all[0, c - 1] = ds
+        done = c
+        if budget_s and time.perf_counter() - t0 > budget_s:
+            break
+    orc.scores_backward(lm["q_lmk"][:, :done], lm["k_lmk"], idx[:, :done], ds_all[:, :done])
+    dt = time.perf_counter() - t0
+    r1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu_s = (r1.ru_utime + r1.ru_stime) - (r0.ru_utime + r0.ru_stime)
+    return done * 64, dt, cpu_s
+
+
+def cpu_baseline(seed, budget_s=20.0):
+    tok, dt, cpu_s = cpu_sample(seed, NC - 1, budget_s)
+    return {"value": round(tok / dt, 2), "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "threads_busy": round(cpu_s / dt, 2), "kind": "oracle",
+            "sample": f"one sequence of the workload, query chunks 1..{tok // 64} ({tok} tokens): retrieval rows, "
+                      f"GCA forward + backward, landmark gradients, float64 numpy; {dt:.1f} s wall"}
+
+
+def reference_arm(args):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if rank != 0:
+        return
+    # Size each step so that warm-up + timed steps end within about two minutes.
+    per_step = max(0.5, min(6.0, 120.0 / max(1, args.steps + args.warmup)))
+    tok, dt, _ = cpu_sample(args.seed, NC - 1, per_step)
+    rows = max(1, tok // 64)
+    for i in range(args.warmup):
+        cpu_sample(args.seed + i, rows)
+    tot_t, tot_tok, tot_cpu = 0.0, 0, 0.0
+    for i in range(args.steps):
+        tk, d, c = cpu_sample(args.seed + i, rows)
+        tot_t += d
+        tot_tok += tk
+        tot_cpu += c
+    v = tot_tok / tot_t
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B, "seq_len": L},
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "kind": "oracle",
+                             "cores": len(os.sched_getaffinity(0)), "threads_busy": round(tot_cpu / tot_t, 2),
+                             "sample": f"per step: one sequence, query chunks 1..{rows} ({rows * 64} tokens)"},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--decode-batch", type=int, default=DEC_B)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gb300":
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

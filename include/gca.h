@@ -1,0 +1,206 @@
+/*
+ * gca.h - C ABI of the GB300 (sm_103a) library for Grouped Cross-Attention (GCA) with
+ * causal chunk retrieval.
+ *
+ * The method (paper "Efficient Length-Generalizable Attention via Causal Retrieval for
+ * Long-Context Language Modeling"; sources cited below):
+ *   - a sequence is cut into chunks of S = 64 tokens, each chunk summarised by a
+ *     landmark vector (Paper-Notes page, section 整体框架 / framework);
+ *   - retrieval: the landmark of chunk i scores every earlier chunk's landmark and keeps
+ *     the top-k (Paper-Notes page, 关键设计 / key design, "causal retrieval"; OpenReview
+ *     forum page, abstract); during training Gumbel noise perturbs the selection
+ *     (Paper-Notes page, 关键设计, "Gumbel top-k");
+ *   - fusion: every token of the NEXT chunk attends to each retrieved chunk with its own
+ *     softmax and the k results are summed with softmax(retrieval score) weights, so
+ *     the scores receive gradient (Paper-Notes page, 关键设计, "Grouped Cross-Attention"
+ *     and 亮点与洞察 / insights).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or retains them.  Every call is asynchronous on `stream`.
+ *   - Sizes: S = 64 tokens per chunk (fixed).  B sequences, nQ query chunks, nC key
+ *     chunks, H heads of size dh, landmark dimension D, top-k = `topk`.
+ *   - Layouts are row-major with the last index contiguous.  "elements" strides count
+ *     elements of the tensor's own dtype.
+ *   - `ws` is caller-owned device workspace of at least the size returned by the
+ *     matching *_workspace_size function, 256-byte aligned.  Its first 256 bytes are a
+ *     sticky device error word: zero it once after allocation; kernels only ever set
+ *     bits in it; gca_check_error() reads and clears it.  Different concurrent calls
+ *     must use different workspaces.
+ *   - Errors: argument problems are reported synchronously (nothing is launched).
+ *     A bad retrieved index met by a kernel (outside [-1, nC)) is treated as an empty
+ *     slot and flagged in the error word; call gca_check_error() to see it.
+ */
+#ifndef GCA_H
+#define GCA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GCA_API __attribute__((visibility("default")))
+#else
+#define GCA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* gca_stream_t;
+
+typedef enum {
+  GCA_OK = 0,
+  GCA_ERR_INVALID_ARG = 1,  /* a pointer, size, stride or flag is out of range          */
+  GCA_ERR_UNSUPPORTED = 2,  /* valid but not provided (e.g. dh not 32/64, topk > 16)    */
+  GCA_ERR_WORKSPACE = 3,    /* ws is NULL, misaligned or smaller than required          */
+  GCA_ERR_CUDA = 4,         /* a CUDA runtime call failed; see gca_last_error_detail()  */
+  GCA_ERR_DEVICE_INDEX = 5  /* (gca_check_error) a kernel met idx outside [-1, nC)      */
+} gca_status;
+
+typedef enum { GCA_F32 = 0, GCA_BF16 = 1 } gca_dtype;
+
+enum { GCA_CHUNK = 64, GCA_MAX_TOPK = 16 };
+
+/* Human-readable name of a status. */
+GCA_API const char* gca_status_string(gca_status s);
+/* Text of the last error raised on the calling host thread ("" if none). */
+GCA_API const char* gca_last_error_detail(void);
+
+/* ---------------------------------------------------------------------------------
+ * gca_retrieve_topk - causal landmark scoring + per-row top-k.
+ *
+ * Paper-Notes page, 关键设计 (causal retrieval; Gumbel top-k); OpenReview abstract.
+ * For every sequence b and query row i, with candidates j = 0 .. n_i - 1 where
+ * n_i = min(nC, i + causal_offset):
+ *     s_ij   = <q_lmk[b,i,:], k_lmk[b,j,:]> / sqrt(D)       (float32 accumulation)
+ *     key_ij = s_ij + g_ij   if use_gumbel, else s_ij       (float32)
+ *     g_ij   = -log(-log U),  U = ((h >> 41) + 0.5) / 2^23,
+ *     h      = splitmix64 output number (ctr + 1) from state `seed`,
+ *     ctr    = group << 56 | b << 48 | i << 24 | j.
+ * The min(topk, n_i) candidates with the largest keys are written in descending key
+ * order (equal keys: lower j first).  Unused slots get idx = -1 and score = -inf.
+ *
+ *   q_lmk   [B][nQ][D] at q_row_stride / q_batch_stride elements (row stride >= D,
+ *           a multiple of 8 elements for bf16 and 4 for f32; strides allow reading the
+ *           landmark rows straight out of a larger tensor).
+ *   k_lmk   [B][nC][D], rows contiguous, batch stride k_batch_stride (>= nC*D, or 0 to
+ *           share one landmark set among all sequences).
+ *   dtype   GCA_F32 or GCA_BF16 (both landmark tensors).
+ *   D       bf16: a multiple of 64 in 64..1024; f32: a multiple of 32 in 32..512.
+ *   topk    1 .. 16.   causal_offset >= 0 (0 in training; nC at decode).
+ *   use_gumbel: requires B <= 256, nQ, nC <= 2^24 and 0 <= group < 256.
+ *   idx     [B][nQ][topk] int32 out.   scores [B][nQ][topk] float32 out (clean s).
+ *   ws      >= gca_retrieve_workspace_size(B, nQ, nC, topk, causal_offset) bytes.
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_retrieve_workspace_size(int B, int nQ, int nC, int topk, int causal_offset);
+GCA_API gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
+                             const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype,
+                             int B, int nQ, int nC, int D, int topk, int causal_offset,
+                             int use_gumbel, uint64_t seed, int group, int32_t* idx,
+                             float* scores, void* ws, size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * gca_forward - grouped cross-attention over the retrieved chunks.
+ *
+ * Paper-Notes page, 关键设计 ("Grouped Cross-Attention"): each retrieved chunk gets its
+ * own softmax; the k outputs are fused with softmax-normalised retrieval scores.
+ * Query chunk c uses retrieval row r = c - shift (shift = 1: the next-chunk rule of
+ * training, where row r's landmark sits at the end of chunk r; shift = 0: decode).
+ * For each valid slot m of row r (j = idx[b,r,m] >= 0) and head h:
+ *     A_m = softmax(Q_c K_j^T / sqrt(dh)) V_j      (64 x 64 logits, no mask)
+ *     O_c = sum_m w_m A_m,   w = softmax over valid slots of scores[b,r,:]
+ * Chunks with r < 0 or without a valid slot get O = 0.
+ *
+ *   q, o    [B][nQ*64][H][dh] contiguous, dtype `dtype`.
+ *   k, v    [B][nC*64][H][dh]; kv_batch_stride elements between sequences
+ *           (nC*64*H*dh when contiguous; 0 = all sequences share one store).
+ *   idx, scores [B][nQ][topk] (idx in [-1, nC); scores float32).
+ *   lse     [B][nQ][H][topk][64] float32 out: log-sum-exp of each slot's scaled
+ *           logits (natural log), -inf for slots that are not valid; kept for backward.
+ *   dh      32 or 64.   topk 1..16.   shift 0 or 1.
+ *   ws      >= gca_forward_workspace_size() bytes (error word only).
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_forward_workspace_size(void);
+GCA_API gca_status gca_forward(const void* q, const void* k, const void* v, int64_t kv_batch_stride,
+                       gca_dtype dtype, int B, int nQ, int nC, int H, int dh,
+                       const int32_t* idx, const float* scores, int topk, int shift,
+                       void* o, float* lse, void* ws, size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * gca_backward - gradients of gca_forward: dQ, dK, dV and the retrieval scores.
+ *
+ * The score gradient is what lets the retriever learn from the language-model loss
+ * (Paper-Notes page, 研究背景与动机 / motivation and 亮点与洞察 / insights).  With
+ * D_m[t] = <dO[t], A_m[t]> and dw_m = sum over tokens and heads of D_m:
+ *     dscores[b,r,m] = w_m (dw_m - sum_n w_n dw_n)
+ *     dS_m = w_m P_m * (dO V_j^T - D_m) / sqrt(dh)
+ *     dQ_c = sum_m dS_m K_j,   dK_j += dS_m^T Q_c,   dV_j += w_m P_m^T dO_c
+ *
+ *   q, k, v, idx, scores, lse: as passed to / produced by gca_forward (K/V contiguous).
+ *   dout    [B][nQ*64][H][dh] gradient of o.
+ *   dq      [B][nQ*64][H][dh] out (chunks without a valid slot get 0).
+ *   dk, dv  [B][nC*64][H][dh] out; every chunk is written (0 if never retrieved), or,
+ *           with accumulate_dkv = 1, the gradient is added to their current contents.
+ *   dscores [B][nQ][topk] float32 out, aligned with idx (0 for unused slots and rows).
+ *   ws      >= gca_backward_workspace_size(B, nQ, nC, H, topk) bytes.
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_backward_workspace_size(int B, int nQ, int nC, int H, int topk);
+GCA_API gca_status gca_backward(const void* q, const void* k, const void* v, gca_dtype dtype, int B,
+                        int nQ, int nC, int H, int dh, const int32_t* idx, const float* scores,
+                        int topk, int shift, const void* dout, const float* lse, void* dq,
+                        void* dk, void* dv, float* dscores, int accumulate_dkv, void* ws,
+                        size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * gca_scores_backward - gradient of the scaled dot-product scores into the landmarks.
+ *
+ *     dq_lmk[b,i] (+)= sum_m dscores[b,i,m] k_lmk[b, idx[b,i,m]] / sqrt(D)
+ *     dk_lmk[b,j]   = sum_{(i,m): idx[b,i,m] = j} dscores[b,i,m] q_lmk[b,i] / sqrt(D)
+ * The Gumbel noise only chose the slots and carries no gradient.
+ *
+ *   q_lmk, k_lmk, dtype, strides: as for gca_retrieve_topk (k_batch_stride may not be 0).
+ *   idx, dscores [B][nQ][topk].
+ *   dq_lmk  output with its own dtype, row and batch strides (elements); with
+ *           dq_accumulate = 1 the gradient is added to the current contents (used to
+ *           push a second group's landmark gradient into the first group's output
+ *           gradient at each chunk's last token).
+ *   dk_lmk  [B][nC][D] float32 out, overwritten.
+ *   ws      >= gca_scores_backward_workspace_size(B, nQ, nC, topk) bytes.
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_scores_backward_workspace_size(int B, int nQ, int nC, int topk);
+GCA_API gca_status gca_scores_backward(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
+                               const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype,
+                               int B, int nQ, int nC, int D, const int32_t* idx,
+                               const float* dscores, int topk, void* dq_lmk,
+                               gca_dtype dq_dtype, int64_t dq_row_stride,
+                               int64_t dq_batch_stride, int dq_accumulate, float* dk_lmk,
+                               void* ws, size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * gca_check_error - synchronise `stream`, read and clear the device error word of `ws`.
+ * Returns GCA_OK, GCA_ERR_DEVICE_INDEX (with the offending index in *bad_value when
+ * bad_value != NULL) or GCA_ERR_CUDA.
+ * ------------------------------------------------------------------------------- */
+GCA_API gca_status gca_check_error(void* ws, gca_stream_t stream, int* bad_value);
+
+/* ---------------------------------------------------------------------------------
+ * Instrumentation (host side, process-wide).
+ *   gca_launch_count  - number of kernels this library has launched so far.
+ *   gca_profile_begin - from now on, bracket every kernel launch with CUDA events on
+ *                       its own stream (adds ~1 us per launch).
+ *   gca_profile_end   - stop recording, wait for the events, and fill a table of
+ *                       (kernel name, launches, total milliseconds); returns the number
+ *                       of rows, reads them with gca_profile_row(i, ...).
+ * ------------------------------------------------------------------------------- */
+GCA_API uint64_t gca_launch_count(void);
+GCA_API gca_status gca_profile_begin(void);
+GCA_API int gca_profile_end(void);
+GCA_API gca_status gca_profile_row(int i, const char** name, int* launches, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCA_H */

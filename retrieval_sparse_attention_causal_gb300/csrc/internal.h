@@ -1,0 +1,83 @@
+// Host-side declarations shared by the entry points (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gca {
+
+struct ErrWord;
+
+// Launch bookkeeping: every kernel launch goes through launch_begin/launch_end so that
+// the library can count launches and, when profiling is on, time them with events.
+void launch_begin(const char* name, cudaStream_t s);
+cudaError_t launch_end(const char* name, cudaStream_t s);
+
+// Sets the dynamic shared-memory limit of `fn` once per device.
+cudaError_t allow_smem(const void* fn, int bytes);
+
+// ---- retrieval (retrieve.cu)
+struct RetrieveArgs {
+  const void* q; int64_t q_rs, q_bs;
+  const void* k; int64_t k_bs;
+  int bf16;
+  int B, nQ, nC, D, topk, off;
+  int gumbel; uint64_t seed; int group;
+  int32_t* idx; float* scores;
+  ErrWord* err;
+  void* part;  // partial-candidate buffer (may be null when nsplit == 1)
+};
+// Plan: number of candidate splits per row (or row block) for the chosen kernel.
+struct RetrievePlan {
+  int rowwise;   // 1: one CTA per (row, split) streaming kernel; 0: 64-row tile kernel
+  int nsplit;    // splits of the candidate range
+  int seg;       // candidates per split
+  size_t part_bytes;
+};
+RetrievePlan retrieve_plan(int B, int nQ, int nC, int topk, int off);
+cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaStream_t s);
+
+// ---- GCA forward (gca_fwd.cu)
+struct FwdArgs {
+  const void* q; const void* k; const void* v; int64_t kv_bs;
+  int bf16, B, nQ, nC, H, dh;
+  const int32_t* idx; const float* scores; int topk, shift;
+  void* o; float* lse; ErrWord* err;
+};
+cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
+
+// ---- GCA backward (gca_bwd.cu)
+struct BwdArgs {
+  const void* q; const void* k; const void* v;
+  int bf16, B, nQ, nC, H, dh;
+  const int32_t* idx; const float* scores; int topk, shift;
+  const void* dout; const float* lse;
+  void* dq; void* dk; void* dv; float* dscores; int acc_dkv;
+  ErrWord* err;
+  float* Dbuf;      // [B][nQ][H][topk][64]
+  float* dwp;       // [B][nQ][H][topk]
+  int32_t* csr_off; // [B][nC+1]
+  int32_t* csr_ent; // [B][nQ*topk]
+  int32_t* csr_cur; // [B][nC]
+};
+cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s);
+
+// ---- CSR of consumers per key chunk (gca_bwd.cu), also used by the score backward.
+// Rows r in [0, nrows) of idx [B][ld_rows][topk] are entries e = r*topk + m.
+cudaError_t launch_csr(const int32_t* idx, int B, int ld_rows, int nrows, int topk, int nC,
+                       int32_t* off, int32_t* ent, int32_t* cur, ErrWord* err, cudaStream_t s);
+
+// ---- landmark gradients (scores_bwd.cu)
+struct ScoresBwdArgs {
+  const void* q; int64_t q_rs, q_bs;
+  const void* k; int64_t k_bs;
+  int bf16, B, nQ, nC, D;
+  const int32_t* idx; const float* ds; int topk;
+  void* dq; int dq_bf16; int64_t dq_rs, dq_bs; int dq_acc;
+  float* dk; ErrWord* err;
+  int32_t* csr_off; int32_t* csr_ent; int32_t* csr_cur;
+};
+cudaError_t launch_scores_backward(const ScoresBwdArgs& a, cudaStream_t s);
+
+}  // namespace gca

@@ -1,0 +1,89 @@
+// Gradient of the retrieval scores s_im = <q_lmk_i, k_lmk_j> / sqrt(D), j = idx[i,m], into
+// both landmark sets.  The scores get their gradient from the fusion weights (Paper-Notes
+// page on "Efficient Length-Generalizable Attention via Causal Retrieval for
+// Long-Context Language Modeling", 关键设计 / key design, "Grouped Cross-Attention");
+// the Gumbel noise only chose the slots and has no gradient.
+//
+//   dq_lmk_kernel  one CTA per query row: sum over its k slots of ds * k_lmk[j].
+//   dk_lmk_kernel  one CTA per key chunk: sum over the rows that retrieved it (from the
+//                  stable CSR, so in a fixed order) of ds * q_lmk[i].
+#include "common.cuh"
+#include "internal.h"
+
+namespace gca {
+namespace {
+
+template <typename T, typename TO>
+__global__ void __launch_bounds__(256) dq_lmk_kernel(ScoresBwdArgs a) {
+  __shared__ int j_s[kMaxTopk];
+  __shared__ float ds_s[kMaxTopk];
+  const int i = blockIdx.x, b = blockIdx.y;
+  if (threadIdx.x < a.topk) {
+    const int64_t o = ((int64_t)b * a.nQ + i) * a.topk + threadIdx.x;
+    int j = a.idx[o];
+    if (j < -1 || j >= a.nC) {
+      flag_bad_index(a.err, j);
+      j = -1;
+    }
+    j_s[threadIdx.x] = j;
+    ds_s[threadIdx.x] = a.ds[o];
+  }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf((float)a.D);
+  const T* kb = reinterpret_cast<const T*>(a.k) + (int64_t)b * a.k_bs;
+  TO* out = reinterpret_cast<TO*>(a.dq) + (int64_t)b * a.dq_bs + (int64_t)i * a.dq_rs;
+  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    float acc = 0.f;
+    for (int m = 0; m < a.topk; ++m) {
+      const int j = j_s[m];
+      if (j >= 0) acc = fmaf(ds_s[m], Elem<T>::ld(kb + (int64_t)j * a.D + d), acc);
+    }
+    acc *= inv;
+    if (a.dq_acc) acc += Elem<TO>::ld(out + d);
+    Elem<TO>::st(out + d, acc);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) dk_lmk_kernel(ScoresBwdArgs a) {
+  const int j = blockIdx.x, b = blockIdx.y;
+  const int e0 = a.csr_off[(int64_t)b * (a.nC + 1) + j];
+  const int e1 = a.csr_off[(int64_t)b * (a.nC + 1) + j + 1];
+  const int32_t* ent = a.csr_ent + (int64_t)b * a.nQ * a.topk;
+  const float inv = 1.0f / sqrtf((float)a.D);
+  const T* qb = reinterpret_cast<const T*>(a.q) + (int64_t)b * a.q_bs;
+  float* out = a.dk + ((int64_t)b * a.nC + j) * a.D;
+  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
+    float acc = 0.f;
+    for (int c = e0; c < e1; ++c) {
+      const int e = ent[c];
+      const int i = e / a.topk;
+      const float ds = a.ds[(int64_t)b * a.nQ * a.topk + e];
+      acc = fmaf(ds, Elem<T>::ld(qb + (int64_t)i * a.q_rs + d), acc);
+    }
+    out[d] = acc * inv;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_scores_backward(const ScoresBwdArgs& a, cudaStream_t s) {
+  cudaError_t e = launch_csr(a.idx, a.B, a.nQ, a.nQ, a.topk, a.nC, a.csr_off, a.csr_ent, a.csr_cur, a.err, s);
+  if (e != cudaSuccess) return e;
+  dim3 gq(a.nQ, a.B), gk(a.nC, a.B);
+  launch_begin("lmk_dq", s);
+  if (a.bf16) {
+    if (a.dq_bf16) dq_lmk_kernel<__nv_bfloat16, __nv_bfloat16><<<gq, 256, 0, s>>>(a);
+    else dq_lmk_kernel<__nv_bfloat16, float><<<gq, 256, 0, s>>>(a);
+  } else {
+    if (a.dq_bf16) dq_lmk_kernel<float, __nv_bfloat16><<<gq, 256, 0, s>>>(a);
+    else dq_lmk_kernel<float, float><<<gq, 256, 0, s>>>(a);
+  }
+  if ((e = launch_end("lmk_dq", s)) != cudaSuccess) return e;
+  launch_begin("lmk_dk", s);
+  if (a.bf16) dk_lmk_kernel<__nv_bfloat16><<<gk, 256, 0, s>>>(a);
+  else dk_lmk_kernel<float><<<gk, 256, 0, s>>>(a);
+  return launch_end("lmk_dk", s);
+}
+
+}  // namespace gca

@@ -1,0 +1,116 @@
+"""CPU tests of the C ABI: the library loads, exports every symbol that include/gca.h
+declares, and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gca():
+    from retrieval_sparse_attention_causal_gb300 import build
+    build.build()
+    import retrieval_sparse_attention_causal_gb300 as m
+    return m
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "gca.h")).read()
+    return sorted(set(re.findall(r"GCA_API\s+[\w\s\*]+?\b(gca_\w+)\s*\(", src)))
+
+
+def test_header_declares_expected_entry_points():
+    syms = declared_symbols()
+    for s in ("gca_retrieve_topk", "gca_forward", "gca_backward", "gca_scores_backward",
+              "gca_check_error"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(gca):
+    lib = ctypes.CDLL(gca.LIB_PATH)
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+    assert sorted(declared_symbols()) == sorted(gca.EXPORTS)
+
+
+def test_status_strings(gca):
+    assert gca.LIB.gca_status_string(0) == b"GCA_OK"
+    assert gca.LIB.gca_status_string(5) == b"GCA_ERR_DEVICE_INDEX"
+
+
+def test_workspace_sizes(gca):
+    L = gca.LIB
+    assert L.gca_forward_workspace_size() == 256
+    small = L.gca_backward_workspace_size(1, 16, 16, 4, 4)
+    big = L.gca_backward_workspace_size(4, 256, 256, 12, 8)
+    assert 256 < small < big
+    # D buffer alone at B=4, nQ=256, H=12, k=8: 4*256*12*8*64*4 bytes
+    assert big >= 4 * 256 * 12 * 8 * 64 * 4
+    assert L.gca_retrieve_workspace_size(1, 1, 262144, 8, 262144) > 256  # split decode scan
+    assert L.gca_scores_backward_workspace_size(4, 256, 256, 8) > 256
+
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced: every call below fails validation
+
+
+def _retr(gca, **kw):
+    args = dict(q=FAKE, qrs=768, qbs=256 * 768, k=FAKE, kbs=256 * 768, dt=gca.GCA_BF16, B=4, nQ=256, nC=256,
+                D=768, topk=8, off=0, gum=1, seed=0, group=0, idx=FAKE, sc=FAKE, ws=FAKE, wsb=1 << 30)
+    args.update(kw)
+    a = args
+    return gca.LIB.gca_retrieve_topk(a["q"], a["qrs"], a["qbs"], a["k"], a["kbs"], a["dt"], a["B"], a["nQ"],
+                                     a["nC"], a["D"], a["topk"], a["off"], a["gum"], a["seed"], a["group"],
+                                     a["idx"], a["sc"], a["ws"], a["wsb"], None)
+
+
+def test_retrieve_rejects_bad_arguments(gca):
+    assert _retr(gca, q=0) == gca.GCA_ERR_INVALID_ARG
+    assert _retr(gca, topk=17) == gca.GCA_ERR_UNSUPPORTED
+    assert _retr(gca, topk=0) == gca.GCA_ERR_UNSUPPORTED
+    assert _retr(gca, D=700) == gca.GCA_ERR_UNSUPPORTED
+    assert _retr(gca, qrs=700) == gca.GCA_ERR_INVALID_ARG
+    assert _retr(gca, q=FAKE + 2) == gca.GCA_ERR_INVALID_ARG
+    assert _retr(gca, off=-1) == gca.GCA_ERR_INVALID_ARG
+    assert _retr(gca, group=300) == gca.GCA_ERR_INVALID_ARG
+    assert _retr(gca, B=300) == gca.GCA_ERR_INVALID_ARG
+    assert _retr(gca, ws=0) == gca.GCA_ERR_WORKSPACE
+    assert _retr(gca, ws=FAKE + 16) == gca.GCA_ERR_WORKSPACE
+    assert _retr(gca, nC=262144, nQ=1, off=262144, kbs=262144 * 768, wsb=256) == gca.GCA_ERR_WORKSPACE
+    assert _retr(gca, topk=99) == gca.GCA_ERR_UNSUPPORTED
+    assert b"topk" in gca.LIB.gca_last_error_detail()
+
+
+def _fwd(gca, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, kvbs=256 * 64 * 768, dt=gca.GCA_BF16, B=4, nQ=256, nC=256, H=12, dh=64,
+             idx=FAKE, sc=FAKE, topk=8, shift=1, o=FAKE, lse=FAKE, ws=FAKE, wsb=256)
+    a.update(kw)
+    return gca.LIB.gca_forward(a["q"], a["k"], a["v"], a["kvbs"], a["dt"], a["B"], a["nQ"], a["nC"], a["H"],
+                               a["dh"], a["idx"], a["sc"], a["topk"], a["shift"], a["o"], a["lse"], a["ws"],
+                               a["wsb"], None)
+
+
+def test_forward_rejects_bad_arguments(gca):
+    assert _fwd(gca, dh=128) == gca.GCA_ERR_UNSUPPORTED
+    assert _fwd(gca, shift=2) == gca.GCA_ERR_INVALID_ARG
+    assert _fwd(gca, dt=7) == gca.GCA_ERR_INVALID_ARG
+    assert _fwd(gca, o=0) == gca.GCA_ERR_INVALID_ARG
+    assert _fwd(gca, kvbs=100) == gca.GCA_ERR_INVALID_ARG
+    assert _fwd(gca, wsb=255) == gca.GCA_ERR_WORKSPACE
+    assert _fwd(gca, H=0) == gca.GCA_ERR_INVALID_ARG
+    assert b"shift" in (_fwd(gca, shift=-1) == gca.GCA_ERR_INVALID_ARG and gca.LIB.gca_last_error_detail())
+
+
+def test_backward_and_scores_backward_reject_bad_arguments(gca):
+    L = gca.LIB
+    r = L.gca_backward(FAKE, FAKE, FAKE, gca.GCA_BF16, 4, 256, 256, 12, 64, FAKE, FAKE, 8, 1, FAKE, FAKE,
+                       FAKE, FAKE, FAKE, 0, 0, FAKE, 1 << 40, None)
+    assert r == gca.GCA_ERR_INVALID_ARG  # dscores NULL
+    r = L.gca_backward(FAKE, FAKE, FAKE, gca.GCA_BF16, 4, 256, 256, 12, 64, FAKE, FAKE, 8, 1, FAKE, FAKE,
+                       FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1024, None)
+    assert r == gca.GCA_ERR_WORKSPACE
+    r = L.gca_scores_backward(FAKE, 768, 256 * 768, FAKE, 0, gca.GCA_BF16, 4, 256, 256, 768, FAKE, FAKE, 8,
+                              FAKE, gca.GCA_F32, 768, 256 * 768, 0, FAKE, FAKE, 1 << 30, None)
+    assert r == gca.GCA_ERR_INVALID_ARG  # shared k_lmk not allowed here

@@ -1,0 +1,189 @@
+"""GPU parity of gca_forward / gca_backward / gca_scores_backward against the float64
+oracle, fed the oracle's retrieval (so fusion numerics are tested apart from ties)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.gca_oracle as orc
+from retrieval_sparse_attention_causal_gb300 import synth
+from tests.gpu_helpers import TOL, assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _g():
+    import retrieval_sparse_attention_causal_gb300 as g
+    return g
+
+
+def make_case(seed, B, nC, H, dh, K, dtype, std=1.0, gumbel=True, D=None, shift=1):
+    nQ = nC
+    x = synth.gca_inputs(seed, B, nQ, nC, H, dh, std, dtype)
+    D = D or H * dh
+    if dtype == "bf16" and D % 64:
+        D = 64
+    lm = synth.landmark_inputs(seed, B, nQ, nC, D, dtype)
+    idx, sc, _ = orc.retrieve_topk(lm["q_lmk"], lm["k_lmk"], K, 0, gumbel, seed)
+    return x, lm, idx, sc
+
+
+def run_fwd_bwd(x, idx, sc, dtype, shift=1, check_bwd=True, poison=True):
+    g = _g()
+    q, k, v, do = (dev(x[n], dtype) for n in ("q", "k", "v", "do"))
+    it = torch.from_numpy(idx).cuda()
+    st = torch.from_numpy(sc.astype(np.float32)).cuda()
+    o = torch.full_like(q, float("nan")) if poison else None
+    o, lse = g.gca_forward(q, k, v, it, st, shift=shift, out=o)
+    res = dict(o=host(o), lse=host(lse))
+    if check_bwd:
+        dq = torch.full_like(q, float("nan")) if poison else None
+        dk = torch.full_like(k, float("nan")) if poison else None
+        dv = torch.full_like(v, float("nan")) if poison else None
+        dq, dk, dv, ds = g.gca_backward(q, k, v, it, st, do, lse, shift=shift, dq=dq, dk=dk, dv=dv)
+        res.update(dq=host(dq), dk=host(dk), dv=host(dv), ds=host(ds))
+    torch.cuda.synchronize()
+    return res
+
+
+def check_against_oracle(x, idx, sc, res, dtype, shift=1, check_bwd=True):
+    o, lse = orc.gca_forward(x["q"], x["k"], x["v"], idx, sc, shift)
+    tol = TOL[dtype]
+    assert_close(res["o"], o, tol, "O")
+    assert_close(res["lse"], lse, tol, "LSE")
+    if check_bwd:
+        dq, dk, dv, ds = orc.gca_backward(x["q"], x["k"], x["v"], idx, sc, x["do"], shift)
+        assert_close(res["dq"], dq, tol, "dQ")
+        assert_close(res["dk"], dk, tol, "dK")
+        assert_close(res["dv"], dv, tol, "dV")
+        assert_close(res["ds"], ds, tol, "dscores")
+
+
+def test_tiny_fp32():
+    """Tiny f32 workload: B=1, 16 chunks, H=4 x dh=32, k=4, no noise, at 1e-5."""
+    x, lm, idx, sc = make_case(0, 1, 16, 4, 32, 4, "f32", gumbel=False, D=128)
+    res = run_fwd_bwd(x, idx, sc, "f32")
+    check_against_oracle(x, idx, sc, res, "f32")
+
+
+@pytest.mark.parametrize("std", [0.125, 1.0])
+def test_bf16_128m_heads_small_sequence(std):
+    """128M-model head shape (H=12, dh=64, k=8, Gumbel) on 24 chunks, with the
+    workload's N(0,1)/8 inputs and with unscaled N(0,1) (sharper attention)."""
+    x, lm, idx, sc = make_case(1, 2, 24, 12, 64, 8, "bf16", std=std, D=768)
+    res = run_fwd_bwd(x, idx, sc, "bf16")
+    check_against_oracle(x, idx, sc, res, "bf16")
+
+
+@pytest.mark.parametrize("dtype,dh", [("bf16", 32), ("f32", 64)])
+def test_other_head_dims(dtype, dh):
+    x, lm, idx, sc = make_case(2, 1, 12, 3, dh, 5, dtype, D=256 if dtype == "bf16" else 96)
+    res = run_fwd_bwd(x, idx, sc, dtype)
+    check_against_oracle(x, idx, sc, res, dtype)
+
+
+def test_irregular_slots_and_shift0():
+    """Holes in the middle of a row, duplicated chunks in one row, a row without valid
+    slots, top-k = 16, and the decode-style shift 0."""
+    B, nC, H, dh, K = 1, 10, 2, 64, 16
+    x = synth.gca_inputs(3, B, nC, nC, H, dh, 1.0, "bf16")
+    rng = np.random.default_rng(3)
+    idx = rng.integers(-1, nC, size=(B, nC, K)).astype(np.int32)
+    idx[0, 4] = -1
+    idx[0, 5, :4] = 7
+    sc = rng.standard_normal((B, nC, K))
+    sc[idx < 0] = -np.inf
+    for shift in (0, 1):
+        res = run_fwd_bwd(x, idx, sc, "bf16", shift=shift)
+        check_against_oracle(x, idx, sc, res, "bf16", shift=shift)
+
+
+def test_kv_shared_across_sequences_forward():
+    """Batch stride 0 for K/V: every sequence reads one store (decode with aliasing)."""
+    g = _g()
+    B, nC, H, dh = 3, 20, 2, 64
+    x = synth.gca_inputs(4, 1, 1, nC, H, dh, 1.0, "bf16")
+    q = synth.normal(4, 99, (B, 64, H, dh), 1.0, "bf16")
+    rng = np.random.default_rng(4)
+    idx = np.stack([rng.permutation(nC)[:8] for _ in range(B)]).astype(np.int32)[:, None, :]
+    sc = rng.standard_normal((B, 1, 8))
+    kk = np.broadcast_to(x["k"], (B,) + x["k"].shape[1:]).copy()
+    vv = np.broadcast_to(x["v"], (B,) + x["v"].shape[1:]).copy()
+    o_ref, lse_ref = orc.gca_forward(q, kk, vv, idx, sc, shift=0)
+    o, lse = g.gca_forward(dev(q, "bf16"), dev(x["k"][0], "bf16"), dev(x["v"][0], "bf16"),
+                           torch.from_numpy(idx).cuda(), torch.from_numpy(sc.astype(np.float32)).cuda(),
+                           shift=0, kv_shared=True)
+    assert_close(host(o), o_ref, TOL["bf16"], "O")
+    assert_close(host(lse), lse_ref, TOL["bf16"], "LSE")
+
+
+def test_accumulate_dkv():
+    g = _g()
+    x, lm, idx, sc = make_case(5, 1, 16, 2, 64, 4, "bf16", D=128)
+    q, k, v, do = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    it, st = torch.from_numpy(idx).cuda(), torch.from_numpy(sc.astype(np.float32)).cuda()
+    o, lse = g.gca_forward(q, k, v, it, st)
+    _, dk1, dv1, _ = g.gca_backward(q, k, v, it, st, do, lse)
+    dk2, dv2 = dk1.clone(), dv1.clone()
+    g.gca_backward(q, k, v, it, st, do, lse, dk=dk2, dv=dv2, accumulate_dkv=True)
+    assert_close(host(dk2), 2 * host(dk1), 1e-2, "2 dK")
+    assert_close(host(dv2), 2 * host(dv1), 1e-2, "2 dV")
+
+
+def test_bad_index_is_flagged_not_faulting():
+    """An index outside [-1, nC) is treated as an empty slot and reported through the
+    workspace error word (host-side check), never read."""
+    g = _g()
+    B, nC, H, dh, K = 1, 6, 2, 64, 3
+    x = synth.gca_inputs(6, B, nC, nC, H, dh, 1.0, "bf16")
+    idx = np.array([[[-1, -1, -1], [0, -1, -1], [1, 0, 12345], [2, 1, 0], [3, -7, 1], [4, 0, 2]]], dtype=np.int32)
+    sc = np.ones((B, nC, K))
+    ws = g.Workspace()
+    q, k, v, do = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    it, st = torch.from_numpy(idx).cuda(), torch.from_numpy(sc.astype(np.float32)).cuda()
+    o, lse = g.gca_forward(q, k, v, it, st, ws=ws)
+    with pytest.raises(g.GCAError) as e:
+        ws.check()
+    assert e.value.status == g.GCA_ERR_DEVICE_INDEX
+    ws.check()  # flag was cleared
+    clean = idx.copy()
+    clean[(clean < -1) | (clean >= nC)] = -1
+    sc_clean = np.where(clean >= 0, 1.0, -np.inf)
+    o_ref, _ = orc.gca_forward(x["q"], x["k"], x["v"], clean, sc_clean, 1)
+    assert_close(host(o), o_ref, TOL["bf16"], "O with bad index dropped")
+    g.gca_backward(q, k, v, it, st, do, lse, ws=ws)
+    with pytest.raises(g.GCAError):
+        ws.check()
+
+
+def test_deterministic_bitwise():
+    g = _g()
+    x, lm, idx, sc = make_case(7, 2, 40, 4, 64, 8, "bf16", D=256)
+    a = run_fwd_bwd(x, idx, sc, "bf16")
+    b = run_fwd_bwd(x, idx, sc, "bf16")
+    for key in a:
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_scores_backward_and_strided_accumulate():
+    """Landmark-score gradient (fp32 out), and the accumulate mode that adds a second
+    group's landmark gradient into a bf16 output gradient at each chunk's last token."""
+    g = _g()
+    B, nC, D, K = 2, 40, 256, 8
+    lm = synth.landmark_inputs(8, B, nC, nC, D, "bf16")
+    idx, sc, _ = orc.retrieve_topk(lm["q_lmk"], lm["k_lmk"], K, 0, True, 8)
+    ds = synth.normal(8, synth.S_DSC, (B, nC, K), 1.0, "f32") * (idx >= 0)
+    dq_ref, dk_ref = orc.scores_backward(lm["q_lmk"], lm["k_lmk"], idx, ds)
+    ql, kl = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
+    it, dst = torch.from_numpy(idx).cuda(), torch.from_numpy(ds.astype(np.float32)).cuda()
+    dq, dk = g.scores_backward(ql, kl, it, dst)
+    assert_close(host(dq), dq_ref, 1e-5, "dq_lmk")
+    assert_close(host(dk), dk_ref, 1e-5, "dk_lmk")
+    # accumulate into rows 63, 127, ... of a [B, nC*64, H, dh] bf16 tensor with H*dh = D
+    H, dh = 4, 64
+    base = synth.normal(8, 77, (B, nC * 64, H, dh), 1.0, "bf16")
+    t = dev(base, "bf16")
+    view = t[:, 63::64].reshape(B, nC, D)
+    g.scores_backward(ql, kl, it, dst, dq_out=view, accumulate=True)
+    want = base.copy()
+    want[:, 63::64] += dq_ref.reshape(B, nC, H, dh)
+    assert_close(host(t), want, TOL["bf16"], "accumulated dO")

@@ -1,0 +1,132 @@
+"""GPU parity of gca_retrieve_topk against the float64 oracle (indices bit-exact on rows
+whose best k+1 keys are at least 1e-3 apart; near-tie rows checked as sets)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.gca_oracle as orc
+from retrieval_sparse_attention_causal_gb300 import synth
+from tests.gpu_helpers import GAP, TOL, assert_close, compare_retrieval, dev, host
+
+pytestmark = pytest.mark.gpu
+
+SCORE_TOL = {"f32": 1e-5, "bf16": 1e-4}  # fp32 accumulation of exact bf16 products
+
+
+def _gca():
+    import retrieval_sparse_attention_causal_gb300 as g
+    return g
+
+
+def run_case(B, nQ, nC, D, K, dtype, off=0, gumbel=False, seed=0, group=0, lm=None, rows=None,
+             expect_all_decidable=False):
+    g = _gca()
+    if lm is None:
+        lm = synth.landmark_inputs(seed, B, nQ, nC, D, dtype)
+    q, k = lm["q_lmk"], lm["k_lmk"]
+    idx_o, sc_o, margin = orc.retrieve_topk(q, k, K, off, gumbel, seed, group, rows=rows)
+    idx_g, sc_g = g.retrieve_topk(dev(q, dtype), dev(k, dtype), K, off, gumbel, seed, group)
+    torch.cuda.synchronize()
+    nd, nt = compare_retrieval(idx_g.cpu().numpy(), host(sc_g), idx_o, sc_o, margin, SCORE_TOL[dtype],
+                               rows=rows, orc=orc, q=q, k=k, gumbel=gumbel, seed=seed, group=group, off=off)
+    if expect_all_decidable:
+        assert nt == 0
+    return idx_g, sc_g, idx_o, nd, nt
+
+
+def test_tiny_fp32_exact():
+    """The tiny f32 workload (B=1, 16 chunks, D=128, k=4, no noise): redraw the seed until
+    every row is decidable (gap >= 1e-3), then require identical indices on every row."""
+    for seed in range(100):
+        lm = synth.landmark_inputs(seed, 1, 16, 16, 128, "f32")
+        _, _, m = orc.retrieve_topk(lm["q_lmk"], lm["k_lmk"], 4, 0)
+        if np.all(m >= GAP):
+            break
+    run_case(1, 16, 16, 128, 4, "f32", seed=seed, lm=lm, expect_all_decidable=True)
+
+
+@pytest.mark.parametrize("B,D,group", [(4, 768, 0), (8, 1024, 0), (8, 1024, 1)])
+def test_training_shapes_with_gumbel(B, D, group):
+    """128M (B=4, D=768) and 350M (B=8, D=1024, both groups) shapes, 256 chunks, k=8."""
+    _, _, _, nd, nt = run_case(B, 256, 256, D, 8, "bf16", gumbel=True, seed=5, group=group)
+    assert nd > 0.9 * (nd + nt)
+
+
+def test_prefill_full_size_sampled_rows():
+    """1M-token prefill: 16384 chunks, D=768, k=8, no noise; every row on the GPU, a
+    sample of rows (first, last, tile edges, random) on the oracle."""
+    nQ = 16384
+    rng = np.random.default_rng(0)
+    sample = sorted(set([0, 1, 2, 63, 64, 65, 8191, 16320, nQ - 2, nQ - 1] + list(rng.integers(0, nQ, 22))))
+    rows = [(0, int(i)) for i in sample]
+    run_case(1, nQ, nQ, 768, 8, "bf16", seed=3, rows=rows)
+
+
+@pytest.mark.parametrize("B", [1, 2])
+def test_decode_16m_context_planted(B):
+    """Decode at 16M context: 262144 past landmarks (D=768) per sequence, one query
+    landmark, one planted chunk equal to the query; the planted chunk must fill slot 0."""
+    g = _gca()
+    nC, D = 262144, 768
+    lm = synth.planted_landmarks(11, B, nC, D, "bf16")
+    idx_g, sc_g, idx_o, nd, nt = run_case(B, 1, nC, D, 8, "bf16", off=nC, lm=lm)
+    for b in range(B):
+        assert int(idx_g[b, 0, 0]) == int(lm["jstar"][b])
+
+
+EDGE = [
+    # B, nQ, nC, D, K, dtype, off, gumbel
+    (1, 1, 1, 64, 1, "bf16", 1, False),       # one candidate
+    (2, 5, 3, 64, 8, "bf16", 0, False),       # more slots than candidates
+    (3, 100, 100, 256, 8, "bf16", 0, True),   # ragged row tile
+    (1, 300, 300, 128, 16, "bf16", 1, False),  # k = 16, offset 1, candidate splits
+    (2, 70, 130, 64, 3, "f32", 5, True),      # f32 tile path, offset 5
+    (1, 3, 5000, 512, 8, "bf16", 5000, True),  # rows path, split merge
+    (2, 8, 3000, 96, 4, "f32", 2990, False),   # rows path f32, partial causal limit
+    (1, 9, 9, 64, 8, "bf16", 0, False),        # smallest tile case
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=[str(c) for c in EDGE])
+def test_edge_cases(case):
+    B, nQ, nC, D, K, dtype, off, gumbel = case
+    run_case(B, nQ, nC, D, K, dtype, off=off, gumbel=gumbel, seed=2)
+
+
+@pytest.mark.parametrize("dtype,nQ", [("bf16", 40), ("f32", 40), ("bf16", 4)])
+def test_all_ties_take_lowest_indices(dtype, nQ):
+    """All-zero landmarks and no noise: every key ties, so the lowest indices win."""
+    g = _gca()
+    D = 64 if dtype == "bf16" else 32
+    q = torch.zeros((2, nQ, D), device="cuda", dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
+    k = torch.zeros((2, 50, D), device="cuda", dtype=q.dtype)
+    idx, sc = g.retrieve_topk(q, k, 5, 3)
+    idx = idx.cpu().numpy()
+    for i in range(nQ):
+        n = min(50, i + 3)
+        want = list(range(min(5, n))) + [-1] * (5 - min(5, n))
+        assert list(idx[1, i]) == want
+
+
+def test_strided_query_rows_and_shared_keys():
+    """Query landmarks read as a strided view (every 3rd row of a larger tensor) and one
+    key-landmark set shared by all sequences (batch stride 0)."""
+    g = _gca()
+    B, nQ, nC, D = 2, 20, 40, 128
+    big = synth.normal(1, 0, (B, nQ * 3, D), 1.0, "bf16")
+    kl = synth.normal(1, 1, (nC, D), 1.0, "bf16")
+    qv = big[:, ::3]
+    ko = np.broadcast_to(kl, (B, nC, D)).copy()
+    idx_o, sc_o, m = orc.retrieve_topk(qv, ko, 6, 2)
+    qt = dev(big, "bf16")[:, ::3]
+    idx_g, sc_g = g.retrieve_topk(qt, dev(kl, "bf16"), 6, 2, k_shared=True)
+    compare_retrieval(idx_g.cpu().numpy(), host(sc_g), idx_o, sc_o, m, 1e-4, orc=orc, q=qv, k=ko, off=2)
+
+
+def test_deterministic():
+    g = _gca()
+    lm = synth.landmark_inputs(4, 2, 200, 200, 256, "bf16")
+    q, k = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
+    a = g.retrieve_topk(q, k, 8, 0, True, 9)
+    b = g.retrieve_topk(q, k, 8, 0, True, 9)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
