@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def gca():
-    from retrieval_sparse_attention_causal_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import retrieval_sparse_attention_causal_gb300 as m
     return m
 
