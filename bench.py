@@ -82,7 +82,7 @@ class ClockSampler:
                 for bit, name in self.REASONS.items():
                     if rs.value & bit:
                         self.reasons.add(name)
-            time.sleep(0.02)
+            time.sleep(0.005)
 
     def __enter__(self):
         self.stop = False
@@ -400,7 +400,7 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--seed", type=int, default=0)

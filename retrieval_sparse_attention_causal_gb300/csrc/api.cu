@@ -94,13 +94,22 @@ cudaError_t allow_smem(const void* fn, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  struct Done {
+    const void* fn;
+    int dev, bytes;
+  };
   static std::mutex mu;
-  static std::vector<std::pair<const void*, int>> done;  // (function, device)
+  static std::vector<Done> done;  // largest limit set so far per (function, device)
   std::lock_guard<std::mutex> lk(mu);
   for (auto& d : done)
-    if (d.first == fn && d.second == dev) return cudaSuccess;
+    if (d.fn == fn && d.dev == dev) {
+      if (d.bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) d.bytes = bytes;
+      return e;
+    }
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.emplace_back(fn, dev);
+  if (e == cudaSuccess) done.push_back(Done{fn, dev, bytes});
   return e;
 }
 
