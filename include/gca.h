@@ -102,6 +102,37 @@ GCA_API gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride, in
                              float* scores, void* ws, size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * gca_retrieve_topk_noalloc - gca_retrieve_topk for callers that cannot allocate.
+ *
+ * The paper has no counterpart: this is a convenience of the library.  Some callers
+ * cannot allocate device memory where they retrieve: a plug-in inside a host
+ * application whose allocator already owns all of the GPU's memory, a latency-bound
+ * decode loop where a cudaMalloc would synchronise the device and stall other streams,
+ * or a plain C caller with no device allocator of its own.  This entry point takes the
+ * arguments of gca_retrieve_topk without the workspace and keeps its scratch (the
+ * per-split candidate lists and an error word) in one static device array of
+ * gca_retrieve_noalloc_max_scratch() = 4 MiB (+256 bytes), which every GPU that loads
+ * the library holds until the process exits.
+ *   - A problem whose candidate scratch is larger (gca_retrieve_workspace_size() minus
+ *     256 bytes above 4 MiB) returns GCA_ERR_UNSUPPORTED with an explanation: decode
+ *     at 16M context with up to 16 sequences and training-size problems fit, a
+ *     1M-token prefill does not.
+ *   - Nothing is allocated (no cudaMalloc or cudaFree).  The first call on a device
+ *     looks up the array's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents.  Calls
+ *     that can overlap on the GPU (several streams or host threads) race on it; issue
+ *     them on one stream.
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_retrieve_noalloc_max_scratch(void);
+GCA_API gca_status gca_retrieve_topk_noalloc(const void* q_lmk, int64_t q_row_stride,
+                                     int64_t q_batch_stride, const void* k_lmk,
+                                     int64_t k_batch_stride, gca_dtype dtype, int B, int nQ,
+                                     int nC, int D, int topk, int causal_offset,
+                                     int use_gumbel, uint64_t seed, int group, int32_t* idx,
+                                     float* scores, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * gca_forward - grouped cross-attention over the retrieved chunks.
  *
  * Paper-Notes page, 关键设计 ("Grouped Cross-Attention"): each retrieved chunk gets its

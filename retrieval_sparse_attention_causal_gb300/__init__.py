@@ -44,6 +44,8 @@ def _load():
         "gca_last_error_detail": (ctypes.c_char_p, []),
         "gca_retrieve_workspace_size": (SZ, [I, I, I, I, I]),
         "gca_retrieve_topk": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P, SZ, P]),
+        "gca_retrieve_noalloc_max_scratch": (SZ, []),
+        "gca_retrieve_topk_noalloc": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P]),
         "gca_forward_workspace_size": (SZ, []),
         "gca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, P, I, I, P, P, P, SZ, P]),
         "gca_backward_workspace_size": (SZ, [I, I, I, I, I]),
@@ -67,6 +69,7 @@ def _load():
 LIB = _load()
 EXPORTS = (
     "gca_status_string", "gca_last_error_detail", "gca_retrieve_workspace_size", "gca_retrieve_topk",
+    "gca_retrieve_noalloc_max_scratch", "gca_retrieve_topk_noalloc",
     "gca_forward_workspace_size", "gca_forward", "gca_backward_workspace_size", "gca_backward",
     "gca_scores_backward_workspace_size", "gca_scores_backward", "gca_check_error", "gca_launch_count",
     "gca_profile_begin", "gca_profile_end", "gca_profile_row",

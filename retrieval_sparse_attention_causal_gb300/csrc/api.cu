@@ -89,6 +89,11 @@ cudaError_t launch_end(const char* name, cudaStream_t s) {
   return e;
 }
 
+int set_error_detail(const char* msg) {
+  t_detail = msg;
+  return 0;
+}
+
 cudaError_t allow_smem(const void* fn, int bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
   int dev = 0;

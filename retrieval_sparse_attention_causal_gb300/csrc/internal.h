@@ -14,6 +14,9 @@ struct ErrWord;
 void launch_begin(const char* name, cudaStream_t s);
 cudaError_t launch_end(const char* name, cudaStream_t s);
 
+// Records `msg` as the calling thread's error detail and returns `s`.
+int set_error_detail(const char* msg);
+
 // Sets the dynamic shared-memory limit of `fn` once per device.
 cudaError_t allow_smem(const void* fn, int bytes);
 
