@@ -56,7 +56,8 @@ typedef enum {
   GCA_ERR_UNSUPPORTED = 2,  /* valid but not provided (e.g. dh not 32/64, topk > 16)    */
   GCA_ERR_WORKSPACE = 3,    /* ws is NULL, misaligned or smaller than required          */
   GCA_ERR_CUDA = 4,         /* a CUDA runtime call failed; see gca_last_error_detail()  */
-  GCA_ERR_DEVICE_INDEX = 5  /* (gca_check_error) a kernel met idx outside [-1, nC)      */
+  GCA_ERR_DEVICE_INDEX = 5, /* (gca_check_error) a kernel met idx outside [-1, nC)      */
+  GCA_ERR_TIMEOUT = 6       /* (gca_check_error) a bounded wait inside a kernel ran out  */
 } gca_status;
 
 typedef enum { GCA_F32 = 0, GCA_BF16 = 1 } gca_dtype;
@@ -211,8 +212,9 @@ GCA_API gca_status gca_scores_backward(const void* q_lmk, int64_t q_row_stride, 
 
 /* ---------------------------------------------------------------------------------
  * gca_check_error - synchronise `stream`, read and clear the device error word of `ws`.
- * Returns GCA_OK, GCA_ERR_DEVICE_INDEX (with the offending index in *bad_value when
- * bad_value != NULL) or GCA_ERR_CUDA.
+ * Returns GCA_OK, GCA_ERR_TIMEOUT (a tensor-core completion wait gave up instead of
+ * hanging; the results of that call are not valid), GCA_ERR_DEVICE_INDEX (with the
+ * offending index in *bad_value when bad_value != NULL) or GCA_ERR_CUDA.
  * ------------------------------------------------------------------------------- */
 GCA_API gca_status gca_check_error(void* ws, gca_stream_t stream, int* bad_value);
 

@@ -21,7 +21,8 @@ MAX_TOPK = 16
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libgca.so")
 
-GCA_OK, GCA_ERR_INVALID_ARG, GCA_ERR_UNSUPPORTED, GCA_ERR_WORKSPACE, GCA_ERR_CUDA, GCA_ERR_DEVICE_INDEX = range(6)
+(GCA_OK, GCA_ERR_INVALID_ARG, GCA_ERR_UNSUPPORTED, GCA_ERR_WORKSPACE, GCA_ERR_CUDA, GCA_ERR_DEVICE_INDEX,
+ GCA_ERR_TIMEOUT) = range(7)
 GCA_F32, GCA_BF16 = 0, 1
 
 

@@ -131,6 +131,7 @@ extern "C" const char* gca_status_string(gca_status s) {
     case GCA_ERR_WORKSPACE: return "GCA_ERR_WORKSPACE";
     case GCA_ERR_CUDA: return "GCA_ERR_CUDA";
     case GCA_ERR_DEVICE_INDEX: return "GCA_ERR_DEVICE_INDEX";
+    case GCA_ERR_TIMEOUT: return "GCA_ERR_TIMEOUT";
   }
   return "unknown gca_status";
 }
@@ -360,6 +361,7 @@ extern "C" gca_status gca_check_error(void* ws, gca_stream_t stream, int* bad_va
   const ErrWord zero{};
   e = cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "gca_check_error clear");
+  if (h.flags & kErrTimeout) return fail(GCA_ERR_TIMEOUT, "a bounded wait for tensor-core completion ran out");
   if (bad_value) *bad_value = h.bad_value;
   return fail(GCA_ERR_DEVICE_INDEX, "a kernel met retrieved index %d outside [-1, nC)", h.bad_value);
 }

@@ -17,6 +17,7 @@ struct ErrWord {
   int bad_value;  // last offending index
 };
 constexpr int kErrIndex = 1;
+constexpr int kErrTimeout = 2;
 constexpr size_t kErrBytes = 256;
 
 __device__ __forceinline__ void flag_bad_index(ErrWord* e, int v) {
@@ -24,6 +25,11 @@ __device__ __forceinline__ void flag_bad_index(ErrWord* e, int v) {
     atomicOr(&e->flags, kErrIndex);
     atomicExch(&e->bad_value, v);
   }
+}
+
+// A bounded wait on an mbarrier ran out (the kernel carried on instead of hanging).
+__device__ __forceinline__ void flag_timeout(ErrWord* e) {
+  if (e) atomicOr(&e->flags, kErrTimeout);
 }
 
 // ---------------------------------------------------------------- element access

@@ -13,6 +13,7 @@
 // 64 x 64 x dh tile S = Q K^T, a row softmax in registers, and O += (w_m / l) P V.
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace gca {
 namespace {
@@ -194,6 +195,245 @@ __global__ void __launch_bounds__(128) gca_fwd_mma_kernel(FwdArgs a) {
   }
 }
 
+
+// ------------------------------------------------------------------ bf16 tcgen05 path (dh = 64)
+// Same decomposition on the 5th-generation tensor cores, warp-specialised.
+//   * Warp 4 (control): lane 0 issues the TMA tile loads (Q once; K and V of each
+//     retrieved chunk into a 2-stage ring), waits on the mbarriers, and issues
+//     tcgen05.mma (M = 64 query rows, N = 64, K steps of 16) with operands in
+//     128-byte-swizzled shared memory and accumulators in TMEM: S = Q K^T in columns
+//     0-63 and the fused output O in columns 64-127, accumulated over all slots.
+//   * Warps 0-3 (softmax): read S with tcgen05.ld, do the row softmax in registers and
+//     write P~ = (w_m / l) P as bf16 to shared memory, the A operand of O += P~ V (V is
+//     the MN-major B operand).
+// The two sides hand over through hardware named barriers (nobody spins): S(m+1) is
+// issued as soon as the softmax warps have read S(m), so the tensor core overlaps the
+// softmax.  128 TMEM columns and ~50 KB of shared memory per CTA let four CTAs share
+// an SM.
+constexpr int kFwdStages = 2;
+constexpr int kFwdTcSmem = 8192 * (2 + 2 * kFwdStages) + 1024;  // Q, P, ring of (K, V)
+constexpr int kFwdThreads = 160;
+enum { kBarSReady = 1, kBarSFree = 2, kBarPFree = 3, kBarPReady = 4 };
+
+__global__ void __launch_bounds__(kFwdThreads, 4)
+gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV) {
+  constexpr int DH = 64, ROWB = 128, TILE = 8192, UPR = 8, NST = kFwdStages, NT = kFwdThreads;
+  constexpr uint32_t kIdS = tc::idesc_bf16(64, 64, false);
+  constexpr uint32_t kIdPV = tc::idesc_bf16(64, DH, true);
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  unsigned char* Qs = sm;
+  unsigned char* Ps = sm + TILE;
+  unsigned char* ring = sm + 2 * TILE;  // stage st: K at ring + 2*st*TILE, V after it
+  __shared__ float w_s[kMaxTopk];
+  __shared__ int j_s[kMaxTopk];
+  __shared__ int slot_s[kMaxTopk];
+  __shared__ int nslot_s;
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bar_q, bar_kv[NST], bar_s, bar_o;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t ts = (int64_t)a.H * DH;
+  bf16* og = reinterpret_cast<bf16*>(a.o) + ((int64_t)b * a.nQ * 64 + (int64_t)c * 64) * ts + h * DH;
+  float* lse = a.lse + (((int64_t)b * a.nQ + c) * a.H + h) * a.topk * 64;
+  const int r = c - a.shift;
+  const int bkv = a.kv_bs == 0 ? 0 : b;
+
+  if (warp == 0) {
+    if (r >= 0) {
+      row_weights_warp(a.idx + ((int64_t)b * a.nQ + r) * a.topk, a.scores + ((int64_t)b * a.nQ + r) * a.topk,
+                       a.topk, a.nC, w_s, j_s, a.err);
+    } else if (lane < a.topk) {
+      w_s[lane] = 0.f;
+      j_s[lane] = -1;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int n = 0;
+      for (int m = 0; m < a.topk; ++m)
+        if (j_s[m] >= 0) slot_s[n++] = m;
+      nslot_s = n;
+      tc::mbar_init(&bar_q, 1);
+      for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_kv[st], 1);
+      tc::mbar_init(&bar_s, 1);
+      tc::mbar_init(&bar_o, 1);
+      tc::fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  const int ns = nslot_s;
+  for (int x = tid; x < a.topk * 64; x += NT)
+    if (j_s[x >> 6] < 0) lse[x] = -CUDART_INF_F;
+  if (ns == 0) {
+    for (int u = tid; u < 64 * UPR; u += NT) {
+      const int row = u / UPR, w = u % UPR;
+      *reinterpret_cast<uint4*>(og + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tS = tmem_slot, tO = tmem_slot + 64;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ control warp
+    bool ok = true;
+    auto load_slot = [&](int x) {  // K, V tiles of slot x into stage x % NST
+      const int st = x % NST;
+      const int j = j_s[slot_s[x]];
+      unsigned char* Ks = ring + 2 * st * TILE;
+      tc::mbar_expect_tx(&bar_kv[st], 2 * TILE);
+      tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, bkv, &bar_kv[st]);
+      tc::tma_load_4d(Ks + TILE, &tmV, 0, h, j * 64, bkv, &bar_kv[st]);
+    };
+    auto issue_s = [&](int x) {
+      unsigned char* Ks = ring + 2 * (x % NST) * TILE;
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks)
+        tc::mma(tS, tc::desc_kmajor(tc::su32(Qs), ks), tc::desc_kmajor(tc::su32(Ks), ks), kIdS, ks > 0);
+      tc::commit(&bar_s);
+    };
+    if (lane == 0) {
+      tc::mbar_expect_tx(&bar_q, TILE);
+      tc::tma_load_4d(Qs, &tmQ, 0, h, c * 64, b, &bar_q);
+      for (int x = 0; x < NST && x < ns; ++x) load_slot(x);
+      ok = tc::mbar_wait(&bar_q, 0) && ok;
+      ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
+      issue_s(0);
+      ok = tc::mbar_wait(&bar_s, 0) && ok;
+    }
+    __syncwarp();
+    tc::named_arrive(kBarSReady, NT);
+    tc::named_arrive(kBarPFree, NT);
+    for (int si = 0; si < ns; ++si) {
+      tc::named_sync(kBarSFree, NT);  // softmax warps have read S(si)
+      if (lane == 0 && si + 1 < ns) {
+        tc::fence_after();
+        ok = tc::mbar_wait(&bar_kv[(si + 1) % NST], ((si + 1) / NST) & 1) && ok;
+        issue_s(si + 1);
+      }
+      __syncwarp();
+      tc::named_sync(kBarPReady, NT);  // P(si) is in shared memory
+      if (lane == 0) {
+        tc::fence_after();
+        unsigned char* Vs = ring + (2 * (si % NST) + 1) * TILE;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma(tO, tc::desc_kmajor(tc::su32(Ps), kk), tc::desc_mnmajor(tc::su32(Vs), kk), kIdPV,
+                  (si > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&bar_o);
+        if (si + 1 < ns) ok = tc::mbar_wait(&bar_s, (si + 1) & 1) && ok;  // S(si+1) ready
+      }
+      __syncwarp();
+      if (si + 1 < ns) tc::named_arrive(kBarSReady, NT);
+      if (lane == 0) {
+        ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // P and ring stage si % NST are free
+        if (si + NST < ns) load_slot(si + NST);
+        if (!ok) flag_timeout(a.err);
+      }
+      __syncwarp();
+      if (si + 1 < ns) tc::named_arrive(kBarPFree, NT);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int g = lane >> 2, cq = lane & 3;
+    const int row0 = 16 * warp + g;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const float scale = 1.0f / sqrtf((float)DH);
+    const float sl2 = scale * 1.4426950408889634f;
+    uint32_t poff0[8], poff1[8];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      poff0[n] = swz<ROWB>(row0, n) + cq * 4;
+      poff1[n] = swz<ROWB>(row0 + 8, n) + cq * 4;
+    }
+    for (int si = 0; si < ns; ++si) {
+      tc::named_sync(kBarSReady, NT);
+      tc::fence_after();
+      float s[8][4];
+#pragma unroll
+      for (int cb = 0; cb < 8; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
+      tc::ld_wait(s);
+      tc::fence_before();
+      tc::named_arrive(kBarSFree, NT);
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+      }
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
+      }
+      const float o0 = -mx0 * sl2, o1 = -mx1 * sl2;
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        s[n][0] = tc::ex2(fmaf(s[n][0], sl2, o0));
+        s[n][1] = tc::ex2(fmaf(s[n][1], sl2, o0));
+        s[n][2] = tc::ex2(fmaf(s[n][2], sl2, o1));
+        s[n][3] = tc::ex2(fmaf(s[n][3], sl2, o1));
+        l0 += s[n][0] + s[n][1];
+        l1 += s[n][2] + s[n][3];
+      }
+#pragma unroll
+      for (int m = 1; m <= 2; m <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, m);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, m);
+      }
+      const int mslot = slot_s[si];
+      const float wm = w_s[mslot];
+      if (cq == 0) {
+        lse[mslot * 64 + row0] = mx0 * scale + __logf(l0);
+        lse[mslot * 64 + row0 + 8] = mx1 * scale + __logf(l1);
+      }
+      const float c0 = __fdividef(wm, l0), c1 = __fdividef(wm, l1);
+      tc::named_sync(kBarPFree, NT);  // O += P~ V of the previous slot has finished
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        *reinterpret_cast<uint32_t*>(Ps + poff0[n]) = pack_bf16(s[n][0] * c0, s[n][1] * c0);
+        *reinterpret_cast<uint32_t*>(Ps + poff1[n]) = pack_bf16(s[n][2] * c1, s[n][3] * c1);
+      }
+      tc::fence_async_smem();
+      tc::named_arrive(kBarPReady, NT);
+    }
+  }
+  // Every O += P~ V has completed (the control warp waited for the last one).
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp < 4) {
+    const int g = lane >> 2, cq = lane & 3;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    float o[8][4];
+#pragma unroll
+    for (int cb = 0; cb < 8; ++cb) tc::ld16x256(tO + lane_base + cb * 8, o[cb]);
+    tc::ld_wait(o);
+    // Stage O through the Q tile (its last reader, the final S = Q K^T, is done).
+#pragma unroll
+    for (int n = 0; n < DH / 8; ++n) {
+      const int r0 = 16 * warp + g;
+      *reinterpret_cast<uint32_t*>(Qs + swz<ROWB>(r0, n) + cq * 4) = pack_bf16(o[n][0], o[n][1]);
+      *reinterpret_cast<uint32_t*>(Qs + swz<ROWB>(r0 + 8, n) + cq * 4) = pack_bf16(o[n][2], o[n][3]);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem_slot, 128);
+  }
+  for (int u = tid; u < 64 * UPR; u += NT) {
+    const int row = u / UPR, w = u % UPR;
+    *reinterpret_cast<uint4*>(og + row * ts + w * 8) = *reinterpret_cast<const uint4*>(Qs + swz<ROWB>(row, w));
+  }
+}
+
 // ------------------------------------------------------------------ f32 SIMT path
 // One thread per query token; exact fp32 products and expf, for the f32 configuration.
 template <int DH>
@@ -274,11 +514,21 @@ __global__ void __launch_bounds__(64) gca_fwd_f32_kernel(FwdArgs a) {
 
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s) {
   dim3 grid(a.nQ, a.H, a.B);
-  if (a.bf16) {
+  if (a.bf16 && a.dh == 64) {
+    CUtensorMap tq, tk, tv;
+    cudaError_t e = make_head_tmap(&tq, a.q, 64, a.H, (int64_t)a.nQ * 64, a.B, (int64_t)a.nQ * 64 * a.H * 64);
+    if (e == cudaSuccess) e = make_head_tmap(&tk, a.k, 64, a.H, (int64_t)a.nC * 64, a.B, a.kv_bs);
+    if (e == cudaSuccess) e = make_head_tmap(&tv, a.v, 64, a.H, (int64_t)a.nC * 64, a.B, a.kv_bs);
+    if (e == cudaSuccess) e = allow_smem((const void*)gca_fwd_tc_kernel, kFwdTcSmem);
+    if (e != cudaSuccess) return e;
     launch_begin("gca_fwd", s);
-    if (a.dh == 64) gca_fwd_mma_kernel<64><<<grid, 128, 0, s>>>(a);
-    else gca_fwd_mma_kernel<32><<<grid, 128, 0, s>>>(a);
+    gca_fwd_tc_kernel<<<grid, kFwdThreads, kFwdTcSmem, s>>>(a, tq, tk, tv);
     return launch_end("gca_fwd", s);
+  }
+  if (a.bf16) {
+    launch_begin("gca_fwd_mma", s);
+    gca_fwd_mma_kernel<32><<<grid, 128, 0, s>>>(a);
+    return launch_end("gca_fwd_mma", s);
   }
   launch_begin("gca_fwd_f32", s);
   if (a.dh == 64) gca_fwd_f32_kernel<64><<<grid, 64, 0, s>>>(a);

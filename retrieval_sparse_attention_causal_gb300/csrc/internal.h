@@ -1,6 +1,7 @@
 // Host-side declarations shared by the entry points (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -19,6 +20,12 @@ int set_error_detail(const char* msg);
 
 // Sets the dynamic shared-memory limit of `fn` once per device.
 cudaError_t allow_smem(const void* fn, int bytes);
+
+// TMA tensor map of a [B][rows][H][dh] bf16 tensor whose box is one head's 64 x dh
+// tile, 128-byte swizzled (tmap.cu).  batch_stride_elems = 0: one tensor shared by all
+// sequences.
+cudaError_t make_head_tmap(CUtensorMap* out, const void* base, int dh, int H, int64_t rows, int B,
+                           int64_t batch_stride_elems);
 
 // ---- retrieval (retrieve.cu)
 struct RetrieveArgs {

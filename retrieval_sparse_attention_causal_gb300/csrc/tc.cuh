@@ -1,0 +1,154 @@
+// Blackwell (sm_103a) tensor-core helpers: tcgen05.mma with operands in shared memory
+// and accumulators in Tensor Memory (TMEM), mbarrier completion, TMEM allocation.
+//
+// Encodings used (checked on GB300 with exact-integer products before use):
+//   * shared-memory operand descriptor: start address >> 4 (bits 0-13), leading byte
+//     offset >> 4 (16-29), stride byte offset >> 4 (32-45), version 1 (bit 46),
+//     swizzle mode 2 = 128-byte swizzle (bits 61-63).  Tiles are 64 rows of 128 bytes,
+//     1024-byte aligned, with 16-byte unit u of row r stored at unit u ^ (r & 7).
+//     K-major operands: stride byte offset 1024 (eight rows), K steps of 16 elements
+//     advance the start address by 32 bytes.  MN-major operands (rows = K): leading and
+//     stride byte offsets 1024, K steps advance by 16 rows = 2048 bytes.
+//   * instruction descriptor (kind::f16): f32 accumulate (bit 4), bf16 A and B
+//     (bits 7, 10), B MN-major (bit 16), N >> 3 at bit 17, M >> 4 at bit 24.
+//   * M = 64 accumulator: row r lives in TMEM lane 32 * (r / 16) + r % 16, one 32-bit
+//     column per output column; warp w reads its 16 rows with tcgen05.ld.16x256b, which
+//     gives thread t rows t/4 and t/4 + 8, columns 2(t%4) and 2(t%4) + 1 of each
+//     8-column block (the same fragment as mma.sync's accumulator).
+#pragma once
+
+#include <stdint.h>
+
+namespace gca {
+namespace tc {
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// K-major 64-row tile, K step ks (16 elements).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int ks) { return sdesc(base + 32 * ks, 16, 1024); }
+// MN-major tile (rows = K), K step ks (16 rows).
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int ks) { return sdesc(base + 2048 * ks, 1024, 1024); }
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Arrive on `bar` when every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar)));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;"); }
+
+// Bounded wait for phase `parity` of `bar`.  Returns false if the limit ran out (the
+// caller records the timeout and carries on, so that nothing hangs).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = 1u << 26) {
+  uint32_t done = 0;
+  for (uint32_t it = 0; it < limit; ++it) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(su32(bar)), "r"(parity));
+    if (done) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;"); }
+// Make generic-proxy shared-memory writes (st.shared, cp.async) visible to tcgen05.mma.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;"); }
+
+// TMEM allocation by one full warp; the base address lands in *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+// 16 lanes x 8 columns (32-bit) from lane base `taddr`: thread t gets lanes t/4, t/4+8,
+// columns 2(t%4), 2(t%4)+1.
+__device__ __forceinline__ void ld16x256(uint32_t taddr, float (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Wait for outstanding tcgen05.ld and tie the 32 loaded registers to the wait, so that
+// the compiler cannot move a use of them above it.
+__device__ __forceinline__ void ld_wait(float (&v)[8][4]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0][0]),"+f"(v[0][1]),"+f"(v[0][2]),"+f"(v[0][3]),"+f"(v[1][0]),"+f"(v[1][1]),"+f"(v[1][2]),"+f"(v[1][3]),"+f"(v[2][0]),"+f"(v[2][1]),"+f"(v[2][2]),"+f"(v[2][3]),"+f"(v[3][0]),"+f"(v[3][1]),"+f"(v[3][2]),"+f"(v[3][3]),"+f"(v[4][0]),"+f"(v[4][1]),"+f"(v[4][2]),"+f"(v[4][3]),"+f"(v[5][0]),"+f"(v[5][1]),"+f"(v[5][2]),"+f"(v[5][3]),"+f"(v[6][0]),"+f"(v[6][1]),"+f"(v[6][2]),"+f"(v[6][3]),"+f"(v[7][0]),"+f"(v[7][1]),"+f"(v[7][2]),"+f"(v[7][3]));
+}
+
+}  // namespace tc
+}  // namespace gca
+
+namespace gca {
+namespace tc {
+
+// mbarrier arrival that also announces `bytes` of incoming TMA data.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes) : "memory");
+}
+
+// TMA tile load of a 4-D tensor map (innermost coordinate first) into shared memory,
+// completing `bytes` on `bar`.  The innermost coordinate must be a multiple of 16 bytes
+// (here always 0).
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(su32(bar))
+      : "memory");
+}
+
+}  // namespace tc
+}  // namespace gca
+
+namespace gca {
+namespace tc {
+
+// Named CTA barriers (ids 1..15) between a producer and consumers: `arrive` does not
+// block, `sync` blocks until `count` threads (a multiple of 32) have arrived.
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// 2^x with the hardware approximation (MUFU.EX2, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace tc
+}  // namespace gca
+

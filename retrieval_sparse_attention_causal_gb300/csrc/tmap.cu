@@ -1,0 +1,48 @@
+// Host-side construction of TMA tensor maps for [B][rows][H][dh] bf16 tensors: one box is
+// the 64 x dh tile of one head (64 consecutive tokens), written to shared memory with the
+// 128-byte swizzle that the tcgen05 operand descriptors expect.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace gca {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+void load_encode() {
+  cudaDriverEntryPointQueryResult q{};
+  void* fn = nullptr;
+  g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (g_encode_err == cudaSuccess && (q != cudaDriverEntryPointSuccess || fn == nullptr))
+    g_encode_err = cudaErrorSymbolNotFound;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+}  // namespace
+
+cudaError_t make_head_tmap(CUtensorMap* out, const void* base, int dh, int H, int64_t rows, int B,
+                           int64_t batch_stride_elems) {
+  std::call_once(g_once, load_encode);
+  if (g_encode_err != cudaSuccess) return g_encode_err;
+  // dims innermost first: dh, head, token, sequence.  A batch stride of 0 (one store
+  // shared by every sequence) becomes a single-sequence map; kernels then use
+  // sequence coordinate 0.
+  const bool shared = batch_stride_elems == 0;
+  cuuint64_t dims[4] = {(cuuint64_t)dh, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)(shared ? 1 : B)};
+  cuuint64_t strides[3] = {(cuuint64_t)dh * 2, (cuuint64_t)H * dh * 2,
+                           (cuuint64_t)(shared ? rows * H * dh * 2 : batch_stride_elems * 2)};
+  cuuint32_t box[4] = {(cuuint32_t)dh, 1, 64, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace gca
