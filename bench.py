@@ -317,13 +317,13 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
     time_loop(retr, args.steps)
     prof = gca.profile_end()
     nbytes = nb * DEC_NC * D * 2
-    rows_ms = prof["retrieve_rows"][1] / prof["retrieve_rows"][0]
+    rows_ms = prof["retrieve_stream"][1] / prof["retrieve_stream"][0]
     ach = nbytes / (rows_ms / 1e3) / 1e9
     del kst, vst
     return {"metric": "landmark top-k GB/s at 16M ctx", "value": round(nbytes * world / (ms_r / 1e3) / 1e9, 1),
             "unit": "GB/s", "batch": nb, "past_chunks": DEC_NC, "landmark_dim": D, "ms_per_retrieval": round(ms_r, 4),
             "ms_per_decode_chunk": round(ms_f, 4), "planted_chunk_found": ok,
-            "roofline": {"kernel": "retrieve_rows", "bound": "hbm", "achieved": round(ach, 1),
+            "roofline": {"kernel": "retrieve_stream", "bound": "hbm", "achieved": round(ach, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                          "traffic": None, "peak_source": f"{src} copy bandwidth", "bytes_per_launch": nbytes},
             "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}}

@@ -690,16 +690,16 @@ cudaError_t launch_csr(const int32_t* idx, int B, int ld_rows, int nrows, int to
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e;
   dim3 gq(a.nQ, a.H, a.B), gk(a.nC, a.H, a.B);
-  if (a.bf16) {
-    const int sq = (int)bwd_q_smem(a.dh), sk = (int)bwd_kv_smem(a.dh);
-    const void* fq = a.dh == 64 ? (const void*)gca_bwd_q_mma_kernel<64> : (const void*)gca_bwd_q_mma_kernel<32>;
-    const void* fk = a.dh == 64 ? (const void*)gca_bwd_kv_mma_kernel<64> : (const void*)gca_bwd_kv_mma_kernel<32>;
+  const bool tc = a.bf16 && a.dh == 64;
+  if (tc) {
+    if ((e = launch_bwd_q_tc(a, s)) != cudaSuccess) return e;
+  } else if (a.bf16) {
+    const int sq = (int)bwd_q_smem(a.dh);
+    const void* fq = (const void*)gca_bwd_q_mma_kernel<32>;
     if ((e = allow_smem(fq, sq)) != cudaSuccess) return e;
-    if ((e = allow_smem(fk, sk)) != cudaSuccess) return e;
-    launch_begin("gca_bwd_q", s);
-    if (a.dh == 64) gca_bwd_q_mma_kernel<64><<<gq, 128, sq, s>>>(a);
-    else gca_bwd_q_mma_kernel<32><<<gq, 128, sq, s>>>(a);
-    if ((e = launch_end("gca_bwd_q", s)) != cudaSuccess) return e;
+    launch_begin("gca_bwd_q_mma", s);
+    gca_bwd_q_mma_kernel<32><<<gq, 128, sq, s>>>(a);
+    if ((e = launch_end("gca_bwd_q_mma", s)) != cudaSuccess) return e;
   } else {
     launch_begin("gca_bwd_q_f32", s);
     if (a.dh == 64) gca_bwd_q_f32_kernel<64><<<gq, 64, 0, s>>>(a);
@@ -713,12 +713,13 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s) {
   if ((e = launch_csr(a.idx, a.B, a.nQ, nrows > 0 ? nrows : 0, a.topk, a.nC, a.csr_off, a.csr_ent,
                       a.csr_cur, a.err, s)) != cudaSuccess)
     return e;
+  if (tc) return launch_bwd_kv_tc(a, s);
   if (a.bf16) {
     const int sk = (int)bwd_kv_smem(a.dh);
-    launch_begin("gca_bwd_kv", s);
-    if (a.dh == 64) gca_bwd_kv_mma_kernel<64><<<gk, 128, sk, s>>>(a);
-    else gca_bwd_kv_mma_kernel<32><<<gk, 128, sk, s>>>(a);
-    return launch_end("gca_bwd_kv", s);
+    if ((e = allow_smem((const void*)gca_bwd_kv_mma_kernel<32>, sk)) != cudaSuccess) return e;
+    launch_begin("gca_bwd_kv_mma", s);
+    gca_bwd_kv_mma_kernel<32><<<gk, 128, sk, s>>>(a);
+    return launch_end("gca_bwd_kv_mma", s);
   }
   launch_begin("gca_bwd_kv_f32", s);
   if (a.dh == 64) gca_bwd_kv_f32_kernel<64><<<gk, 64, 0, s>>>(a);

@@ -1,0 +1,563 @@
+// GCA backward on the 5th-generation tensor cores (bf16, dh = 64).
+//
+// The same two passes as the mma.sync kernels (query side: P, D = rowsum(P * dO V^T),
+// dQ and per-head dw; key side: dK and dV over the consumers of each chunk), here
+// warp-specialised like the forward: warp 4 is the control warp (lane 0 issues the TMA
+// tile loads into a ring of stages, waits on the mbarriers and issues tcgen05.mma with
+// operands in 128-byte-swizzled shared memory and accumulators in TMEM); warps 0-3 read
+// the products with tcgen05.ld, do the element-wise part in registers and write the bf16
+// operand of the next product back to shared memory.  The two sides hand over through
+// hardware named barriers.  One 64 x 64 tile in shared memory serves as a K-major
+// operand in one product and as an MN-major operand in another (K as the B of S = Q K^T
+// and of dQ = dS K; Q and dO as the B of S^T and dPo^T and of dK, dV).
+//
+// Source of the method: Paper-Notes page on "Efficient Length-Generalizable Attention via
+// Causal Retrieval for Long-Context Language Modeling", 关键设计 / key design, item
+// "Grouped Cross-Attention" (the retrieval scores are trained through the fusion weights).
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace gca {
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr float kLog2e = 1.4426950408889634f;
+// Eight element-wise warps (warp w reads TMEM lane quarter w % 4, i.e. 16 rows, and
+// column half w / 4) and one control warp.
+constexpr int kEW = 8;
+constexpr int kThreads = 32 * (kEW + 1);
+constexpr int kCtl = kEW;  // control warp index
+constexpr int TILE = 8192, ROWB = 128, UPR = 8, DH = 64;
+enum { kBarSReady = 1, kBarSFree = 2, kBarOpFree = 3, kBarOpReady = 4, kBarEW = 5 };
+
+// ================================================================== query side
+constexpr int kQStages = 5;
+constexpr int kQSmem = TILE * (3 + 2 * kQStages) + 1024;  // Q, dO, dS, ring of (K, V)
+
+__global__ void __launch_bounds__(kThreads, 2)
+gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  constexpr int NST = kQStages, NT = kThreads;
+  constexpr uint32_t kIdKm = tc::idesc_bf16(64, 64, false);  // B K-major
+  constexpr uint32_t kIdMn = tc::idesc_bf16(64, 64, true);   // B MN-major
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  unsigned char* Qs = sm;
+  unsigned char* dOs = sm + TILE;
+  unsigned char* dSs = sm + 2 * TILE;
+  unsigned char* ring = sm + 3 * TILE;
+  __shared__ float w_s[kMaxTopk];
+  __shared__ int j_s[kMaxTopk];
+  __shared__ int slot_s[kMaxTopk];
+  __shared__ int nslot_s;
+  __shared__ float dwred[4][kMaxTopk];
+  __shared__ float Dx[2][2][64];  // [slot parity][column half][row]: partial row sums of D
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bar_q, bar_kv[NST], bar_s, bar_o;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t ts = (int64_t)a.H * DH;
+  const int64_t tok0 = ((int64_t)b * a.nQ * 64 + (int64_t)c * 64) * ts + h * DH;
+  bf16* dqg = reinterpret_cast<bf16*>(a.dq) + tok0;
+  const int64_t rowbase = ((int64_t)b * a.nQ + c) * a.H + h;
+  const float* lse = a.lse + rowbase * a.topk * 64;
+  float* Dg = a.Dbuf + rowbase * a.topk * 64;
+  float* dwp = a.dwp + rowbase * a.topk;
+  const int r = c - a.shift;
+
+  if (warp == 0) {
+    if (r >= 0) {
+      row_weights_warp(a.idx + ((int64_t)b * a.nQ + r) * a.topk, a.scores + ((int64_t)b * a.nQ + r) * a.topk,
+                       a.topk, a.nC, w_s, j_s, a.err);
+    } else if (lane < a.topk) {
+      w_s[lane] = 0.f;
+      j_s[lane] = -1;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int n = 0;
+      for (int m = 0; m < a.topk; ++m)
+        if (j_s[m] >= 0) slot_s[n++] = m;
+      nslot_s = n;
+      tc::mbar_init(&bar_q, 1);
+      for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_kv[st], 1);
+      tc::mbar_init(&bar_s, 1);
+      tc::mbar_init(&bar_o, 1);
+      tc::fence_mbar_init();
+    }
+  }
+  if (tid < 4 * kMaxTopk) dwred[tid / kMaxTopk][tid % kMaxTopk] = 0.f;
+  __syncthreads();
+  const int ns = nslot_s;
+  if (ns == 0) {
+    for (int u = tid; u < 64 * UPR; u += NT) {
+      const int row = u / UPR, w = u % UPR;
+      *reinterpret_cast<uint4*>(dqg + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
+    }
+    if (tid < a.topk) dwp[tid] = 0.f;
+    return;
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tQ = tmem_slot + 128;
+  const int bkv = b;
+
+  if (warp == kCtl) {
+    // ------------------------------------------------------------ control warp
+    bool ok = true;
+    auto load_slot = [&](int x) {
+      const int st = x % NST;
+      const int j = j_s[slot_s[x]];
+      unsigned char* Ks = ring + 2 * st * TILE;
+      tc::mbar_expect_tx(&bar_kv[st], 2 * TILE);
+      tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, bkv, &bar_kv[st]);
+      tc::tma_load_4d(Ks + TILE, &tmV, 0, h, j * 64, bkv, &bar_kv[st]);
+    };
+    auto issue_s = [&](int x) {  // S = Q K^T and dPo = dO V^T of slot x
+      unsigned char* Ks = ring + 2 * (x % NST) * TILE;
+      unsigned char* Vs = Ks + TILE;
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks) {
+        tc::mma(tS, tc::desc_kmajor(tc::su32(Qs), ks), tc::desc_kmajor(tc::su32(Ks), ks), kIdKm, ks > 0);
+        tc::mma(tP, tc::desc_kmajor(tc::su32(dOs), ks), tc::desc_kmajor(tc::su32(Vs), ks), kIdKm, ks > 0);
+      }
+      tc::commit(&bar_s);
+    };
+    if (lane == 0) {
+      tc::mbar_expect_tx(&bar_q, 2 * TILE);
+      tc::tma_load_4d(Qs, &tmQ, 0, h, c * 64, b, &bar_q);
+      tc::tma_load_4d(dOs, &tmdO, 0, h, c * 64, b, &bar_q);
+      for (int x = 0; x < NST && x < ns; ++x) load_slot(x);
+      ok = tc::mbar_wait(&bar_q, 0) && ok;
+      ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
+      issue_s(0);
+      ok = tc::mbar_wait(&bar_s, 0) && ok;
+    }
+    __syncwarp();
+    tc::named_arrive(kBarSReady, NT);
+    tc::named_arrive(kBarOpFree, NT);
+    for (int si = 0; si < ns; ++si) {
+      tc::named_sync(kBarSFree, NT);  // S(si), dPo(si) have been read
+      if (lane == 0 && si + 1 < ns) {
+        tc::fence_after();
+        ok = tc::mbar_wait(&bar_kv[(si + 1) % NST], ((si + 1) / NST) & 1) && ok;
+        issue_s(si + 1);
+      }
+      __syncwarp();
+      tc::named_sync(kBarOpReady, NT);  // dS(si) is in shared memory
+      if (lane == 0) {
+        tc::fence_after();
+        unsigned char* Ks = ring + 2 * (si % NST) * TILE;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
+          tc::mma(tQ, tc::desc_kmajor(tc::su32(dSs), kk), tc::desc_mnmajor(tc::su32(Ks), kk), kIdMn,
+                  (si > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&bar_o);
+        if (si + 1 < ns) ok = tc::mbar_wait(&bar_s, (si + 1) & 1) && ok;
+      }
+      __syncwarp();
+      if (si + 1 < ns) tc::named_arrive(kBarSReady, NT);
+      if (lane == 0) {
+        ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // dS buffer and stage si % NST are free
+        if (si + NST < ns) load_slot(si + NST);
+        if (!ok) flag_timeout(a.err);
+      }
+      __syncwarp();
+      if (si + 1 < ns) tc::named_arrive(kBarOpFree, NT);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise warps
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const int row0 = 16 * quarter + g;
+    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    const float scale = 1.0f / sqrtf((float)DH);
+    const float sl2 = scale * kLog2e;
+    uint32_t off0[4], off1[4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      off0[n] = swz<ROWB>(row0, 4 * hc + n) + cq * 4;
+      off1[n] = swz<ROWB>(row0 + 8, 4 * hc + n) + cq * 4;
+    }
+    for (int si = 0; si < ns; ++si) {
+      const int m = slot_s[si];
+      const float lse0 = lse[m * 64 + row0] * kLog2e, lse1 = lse[m * 64 + row0 + 8] * kLog2e;
+      tc::named_sync(kBarSReady, NT);
+      tc::fence_after();
+      float s[4][4], dp[4][4];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
+      tc::ld_wait(s);
+      tc::ld_wait(dp);
+      tc::fence_before();
+      tc::named_arrive(kBarSFree, NT);
+      float D0 = 0.f, D1 = 0.f;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        s[n][0] = tc::ex2(fmaf(s[n][0], sl2, -lse0));
+        s[n][1] = tc::ex2(fmaf(s[n][1], sl2, -lse0));
+        s[n][2] = tc::ex2(fmaf(s[n][2], sl2, -lse1));
+        s[n][3] = tc::ex2(fmaf(s[n][3], sl2, -lse1));
+        D0 = fmaf(s[n][0], dp[n][0], fmaf(s[n][1], dp[n][1], D0));
+        D1 = fmaf(s[n][2], dp[n][2], fmaf(s[n][3], dp[n][3], D1));
+      }
+#pragma unroll
+      for (int k = 1; k <= 2; k <<= 1) {
+        D0 += __shfl_xor_sync(0xffffffffu, D0, k);
+        D1 += __shfl_xor_sync(0xffffffffu, D1, k);
+      }
+      // Combine the two column halves in a fixed order (deterministic).
+      if (cq == 0) {
+        Dx[si & 1][hc][row0] = D0;
+        Dx[si & 1][hc][row0 + 8] = D1;
+      }
+      tc::named_sync(kBarEW, 32 * kEW);
+      D0 = Dx[si & 1][0][row0] + Dx[si & 1][1][row0];
+      D1 = Dx[si & 1][0][row0 + 8] + Dx[si & 1][1][row0 + 8];
+      if (hc == 0) {
+        float part = 0.f;
+        if (cq == 0) {
+          Dg[m * 64 + row0] = D0;
+          Dg[m * 64 + row0 + 8] = D1;
+          part = D0 + D1;
+        }
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) part += __shfl_xor_sync(0xffffffffu, part, k);
+        if (lane == 0) dwred[quarter][m] = part;
+      }
+      const float cs = w_s[m] * scale;
+      tc::named_sync(kBarOpFree, NT);  // dQ += dS K of the previous slot has finished
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        *reinterpret_cast<uint32_t*>(dSs + off0[n]) =
+            pack_bf16(s[n][0] * (dp[n][0] - D0) * cs, s[n][1] * (dp[n][1] - D0) * cs);
+        *reinterpret_cast<uint32_t*>(dSs + off1[n]) =
+            pack_bf16(s[n][2] * (dp[n][2] - D1) * cs, s[n][3] * (dp[n][3] - D1) * cs);
+      }
+      tc::fence_async_smem();
+      tc::named_arrive(kBarOpReady, NT);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (tid < a.topk) dwp[tid] = ((dwred[0][tid] + dwred[1][tid]) + dwred[2][tid]) + dwred[3][tid];
+  if (warp < kEW) {
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    float o[4][4];
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tQ + lane_base + cb * 8, o[cb]);
+    tc::ld_wait(o);
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int r0 = 16 * quarter + g;
+      *reinterpret_cast<uint32_t*>(Qs + swz<ROWB>(r0, 4 * hc + n) + cq * 4) = pack_bf16(o[n][0], o[n][1]);
+      *reinterpret_cast<uint32_t*>(Qs + swz<ROWB>(r0 + 8, 4 * hc + n) + cq * 4) = pack_bf16(o[n][2], o[n][3]);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem_slot, 256);
+  }
+  for (int u = tid; u < 64 * UPR; u += NT) {
+    const int row = u / UPR, w = u % UPR;
+    *reinterpret_cast<uint4*>(dqg + row * ts + w * 8) = *reinterpret_cast<const uint4*>(Qs + swz<ROWB>(row, w));
+  }
+}
+
+// ================================================================== key side
+constexpr int kKVStages = 4;
+constexpr int kKVStageBytes = 2 * TILE + 1024;  // Q, dO tiles + LSE and D rows (1 KB keeps tiles aligned)
+constexpr int kKVSmem = TILE * 4 + kKVStages * kKVStageBytes + 1024;  // K, V, wP^T, dS^T, ring
+
+__global__ void __launch_bounds__(kThreads, 2)
+gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  constexpr int NST = kKVStages, NT = kThreads;
+  constexpr uint32_t kIdKm = tc::idesc_bf16(64, 64, false);
+  constexpr uint32_t kIdMn = tc::idesc_bf16(64, 64, true);
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  unsigned char* Ks = sm;
+  unsigned char* Vs = sm + TILE;
+  unsigned char* PTs = sm + 2 * TILE;   // w P^T (keys x queries)
+  unsigned char* dSTs = sm + 3 * TILE;  // dS^T
+  unsigned char* ring = sm + 4 * TILE;  // stage st at ring + st * kKVStageBytes: Q, dO, lse[64], D[64]
+  __shared__ float w_st[NST];
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bar_k, bar_c[NST], bar_s, bar_o;
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t ts = (int64_t)a.H * DH;
+  const int64_t ktok0 = ((int64_t)b * a.nC * 64 + (int64_t)j * 64) * ts + h * DH;
+  const int e0 = a.csr_off[(int64_t)b * (a.nC + 1) + j];
+  const int e1 = a.csr_off[(int64_t)b * (a.nC + 1) + j + 1];
+  const int32_t* ent = a.csr_ent + (int64_t)b * a.nQ * a.topk;
+  bf16* dkg = reinterpret_cast<bf16*>(a.dk) + ktok0;
+  bf16* dvg = reinterpret_cast<bf16*>(a.dv) + ktok0;
+  const int ncons = e1 - e0;
+  if (ncons == 0) {
+    if (!a.acc_dkv) {
+      for (int u = tid; u < 64 * UPR; u += NT) {
+        const int row = u / UPR, w = u % UPR;
+        *reinterpret_cast<uint4*>(dkg + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(dvg + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    return;
+  }
+  if (tid == 0) {
+    tc::mbar_init(&bar_k, 1);
+    for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_c[st], 1);
+    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_o, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tdV = tmem_slot + 128, tdK = tmem_slot + 192;
+
+  if (warp == kCtl) {
+    // ------------------------------------------------------------ control warp
+    bool ok = true;
+    auto load_cons = [&](int x) {  // consumer x: Q, dO tiles, LSE and D rows, weight
+      const int st = x % NST;
+      const int e = ent[e0 + x];
+      const int r = e / a.topk, m = e % a.topk;
+      const int c = r + a.shift;
+      // Every lane takes part in the weight (a warp reduction); lane 0 issues the copies.
+      const float wv = [&]() {
+        const int32_t* idx_row = a.idx + ((int64_t)b * a.nQ + r) * a.topk;
+        const float* sc_row = a.scores + ((int64_t)b * a.nQ + r) * a.topk;
+        int jj = -1;
+        float sv = -CUDART_INF_F;
+        if (lane < a.topk) {
+          jj = idx_row[lane];
+          if (jj < -1 || jj >= a.nC) jj = -1;
+          if (jj >= 0) sv = sc_row[lane];
+        }
+        float mx = sv;
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+        const float ev = (jj >= 0) ? expf(sv - mx) : 0.f;
+        float sum = ev;
+#pragma unroll
+        for (int k = 16; k >= 1; k >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, k);
+        return __shfl_sync(0xffffffffu, (jj >= 0) ? ev / sum : 0.f, m);
+      }();
+      if (lane == 0) {
+        w_st[st] = wv;
+        unsigned char* base = ring + st * kKVStageBytes;
+        const int64_t rb = ((((int64_t)b * a.nQ + c) * a.H + h) * a.topk + m) * 64;
+        tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
+        tc::tma_load_4d(base, &tmQ, 0, h, c * 64, b, &bar_c[st]);
+        tc::tma_load_4d(base + TILE, &tmdO, 0, h, c * 64, b, &bar_c[st]);
+        tc::bulk_load(base + 2 * TILE, a.lse + rb, 256, &bar_c[st]);
+        tc::bulk_load(base + 2 * TILE + 256, a.Dbuf + rb, 256, &bar_c[st]);
+      }
+    };
+    auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x
+      unsigned char* base = ring + (x % NST) * kKVStageBytes;
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks) {
+        tc::mma(tS, tc::desc_kmajor(tc::su32(Ks), ks), tc::desc_kmajor(tc::su32(base), ks), kIdKm, ks > 0);
+        tc::mma(tP, tc::desc_kmajor(tc::su32(Vs), ks), tc::desc_kmajor(tc::su32(base + TILE), ks), kIdKm, ks > 0);
+      }
+      tc::commit(&bar_s);
+    };
+    for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
+    if (lane == 0) {
+      tc::mbar_expect_tx(&bar_k, 2 * TILE);
+      tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, b, &bar_k);
+      tc::tma_load_4d(Vs, &tmV, 0, h, j * 64, b, &bar_k);
+      ok = tc::mbar_wait(&bar_k, 0) && ok;
+      ok = tc::mbar_wait(&bar_c[0], 0) && ok;
+      issue_s(0);
+      ok = tc::mbar_wait(&bar_s, 0) && ok;
+    }
+    __syncwarp();
+    tc::named_arrive(kBarSReady, NT);
+    tc::named_arrive(kBarOpFree, NT);
+    for (int ci = 0; ci < ncons; ++ci) {
+      tc::named_sync(kBarSFree, NT);
+      if (lane == 0 && ci + 1 < ncons) {
+        tc::fence_after();
+        ok = tc::mbar_wait(&bar_c[(ci + 1) % NST], ((ci + 1) / NST) & 1) && ok;
+        issue_s(ci + 1);
+      }
+      __syncwarp();
+      tc::named_sync(kBarOpReady, NT);  // w P^T and dS^T are in shared memory
+      if (lane == 0) {
+        tc::fence_after();
+        unsigned char* base = ring + (ci % NST) * kKVStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
+          tc::mma(tdV, tc::desc_kmajor(tc::su32(PTs), kk), tc::desc_mnmajor(tc::su32(base + TILE), kk), kIdMn, acc);
+          tc::mma(tdK, tc::desc_kmajor(tc::su32(dSTs), kk), tc::desc_mnmajor(tc::su32(base), kk), kIdMn, acc);
+        }
+        tc::commit(&bar_o);
+        if (ci + 1 < ncons) ok = tc::mbar_wait(&bar_s, (ci + 1) & 1) && ok;
+      }
+      __syncwarp();
+      if (ci + 1 < ncons) tc::named_arrive(kBarSReady, NT);
+      if (lane == 0) {
+        ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // operands and stage ci % NST are free
+        if (!ok) flag_timeout(a.err);
+      }
+      __syncwarp();
+      if (ci + NST < ncons) load_cons(ci + NST);
+      if (ci + 1 < ncons) tc::named_arrive(kBarOpFree, NT);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise warps
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const int row0 = 16 * quarter + g;  // key rows row0, row0 + 8
+    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    const float scale = 1.0f / sqrtf((float)DH);
+    const float sl2 = scale * kLog2e;
+    uint32_t off0[4], off1[4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      off0[n] = swz<ROWB>(row0, 4 * hc + n) + cq * 4;
+      off1[n] = swz<ROWB>(row0 + 8, 4 * hc + n) + cq * 4;
+    }
+    for (int ci = 0; ci < ncons; ++ci) {
+      tc::named_sync(kBarSReady, NT);
+      tc::fence_after();
+      const int st = ci % NST;
+      // The rows came in by bulk copy: observe their mbarrier phase (already complete).
+      tc::mbar_wait(&bar_c[st], (ci / NST) & 1);
+      const float* lrow = reinterpret_cast<const float*>(ring + st * kKVStageBytes + 2 * TILE) + 32 * hc;
+      const float* drow = lrow + 64;
+      const float w = w_st[st];
+      float s[4][4], dp[4][4];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
+      tc::ld_wait(s);
+      tc::ld_wait(dp);
+      tc::fence_before();
+      tc::named_arrive(kBarSFree, NT);
+      const float cs = w * scale;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {  // columns are queries 32hc + 8n + 2cq (+1)
+        const float2 l2 = *reinterpret_cast<const float2*>(lrow + 8 * n + 2 * cq);
+        const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
+        const float la = l2.x * kLog2e, lb = l2.y * kLog2e;
+        const float p0 = tc::ex2(fmaf(s[n][0], sl2, -la)), p1 = tc::ex2(fmaf(s[n][1], sl2, -lb));
+        const float p2 = tc::ex2(fmaf(s[n][2], sl2, -la)), p3 = tc::ex2(fmaf(s[n][3], sl2, -lb));
+        dp[n][0] = p0 * (dp[n][0] - d2.x) * cs;
+        dp[n][1] = p1 * (dp[n][1] - d2.y) * cs;
+        dp[n][2] = p2 * (dp[n][2] - d2.x) * cs;
+        dp[n][3] = p3 * (dp[n][3] - d2.y) * cs;
+        s[n][0] = p0 * w;
+        s[n][1] = p1 * w;
+        s[n][2] = p2 * w;
+        s[n][3] = p3 * w;
+      }
+      tc::named_sync(kBarOpFree, NT);  // the previous consumer's dV, dK products are done
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        *reinterpret_cast<uint32_t*>(PTs + off0[n]) = pack_bf16(s[n][0], s[n][1]);
+        *reinterpret_cast<uint32_t*>(PTs + off1[n]) = pack_bf16(s[n][2], s[n][3]);
+        *reinterpret_cast<uint32_t*>(dSTs + off0[n]) = pack_bf16(dp[n][0], dp[n][1]);
+        *reinterpret_cast<uint32_t*>(dSTs + off1[n]) = pack_bf16(dp[n][2], dp[n][3]);
+      }
+      tc::fence_async_smem();
+      tc::named_arrive(kBarOpReady, NT);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  // Epilogue: dK from TMEM columns 192-255 into the K tile, dV (128-191) into the V tile
+  // (fp32 values staged as bf16 in the same swizzled layout), then 16-byte rows.
+  if (warp < kEW) {
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    float o[4][4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      unsigned char* dst = half ? Vs : Ks;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256((half ? tdV : tdK) + lane_base + cb * 8, o[cb]);
+      tc::ld_wait(o);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int r0 = 16 * quarter + g;
+        *reinterpret_cast<uint32_t*>(dst + swz<ROWB>(r0, 4 * hc + n) + cq * 4) = pack_bf16(o[n][0], o[n][1]);
+        *reinterpret_cast<uint32_t*>(dst + swz<ROWB>(r0 + 8, 4 * hc + n) + cq * 4) = pack_bf16(o[n][2], o[n][3]);
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem_slot, 256);
+  }
+  for (int u = tid; u < 64 * UPR; u += NT) {
+    const int row = u / UPR, w = u % UPR;
+    uint4 vk = *reinterpret_cast<const uint4*>(Ks + swz<ROWB>(row, w));
+    uint4 vv = *reinterpret_cast<const uint4*>(Vs + swz<ROWB>(row, w));
+    if (a.acc_dkv) {
+      const uint4 ok = *reinterpret_cast<const uint4*>(dkg + row * ts + w * 8);
+      const uint4 ov = *reinterpret_cast<const uint4*>(dvg + row * ts + w * 8);
+      float fk[8], fv[8], nk[8], nv[8];
+      unpack16(ok, fk, (const bf16*)nullptr);
+      unpack16(ov, fv, (const bf16*)nullptr);
+      unpack16(vk, nk, (const bf16*)nullptr);
+      unpack16(vv, nv, (const bf16*)nullptr);
+      vk.x = pack_bf16(nk[0] + fk[0], nk[1] + fk[1]); vk.y = pack_bf16(nk[2] + fk[2], nk[3] + fk[3]);
+      vk.z = pack_bf16(nk[4] + fk[4], nk[5] + fk[5]); vk.w = pack_bf16(nk[6] + fk[6], nk[7] + fk[7]);
+      vv.x = pack_bf16(nv[0] + fv[0], nv[1] + fv[1]); vv.y = pack_bf16(nv[2] + fv[2], nv[3] + fv[3]);
+      vv.z = pack_bf16(nv[4] + fv[4], nv[5] + fv[5]); vv.w = pack_bf16(nv[6] + fv[6], nv[7] + fv[7]);
+    }
+    *reinterpret_cast<uint4*>(dkg + row * ts + w * 8) = vk;
+    *reinterpret_cast<uint4*>(dvg + row * ts + w * 8) = vv;
+  }
+}
+
+}  // namespace
+
+// Launch the tensor-core query-side and key-side kernels (bf16, dh = 64).
+cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t s) {
+  CUtensorMap tq, tdo, tk, tv;
+  const int64_t qb = (int64_t)a.nQ * 64 * a.H * 64, kb = (int64_t)a.nC * 64 * a.H * 64;
+  cudaError_t e = make_head_tmap(&tq, a.q, 64, a.H, (int64_t)a.nQ * 64, a.B, qb);
+  if (e == cudaSuccess) e = make_head_tmap(&tdo, a.dout, 64, a.H, (int64_t)a.nQ * 64, a.B, qb);
+  if (e == cudaSuccess) e = make_head_tmap(&tk, a.k, 64, a.H, (int64_t)a.nC * 64, a.B, kb);
+  if (e == cudaSuccess) e = make_head_tmap(&tv, a.v, 64, a.H, (int64_t)a.nC * 64, a.B, kb);
+  if (e == cudaSuccess) e = allow_smem((const void*)gca_bwd_q_tc_kernel, kQSmem);
+  if (e != cudaSuccess) return e;
+  launch_begin("gca_bwd_q", s);
+  gca_bwd_q_tc_kernel<<<dim3(a.nQ, a.H, a.B), kThreads, kQSmem, s>>>(a, tq, tdo, tk, tv);
+  return launch_end("gca_bwd_q", s);
+}
+
+cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t s) {
+  CUtensorMap tq, tdo, tk, tv;
+  const int64_t qb = (int64_t)a.nQ * 64 * a.H * 64, kb = (int64_t)a.nC * 64 * a.H * 64;
+  cudaError_t e = make_head_tmap(&tq, a.q, 64, a.H, (int64_t)a.nQ * 64, a.B, qb);
+  if (e == cudaSuccess) e = make_head_tmap(&tdo, a.dout, 64, a.H, (int64_t)a.nQ * 64, a.B, qb);
+  if (e == cudaSuccess) e = make_head_tmap(&tk, a.k, 64, a.H, (int64_t)a.nC * 64, a.B, kb);
+  if (e == cudaSuccess) e = make_head_tmap(&tv, a.v, 64, a.H, (int64_t)a.nC * 64, a.B, kb);
+  if (e == cudaSuccess) e = allow_smem((const void*)gca_bwd_kv_tc_kernel, kKVSmem);
+  if (e != cudaSuccess) return e;
+  launch_begin("gca_bwd_kv", s);
+  gca_bwd_kv_tc_kernel<<<dim3(a.nC, a.H, a.B), kThreads, kKVSmem, s>>>(a, tq, tdo, tk, tv);
+  return launch_end("gca_bwd_kv", s);
+}
+
+}  // namespace gca

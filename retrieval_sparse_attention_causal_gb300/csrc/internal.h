@@ -72,6 +72,9 @@ struct BwdArgs {
   int32_t* csr_cur; // [B][nC]
 };
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s);
+// Tensor-core (tcgen05) query-side and key-side passes, bf16 with dh = 64 (gca_bwd_tc.cu).
+cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t s);
 
 // ---- CSR of consumers per key chunk (gca_bwd.cu), also used by the score backward.
 // Rows r in [0, nrows) of idx [B][ld_rows][topk] are entries e = r*topk + m.

@@ -7,10 +7,12 @@
 // product <q_i, k_j> / sqrt(D).
 //
 // Two stage-1 kernels feed one merge kernel:
-//   retrieve_rows_kernel  few query rows, very many candidates (decode at 16M context):
+//   retrieve_stream_kernel few query rows, very many candidates (decode at 16M context):
 //                         each CTA streams a contiguous slice of one row's candidate
-//                         landmarks with 16-byte loads straight from HBM, one warp per
-//                         candidate row group; an HBM-bound dot-product sweep.
+//                         landmarks through a 4-stage shared-memory ring filled by 1-D
+//                         bulk copies (TMA) from a producer warp; eight consumer warps
+//                         take the dot products out of shared memory.  One CTA per SM,
+//                         one wave; an HBM-bound sweep.
 //   retrieve_tile_kernel  many query rows (training, prefill): 64 query rows stay in
 //                         shared memory while 64-candidate tiles stream through a
 //                         double-buffered cp.async pipeline; the 64x64 score tile is a
@@ -22,14 +24,13 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace gca {
 
 namespace {
 
-constexpr int kRowsThreads = 256;
 constexpr int kTileThreads = 256;
-constexpr int kTargetCtas = 152 * 4;  // four resident CTAs on each of GB300's 152 SMs
 
 __device__ __forceinline__ int n_cand_row(int i, int off, int nC) {
   long long n = (long long)i + off;
@@ -55,85 +56,127 @@ __device__ __forceinline__ void write_part(const RetrieveArgs& a, int nsplit, in
   for (int r = 0; r < a.topk; ++r) p[r] = sel[r];
 }
 
-// ------------------------------------------------------------------ rows kernel
-template <typename T, int NVMAX, int KC>
-__global__ void __launch_bounds__(kRowsThreads)
-retrieve_rows_kernel(RetrieveArgs a, int nsplit, int seg) {
-  constexpr int EPV = 16 / sizeof(T);
-  __shared__ Cand red[kRowsThreads / 32];
+// ------------------------------------------------------------------ stream kernel
+constexpr int kStreamStages = 4;
+constexpr int kStreamConsumers = 8;
+constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
+constexpr int kStreamStageBytes = 48 * 1024;
+
+// Candidate rows per stage: a multiple of 8 (one row per consumer warp per step), at
+// most 32, within one 48 KB stage.
+__host__ __device__ inline int stream_rows(int D, int elem) {
+  int r = kStreamStageBytes / (D * elem);
+  r = r > 32 ? 32 : r;
+  return r / 8 * 8;
+}
+
+template <typename T, int NV, int KC>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+retrieve_stream_kernel(RetrieveArgs a, int nsplit, int seg) {
+  constexpr int EPV = 16 / sizeof(T), NST = kStreamStages, NCW = kStreamConsumers;
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ Cand red[kStreamThreads / 32];
   __shared__ Cand sel[kMaxTopk];
+  __shared__ __align__(8) uint64_t full[NST], empty[NST];
   const int split = blockIdx.x, i = blockIdx.y, b = blockIdx.z;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = kRowsThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_i = n_cand_row(i, a.off, a.nC);
   const int j0 = split * seg;
   const int j1 = min(n_i, j0 + seg);
-  const T* q = reinterpret_cast<const T*>(a.q) + (int64_t)b * a.q_bs + (int64_t)i * a.q_rs;
+  const int rows = stream_rows(a.D, sizeof(T));
+  const int nchunks = j1 > j0 ? (j1 - j0 + rows - 1) / rows : 0;
+  const size_t row_bytes = (size_t)a.D * sizeof(T);
   const T* kb = reinterpret_cast<const T*>(a.k) + (int64_t)b * a.k_bs;
-  const int nvec = a.D / EPV;
-  const float inv = 1.0f / sqrtf((float)a.D);
-
-  float qf[NVMAX][EPV];
-#pragma unroll
-  for (int t = 0; t < NVMAX; ++t) {
-    const int vi = lane + 32 * t;
-    if (vi < nvec) {
-      const uint4 u = *reinterpret_cast<const uint4*>(q + vi * EPV);
-      unpack16(u, qf[t], (const T*)nullptr);
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) qf[t][e] = 0.f;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) {
+      tc::mbar_init(&full[st], 1);
+      tc::mbar_init(&empty[st], NCW);
     }
+    tc::fence_mbar_init();
   }
-
+  __syncthreads();
   Cand L[KC];
   list_init(L);
-  constexpr int R = 4;  // candidate rows in flight per warp
-  for (int jb = j0 + warp * R; jb < j1; jb += nwarp * R) {
-    uint4 raw[R][NVMAX];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int j = jb + r;
-#pragma unroll
-      for (int t = 0; t < NVMAX; ++t) {
-        const int vi = lane + 32 * t;
-        if (j < j1 && vi < nvec)
-          raw[r][t] = ldg_stream(kb + (int64_t)j * a.D + vi * EPV);
-        else
-          raw[r][t] = make_uint4(0, 0, 0, 0);
+  bool ok = true;
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer warp
+    if (lane == 0) {
+      for (int c = 0; c < nchunks; ++c) {
+        const int st = c % NST;
+        if (c >= NST) ok = tc::mbar_wait(&empty[st], (c / NST - 1) & 1) && ok;
+        const int r0 = j0 + c * rows;
+        const int nr = min(rows, j1 - r0);
+        const uint32_t bytes = (uint32_t)(nr * row_bytes);
+        tc::mbar_expect_tx(&full[st], bytes);
+        tc::bulk_load(ring + (size_t)st * kStreamStageBytes, kb + (int64_t)r0 * a.D, bytes, &full[st]);
       }
     }
-    float acc[R];
+  } else {
+    // ------------------------------------------------------------ consumer warps
+    const T* q = reinterpret_cast<const T*>(a.q) + (int64_t)b * a.q_bs + (int64_t)i * a.q_rs;
+    const int nvec = a.D / EPV;
+    const float inv = 1.0f / sqrtf((float)a.D);
+    float qf[NV][EPV];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      float s = 0.f;
+    for (int t = 0; t < NV; ++t) {
+      const int vi = lane + 32 * t;
+      if (vi < nvec) {
+        const uint4 u = *reinterpret_cast<const uint4*>(q + vi * EPV);
+        unpack16(u, qf[t], (const T*)nullptr);
+      } else {
 #pragma unroll
-      for (int t = 0; t < NVMAX; ++t) {
-        float f[EPV];
-        unpack16(raw[r][t], f, (const T*)nullptr);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) s = fmaf(qf[t][e], f[e], s);
+        for (int e = 0; e < EPV; ++e) qf[t][e] = 0.f;
       }
-      acc[r] = s;
     }
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % NST;
+      ok = tc::mbar_wait(&full[st], (c / NST) & 1) && ok;
+      const int r0 = j0 + c * rows;
+      const int nr = min(rows, j1 - r0);
+      const unsigned char* stage = ring + (size_t)st * kStreamStageBytes;
+      float acc[4];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+      for (int t = 0; t < 4; ++t) {  // this warp's rows: warp, warp + 8, ...
+        const int rr = warp + NCW * t;
+        float sum = 0.f;
+        if (rr < nr) {
+          const T* row = reinterpret_cast<const T*>(stage + (size_t)rr * row_bytes);
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], m);
-    }
-    if (lane < R) {
-      const int j = jb + lane;
-      float mine = acc[0];
+          for (int v = 0; v < NV; ++v) {
+            const int vi = lane + 32 * v;
+            if (vi < nvec) {
+              float f[EPV];
+              unpack16(*reinterpret_cast<const uint4*>(row + vi * EPV), f, (const T*)nullptr);
 #pragma unroll
-      for (int r = 1; r < R; ++r) mine = (lane == r) ? acc[r] : mine;
-      if (j < j1) {
-        Cand c;
-        c.score = mine * inv;
-        c.key = a.gumbel ? c.score + gumbel_noise(a.seed, a.group, b, i, j) : c.score;
-        c.j = j;
-        list_insert(L, c);
+              for (int e = 0; e < EPV; ++e) sum = fmaf(qf[v][e], f[e], sum);
+            }
+          }
+        }
+        acc[t] = sum;
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], m);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[st]);
+      if (lane < 4) {
+        const int rr = warp + NCW * lane;
+        float mine = acc[0];
+#pragma unroll
+        for (int t = 1; t < 4; ++t) mine = (lane == t) ? acc[t] : mine;
+        if (rr < nr) {
+          const int j = r0 + rr;
+          Cand cnd;
+          cnd.score = mine * inv;
+          cnd.key = a.gumbel ? cnd.score + gumbel_noise(a.seed, a.group, b, i, j) : cnd.score;
+          cnd.j = j;
+          list_insert(L, cnd);
+        }
       }
     }
   }
+  if (!ok) flag_timeout(a.err);
   block_select(L, a.topk, sel, red);
   if (threadIdx.x == 0) {
     if (nsplit == 1) write_row(a, b, i, sel);
@@ -379,19 +422,18 @@ RetrievePlan retrieve_plan(int B, int nQ, int nC, int topk, int off) {
   if (ncand_max > nC) ncand_max = nC;
   if (ncand_max < 0) ncand_max = 0;
   if (nQ <= 8) {
+    // Streaming kernel, one CTA per SM: at launch the candidates of each row are split
+    // so that all CTAs form one wave.  The workspace holds the largest split count the
+    // launch can choose (sized for up to 1216 SMs' worth of CTAs, at least 256
+    // candidates per split).
     p.rowwise = 1;
     long long rows = (long long)B * nQ;
-    long long ns = (kTargetCtas + rows - 1) / rows;
-    long long ns_max = (ncand_max + 255) / 256;  // at least 256 candidates per split
+    long long ns = (1216 + rows - 1) / rows;
+    long long ns_max = (ncand_max + 255) / 256;
     if (ns > ns_max) ns = ns_max;
     if (ns < 1) ns = 1;
-    long long seg = (ncand_max + ns - 1) / ns;
-    seg = (seg + 31) / 32 * 32;
-    if (seg < 32) seg = 32;
-    ns = (ncand_max + seg - 1) / seg;
-    if (ns < 1) ns = 1;
     p.nsplit = (int)ns;
-    p.seg = (int)seg;
+    p.seg = 0;
   } else {
     p.rowwise = 0;
     // Spread the (triangular) candidate work over about 8 CTAs per SM.
@@ -420,23 +462,41 @@ RetrievePlan retrieve_plan(int B, int nQ, int nC, int topk, int off) {
 
 cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
+  int nsplit = p.nsplit;
   if (p.rowwise) {
-    dim3 grid(p.nsplit, a.nQ, a.B);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long rows = (long long)a.B * a.nQ;
+    long long ns = sms / rows;
+    if (ns < 1) ns = 1;
+    if (ns > p.nsplit) ns = p.nsplit;
+    long long ncand_max = (long long)(a.nQ - 1) + a.off;
+    if (ncand_max > a.nC) ncand_max = a.nC;
+    if (ncand_max < 1) ncand_max = 1;
+    const int seg = (int)((ncand_max + ns - 1) / ns);
+    nsplit = (int)ns;
+    dim3 grid(nsplit, a.nQ, a.B);
+    const int elem = a.bf16 ? 2 : 4;
+    const int smem = kStreamStages * kStreamStageBytes;
     e = with_kc(a.topk, [&](auto kc) -> cudaError_t {
       constexpr int KC = decltype(kc)::value;
-      const int epv = a.bf16 ? 8 : 4;
-      const int nv = (a.D / epv + 31) / 32;  // 16-byte vectors per lane per row (1..4)
-      launch_begin("retrieve_rows", s);
-      auto go = [&](auto nvc) {
+      const int nv = (a.D / (16 / elem) + 31) / 32;  // 16-byte vectors per lane per row (1..4)
+      auto go = [&](auto nvc) -> cudaError_t {
         constexpr int NV = decltype(nvc)::value;
-        if (a.bf16) retrieve_rows_kernel<__nv_bfloat16, NV, KC><<<grid, kRowsThreads, 0, s>>>(a, p.nsplit, p.seg);
-        else retrieve_rows_kernel<float, NV, KC><<<grid, kRowsThreads, 0, s>>>(a, p.nsplit, p.seg);
+        const void* fn = a.bf16 ? (const void*)retrieve_stream_kernel<__nv_bfloat16, NV, KC>
+                                : (const void*)retrieve_stream_kernel<float, NV, KC>;
+        cudaError_t e2 = allow_smem(fn, smem);
+        if (e2 != cudaSuccess) return e2;
+        launch_begin("retrieve_stream", s);
+        if (a.bf16) retrieve_stream_kernel<__nv_bfloat16, NV, KC><<<grid, kStreamThreads, smem, s>>>(a, nsplit, seg);
+        else retrieve_stream_kernel<float, NV, KC><<<grid, kStreamThreads, smem, s>>>(a, nsplit, seg);
+        return launch_end("retrieve_stream", s);
       };
-      if (nv <= 1) go(std::integral_constant<int, 1>{});
-      else if (nv == 2) go(std::integral_constant<int, 2>{});
-      else if (nv == 3) go(std::integral_constant<int, 3>{});
-      else go(std::integral_constant<int, 4>{});
-      return launch_end("retrieve_rows", s);
+      if (nv <= 1) return go(std::integral_constant<int, 1>{});
+      if (nv == 2) return go(std::integral_constant<int, 2>{});
+      if (nv == 3) return go(std::integral_constant<int, 3>{});
+      return go(std::integral_constant<int, 4>{});
     });
   } else {
     dim3 grid(p.nsplit, (a.nQ + 63) / 64, a.B);
@@ -453,12 +513,12 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
       return launch_end("retrieve_tile", s);
     });
   }
-  if (e != cudaSuccess || p.nsplit == 1) return e;
+  if (e != cudaSuccess || nsplit == 1) return e;
   dim3 mg(a.nQ, a.B);
   return with_kc(a.topk, [&](auto kc) -> cudaError_t {
     constexpr int KC = decltype(kc)::value;
     launch_begin("retrieve_merge", s);
-    retrieve_merge_kernel<KC><<<mg, 128, 0, s>>>(a, p.nsplit);
+    retrieve_merge_kernel<KC><<<mg, 128, 0, s>>>(a, nsplit);
     return launch_end("retrieve_merge", s);
   });
 }

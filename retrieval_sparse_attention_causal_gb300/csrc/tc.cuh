@@ -60,16 +60,18 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;"); }
 
-// Bounded wait for phase `parity` of `bar`.  Returns false if the limit ran out (the
-// caller records the timeout and carries on, so that nothing hangs).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = 1u << 26) {
+// Bounded wait for phase `parity` of `bar`.  Each try_wait may suspend the thread in
+// hardware (hint: 1 us) until the phase completes, so a waiting thread does not keep
+// re-issuing shared-memory requests.  Returns false if the limit ran out (the caller
+// records the timeout and carries on, so that nothing hangs).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = 1u << 21) {
   uint32_t done = 0;
   for (uint32_t it = 0; it < limit; ++it) {
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(su32(bar)), "r"(parity));
+        : "r"(su32(bar)), "r"(parity), "r"(1000u));
     if (done) return true;
   }
   return false;
@@ -147,6 +149,44 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+}  // namespace tc
+}  // namespace gca
+
+namespace gca {
+namespace tc {
+
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16), completing
+// `bytes` on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   su32(dst)),
+               "l"(src), "r"(bytes), "r"(su32(bar))
+               : "memory");
+}
+
+}  // namespace tc
+}  // namespace gca
+
+namespace gca {
+namespace tc {
+
+// Wait for outstanding tcgen05.ld, tied to 16 loaded registers.
+__device__ __forceinline__ void ld_wait(float (&v)[4][4]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0][0]),"+f"(v[0][1]),"+f"(v[0][2]),"+f"(v[0][3]),"+f"(v[1][0]),"+f"(v[1][1]),"+f"(v[1][2]),"+f"(v[1][3]),"+f"(v[2][0]),"+f"(v[2][1]),"+f"(v[2][2]),"+f"(v[2][3]),"+f"(v[3][0]),"+f"(v[3][1]),"+f"(v[3][2]),"+f"(v[3][3]));
+}
+
+}  // namespace tc
+}  // namespace gca
+
+namespace gca {
+namespace tc {
+
+// Plain arrival (count 1) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
 }
 
 }  // namespace tc
