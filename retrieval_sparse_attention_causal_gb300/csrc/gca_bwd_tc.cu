@@ -29,7 +29,7 @@ constexpr int kEW = 8;
 constexpr int kThreads = 32 * (kEW + 1);
 constexpr int kCtl = kEW;  // control warp index
 constexpr int TILE = 8192, ROWB = 128, UPR = 8, DH = 64;
-enum { kBarSReady = 1, kBarSFree = 2, kBarOpFree = 3, kBarOpReady = 4, kBarEW = 5 };
+enum { kBarSFree = 2, kBarOpFree = 3, kBarOpReady = 4, kBarEW = 5 };
 
 // ================================================================== query side
 constexpr int kQStages = 5;
@@ -134,39 +134,36 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       ok = tc::mbar_wait(&bar_q, 0) && ok;
       ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
       issue_s(0);
-      ok = tc::mbar_wait(&bar_s, 0) && ok;
     }
     __syncwarp();
-    tc::named_arrive(kBarSReady, NT);
     tc::named_arrive(kBarOpFree, NT);
     for (int si = 0; si < ns; ++si) {
-      tc::named_sync(kBarSFree, NT);  // S(si), dPo(si) have been read
+      // S(si), dPo(si) have been loaded (tcgen05.wait::ld done before the arrival); no
+      // tcgen05 fence, which after a thread barrier would wait for every MMA in flight.
+      tc::named_sync(kBarSFree, NT);
       if (lane == 0 && si + 1 < ns) {
-        tc::fence_after();
         ok = tc::mbar_wait(&bar_kv[(si + 1) % NST], ((si + 1) / NST) & 1) && ok;
         issue_s(si + 1);
       }
       __syncwarp();
-      tc::named_sync(kBarOpReady, NT);  // dS(si) is in shared memory
+      tc::named_sync(kBarOpReady, NT);  // dS(si) is in shared memory (proxy-fenced)
       if (lane == 0) {
-        tc::fence_after();
         unsigned char* Ks = ring + 2 * (si % NST) * TILE;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
           tc::mma(tQ, tc::desc_kmajor(tc::su32(dSs), kk), tc::desc_mnmajor(tc::su32(Ks), kk), kIdMn,
                   (si > 0 || kk > 0) ? 1u : 0u);
         tc::commit(&bar_o);
-        if (si + 1 < ns) ok = tc::mbar_wait(&bar_s, (si + 1) & 1) && ok;
       }
       __syncwarp();
-      if (si + 1 < ns) tc::named_arrive(kBarSReady, NT);
+      if (lane == 0) ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // dS buffer and stage si % NST are free
+      __syncwarp();
+      if (si + 1 < ns) tc::named_arrive(kBarOpFree, NT);
       if (lane == 0) {
-        ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // dS buffer and stage si % NST are free
         if (si + NST < ns) load_slot(si + NST);
         if (!ok) flag_timeout(a.err);
       }
       __syncwarp();
-      if (si + 1 < ns) tc::named_arrive(kBarOpFree, NT);
     }
   } else {
     // ------------------------------------------------------------ element-wise warps
@@ -184,8 +181,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     for (int si = 0; si < ns; ++si) {
       const int m = slot_s[si];
       const float lse0 = lse[m * 64 + row0] * kLog2e, lse1 = lse[m * 64 + row0 + 8] * kLog2e;
-      tc::named_sync(kBarSReady, NT);
-      tc::fence_after();
+      if (!tc::mbar_wait(&bar_s, si & 1)) flag_timeout(a.err);  // acquire S(si), dPo(si)
       float s[4][4], dp[4][4];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
@@ -276,6 +272,29 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
 constexpr int kKVStages = 4;
 constexpr int kKVStageBytes = 2 * TILE + 1024;  // Q, dO tiles + LSE and D rows (1 KB keeps tiles aligned)
 constexpr int kKVSmem = TILE * 4 + kKVStages * kKVStageBytes + 1024;  // K, V, wP^T, dS^T, ring
+constexpr int kConsTab = 256;
+
+// Fusion weight w_m of slot m of retrieval row r (softmax over the row's valid slots),
+// computed by one thread.
+__device__ __forceinline__ float slot_weight_thread(const BwdArgs& a, int b, int r, int m) {
+  const int32_t* idx_row = a.idx + ((int64_t)b * a.nQ + r) * a.topk;
+  const float* sc_row = a.scores + ((int64_t)b * a.nQ + r) * a.topk;
+  float mx = -CUDART_INF_F;
+  for (int t = 0; t < a.topk; ++t) {
+    const int jj = idx_row[t];
+    if (jj >= 0 && jj < a.nC) mx = fmaxf(mx, sc_row[t]);
+  }
+  float sum = 0.f, mine = 0.f;
+  for (int t = 0; t < a.topk; ++t) {
+    const int jj = idx_row[t];
+    if (jj >= 0 && jj < a.nC) {
+      const float e = expf(sc_row[t] - mx);
+      sum += e;
+      if (t == m) mine = e;
+    }
+  }
+  return sum > 0.f ? mine / sum : 0.f;
+}
 
 __global__ void __launch_bounds__(kThreads, 2)
 gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -291,6 +310,8 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
   unsigned char* dSTs = sm + 3 * TILE;  // dS^T
   unsigned char* ring = sm + 4 * TILE;  // stage st at ring + st * kKVStageBytes: Q, dO, lse[64], D[64]
   __shared__ float w_st[NST];
+  __shared__ float wtab[kConsTab];  // weight of each consumer (first kConsTab consumers)
+  __shared__ int etab[kConsTab];    // its (row, slot) entry
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t bar_k, bar_c[NST], bar_s, bar_o;
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -329,41 +350,27 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
   if (warp == kCtl) {
     // ------------------------------------------------------------ control warp
     bool ok = true;
-    auto load_cons = [&](int x) {  // consumer x: Q, dO tiles, LSE and D rows, weight
-      const int st = x % NST;
+    // Consumer table: entry and fusion weight of every consumer (the first kConsTab in
+    // shared memory, computed here once; later ones on demand).
+    for (int x = lane; x < ncons && x < kConsTab; x += 32) {
       const int e = ent[e0 + x];
+      etab[x] = e;
+      wtab[x] = slot_weight_thread(a, b, e / a.topk, e % a.topk);
+    }
+    __syncwarp();
+    auto load_cons = [&](int x) {  // lane 0: consumer x's Q, dO tiles, LSE and D rows
+      const int st = x % NST;
+      const int e = x < kConsTab ? etab[x] : ent[e0 + x];
       const int r = e / a.topk, m = e % a.topk;
       const int c = r + a.shift;
-      // Every lane takes part in the weight (a warp reduction); lane 0 issues the copies.
-      const float wv = [&]() {
-        const int32_t* idx_row = a.idx + ((int64_t)b * a.nQ + r) * a.topk;
-        const float* sc_row = a.scores + ((int64_t)b * a.nQ + r) * a.topk;
-        int jj = -1;
-        float sv = -CUDART_INF_F;
-        if (lane < a.topk) {
-          jj = idx_row[lane];
-          if (jj < -1 || jj >= a.nC) jj = -1;
-          if (jj >= 0) sv = sc_row[lane];
-        }
-        float mx = sv;
-#pragma unroll
-        for (int k = 16; k >= 1; k >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
-        const float ev = (jj >= 0) ? expf(sv - mx) : 0.f;
-        float sum = ev;
-#pragma unroll
-        for (int k = 16; k >= 1; k >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, k);
-        return __shfl_sync(0xffffffffu, (jj >= 0) ? ev / sum : 0.f, m);
-      }();
-      if (lane == 0) {
-        w_st[st] = wv;
-        unsigned char* base = ring + st * kKVStageBytes;
-        const int64_t rb = ((((int64_t)b * a.nQ + c) * a.H + h) * a.topk + m) * 64;
-        tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
-        tc::tma_load_4d(base, &tmQ, 0, h, c * 64, b, &bar_c[st]);
-        tc::tma_load_4d(base + TILE, &tmdO, 0, h, c * 64, b, &bar_c[st]);
-        tc::bulk_load(base + 2 * TILE, a.lse + rb, 256, &bar_c[st]);
-        tc::bulk_load(base + 2 * TILE + 256, a.Dbuf + rb, 256, &bar_c[st]);
-      }
+      w_st[st] = x < kConsTab ? wtab[x] : slot_weight_thread(a, b, r, m);
+      unsigned char* base = ring + st * kKVStageBytes;
+      const int64_t rb = ((((int64_t)b * a.nQ + c) * a.H + h) * a.topk + m) * 64;
+      tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
+      tc::tma_load_4d(base, &tmQ, 0, h, c * 64, b, &bar_c[st]);
+      tc::tma_load_4d(base + TILE, &tmdO, 0, h, c * 64, b, &bar_c[st]);
+      tc::bulk_load(base + 2 * TILE, a.lse + rb, 256, &bar_c[st]);
+      tc::bulk_load(base + 2 * TILE + 256, a.Dbuf + rb, 256, &bar_c[st]);
     };
     auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x
       unsigned char* base = ring + (x % NST) * kKVStageBytes;
@@ -374,30 +381,27 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       }
       tc::commit(&bar_s);
     };
-    for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
     if (lane == 0) {
+      for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
       tc::mbar_expect_tx(&bar_k, 2 * TILE);
       tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, b, &bar_k);
       tc::tma_load_4d(Vs, &tmV, 0, h, j * 64, b, &bar_k);
       ok = tc::mbar_wait(&bar_k, 0) && ok;
       ok = tc::mbar_wait(&bar_c[0], 0) && ok;
       issue_s(0);
-      ok = tc::mbar_wait(&bar_s, 0) && ok;
     }
     __syncwarp();
-    tc::named_arrive(kBarSReady, NT);
     tc::named_arrive(kBarOpFree, NT);
     for (int ci = 0; ci < ncons; ++ci) {
+      // S^T(ci), dPo^T(ci) have been loaded; no tcgen05 fence (see the query side).
       tc::named_sync(kBarSFree, NT);
       if (lane == 0 && ci + 1 < ncons) {
-        tc::fence_after();
         ok = tc::mbar_wait(&bar_c[(ci + 1) % NST], ((ci + 1) / NST) & 1) && ok;
         issue_s(ci + 1);
       }
       __syncwarp();
-      tc::named_sync(kBarOpReady, NT);  // w P^T and dS^T are in shared memory
+      tc::named_sync(kBarOpReady, NT);  // w P^T and dS^T are in shared memory (proxy-fenced)
       if (lane == 0) {
-        tc::fence_after();
         unsigned char* base = ring + (ci % NST) * kKVStageBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -406,17 +410,16 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
           tc::mma(tdK, tc::desc_kmajor(tc::su32(dSTs), kk), tc::desc_mnmajor(tc::su32(base), kk), kIdMn, acc);
         }
         tc::commit(&bar_o);
-        if (ci + 1 < ncons) ok = tc::mbar_wait(&bar_s, (ci + 1) & 1) && ok;
       }
       __syncwarp();
-      if (ci + 1 < ncons) tc::named_arrive(kBarSReady, NT);
+      if (lane == 0) ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // operands and stage ci % NST are free
+      __syncwarp();
+      if (ci + 1 < ncons) tc::named_arrive(kBarOpFree, NT);
       if (lane == 0) {
-        ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // operands and stage ci % NST are free
+        if (ci + NST < ncons) load_cons(ci + NST);
         if (!ok) flag_timeout(a.err);
       }
       __syncwarp();
-      if (ci + NST < ncons) load_cons(ci + NST);
-      if (ci + 1 < ncons) tc::named_arrive(kBarOpFree, NT);
     }
   } else {
     // ------------------------------------------------------------ element-wise warps
@@ -432,8 +435,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       off1[n] = swz<ROWB>(row0 + 8, 4 * hc + n) + cq * 4;
     }
     for (int ci = 0; ci < ncons; ++ci) {
-      tc::named_sync(kBarSReady, NT);
-      tc::fence_after();
+      if (!tc::mbar_wait(&bar_s, ci & 1)) flag_timeout(a.err);  // acquire S^T(ci), dPo^T(ci)
       const int st = ci % NST;
       // The rows came in by bulk copy: observe their mbarrier phase (already complete).
       tc::mbar_wait(&bar_c[st], (ci / NST) & 1);

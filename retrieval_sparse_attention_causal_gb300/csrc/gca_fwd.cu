@@ -206,14 +206,14 @@ __global__ void __launch_bounds__(128) gca_fwd_mma_kernel(FwdArgs a) {
 //   * Warps 0-3 (softmax): read S with tcgen05.ld, do the row softmax in registers and
 //     write P~ = (w_m / l) P as bf16 to shared memory, the A operand of O += P~ V (V is
 //     the MN-major B operand).
-// The two sides hand over through hardware named barriers (nobody spins): S(m+1) is
-// issued as soon as the softmax warps have read S(m), so the tensor core overlaps the
-// softmax.  128 TMEM columns and ~50 KB of shared memory per CTA let four CTAs share
+// The softmax warps take S straight from the MMA-completion mbarrier; the other
+// handovers are hardware named barriers.  S(m+1) is issued as soon as the softmax warps
+// have read S(m), so the tensor core overlaps the softmax.  128 TMEM columns and ~50 KB of shared memory per CTA let four CTAs share
 // an SM.
 constexpr int kFwdStages = 2;
 constexpr int kFwdTcSmem = 8192 * (2 + 2 * kFwdStages) + 1024;  // Q, P, ring of (K, V)
 constexpr int kFwdThreads = 160;
-enum { kBarSReady = 1, kBarSFree = 2, kBarPFree = 3, kBarPReady = 4 };
+enum { kBarSFree = 2, kBarPFree = 3, kBarPReady = 4 };
 
 __global__ void __launch_bounds__(kFwdThreads, 4)
 gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -303,39 +303,37 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       ok = tc::mbar_wait(&bar_q, 0) && ok;
       ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
       issue_s(0);
-      ok = tc::mbar_wait(&bar_s, 0) && ok;
     }
     __syncwarp();
-    tc::named_arrive(kBarSReady, NT);
     tc::named_arrive(kBarPFree, NT);
     for (int si = 0; si < ns; ++si) {
-      tc::named_sync(kBarSFree, NT);  // softmax warps have read S(si)
+      // The softmax warps have loaded S(si) (tcgen05.wait::ld done before they arrived),
+      // so S(si+1) may overwrite it.  No tcgen05 fence here: after a thread barrier it
+      // would wait for every MMA in flight.
+      tc::named_sync(kBarSFree, NT);
       if (lane == 0 && si + 1 < ns) {
-        tc::fence_after();
         ok = tc::mbar_wait(&bar_kv[(si + 1) % NST], ((si + 1) / NST) & 1) && ok;
         issue_s(si + 1);
       }
       __syncwarp();
-      tc::named_sync(kBarPReady, NT);  // P(si) is in shared memory
+      tc::named_sync(kBarPReady, NT);  // P(si) is in shared memory (proxy-fenced)
       if (lane == 0) {
-        tc::fence_after();
         unsigned char* Vs = ring + (2 * (si % NST) + 1) * TILE;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc::mma(tO, tc::desc_kmajor(tc::su32(Ps), kk), tc::desc_mnmajor(tc::su32(Vs), kk), kIdPV,
                   (si > 0 || kk > 0) ? 1u : 0u);
         tc::commit(&bar_o);
-        if (si + 1 < ns) ok = tc::mbar_wait(&bar_s, (si + 1) & 1) && ok;  // S(si+1) ready
       }
       __syncwarp();
-      if (si + 1 < ns) tc::named_arrive(kBarSReady, NT);
+      if (lane == 0) ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // P and ring stage si % NST are free
+      __syncwarp();
+      if (si + 1 < ns) tc::named_arrive(kBarPFree, NT);
       if (lane == 0) {
-        ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // P and ring stage si % NST are free
         if (si + NST < ns) load_slot(si + NST);
         if (!ok) flag_timeout(a.err);
       }
       __syncwarp();
-      if (si + 1 < ns) tc::named_arrive(kBarPFree, NT);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -351,8 +349,9 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       poff1[n] = swz<ROWB>(row0 + 8, n) + cq * 4;
     }
     for (int si = 0; si < ns; ++si) {
-      tc::named_sync(kBarSReady, NT);
-      tc::fence_after();
+      // Acquire S(si) straight from the MMA-completion barrier (S(si+1) is only issued
+      // after every softmax thread has passed this point, so the phase cannot run ahead).
+      if (!tc::mbar_wait(&bar_s, si & 1)) flag_timeout(a.err);
       float s[8][4];
 #pragma unroll
       for (int cb = 0; cb < 8; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
