@@ -122,6 +122,35 @@ def algorithmic_flops(B_, nC, H_, dh, k):
             "step": 14 * u * units, "units": units}
 
 
+# ----------------------------------------------------------------------------- replicas
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Slowest rank's time (the job's time).  Works with any initialised backend: NCCL
+    on the GPU machine, gloo in the CPU tests."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own replica of the workload (weak
+    scaling), so the job does world x units per step in the slowest rank's time."""
+    return units_per_rank * world / (ms_per_step / 1e3)
+
+
+# Measured DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# current kernels on this workload, from the captures summarised under profiles/.
+KNOWN_TRAFFIC = {
+    "gca_bwd_kv": 607.2e6,   # profiles/gca_tc_kernels_128m.md
+    "gca_bwd_q": 512.6e6,
+    "gca_fwd": 383.3e6,
+}
+STREAM_TRAFFIC_PER_SEQ = 808.6e6 / 2  # profiles/retrieve_stream_decode_16m.md (B = 2 capture)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def gpu_arm(args):
     import torch
@@ -175,12 +204,7 @@ def gpu_arm(args):
         e1.record(s)
         torch.cuda.synchronize()
         barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(e0.elapsed_time(e1), world, "cuda")
 
     for i in range(args.warmup):
         step(i)
@@ -191,7 +215,7 @@ def gpu_arm(args):
     launches = gca.launch_count() - n0
     ms_step = ms / args.steps
     tokens = B * L
-    value = tokens * world / (ms_step / 1e3)
+    value = job_throughput(tokens, world, ms_step)
 
     # Per-kernel durations: the same loop again with event brackets around each launch.
     gca.profile_begin()
@@ -207,32 +231,15 @@ def gpu_arm(args):
         avg_s = kern[dom]["avg_ms"] / 1e3
         ach = dom_flops / avg_s / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": KNOWN_TRAFFIC.get(dom),
                 "peak_source": f"{src} bf16 dense (burst)", "flops_per_launch": dom_flops}
     step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
 
     # End to end through the public API from pinned host buffers.
     e2e = None
     if not args.no_e2e:
-        hin = {n: t.cpu().pin_memory() for n, t in dict(q=q, k=k, v=v, do=do, ql=ql, kl=kl).items()}
-        din = {n: torch.empty_like(t) for n, t in dict(q=q, k=k, v=v, do=do, ql=ql, kl=kl).items()}
-        res = ["dq", "dk", "dv", "dql", "dkl", "idx", "sc", "ds"]
-        hout = {n: torch.empty(out[n].shape, dtype=out[n].dtype, pin_memory=True) for n in res}
-
-        def e2e_step(i):
-            for n in hin:
-                din[n].copy_(hin[n], non_blocking=True)
-            step(i, **din)
-            for n in res:
-                hout[n].copy_(out[n], non_blocking=True)
-
-        for i in range(max(1, args.warmup // 2)):
-            e2e_step(i)
-        ms_e = timed(e2e_step, args.steps) / args.steps
-        e2e = {"value": tokens * world / (ms_e / 1e3), "unit": "tokens/s", "ms_per_step": ms_e,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout.values())}
-        del hin, din, hout
+        e2e = e2e_leg(args, torch, gca, step_outputs_template=out, inputs=dict(q=q, k=k, v=v, do=do, ql=ql, kl=kl),
+                      seed=seed, world=world, timed_barrier=barrier, tokens=tokens)
 
     dec = None if args.no_decode else decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world)
 
@@ -255,6 +262,83 @@ def gpu_arm(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def e2e_leg(args, torch, gca, step_outputs_template, inputs, seed, world, timed_barrier, tokens):
+    """The training step end to end through the public API: every step copies its inputs
+    from pinned host memory to the device and its results (gradients, indices, scores)
+    back.  Copies run on their own streams and overlap the previous/next step's compute
+    (inputs and outputs are double-buffered); the timed region covers all of it."""
+    res = ["dq", "dk", "dv", "dql", "dkl", "idx", "sc", "ds"]
+    hin = {n: t.cpu().pin_memory() for n, t in inputs.items()}
+    din = [{n: torch.empty_like(t) for n, t in inputs.items()} for _ in range(2)]
+    dout = [{n: torch.empty_like(t) for n, t in step_outputs_template.items()} for _ in range(2)]
+    hout = [{n: torch.empty(step_outputs_template[n].shape, dtype=step_outputs_template[n].dtype, pin_memory=True)
+             for n in res} for _ in range(2)]
+    cs, h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ws = gca.Workspace()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of buffer set landed
+    ev_comp = [torch.cuda.Event() for _ in range(2)]   # compute on buffer set done
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # results of buffer set copied out
+
+    def copy_in(i):
+        x = i & 1
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(ev_comp[x])  # the compute that last read this set is done
+            for n in hin:
+                din[x][n].copy_(hin[n], non_blocking=True)
+            ev_in[x].record(h2d)
+
+    def compute(i):
+        x = i & 1
+        o, d = dout[x], din[x]
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev_in[x])
+            cs.wait_event(ev_out[x])  # the previous results of this set have been copied out
+            gca.retrieve_topk(d["ql"], d["kl"], K, 0, True, seed + i, 0, ws=ws, idx=o["idx"], scores=o["sc"])
+            gca.gca_forward(d["q"], d["k"], d["v"], o["idx"], o["sc"], shift=1, ws=ws, out=o["o"], lse=o["lse"])
+            gca.gca_backward(d["q"], d["k"], d["v"], o["idx"], o["sc"], d["do"], o["lse"], shift=1, ws=ws,
+                             dq=o["dq"], dk=o["dk"], dv=o["dv"], dscores=o["ds"])
+            gca.scores_backward(d["ql"], d["kl"], o["idx"], o["ds"], ws=ws, dq_out=o["dql"], dk_lmk=o["dkl"])
+            ev_comp[x].record(cs)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_comp[x])
+            for n in res:
+                hout[x][n].copy_(o[n], non_blocking=True)
+            ev_out[x].record(d2h)
+
+    def run(n):
+        copy_in(0)
+        for i in range(n):
+            if i + 1 < n:
+                copy_in(i + 1)
+            compute(i)
+
+    for e in ev_comp + ev_out:
+        e.record(torch.cuda.current_stream())
+    run(max(2, args.warmup // 2))
+    torch.cuda.synchronize()
+    timed_barrier()
+    t0 = time.perf_counter()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(h2d)
+    cs.wait_stream(h2d)
+    d2h.wait_stream(h2d)
+    run(args.steps)
+    d2h.wait_stream(cs)
+    h2d.wait_stream(d2h)
+    end.record(h2d)
+    torch.cuda.synchronize()
+    ms_wall = (time.perf_counter() - t0) * 1e3
+    timed_barrier()
+    ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
+    ms_e = ms / args.steps
+    return {"value": job_throughput(tokens, world, ms_e), "unit": "tokens/s", "ms_per_step": ms_e,
+            "host_wall_ms_per_step": ms_wall / args.steps,
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout[0].values()),
+            "overlap": "inputs of step i+1 and results of step i-1 move while step i computes"}
 
 
 def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
@@ -325,8 +409,29 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
             "ms_per_decode_chunk": round(ms_f, 4), "planted_chunk_found": ok,
             "roofline": {"kernel": "retrieve_stream", "bound": "hbm", "achieved": round(ach, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                         "traffic": None, "peak_source": f"{src} copy bandwidth", "bytes_per_launch": nbytes},
+                         "traffic": round(STREAM_TRAFFIC_PER_SEQ * nb), "peak_source": f"{src} copy bandwidth",
+                         "bytes_per_launch": nbytes},
             "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}}
+
+
+def decode_retrieval_only(args):
+    """Only the decode-time retrieval (no training step, no K/V store), for ncu captures
+    of the landmark stream kernel; prints per-launch timings."""
+    import torch
+    import retrieval_sparse_attention_causal_gb300 as gca
+    from retrieval_sparse_attention_causal_gb300 import synth
+    bf = torch.bfloat16
+    nb = args.decode_batch
+    ql = synth.device_normal(args.seed, synth.S_QL, (nb, 1, D), 1.0, bf)
+    kl = synth.device_normal(args.seed, synth.S_KL, (nb, DEC_NC, D), 1.0, bf)
+    ws = gca.Workspace()
+    idx = torch.empty((nb, 1, K), dtype=torch.int32, device="cuda")
+    sc = torch.empty((nb, 1, K), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        gca.retrieve_topk(ql, kl, K, DEC_NC, False, ws=ws, idx=idx, scores=sc)
+    torch.cuda.synchronize()
+    ws.check()
+    print(json.dumps({"decode_retrieval_only": True, "batch": nb, "launches": args.warmup + args.steps}))
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -409,11 +514,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--decode-retrieval-only", action="store_true",
+                    help="run only the 16M-context landmark retrieval (for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3
     if args.impl == "reference":
         reference_arm(args)
+    elif args.decode_retrieval_only:
+        decode_retrieval_only(args)
     else:
         gpu_arm(args)
 

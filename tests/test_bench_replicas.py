@@ -1,0 +1,54 @@
+"""CPU test of the multi-rank path of bench.py with the gloo backend (world size 2): each
+rank runs its own replica and reports its step time; the job's time is the slowest
+rank's, and the job throughput counts every rank's work (weak scaling)."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms_local = 10.0 + 5.0 * rank  # rank 1 is the slow one
+    ms = bench.max_over_ranks(ms_local, world, "cpu")
+    value = bench.job_throughput(65536, world, ms)
+    q.put((rank, ms, value))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_replicas_take_max_time_and_sum_work():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for rank, ms, value in out:
+        assert ms == pytest.approx(15.0)
+        assert value == pytest.approx(65536 * 2 / 0.015)
+
+
+def test_single_rank_is_local_time():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(12.5, 1) == 12.5
+    assert bench.job_throughput(1000, 1, 2.0) == pytest.approx(500000.0)
