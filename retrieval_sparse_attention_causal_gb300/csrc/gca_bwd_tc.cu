@@ -116,13 +116,16 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, bkv, &bar_kv[st]);
       tc::tma_load_4d(Ks + TILE, &tmV, 0, h, j * 64, bkv, &bar_kv[st]);
     };
+    // Operand descriptors, built once (ring stages: base + stage offset).
+    const uint64_t dQd = tc::desc_km(tc::su32(Qs)), dOd = tc::desc_km(tc::su32(dOs)), dSd = tc::desc_km(tc::su32(dSs));
+    const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
+    constexpr uint64_t kStage = (2 * TILE) >> 4, kTileStep = TILE >> 4;
     auto issue_s = [&](int x) {  // S = Q K^T and dPo = dO V^T of slot x
-      unsigned char* Ks = ring + 2 * (x % NST) * TILE;
-      unsigned char* Vs = Ks + TILE;
+      const uint64_t dk = dRingKm + (x % NST) * kStage, dv = dk + kTileStep;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma(tS, tc::desc_kmajor(tc::su32(Qs), ks), tc::desc_kmajor(tc::su32(Ks), ks), kIdKm, ks > 0);
-        tc::mma(tP, tc::desc_kmajor(tc::su32(dOs), ks), tc::desc_kmajor(tc::su32(Vs), ks), kIdKm, ks > 0);
+        tc::mma(tS, dQd + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdKm, ks > 0);
+        tc::mma(tP, dOd + ks * tc::kKStepKm, dv + ks * tc::kKStepKm, kIdKm, ks > 0);
       }
       tc::commit(&bar_s);
     };
@@ -148,11 +151,10 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       __syncwarp();
       tc::named_sync(kBarOpReady, NT);  // dS(si) is in shared memory (proxy-fenced)
       if (lane == 0) {
-        unsigned char* Ks = ring + 2 * (si % NST) * TILE;
+        const uint64_t dk = dRingMn + (si % NST) * kStage;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
-          tc::mma(tQ, tc::desc_kmajor(tc::su32(dSs), kk), tc::desc_mnmajor(tc::su32(Ks), kk), kIdMn,
-                  (si > 0 || kk > 0) ? 1u : 0u);
+          tc::mma(tQ, dSd + kk * tc::kKStepKm, dk + kk * tc::kKStepMn, kIdMn, (si > 0 || kk > 0) ? 1u : 0u);
         tc::commit(&bar_o);
       }
       __syncwarp();
@@ -372,12 +374,17 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       tc::bulk_load(base + 2 * TILE, a.lse + rb, 256, &bar_c[st]);
       tc::bulk_load(base + 2 * TILE + 256, a.Dbuf + rb, 256, &bar_c[st]);
     };
+    // Operand descriptors, built once (ring stages: base + stage offset).
+    const uint64_t dKd = tc::desc_km(tc::su32(Ks)), dVd = tc::desc_km(tc::su32(Vs));
+    const uint64_t dPT = tc::desc_km(tc::su32(PTs)), dST = tc::desc_km(tc::su32(dSTs));
+    const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
+    constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
     auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x
-      unsigned char* base = ring + (x % NST) * kKVStageBytes;
+      const uint64_t dq = dRingKm + (x % NST) * kStage, ddo = dq + kTileStep;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma(tS, tc::desc_kmajor(tc::su32(Ks), ks), tc::desc_kmajor(tc::su32(base), ks), kIdKm, ks > 0);
-        tc::mma(tP, tc::desc_kmajor(tc::su32(Vs), ks), tc::desc_kmajor(tc::su32(base + TILE), ks), kIdKm, ks > 0);
+        tc::mma(tS, dKd + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0);
+        tc::mma(tP, dVd + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0);
       }
       tc::commit(&bar_s);
     };
@@ -402,12 +409,12 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       __syncwarp();
       tc::named_sync(kBarOpReady, NT);  // w P^T and dS^T are in shared memory (proxy-fenced)
       if (lane == 0) {
-        unsigned char* base = ring + (ci % NST) * kKVStageBytes;
+        const uint64_t bq = dRingMn + (ci % NST) * kStage, bdo = bq + kTileStep;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
-          tc::mma(tdV, tc::desc_kmajor(tc::su32(PTs), kk), tc::desc_mnmajor(tc::su32(base + TILE), kk), kIdMn, acc);
-          tc::mma(tdK, tc::desc_kmajor(tc::su32(dSTs), kk), tc::desc_mnmajor(tc::su32(base), kk), kIdMn, acc);
+          tc::mma(tdV, dPT + kk * tc::kKStepKm, bdo + kk * tc::kKStepMn, kIdMn, acc);
+          tc::mma(tdK, dST + kk * tc::kKStepKm, bq + kk * tc::kKStepMn, kIdMn, acc);
         }
         tc::commit(&bar_o);
       }

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(128) gca_fwd_mma_kernel(FwdArgs a) {
 // handovers are hardware named barriers.  S(m+1) is issued as soon as the softmax warps
 // have read S(m), so the tensor core overlaps the softmax.  128 TMEM columns and ~50 KB of shared memory per CTA let four CTAs share
 // an SM.
-constexpr int kFwdStages = 2;
+constexpr int kFwdStages = 2;  // the descriptor selection below assumes two stages
 constexpr int kFwdTcSmem = 8192 * (2 + 2 * kFwdStages) + 1024;  // Q, P, ring of (K, V)
 constexpr int kFwdThreads = 160;
 enum { kBarSFree = 2, kBarPFree = 3, kBarPReady = 4 };
@@ -289,11 +289,18 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, bkv, &bar_kv[st]);
       tc::tma_load_4d(Ks + TILE, &tmV, 0, h, j * 64, bkv, &bar_kv[st]);
     };
-    auto issue_s = [&](int x) {
-      unsigned char* Ks = ring + 2 * (x % NST) * TILE;
+    // Operand descriptors, built once: Q, P and the K / V tile of every ring stage.
+    const uint64_t dQ = tc::desc_km(tc::su32(Qs)), dP = tc::desc_km(tc::su32(Ps));
+    uint64_t dK[NST], dV[NST];
 #pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks)
-        tc::mma(tS, tc::desc_kmajor(tc::su32(Qs), ks), tc::desc_kmajor(tc::su32(Ks), ks), kIdS, ks > 0);
+    for (int st = 0; st < NST; ++st) {
+      dK[st] = tc::desc_km(tc::su32(ring + 2 * st * TILE));
+      dV[st] = tc::desc_mn(tc::su32(ring + (2 * st + 1) * TILE));
+    }
+    auto issue_s = [&](int x) {
+      const uint64_t dk = x % NST == 0 ? dK[0] : dK[1];
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks) tc::mma(tS, dQ + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdS, ks > 0);
       tc::commit(&bar_s);
     };
     if (lane == 0) {
@@ -318,11 +325,10 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       __syncwarp();
       tc::named_sync(kBarPReady, NT);  // P(si) is in shared memory (proxy-fenced)
       if (lane == 0) {
-        unsigned char* Vs = ring + (2 * (si % NST) + 1) * TILE;
+        const uint64_t dv = si % NST == 0 ? dV[0] : dV[1];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma(tO, tc::desc_kmajor(tc::su32(Ps), kk), tc::desc_mnmajor(tc::su32(Vs), kk), kIdPV,
-                  (si > 0 || kk > 0) ? 1u : 0u);
+          tc::mma(tO, dP + kk * tc::kKStepKm, dv + kk * tc::kKStepMn, kIdPV, (si > 0 || kk > 0) ? 1u : 0u);
         tc::commit(&bar_o);
       }
       __syncwarp();

@@ -33,6 +33,14 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   d |= (uint64_t)2 << 61;
   return d;
 }
+// Descriptors with every field fixed except the start address: desc(addr) = base +
+// (addr >> 4) for any shared-memory address (below 256 KB, so no carry leaves the
+// 14-bit field).  K steps then add a constant: 2 (32 bytes) for K-major operands, 128
+// (2048 bytes) for MN-major ones.
+__device__ __forceinline__ uint64_t desc_km(uint32_t addr) { return sdesc(0, 16, 1024) + (addr >> 4); }
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr) { return sdesc(0, 1024, 1024) + (addr >> 4); }
+constexpr uint64_t kKStepKm = 2, kKStepMn = 128;
+
 // K-major 64-row tile, K step ks (16 elements).
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int ks) { return sdesc(base + 32 * ks, 16, 1024); }
 // MN-major tile (rows = K), K step ks (16 rows).
