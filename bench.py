@@ -141,14 +141,45 @@ def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> flo
     return units_per_rank * world / (ms_per_step / 1e3)
 
 
-# Measured DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# current kernels on this workload, from the captures summarised under profiles/.
-KNOWN_TRAFFIC = {
-    "gca_bwd_kv": 607.2e6,   # profiles/gca_tc_kernels_128m.md
-    "gca_bwd_q": 512.6e6,
-    "gca_fwd": 383.3e6,
+# Measured DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) on this
+# workload, from the ncu captures summarised under profiles/. Each figure carries a
+# fingerprint of the sources the kernel is built from at capture time; once the sources
+# change, the figure no longer describes the kernel and the bench reports null.
+KERNEL_SOURCES = {
+    "gca_fwd": ("gca_fwd.cu", "tc.cuh", "common.cuh"),
+    "gca_bwd_q": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh"),
+    "gca_bwd_kv": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh"),
+    "retrieve_stream": ("retrieve.cu", "common.cuh"),
 }
-STREAM_TRAFFIC_PER_SEQ = 808.6e6 / 2  # profiles/retrieve_stream_decode_16m.md (B = 2 capture)
+KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture)
+}
+STREAM_TRAFFIC_PER_SEQ = (808.6e6 / 2, "2e400421debd867c")  # profiles/retrieve_stream_decode_16m.md, B = 2
+
+
+def source_fingerprint(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "retrieval_sparse_attention_causal_gb300", "csrc")
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stream_traffic(nb: int):
+    if STREAM_TRAFFIC_PER_SEQ is None:
+        return None
+    per_seq, fp = STREAM_TRAFFIC_PER_SEQ
+    return round(per_seq * nb) if fp == source_fingerprint("retrieve_stream") else None
+
+
+def measured_traffic(kernel: str, table=None):
+    """Traffic per launch for `kernel` if it was captured from the current sources, else None."""
+    entry = (table if table is not None else KNOWN_TRAFFIC).get(kernel)
+    if entry is None:
+        return None
+    value, fp = entry
+    return value if fp == source_fingerprint(kernel) else None
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -231,7 +262,7 @@ def gpu_arm(args):
         avg_s = kern[dom]["avg_ms"] / 1e3
         ach = dom_flops / avg_s / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": KNOWN_TRAFFIC.get(dom),
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": measured_traffic(dom),
                 "peak_source": f"{src} bf16 dense (burst)", "flops_per_launch": dom_flops}
     step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
 
@@ -409,7 +440,7 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
             "ms_per_decode_chunk": round(ms_f, 4), "planted_chunk_found": ok,
             "roofline": {"kernel": "retrieve_stream", "bound": "hbm", "achieved": round(ach, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
-                         "traffic": round(STREAM_TRAFFIC_PER_SEQ * nb), "peak_source": f"{src} copy bandwidth",
+                         "traffic": stream_traffic(nb), "peak_source": f"{src} copy bandwidth",
                          "bytes_per_launch": nbytes},
             "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}}
 
