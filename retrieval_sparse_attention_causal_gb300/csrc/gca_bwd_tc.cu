@@ -2,14 +2,20 @@
 //
 // The same two passes as the mma.sync kernels (query side: P, D = rowsum(P * dO V^T),
 // dQ and per-head dw; key side: dK and dV over the consumers of each chunk), here
-// warp-specialised like the forward: warp 4 is the control warp (lane 0 issues the TMA
-// tile loads into a ring of stages, waits on the mbarriers and issues tcgen05.mma with
-// operands in 128-byte-swizzled shared memory and accumulators in TMEM); warps 0-3 read
-// the products with tcgen05.ld, do the element-wise part in registers and write the bf16
-// operand of the next product back to shared memory.  The two sides hand over through
-// hardware named barriers.  One 64 x 64 tile in shared memory serves as a K-major
-// operand in one product and as an MN-major operand in another (K as the B of S = Q K^T
-// and of dQ = dS K; Q and dO as the B of S^T and dPo^T and of dK, dV).
+// warp-specialised like the forward: warp 8 is the control warp (lane 0 issues the TMA
+// tile loads into a ring of stages; the whole warp waits on the mbarriers and issues
+// tcgen05.mma through an elected lane, accumulators in TMEM); warps 0-7 read the
+// products with tcgen05.ld, do the element-wise part in registers and store the bf16
+// operand of the next product (dS, or w P^T and dS^T) into TMEM over the columns they
+// have read, where the next MMA takes it as its A operand.  One 64 x 64 tile in shared
+// memory serves as a K-major operand in one product and as an MN-major operand in
+// another (K as the B of S = Q K^T and of dQ = dS K; Q and dO as the B of S^T and dPo^T
+// and of dK, dV).
+//
+// Per slot (consumer) the control warp issues the products that read the element warps'
+// operand, then the next S / dPo pair into the same columns: the tensor pipe runs one
+// CTA's MMAs in issue order, so the overwrite follows the read, and the completion of
+// the next pair (the element warps' mbarrier) implies that of the products before it.
 //
 // Source of the method: Paper-Notes page on "Efficient Length-Generalizable Attention via
 // Causal Retrieval for Long-Context Language Modeling", 关键设计 / key design, item
@@ -29,11 +35,11 @@ constexpr int kEW = 8;
 constexpr int kThreads = 32 * (kEW + 1);
 constexpr int kCtl = kEW;  // control warp index
 constexpr int TILE = 8192, ROWB = 128, UPR = 8, DH = 64;
-enum { kBarSFree = 2, kBarOpFree = 3, kBarOpReady = 4, kBarEW = 5 };
+enum { kBarOpReady = 2, kBarEW = 3 };
 
 // ================================================================== query side
 constexpr int kQStages = 5;
-constexpr int kQSmem = TILE * (3 + 2 * kQStages) + 1024;  // Q, dO, dS, ring of (K, V)
+constexpr int kQSmem = TILE * (2 + 2 * kQStages) + 1024;  // Q, dO, ring of (K, V)
 
 __global__ void __launch_bounds__(kThreads, 2)
 gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -45,8 +51,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   unsigned char* Qs = sm;
   unsigned char* dOs = sm + TILE;
-  unsigned char* dSs = sm + 2 * TILE;
-  unsigned char* ring = sm + 3 * TILE;
+  unsigned char* ring = sm + 2 * TILE;
   __shared__ float w_s[kMaxTopk];
   __shared__ int j_s[kMaxTopk];
   __shared__ int slot_s[kMaxTopk];
@@ -108,7 +113,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   if (warp == kCtl) {
     // ------------------------------------------------------------ control warp
     bool ok = true;
-    auto load_slot = [&](int x) {
+    auto load_slot = [&](int x) {  // lane 0
       const int st = x % NST;
       const int j = j_s[slot_s[x]];
       unsigned char* Ks = ring + 2 * st * TILE;
@@ -117,50 +122,41 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       tc::tma_load_4d(Ks + TILE, &tmV, 0, h, j * 64, bkv, &bar_kv[st]);
     };
     // Operand descriptors, built once (ring stages: base + stage offset).
-    const uint64_t dQd = tc::desc_km(tc::su32(Qs)), dOd = tc::desc_km(tc::su32(dOs)), dSd = tc::desc_km(tc::su32(dSs));
+    const uint64_t dQd = tc::desc_km(tc::su32(Qs)), dOd = tc::desc_km(tc::su32(dOs));
     const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
     constexpr uint64_t kStage = (2 * TILE) >> 4, kTileStep = TILE >> 4;
-    auto issue_s = [&](int x) {  // S = Q K^T and dPo = dO V^T of slot x
+    auto issue_s = [&](int x) {  // S = Q K^T and dPo = dO V^T of slot x (whole warp)
       const uint64_t dk = dRingKm + (x % NST) * kStage, dv = dk + kTileStep;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma(tS, dQd + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdKm, ks > 0);
-        tc::mma(tP, dOd + ks * tc::kKStepKm, dv + ks * tc::kKStepKm, kIdKm, ks > 0);
+        tc::mma_warp(tS, dQd + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+        tc::mma_warp(tP, dOd + ks * tc::kKStepKm, dv + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
       }
-      tc::commit(&bar_s);
+      tc::commit_warp(&bar_s);
     };
     if (lane == 0) {
       tc::mbar_expect_tx(&bar_q, 2 * TILE);
       tc::tma_load_4d(Qs, &tmQ, 0, h, c * 64, b, &bar_q);
       tc::tma_load_4d(dOs, &tmdO, 0, h, c * 64, b, &bar_q);
       for (int x = 0; x < NST && x < ns; ++x) load_slot(x);
-      ok = tc::mbar_wait(&bar_q, 0) && ok;
-      ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
-      issue_s(0);
     }
     __syncwarp();
-    tc::named_arrive(kBarOpFree, NT);
+    ok = tc::mbar_wait(&bar_q, 0) && ok;
+    ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
+    issue_s(0);
     for (int si = 0; si < ns; ++si) {
-      // S(si), dPo(si) have been loaded (tcgen05.wait::ld done before the arrival); no
-      // tcgen05 fence, which after a thread barrier would wait for every MMA in flight.
-      tc::named_sync(kBarSFree, NT);
-      if (lane == 0 && si + 1 < ns) {
+      tc::named_sync(kBarOpReady, NT);  // dS(si) is in TMEM columns 0-31
+      tc::fence_after();
+      const uint64_t dk = dRingMn + (si % NST) * kStage;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
+        tc::mma_ts_warp(tQ, tS + 8 * kk, dk + kk * tc::kKStepMn, kIdMn, (si > 0 || kk > 0) ? 1u : 0u);
+      tc::commit_warp(&bar_o);
+      if (si + 1 < ns) {
         ok = tc::mbar_wait(&bar_kv[(si + 1) % NST], ((si + 1) / NST) & 1) && ok;
         issue_s(si + 1);
       }
-      __syncwarp();
-      tc::named_sync(kBarOpReady, NT);  // dS(si) is in shared memory (proxy-fenced)
-      if (lane == 0) {
-        const uint64_t dk = dRingMn + (si % NST) * kStage;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
-          tc::mma(tQ, dSd + kk * tc::kKStepKm, dk + kk * tc::kKStepMn, kIdMn, (si > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bar_o);
-      }
-      __syncwarp();
-      if (lane == 0) ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // dS buffer and stage si % NST are free
-      __syncwarp();
-      if (si + 1 < ns) tc::named_arrive(kBarOpFree, NT);
+      ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // ring stage si % NST is free
       if (lane == 0) {
         if (si + NST < ns) load_slot(si + NST);
         if (!ok) flag_timeout(a.err);
@@ -171,15 +167,10 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     // ------------------------------------------------------------ element-wise warps
     const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
     const int row0 = 16 * quarter + g;
-    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    const uint32_t lane_q = (uint32_t)(32 * quarter) << 16;
+    const uint32_t lane_base = lane_q + 32 * hc;
     const float scale = 1.0f / sqrtf((float)DH);
     const float sl2 = scale * kLog2e;
-    uint32_t off0[4], off1[4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      off0[n] = swz<ROWB>(row0, 4 * hc + n) + cq * 4;
-      off1[n] = swz<ROWB>(row0 + 8, 4 * hc + n) + cq * 4;
-    }
     for (int si = 0; si < ns; ++si) {
       const int m = slot_s[si];
       const float lse0 = lse[m * 64 + row0] * kLog2e, lse1 = lse[m * 64 + row0 + 8] * kLog2e;
@@ -191,8 +182,6 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
       tc::ld_wait(s);
       tc::ld_wait(dp);
-      tc::fence_before();
-      tc::named_arrive(kBarSFree, NT);
       float D0 = 0.f, D1 = 0.f;
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
@@ -208,7 +197,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         D0 += __shfl_xor_sync(0xffffffffu, D0, k);
         D1 += __shfl_xor_sync(0xffffffffu, D1, k);
       }
-      // Combine the two column halves in a fixed order (deterministic).
+      // Combine the two column halves in a fixed order (deterministic).  The barrier
+      // also orders both halves' loads of S before either half's dS store below.
       if (cq == 0) {
         Dx[si & 1][hc][row0] = D0;
         Dx[si & 1][hc][row0 + 8] = D1;
@@ -228,15 +218,17 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         if (lane == 0) dwred[quarter][m] = part;
       }
       const float cs = w_s[m] * scale;
-      tc::named_sync(kBarOpFree, NT);  // dQ += dS K of the previous slot has finished
+      // dS as the TMEM A operand of dQ += dS K: keys (32hc + 8n + 2cq, +1) of rows g and
+      // g + 8 go to column 16hc + 4n + cq.
+      uint32_t dv[8];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
-        *reinterpret_cast<uint32_t*>(dSs + off0[n]) =
-            pack_bf16(s[n][0] * (dp[n][0] - D0) * cs, s[n][1] * (dp[n][1] - D0) * cs);
-        *reinterpret_cast<uint32_t*>(dSs + off1[n]) =
-            pack_bf16(s[n][2] * (dp[n][2] - D1) * cs, s[n][3] * (dp[n][3] - D1) * cs);
+        dv[2 * n] = pack_bf16(s[n][0] * (dp[n][0] - D0) * cs, s[n][1] * (dp[n][1] - D0) * cs);
+        dv[2 * n + 1] = pack_bf16(s[n][2] * (dp[n][2] - D1) * cs, s[n][3] * (dp[n][3] - D1) * cs);
       }
-      tc::fence_async_smem();
+      tc::st16x128_x4(tS + lane_q + 16 * hc, dv);
+      tc::st_wait();
+      tc::fence_before();
       tc::named_arrive(kBarOpReady, NT);
     }
   }
@@ -273,7 +265,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
 // ================================================================== key side
 constexpr int kKVStages = 4;
 constexpr int kKVStageBytes = 2 * TILE + 1024;  // Q, dO tiles + LSE and D rows (1 KB keeps tiles aligned)
-constexpr int kKVSmem = TILE * 4 + kKVStages * kKVStageBytes + 1024;  // K, V, wP^T, dS^T, ring
+constexpr int kKVSmem = TILE * 2 + kKVStages * kKVStageBytes + 1024;  // K, V, ring
 constexpr int kConsTab = 256;
 
 // Fusion weight w_m of slot m of retrieval row r (softmax over the row's valid slots),
@@ -308,9 +300,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   unsigned char* Ks = sm;
   unsigned char* Vs = sm + TILE;
-  unsigned char* PTs = sm + 2 * TILE;   // w P^T (keys x queries)
-  unsigned char* dSTs = sm + 3 * TILE;  // dS^T
-  unsigned char* ring = sm + 4 * TILE;  // stage st at ring + st * kKVStageBytes: Q, dO, lse[64], D[64]
+  unsigned char* ring = sm + 2 * TILE;  // stage st at ring + st * kKVStageBytes: Q, dO, lse[64], D[64]
   __shared__ float w_st[NST];
   __shared__ float wtab[kConsTab];  // weight of each consumer (first kConsTab consumers)
   __shared__ int etab[kConsTab];    // its (row, slot) entry
@@ -376,52 +366,43 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     };
     // Operand descriptors, built once (ring stages: base + stage offset).
     const uint64_t dKd = tc::desc_km(tc::su32(Ks)), dVd = tc::desc_km(tc::su32(Vs));
-    const uint64_t dPT = tc::desc_km(tc::su32(PTs)), dST = tc::desc_km(tc::su32(dSTs));
     const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
     constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
-    auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x
+    auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x (whole warp)
       const uint64_t dq = dRingKm + (x % NST) * kStage, ddo = dq + kTileStep;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma(tS, dKd + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0);
-        tc::mma(tP, dVd + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0);
+        tc::mma_warp(tS, dKd + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+        tc::mma_warp(tP, dVd + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
       }
-      tc::commit(&bar_s);
+      tc::commit_warp(&bar_s);
     };
     if (lane == 0) {
-      for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
       tc::mbar_expect_tx(&bar_k, 2 * TILE);
       tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, b, &bar_k);
       tc::tma_load_4d(Vs, &tmV, 0, h, j * 64, b, &bar_k);
-      ok = tc::mbar_wait(&bar_k, 0) && ok;
-      ok = tc::mbar_wait(&bar_c[0], 0) && ok;
-      issue_s(0);
+      for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
     }
     __syncwarp();
-    tc::named_arrive(kBarOpFree, NT);
+    ok = tc::mbar_wait(&bar_k, 0) && ok;
+    ok = tc::mbar_wait(&bar_c[0], 0) && ok;
+    issue_s(0);
     for (int ci = 0; ci < ncons; ++ci) {
-      // S^T(ci), dPo^T(ci) have been loaded; no tcgen05 fence (see the query side).
-      tc::named_sync(kBarSFree, NT);
-      if (lane == 0 && ci + 1 < ncons) {
+      tc::named_sync(kBarOpReady, NT);  // w P^T and dS^T are in TMEM columns 0-31, 64-95
+      tc::fence_after();
+      const uint64_t bq = dRingMn + (ci % NST) * kStage, bdo = bq + kTileStep;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
+        tc::mma_ts_warp(tdV, tS + 8 * kk, bdo + kk * tc::kKStepMn, kIdMn, acc);
+        tc::mma_ts_warp(tdK, tP + 8 * kk, bq + kk * tc::kKStepMn, kIdMn, acc);
+      }
+      tc::commit_warp(&bar_o);
+      if (ci + 1 < ncons) {
         ok = tc::mbar_wait(&bar_c[(ci + 1) % NST], ((ci + 1) / NST) & 1) && ok;
         issue_s(ci + 1);
       }
-      __syncwarp();
-      tc::named_sync(kBarOpReady, NT);  // w P^T and dS^T are in shared memory (proxy-fenced)
-      if (lane == 0) {
-        const uint64_t bq = dRingMn + (ci % NST) * kStage, bdo = bq + kTileStep;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
-          tc::mma(tdV, dPT + kk * tc::kKStepKm, bdo + kk * tc::kKStepMn, kIdMn, acc);
-          tc::mma(tdK, dST + kk * tc::kKStepKm, bq + kk * tc::kKStepMn, kIdMn, acc);
-        }
-        tc::commit(&bar_o);
-      }
-      __syncwarp();
-      if (lane == 0) ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // operands and stage ci % NST are free
-      __syncwarp();
-      if (ci + 1 < ncons) tc::named_arrive(kBarOpFree, NT);
+      ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // ring stage ci % NST is free
       if (lane == 0) {
         if (ci + NST < ncons) load_cons(ci + NST);
         if (!ok) flag_timeout(a.err);
@@ -430,17 +411,11 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     }
   } else {
     // ------------------------------------------------------------ element-wise warps
-    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
-    const int row0 = 16 * quarter + g;  // key rows row0, row0 + 8
-    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    const int cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const uint32_t lane_q = (uint32_t)(32 * quarter) << 16;
+    const uint32_t lane_base = lane_q + 32 * hc;
     const float scale = 1.0f / sqrtf((float)DH);
     const float sl2 = scale * kLog2e;
-    uint32_t off0[4], off1[4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) {
-      off0[n] = swz<ROWB>(row0, 4 * hc + n) + cq * 4;
-      off1[n] = swz<ROWB>(row0 + 8, 4 * hc + n) + cq * 4;
-    }
     for (int ci = 0; ci < ncons; ++ci) {
       if (!tc::mbar_wait(&bar_s, ci & 1)) flag_timeout(a.err);  // acquire S^T(ci), dPo^T(ci)
       const int st = ci % NST;
@@ -456,8 +431,6 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
       tc::ld_wait(s);
       tc::ld_wait(dp);
-      tc::fence_before();
-      tc::named_arrive(kBarSFree, NT);
       const float cs = w * scale;
 #pragma unroll
       for (int n = 0; n < 4; ++n) {  // columns are queries 32hc + 8n + 2cq (+1)
@@ -475,15 +448,22 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         s[n][2] = p2 * w;
         s[n][3] = p3 * w;
       }
-      tc::named_sync(kBarOpFree, NT);  // the previous consumer's dV, dK products are done
+      // w P^T and dS^T as TMEM A operands (keys are rows): queries (32hc + 8n + 2cq, +1)
+      // of key rows g and g + 8 go to column 16hc + 4n + cq of S^T's and dPo^T's columns.
+      // Both column halves must have read S^T and dPo^T before either half stores.
+      uint32_t pv[8], dv[8];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
-        *reinterpret_cast<uint32_t*>(PTs + off0[n]) = pack_bf16(s[n][0], s[n][1]);
-        *reinterpret_cast<uint32_t*>(PTs + off1[n]) = pack_bf16(s[n][2], s[n][3]);
-        *reinterpret_cast<uint32_t*>(dSTs + off0[n]) = pack_bf16(dp[n][0], dp[n][1]);
-        *reinterpret_cast<uint32_t*>(dSTs + off1[n]) = pack_bf16(dp[n][2], dp[n][3]);
+        pv[2 * n] = pack_bf16(s[n][0], s[n][1]);
+        pv[2 * n + 1] = pack_bf16(s[n][2], s[n][3]);
+        dv[2 * n] = pack_bf16(dp[n][0], dp[n][1]);
+        dv[2 * n + 1] = pack_bf16(dp[n][2], dp[n][3]);
       }
-      tc::fence_async_smem();
+      tc::named_sync(kBarEW, 32 * kEW);
+      tc::st16x128_x4(tS + lane_q + 16 * hc, pv);
+      tc::st16x128_x4(tP + lane_q + 16 * hc, dv);
+      tc::st_wait();
+      tc::fence_before();
       tc::named_arrive(kBarOpReady, NT);
     }
   }

@@ -199,21 +199,24 @@ __global__ void __launch_bounds__(128) gca_fwd_mma_kernel(FwdArgs a) {
 // ------------------------------------------------------------------ bf16 tcgen05 path (dh = 64)
 // Same decomposition on the 5th-generation tensor cores, warp-specialised.
 //   * Warp 4 (control): lane 0 issues the TMA tile loads (Q once; K and V of each
-//     retrieved chunk into a 2-stage ring), waits on the mbarriers, and issues
-//     tcgen05.mma (M = 64 query rows, N = 64, K steps of 16) with operands in
-//     128-byte-swizzled shared memory and accumulators in TMEM: S = Q K^T in columns
-//     0-63 and the fused output O in columns 64-127, accumulated over all slots.
+//     retrieved chunk into a 2-stage ring); the whole warp waits on the mbarriers and
+//     issues tcgen05.mma through an elected lane (M = 64 query rows, N = 64, K steps of
+//     16).  S = Q K^T goes to TMEM columns 0-63; the fused output O, accumulated over
+//     all slots, to columns 64-127.
 //   * Warps 0-3 (softmax): read S with tcgen05.ld, do the row softmax in registers and
-//     write P~ = (w_m / l) P as bf16 to shared memory, the A operand of O += P~ V (V is
-//     the MN-major B operand).
-// The softmax warps take S straight from the MMA-completion mbarrier; the other
-// handovers are hardware named barriers.  S(m+1) is issued as soon as the softmax warps
-// have read S(m), so the tensor core overlaps the softmax.  128 TMEM columns and ~50 KB of shared memory per CTA let four CTAs share
-// an SM.
+//     store P~ = (w_m / l) P as bf16 pairs into TMEM columns 0-31 (over the S they have
+//     read), where it is the A operand of O += P~ V (V from shared memory, MN-major).
+// Per slot: the softmax warps take S(m) from the MMA-completion mbarrier and hand P~(m)
+// back through a named barrier; the control warp then issues O += P~(m) V(m) followed by
+// S(m+1) = Q K(m+1)^T.  The tensor pipe runs one CTA's MMAs in issue order, so S(m+1)
+// overwrites columns 0-63 only after the PV product has read P~(m); and S(m+1) complete
+// implies PV(m) complete, so P~(m+1) may be stored once S(m+1) has been read.  128 TMEM
+// columns and 41 KB of shared memory per CTA let four CTAs share an SM and overlap one
+// another's softmax and MMAs.
 constexpr int kFwdStages = 2;  // the descriptor selection below assumes two stages
-constexpr int kFwdTcSmem = 8192 * (2 + 2 * kFwdStages) + 1024;  // Q, P, ring of (K, V)
+constexpr int kFwdTcSmem = 8192 * (1 + 2 * kFwdStages) + 1024;  // Q, ring of (K, V)
 constexpr int kFwdThreads = 160;
-enum { kBarSFree = 2, kBarPFree = 3, kBarPReady = 4 };
+enum { kBarPReady = 2 };
 
 __global__ void __launch_bounds__(kFwdThreads, 4)
 gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -224,8 +227,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
   extern __shared__ __align__(1024) unsigned char dsm[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   unsigned char* Qs = sm;
-  unsigned char* Ps = sm + TILE;
-  unsigned char* ring = sm + 2 * TILE;  // stage st: K at ring + 2*st*TILE, V after it
+  unsigned char* ring = sm + TILE;  // stage st: K at ring + 2*st*TILE, V after it
   __shared__ float w_s[kMaxTopk];
   __shared__ int j_s[kMaxTopk];
   __shared__ int slot_s[kMaxTopk];
@@ -281,7 +283,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
   if (warp == 4) {
     // ------------------------------------------------------------ control warp
     bool ok = true;
-    auto load_slot = [&](int x) {  // K, V tiles of slot x into stage x % NST
+    auto load_slot = [&](int x) {  // K, V tiles of slot x into stage x % NST (lane 0)
       const int st = x % NST;
       const int j = j_s[slot_s[x]];
       unsigned char* Ks = ring + 2 * st * TILE;
@@ -289,52 +291,43 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, bkv, &bar_kv[st]);
       tc::tma_load_4d(Ks + TILE, &tmV, 0, h, j * 64, bkv, &bar_kv[st]);
     };
-    // Operand descriptors, built once: Q, P and the K / V tile of every ring stage.
-    const uint64_t dQ = tc::desc_km(tc::su32(Qs)), dP = tc::desc_km(tc::su32(Ps));
+    // Operand descriptors, built once: Q and the K / V tile of every ring stage.
+    const uint64_t dQ = tc::desc_km(tc::su32(Qs));
     uint64_t dK[NST], dV[NST];
 #pragma unroll
     for (int st = 0; st < NST; ++st) {
       dK[st] = tc::desc_km(tc::su32(ring + 2 * st * TILE));
       dV[st] = tc::desc_mn(tc::su32(ring + (2 * st + 1) * TILE));
     }
-    auto issue_s = [&](int x) {
+    auto issue_s = [&](int x) {  // whole warp
       const uint64_t dk = x % NST == 0 ? dK[0] : dK[1];
 #pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks) tc::mma(tS, dQ + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdS, ks > 0);
-      tc::commit(&bar_s);
+      for (int ks = 0; ks < DH / 16; ++ks)
+        tc::mma_warp(tS, dQ + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdS, ks > 0 ? 1u : 0u);
+      tc::commit_warp(&bar_s);
     };
     if (lane == 0) {
       tc::mbar_expect_tx(&bar_q, TILE);
       tc::tma_load_4d(Qs, &tmQ, 0, h, c * 64, b, &bar_q);
       for (int x = 0; x < NST && x < ns; ++x) load_slot(x);
-      ok = tc::mbar_wait(&bar_q, 0) && ok;
-      ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
-      issue_s(0);
     }
     __syncwarp();
-    tc::named_arrive(kBarPFree, NT);
+    ok = tc::mbar_wait(&bar_q, 0) && ok;
+    ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
+    issue_s(0);
     for (int si = 0; si < ns; ++si) {
-      // The softmax warps have loaded S(si) (tcgen05.wait::ld done before they arrived),
-      // so S(si+1) may overwrite it.  No tcgen05 fence here: after a thread barrier it
-      // would wait for every MMA in flight.
-      tc::named_sync(kBarSFree, NT);
-      if (lane == 0 && si + 1 < ns) {
+      tc::named_sync(kBarPReady, NT);  // P~(si) is in TMEM columns 0-31
+      tc::fence_after();
+      const uint64_t dv = si % NST == 0 ? dV[0] : dV[1];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_ts_warp(tO, tS + 8 * kk, dv + kk * tc::kKStepMn, kIdPV, (si > 0 || kk > 0) ? 1u : 0u);
+      tc::commit_warp(&bar_o);
+      if (si + 1 < ns) {
         ok = tc::mbar_wait(&bar_kv[(si + 1) % NST], ((si + 1) / NST) & 1) && ok;
         issue_s(si + 1);
       }
-      __syncwarp();
-      tc::named_sync(kBarPReady, NT);  // P(si) is in shared memory (proxy-fenced)
-      if (lane == 0) {
-        const uint64_t dv = si % NST == 0 ? dV[0] : dV[1];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma(tO, dP + kk * tc::kKStepKm, dv + kk * tc::kKStepMn, kIdPV, (si > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bar_o);
-      }
-      __syncwarp();
-      if (lane == 0) ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // P and ring stage si % NST are free
-      __syncwarp();
-      if (si + 1 < ns) tc::named_arrive(kBarPFree, NT);
+      ok = tc::mbar_wait(&bar_o, si & 1) && ok;  // ring stage si % NST is free
       if (lane == 0) {
         if (si + NST < ns) load_slot(si + NST);
         if (!ok) flag_timeout(a.err);
@@ -348,22 +341,14 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const float scale = 1.0f / sqrtf((float)DH);
     const float sl2 = scale * 1.4426950408889634f;
-    uint32_t poff0[8], poff1[8];
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      poff0[n] = swz<ROWB>(row0, n) + cq * 4;
-      poff1[n] = swz<ROWB>(row0 + 8, n) + cq * 4;
-    }
     for (int si = 0; si < ns; ++si) {
       // Acquire S(si) straight from the MMA-completion barrier (S(si+1) is only issued
-      // after every softmax thread has passed this point, so the phase cannot run ahead).
+      // after every softmax thread has handed over P~(si), so the phase cannot run ahead).
       if (!tc::mbar_wait(&bar_s, si & 1)) flag_timeout(a.err);
       float s[8][4];
 #pragma unroll
       for (int cb = 0; cb < 8; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
       tc::ld_wait(s);
-      tc::fence_before();
-      tc::named_arrive(kBarSFree, NT);
       float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
       for (int n = 0; n < 8; ++n) {
@@ -398,13 +383,20 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
         lse[mslot * 64 + row0 + 8] = mx1 * scale + __logf(l1);
       }
       const float c0 = __fdividef(wm, l0), c1 = __fdividef(wm, l1);
-      tc::named_sync(kBarPFree, NT);  // O += P~ V of the previous slot has finished
+      // P~ as the TMEM A operand: the pair of keys (8n + 2cq, +1) of rows g and g + 8
+      // goes to column 4n + cq (two 16-column stores).
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        *reinterpret_cast<uint32_t*>(Ps + poff0[n]) = pack_bf16(s[n][0] * c0, s[n][1] * c0);
-        *reinterpret_cast<uint32_t*>(Ps + poff1[n]) = pack_bf16(s[n][2] * c1, s[n][3] * c1);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pv[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          pv[2 * i] = pack_bf16(s[4 * half + i][0] * c0, s[4 * half + i][1] * c0);
+          pv[2 * i + 1] = pack_bf16(s[4 * half + i][2] * c1, s[4 * half + i][3] * c1);
+        }
+        tc::st16x128_x4(tS + lane_base + 16 * half, pv);
       }
-      tc::fence_async_smem();
+      tc::st_wait();
+      tc::fence_before();
       tc::named_arrive(kBarPReady, NT);
     }
   }

@@ -15,6 +15,16 @@
 //     column per output column; warp w reads its 16 rows with tcgen05.ld.16x256b, which
 //     gives thread t rows t/4 and t/4 + 8, columns 2(t%4) and 2(t%4) + 1 of each
 //     8-column block (the same fragment as mma.sync's accumulator).
+//   * A operand in TMEM (K-major): row r in the same lane as the accumulator's row r for
+//     that M (M = 128: lane r), two 16-bit elements per 32-bit column with the even K
+//     index in the low half, so a K step of 16 advances the address by 8 columns.
+//   * tcgen05.st.16x128b.x4: register 2i of thread t goes to (lane t/4, column
+//     4i + t%4), register 2i + 1 to (lane t/4 + 8, column 4i + t%4); with the 16x256b
+//     load fragment above, a thread's packed pair from 8-column block n of a row lands
+//     in column 4n + t%4, the A-operand position of that pair.
+//   * Issue cost: an MMA issued from a one-lane branch costs about 44 cycles of issue,
+//     more than an M = 64, N = 64, K = 16 MMA takes in the pipe (about 35); issued by
+//     an elected lane of a converged warp it costs less than the pipe time.
 #pragma once
 
 #include <stdint.h>
@@ -56,6 +66,30 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// The same MMA issued by one elected lane of a converged warp: every lane of the warp
+// executes the call with the same operands.
+__device__ __forceinline__ void mma_warp(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// A operand from TMEM (address a_tmem, lane 0 of the operand), B from shared memory.
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// tcgen05.commit by the same elected lane (elect.sync picks the lowest active lane, so
+// the lane that issued the MMAs above).
+__device__ __forceinline__ void commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(su32(bar)));
 }
 
 // Arrive on `bar` when every tcgen05.mma issued so far by this thread has completed.
@@ -107,6 +141,13 @@ __device__ __forceinline__ void ld16x256(uint32_t taddr, float (&v)[4]) {
                : "r"(taddr));
 }
 __device__ __forceinline__ void ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 lanes x 16 columns from lane base `taddr` (layout in the header comment).
+__device__ __forceinline__ void st16x128_x4(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Wait for outstanding tcgen05.ld and tie the 32 loaded registers to the wait, so that
 // the compiler cannot move a use of them above it.
 __device__ __forceinline__ void ld_wait(float (&v)[8][4]) {
