@@ -361,7 +361,11 @@ extern "C" gca_status gca_check_error(void* ws, gca_stream_t stream, int* bad_va
   const ErrWord zero{};
   e = cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "gca_check_error clear");
-  if (h.flags & kErrTimeout) return fail(GCA_ERR_TIMEOUT, "a bounded wait for tensor-core completion ran out");
+  if (h.flags & kErrTimeout)
+    return fail(GCA_ERR_TIMEOUT,
+                "a bounded wait for tensor-core or copy completion ran out (wait sites 0x%x; first: site %d, "
+                "CTA %d, tile %d, slot %d)",
+                (unsigned)h.wait_sites, h.first[0] - 1, h.first[1], h.first[2], h.first[3]);
   if (bad_value) *bad_value = h.bad_value;
   return fail(GCA_ERR_DEVICE_INDEX, "a kernel met retrieved index %d outside [-1, nC)", h.bad_value);
 }

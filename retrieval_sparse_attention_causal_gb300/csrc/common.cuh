@@ -13,8 +13,10 @@ constexpr int kMaxTopk = 16;  // largest supported top-k
 
 // Device error word: the first 256 bytes of every workspace.
 struct ErrWord {
-  int flags;      // bit 0: an index outside [-1, nC) was met
+  int flags;      // bit 0: an index outside [-1, nC) was met; bit 1: a bounded wait ran out
   int bad_value;  // last offending index
+  int wait_sites; // bit s: the wait at site s ran out (sites are numbered per kernel)
+  int first[4];   // the first wait that ran out: site + 1, CTA, tile, slot (0 until then)
 };
 constexpr int kErrIndex = 1;
 constexpr int kErrTimeout = 2;
@@ -28,8 +30,16 @@ __device__ __forceinline__ void flag_bad_index(ErrWord* e, int v) {
 }
 
 // A bounded wait on an mbarrier ran out (the kernel carried on instead of hanging).
-__device__ __forceinline__ void flag_timeout(ErrWord* e) {
-  if (e) atomicOr(&e->flags, kErrTimeout);
+__device__ __forceinline__ void flag_timeout(ErrWord* e, int site = 0, int cta = -1, int tile = -1, int slot = -1) {
+  if (e) {
+    atomicOr(&e->flags, kErrTimeout);
+    atomicOr(&e->wait_sites, 1 << site);
+    if (atomicCAS(&e->first[0], 0, site + 1) == 0) {
+      e->first[1] = cta;
+      e->first[2] = tile;
+      e->first[3] = slot;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- element access
@@ -182,12 +192,13 @@ __device__ __forceinline__ void row_weights_warp(const int32_t* idx_row, const f
   int j = -1;
   float s = -CUDART_INF_F;
   if (lane < topk) {
-    j = idx_row[lane];
+    j = idx_row[lane];   // both loads in flight at once (the score of an empty slot is
+    s = sc_row[lane];    // read and discarded)
     if (j < -1 || j >= nC) {
       flag_bad_index(err, j);
       j = -1;
     }
-    if (j >= 0) s = sc_row[lane];
+    if (j < 0) s = -CUDART_INF_F;
   }
   float mx = s;
 #pragma unroll

@@ -576,31 +576,52 @@ __global__ void __launch_bounds__(64) gca_bwd_kv_f32_kernel(BwdArgs a) {
 }
 
 // ------------------------------------------------------------------ dscores
-__global__ void __launch_bounds__(32) gca_dscores_kernel(BwdArgs a) {
-  const int r = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
+__global__ void __launch_bounds__(256) gca_dscores_kernel(BwdArgs a) {
+  // One CTA per retrieval row r (query chunk c = r + shift).  dw_m, the gradient of the
+  // fused output with respect to fusion weight m, is the sum of the D rows of slot m over
+  // heads and query rows (D = rowsum(P * dO V^T) = dO . O_m per row); then
+  // ds_m = w_m (dw_m - sum_n w_n dw_n), the softmax backward.  Fixed summation order.
+  const int r = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = r + a.shift;
   float* out = a.dscores + ((int64_t)b * a.nQ + r) * a.topk;
   if (c >= a.nQ) {
-    if (lane < a.topk) out[lane] = 0.f;
+    if (tid < a.topk) out[tid] = 0.f;
     return;
   }
   __shared__ float w_s[kMaxTopk];
   __shared__ int j_s[kMaxTopk];
-  row_weights_warp(a.idx + ((int64_t)b * a.nQ + r) * a.topk, a.scores + ((int64_t)b * a.nQ + r) * a.topk,
-                   a.topk, a.nC, w_s, j_s, nullptr);
-  __syncwarp();
-  float w = 0.f, dw = 0.f;
-  bool valid = false;
-  if (lane < a.topk) {
-    w = w_s[lane];
-    valid = j_s[lane] >= 0;
-    const float* p = a.dwp + ((int64_t)b * a.nQ + c) * a.H * a.topk + lane;
-    for (int h = 0; h < a.H; ++h) dw += p[(int64_t)h * a.topk];
-  }
-  float sum = w * dw;
+  __shared__ float dw_s[kMaxTopk];
+  if (warp == 0)
+    row_weights_warp(a.idx + ((int64_t)b * a.nQ + r) * a.topk, a.scores + ((int64_t)b * a.nQ + r) * a.topk,
+                     a.topk, a.nC, w_s, j_s, nullptr);
+  __syncthreads();
+  const float* Dc = a.Dbuf + ((int64_t)b * a.nQ + c) * a.H * a.topk * 64;
+  for (int m = warp; m < a.topk; m += 8) {
+    float acc = 0.f;
+    if (j_s[m] >= 0) {
+      for (int h = 0; h < a.H; ++h) {
+        const float* p = Dc + ((int64_t)h * a.topk + m) * 64;
+        acc += p[lane] + p[lane + 32];
+      }
+    }
 #pragma unroll
-  for (int k = 16; k >= 1; k >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, k);
-  if (lane < a.topk) out[lane] = valid ? w * (dw - sum) : 0.f;
+    for (int k = 16; k >= 1; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
+    if (lane == 0) dw_s[m] = acc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float w = 0.f, dw = 0.f;
+    bool valid = false;
+    if (lane < a.topk) {
+      w = w_s[lane];
+      valid = j_s[lane] >= 0;
+      dw = valid ? dw_s[lane] : 0.f;
+    }
+    float sum = w * dw;
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, k);
+    if (lane < a.topk) out[lane] = valid ? w * (dw - sum) : 0.f;
+  }
 }
 
 // ------------------------------------------------------------------ CSR of consumers
@@ -707,7 +728,7 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s) {
     if ((e = launch_end("gca_bwd_q_f32", s)) != cudaSuccess) return e;
   }
   launch_begin("gca_dscores", s);
-  gca_dscores_kernel<<<dim3(a.nQ, a.B), 32, 0, s>>>(a);
+  gca_dscores_kernel<<<dim3(a.nQ, a.B), 256, 0, s>>>(a);
   if ((e = launch_end("gca_dscores", s)) != cudaSuccess) return e;
   const int nrows = a.nQ - a.shift;
   if ((e = launch_csr(a.idx, a.B, a.nQ, nrows > 0 ? nrows : 0, a.topk, a.nC, a.csr_off, a.csr_ent,

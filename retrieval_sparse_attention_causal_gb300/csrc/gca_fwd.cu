@@ -211,10 +211,11 @@ __global__ void __launch_bounds__(128) gca_fwd_mma_kernel(FwdArgs a) {
 // S(m+1) = Q K(m+1)^T.  The tensor pipe runs one CTA's MMAs in issue order, so S(m+1)
 // overwrites columns 0-63 only after the PV product has read P~(m); and S(m+1) complete
 // implies PV(m) complete, so P~(m+1) may be stored once S(m+1) has been read.  128 TMEM
-// columns and 41 KB of shared memory per CTA let four CTAs share an SM and overlap one
-// another's softmax and MMAs.
+// columns per CTA let four CTAs share an SM and overlap one another's softmax and MMAs.
 constexpr int kFwdStages = 2;  // the descriptor selection below assumes two stages
-constexpr int kFwdTcSmem = 8192 * (1 + 2 * kFwdStages) + 1024;  // Q, ring of (K, V)
+// Q and the ring of (K, V) take 41 KB; the request is padded to 46 KB so that at most
+// four CTAs share an SM: a fifth would find all 512 TMEM columns taken.
+constexpr int kFwdTcSmem = 46 * 1024 + 1024;
 constexpr int kFwdThreads = 160;
 enum { kBarPReady = 2 };
 

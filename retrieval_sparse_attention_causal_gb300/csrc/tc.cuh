@@ -119,6 +119,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// One probe of phase `parity` of `bar` (try_wait without a suspend-time hint: the thread
+// may wait in hardware for a short, implementation-defined time; measured faster to
+// resume than with a 1 us hint when the phase completes).
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(su32(bar)), "r"(parity));
+  return done != 0;
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;"); }
 // Make generic-proxy shared-memory writes (st.shared, cp.async) visible to tcgen05.mma.

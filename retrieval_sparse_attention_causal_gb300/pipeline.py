@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (CHUNK, Workspace, gca_backward, gca_forward, retrieve_topk, scores_backward)
+from . import CHUNK, default_workspace, gca_backward, gca_forward, retrieve_topk, scores_backward
 
 
 def landmark_view(o: torch.Tensor) -> torch.Tensor:
@@ -30,7 +30,7 @@ def landmark_view(o: torch.Tensor) -> torch.Tensor:
 
 def train_step(q, k, v, q_lmk, k_lmk, dout, topk=8, seed=0, group=0, use_gumbel=True, ws=None):
     """One retrieval group, forward and backward.  Returns a dict of every result."""
-    ws = ws or Workspace(q.device)
+    ws = ws or default_workspace(q.device)
     idx, scores = retrieve_topk(q_lmk, k_lmk, topk, 0, use_gumbel, seed, group, ws=ws)
     o, lse = gca_forward(q, k, v, idx, scores, shift=1, ws=ws)
     dq, dk, dv, ds = gca_backward(q, k, v, idx, scores, dout, lse, shift=1, ws=ws)
@@ -43,7 +43,7 @@ def train_step_two_groups(q1, q2, k, v, q1_lmk, k1_lmk, k2_lmk, dout1, dout2, to
                           use_gumbel=True, ws=None, dout1_work=None):
     """Two retrieval groups sharing K/V.  `dout1_work` (optional) is a scratch tensor
     like dout1 that receives dout1 plus group 2's landmark gradient."""
-    ws = ws or Workspace(q1.device)
+    ws = ws or default_workspace(q1.device)
     idx1, s1 = retrieve_topk(q1_lmk, k1_lmk, topk, 0, use_gumbel, seed, 0, ws=ws)
     o1, lse1 = gca_forward(q1, k, v, idx1, s1, shift=1, ws=ws)
     q2_lmk = landmark_view(o1)
@@ -64,7 +64,7 @@ def train_step_two_groups(q1, q2, k, v, q1_lmk, k1_lmk, k2_lmk, dout1, dout2, to
 
 
 def prefill(q, k, v, q_lmk, k_lmk, topk=8, ws=None):
-    ws = ws or Workspace(q.device)
+    ws = ws or default_workspace(q.device)
     idx, scores = retrieve_topk(q_lmk, k_lmk, topk, 0, False, ws=ws)
     o, lse = gca_forward(q, k, v, idx, scores, shift=1, ws=ws)
     return dict(idx=idx, scores=scores, o=o, lse=lse)
@@ -73,7 +73,7 @@ def prefill(q, k, v, q_lmk, k_lmk, topk=8, ws=None):
 def decode(q_new, k_store, v_store, q_lmk_new, k_lmk_store, topk=8, kv_shared=False, ws=None):
     """q_new [B, 64, H, dh]: the new chunk's queries; q_lmk_new [B, 1, D]; k_lmk_store
     [B, nC, D]; k_store/v_store [B, nC*64, H, dh] (or [nC*64, H, dh] when kv_shared)."""
-    ws = ws or Workspace(q_new.device)
+    ws = ws or default_workspace(q_new.device)
     nC = k_lmk_store.shape[1]
     idx, scores = retrieve_topk(q_lmk_new, k_lmk_store, topk, nC, False, ws=ws)
     o, lse = gca_forward(q_new, k_store, v_store, idx, scores, shift=0, kv_shared=kv_shared, ws=ws)
