@@ -246,7 +246,7 @@ extern "C" gca_status gca_forward(const void* q, const void* k, const void* v, i
 // ==================================================================== GCA backward
 namespace {
 struct BwdLayout {
-  size_t D, dwp, off, ent, cur, total;
+  size_t D, dwp, off, ent, cur, wrow, total;
 };
 BwdLayout bwd_layout(int B, int nQ, int nC, int H, int topk) {
   BwdLayout L{};
@@ -256,6 +256,7 @@ BwdLayout bwd_layout(int B, int nQ, int nC, int H, int topk) {
   L.off = p; p += align256((size_t)B * (nC + 1) * 4);
   L.ent = p; p += align256((size_t)B * nQ * topk * 4);
   L.cur = p; p += align256((size_t)B * nC * 4);
+  L.wrow = p; p += align256((size_t)B * nQ * topk * 4);
   L.total = p;
   return L;
 }
@@ -291,6 +292,7 @@ extern "C" gca_status gca_backward(const void* q, const void* k, const void* v, 
   a.csr_off = reinterpret_cast<int32_t*>(w + L.off);
   a.csr_ent = reinterpret_cast<int32_t*>(w + L.ent);
   a.csr_cur = reinterpret_cast<int32_t*>(w + L.cur);
+  a.wrow = reinterpret_cast<float*>(w + L.wrow);
   cudaError_t e = launch_backward(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gca_backward launch");
   return GCA_OK;

@@ -175,6 +175,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         M.j[lane] = -1;
       }
       __syncwarp();
+      // The key side takes every consumer's fusion weight from this table (one head writes it).
+      if (r >= 0 && (t / a.nQ) % a.H == 0 && lane < a.topk) a.wrow[((int64_t)b * a.nQ + r) * a.topk + lane] = M.w[lane];
       if (lane == 0) {
         int n = 0;
         for (int m = 0; m < a.topk; ++m)
@@ -457,28 +459,6 @@ constexpr int kKVStageBytes = 2 * TILE + 1024;  // Q, dO tiles + LSE and D rows 
 constexpr int kKVSmem = TILE * 2 + kKVStages * kKVStageBytes + 1024;  // K, V, ring
 constexpr int kConsTab = 256;
 
-// Fusion weight w_m of slot m of retrieval row r (softmax over the row's valid slots),
-// computed by one thread.
-__device__ __forceinline__ float slot_weight_thread(const BwdArgs& a, int b, int r, int m) {
-  const int32_t* idx_row = a.idx + ((int64_t)b * a.nQ + r) * a.topk;
-  const float* sc_row = a.scores + ((int64_t)b * a.nQ + r) * a.topk;
-  float mx = -CUDART_INF_F;
-  for (int t = 0; t < a.topk; ++t) {
-    const int jj = idx_row[t];
-    if (jj >= 0 && jj < a.nC) mx = fmaxf(mx, sc_row[t]);
-  }
-  float sum = 0.f, mine = 0.f;
-  for (int t = 0; t < a.topk; ++t) {
-    const int jj = idx_row[t];
-    if (jj >= 0 && jj < a.nC) {
-      const float e = expf(sc_row[t] - mx);
-      sum += e;
-      if (t == m) mine = e;
-    }
-  }
-  return sum > 0.f ? mine / sum : 0.f;
-}
-
 __global__ void __launch_bounds__(kThreads, 2)
 gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -502,6 +482,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
   const int e0 = a.csr_off[(int64_t)b * (a.nC + 1) + j];
   const int e1 = a.csr_off[(int64_t)b * (a.nC + 1) + j + 1];
   const int32_t* ent = a.csr_ent + (int64_t)b * a.nQ * a.topk;
+  const float* wrow = a.wrow + (int64_t)b * a.nQ * a.topk;
   bf16* dkg = reinterpret_cast<bf16*>(a.dk) + ktok0;
   bf16* dvg = reinterpret_cast<bf16*>(a.dv) + ktok0;
   const int ncons = e1 - e0;
@@ -515,12 +496,25 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     }
     return;
   }
-  if (tid == 0) {
+  if (warp == kCtl && lane == 0) {
     tc::mbar_init(&bar_k, 1);
     for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_c[st], 1);
     tc::mbar_init(&bar_s, 1);
     tc::mbar_init(&bar_o, 1);
     tc::fence_mbar_init();
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmdO);
+    // K and V of this chunk first: they do not depend on the consumer table.
+    tc::mbar_expect_tx(&bar_k, 2 * TILE);
+    tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, b, &bar_k);
+    tc::tma_load_4d(Vs, &tmV, 0, h, j * 64, b, &bar_k);
+  }
+  if (warp == kCtl) {  // consumer table: entries and fusion weights (from the query side)
+    for (int x = lane; x < ncons && x < kConsTab; x += 32) {
+      const int e = ent[e0 + x];
+      etab[x] = e;
+      wtab[x] = wrow[e];
+    }
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
   tc::fence_before();
@@ -531,20 +525,12 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
   if (warp == kCtl) {
     // ------------------------------------------------------------ control warp
     bool ok = true;
-    // Consumer table: entry and fusion weight of every consumer (the first kConsTab in
-    // shared memory, computed here once; later ones on demand).
-    for (int x = lane; x < ncons && x < kConsTab; x += 32) {
-      const int e = ent[e0 + x];
-      etab[x] = e;
-      wtab[x] = slot_weight_thread(a, b, e / a.topk, e % a.topk);
-    }
-    __syncwarp();
     auto load_cons = [&](int x) {  // lane 0: consumer x's Q, dO tiles, LSE and D rows
       const int st = x % NST;
       const int e = x < kConsTab ? etab[x] : ent[e0 + x];
       const int r = e / a.topk, m = e % a.topk;
       const int c = r + a.shift;
-      w_st[st] = x < kConsTab ? wtab[x] : slot_weight_thread(a, b, r, m);
+      w_st[st] = x < kConsTab ? wtab[x] : wrow[e];
       unsigned char* base = ring + st * kKVStageBytes;
       const int64_t rb = ((((int64_t)b * a.nQ + c) * a.H + h) * a.topk + m) * 64;
       tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
@@ -566,12 +552,8 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       }
       tc::commit_warp(&bar_s);
     };
-    if (lane == 0) {
-      tc::mbar_expect_tx(&bar_k, 2 * TILE);
-      tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, b, &bar_k);
-      tc::tma_load_4d(Vs, &tmV, 0, h, j * 64, b, &bar_k);
+    if (lane == 0)
       for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
-    }
     __syncwarp();
     ok = tc::mbar_wait(&bar_k, 0) && ok;
     ok = tc::mbar_wait(&bar_c[0], 0) && ok;

@@ -70,6 +70,7 @@ struct BwdArgs {
   int32_t* csr_off; // [B][nC+1]
   int32_t* csr_ent; // [B][nQ*topk]
   int32_t* csr_cur; // [B][nC]
+  float* wrow;      // [B][nQ][topk] fusion weight of every slot (written by the tensor-core query side)
 };
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s);
 // Tensor-core (tcgen05) query-side and key-side passes, bf16 with dh = 64 (gca_bwd_tc.cu).

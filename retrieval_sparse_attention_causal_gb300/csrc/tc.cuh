@@ -103,17 +103,17 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;"); }
 
 // Bounded wait for phase `parity` of `bar`.  Each try_wait may suspend the thread in
-// hardware (hint: 1 us) until the phase completes, so a waiting thread does not keep
-// re-issuing shared-memory requests.  Returns false if the limit ran out (the caller
-// records the timeout and carries on, so that nothing hangs).
+// hardware for a short, implementation-defined time until the phase completes, so a
+// waiting thread does not keep re-issuing shared-memory requests.  Returns false if the
+// limit ran out (the caller records the timeout and carries on, so that nothing hangs).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = 1u << 21) {
   uint32_t done = 0;
   for (uint32_t it = 0; it < limit; ++it) {
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(su32(bar)), "r"(parity), "r"(1000u));
+        : "r"(su32(bar)), "r"(parity));
     if (done) return true;
   }
   return false;
