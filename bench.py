@@ -151,9 +151,13 @@ KERNEL_SOURCES = {
     "gca_bwd_kv": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh"),
     "retrieve_stream": ("retrieve.cu", "common.cuh"),
 }
-KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture)
+KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
+    "gca_fwd": (382.8e6, "55be0ffd024a817d"),
+    "gca_bwd_q": (514.6e6, "dcb2b906194b5e0b"),
+    "gca_bwd_kv": (606.5e6, "dcb2b906194b5e0b"),
 }
-STREAM_TRAFFIC_PER_SEQ = (808.6e6 / 2, "2e400421debd867c")  # profiles/retrieve_stream_decode_16m.md, B = 2
+# profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
+STREAM_TRAFFIC_PER_SEQ = (808.35e6 / 2, "74df39448ea668d2")
 
 
 def source_fingerprint(kernel: str) -> str:

@@ -160,6 +160,18 @@ __device__ __forceinline__ void st16x128_x4(uint32_t taddr, const uint32_t (&v)[
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
+// 16 lanes x 8 columns (registers 0-3 as in the x4 form, columns 0-7).
+__device__ __forceinline__ void st16x128_x2(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+// Wait for outstanding tcgen05.ld, tied to 8 loaded registers.
+__device__ __forceinline__ void ld_wait(float (&v)[2][4]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0][0]), "+f"(v[0][1]), "+f"(v[0][2]), "+f"(v[0][3]), "+f"(v[1][0]), "+f"(v[1][1]),
+                 "+f"(v[1][2]), "+f"(v[1][3]));
+}
 __device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Wait for outstanding tcgen05.ld and tie the 32 loaded registers to the wait, so that
 // the compiler cannot move a use of them above it.
