@@ -438,6 +438,9 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
     nbytes = nb * DEC_NC * D * 2
     rows_ms = prof["retrieve_stream"][1] / prof["retrieve_stream"][0]
     ach = nbytes / (rows_ms / 1e3) / 1e9
+    offload = None
+    if not args.no_offload:
+        offload = offload_leg(args, torch, gca, kst, vst, qn, ql, kl, ws, o, lse, idx, sc, time_loop)
     del kst, vst
     return {"metric": "landmark top-k GB/s at 16M ctx", "value": round(nbytes * world / (ms_r / 1e3) / 1e9, 1),
             "unit": "GB/s", "batch": nb, "past_chunks": DEC_NC, "landmark_dim": D, "ms_per_retrieval": round(ms_r, 4),
@@ -446,7 +449,46 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                          "traffic": stream_traffic(nb), "peak_source": f"{src} copy bandwidth",
                          "bytes_per_launch": nbytes},
-            "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}}
+            "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "offload": offload}
+
+
+def offload_leg(args, torch, gca, kst, vst, qn, ql, kl, ws, o, lse, idx, sc, time_loop):
+    """Decode with the K/V store in pinned host memory (the inference offload): the same
+    store as the device-resident decode copied to a pinned host buffer (2 x 25.8 GB, shared
+    by the batch), then per step retrieval over the device landmarks, a GPU gather of the 8
+    retrieved chunks per sequence from host memory, and the forward on the compact buffer.
+    The output must equal the device-resident decode's bit for bit."""
+    nb = qn.shape[0]
+    kh = torch.empty(kst.shape, dtype=kst.dtype, pin_memory=True)
+    vh = torch.empty(vst.shape, dtype=vst.dtype, pin_memory=True)
+    kh.copy_(kst)
+    vh.copy_(vst)
+    torch.cuda.synchronize()
+    kd = torch.empty((nb, K * 64, H, DH), dtype=kst.dtype, device="cuda")
+    vd = torch.empty_like(kd)
+    il = torch.empty_like(idx)
+    o2 = torch.empty_like(o)
+    lse2 = torch.empty_like(lse)
+
+    def gather(i):
+        gca.gather_chunks(kh, vh, idx, kv_shared=True, ws=ws, k_dst=kd, v_dst=vd, idx_local=il)
+
+    def step(i):
+        gca.retrieve_topk(ql, kl, K, DEC_NC, False, ws=ws, idx=idx, scores=sc)
+        gather(i)
+        gca.gca_forward(qn, kd, vd, il, sc, shift=0, ws=ws, out=o2, lse=lse2)
+
+    for i in range(args.warmup):
+        step(i)
+    ws.check()
+    same = bool(torch.equal(o, o2) and torch.equal(lse, lse2))
+    ms_g = time_loop(gather, args.steps)
+    ms_s = time_loop(step, args.steps)
+    gbytes = nb * K * 2 * 64 * H * DH * 2  # K and V of the retrieved chunks
+    del kh, vh
+    return {"host_store_GB": round(2 * kst.numel() * kst.element_size() / 1e9, 1), "ms_per_decode_chunk": round(ms_s, 4),
+            "gather_ms": round(ms_g, 4), "gather_bytes": gbytes, "gather_GBps": round(gbytes / (ms_g / 1e3) / 1e9, 1),
+            "equals_device_decode": same}
 
 
 def decode_retrieval_only(args):
@@ -546,6 +588,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--decode-batch", type=int, default=DEC_B)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-offload", action="store_true", help="skip the host-memory K/V store decode")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -161,6 +161,32 @@ GCA_API gca_status gca_forward(const void* q, const void* k, const void* v, int6
                        void* o, float* lse, void* ws, size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * gca_gather_chunks - copy the retrieved chunks' keys and values into a compact buffer.
+ *
+ * Paper-Notes page, 关键设计 / key design (inference memory offload): the past chunks'
+ * K/V may live in host memory; only the k retrieved chunks are brought to the GPU.  The
+ * copy is a GPU kernel driven by the device-side idx, so nothing returns to the host.
+ * For each (b, r, m) with j = idx[b,r,m] in [0, nC): chunk j of the store (64 tokens x H
+ * x dh of K and of V) goes to slot s = r*topk + m of the destination, and
+ * idx_local[b,r,m] = s; other slots get idx_local = -1 and are left untouched.
+ * gca_forward(q, k_dst, v_dst, kv_batch_stride = nQ*topk*64*H*dh, nC' = nQ*topk,
+ * idx_local, scores, ...) then gives the same result as on the full store.
+ *
+ *   k_src, v_src [B][nC*64][H][dh] (src_batch_stride elements between sequences, 0 = one
+ *           store shared by all).  Any memory the device can read: device memory, or
+ *           pinned host memory (read directly by the GPU over its host link).
+ *   k_dst, v_dst [B][nQ*topk*64][H][dh] device memory.   idx, idx_local [B][nQ][topk].
+ *   dtype   GCA_F32 or GCA_BF16.   dh 32 or 64.   topk 1..16.   Pointers 16-byte aligned.
+ *   ws      >= gca_gather_workspace_size() bytes (error word only); idx outside [-1, nC)
+ *           is flagged there (GCA_ERR_DEVICE_INDEX) and treated as -1.
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_gather_workspace_size(void);
+GCA_API gca_status gca_gather_chunks(const void* k_src, const void* v_src, int64_t src_batch_stride,
+                             gca_dtype dtype, int B, int nQ, int nC, int H, int dh,
+                             const int32_t* idx, int topk, void* k_dst, void* v_dst,
+                             int32_t* idx_local, void* ws, size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * gca_backward - gradients of gca_forward: dQ, dK, dV and the retrieval scores.
  *
  * The score gradient is what lets the retriever learn from the language-model loss

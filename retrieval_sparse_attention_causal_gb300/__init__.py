@@ -49,6 +49,8 @@ def _load():
         "gca_retrieve_topk_noalloc": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P]),
         "gca_forward_workspace_size": (SZ, []),
         "gca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, P, I, I, P, P, P, SZ, P]),
+        "gca_gather_workspace_size": (SZ, []),
+        "gca_gather_chunks": (I, [P, P, I64, I, I, I, I, I, I, P, I, P, P, P, P, SZ, P]),
         "gca_backward_workspace_size": (SZ, [I, I, I, I, I]),
         "gca_backward": (I, [P, P, P, I, I, I, I, I, I, P, P, I, I, P, P, P, P, P, P, I, P, SZ, P]),
         "gca_scores_backward_workspace_size": (SZ, [I, I, I, I]),
@@ -71,7 +73,8 @@ LIB = _load()
 EXPORTS = (
     "gca_status_string", "gca_last_error_detail", "gca_retrieve_workspace_size", "gca_retrieve_topk",
     "gca_retrieve_noalloc_max_scratch", "gca_retrieve_topk_noalloc",
-    "gca_forward_workspace_size", "gca_forward", "gca_backward_workspace_size", "gca_backward",
+    "gca_forward_workspace_size", "gca_forward", "gca_gather_workspace_size", "gca_gather_chunks",
+    "gca_backward_workspace_size", "gca_backward",
     "gca_scores_backward_workspace_size", "gca_scores_backward", "gca_check_error", "gca_launch_count",
     "gca_profile_begin", "gca_profile_end", "gca_profile_row",
 )
@@ -211,6 +214,43 @@ def gca_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Te
     _check(LIB.gca_forward(_ptr(q), _ptr(k), _ptr(v), kv_bs, _dtype(q), B, nQ, nC, H, dh, _ptr(idx),
                            _ptr(scores), topk, shift, _ptr(out), _ptr(lse), _ptr(buf), buf.numel(), _stream()))
     return out, lse
+
+
+def gather_chunks(k_src: torch.Tensor, v_src: torch.Tensor, idx: torch.Tensor, kv_shared: bool = False,
+                  ws: Workspace = None, k_dst: torch.Tensor = None, v_dst: torch.Tensor = None,
+                  idx_local: torch.Tensor = None):
+    """Copy the retrieved chunks' K/V into a compact device buffer (gca_gather_chunks).
+    k_src, v_src: the store, [B, nC*64, H, dh] (or [nC*64, H, dh] shared by all sequences
+    when kv_shared), on the GPU or in pinned host memory (read by the GPU directly).
+    idx [B, nQ, topk] on the GPU.  Returns k_dst, v_dst [B, nQ*topk*64, H, dh] and
+    idx_local [B, nQ, topk] for gca_forward on the compact buffer."""
+    _cuda(idx)
+    for t in (k_src, v_src):
+        _need(t.is_cuda or t.is_pinned(), "the K/V store must be on the GPU or in pinned host memory")
+        _need(t.is_contiguous(), "the K/V store must be contiguous")
+    _need(k_src.shape == v_src.shape and k_src.dtype == v_src.dtype, "k/v store shape or dtype mismatch")
+    B, nQ, topk = idx.shape
+    _need(idx.dtype == torch.int32 and idx.is_contiguous(), "idx must be int32 [B, nQ, topk]")
+    if kv_shared:
+        _need(k_src.dim() == 3, "a shared store is [nC*64, H, dh]")
+        nC, (H, dh), src_bs = k_src.shape[0] // CHUNK, k_src.shape[1:], 0
+    else:
+        _need(k_src.dim() == 4 and k_src.shape[0] == B, "the store must be [B, nC*64, H, dh]")
+        nC, (H, dh), src_bs = k_src.shape[1] // CHUNK, k_src.shape[2:], k_src.stride(0)
+    shape = (B, nQ * topk * CHUNK, H, dh)
+    if k_dst is None:
+        k_dst = torch.empty(shape, dtype=k_src.dtype, device=idx.device)
+    if v_dst is None:
+        v_dst = torch.empty(shape, dtype=k_src.dtype, device=idx.device)
+    _need(tuple(k_dst.shape) == shape and tuple(v_dst.shape) == shape, "destination must be [B, nQ*topk*64, H, dh]")
+    if idx_local is None:
+        idx_local = torch.empty_like(idx)
+    ws = ws or default_workspace(idx.device)
+    buf = ws.get(LIB.gca_gather_workspace_size())
+    _check(LIB.gca_gather_chunks(_ptr(k_src), _ptr(v_src), src_bs, _dtype(k_src), B, nQ, nC, H, dh, _ptr(idx),
+                                 topk, _ptr(k_dst), _ptr(v_dst), _ptr(idx_local), _ptr(buf), buf.numel(),
+                                 _stream()))
+    return k_dst, v_dst, idx_local
 
 
 # --------------------------------------------------------------------------- backward

@@ -243,6 +243,37 @@ extern "C" gca_status gca_forward(const void* q, const void* k, const void* v, i
   return GCA_OK;
 }
 
+// ==================================================================== chunk gather
+extern "C" size_t gca_gather_workspace_size(void) { return kErrBytes; }
+
+extern "C" gca_status gca_gather_chunks(const void* k_src, const void* v_src, int64_t src_batch_stride,
+                                        gca_dtype dtype, int B, int nQ, int nC, int H, int dh,
+                                        const int32_t* idx, int topk, void* k_dst, void* v_dst,
+                                        int32_t* idx_local, void* ws, size_t ws_bytes, gca_stream_t stream) {
+  if (dtype != GCA_F32 && dtype != GCA_BF16) return fail(GCA_ERR_INVALID_ARG, "dtype must be GCA_F32 or GCA_BF16");
+  if (B < 1 || nQ < 1 || nC < 1 || H < 1) return fail(GCA_ERR_INVALID_ARG, "B, nQ, nC, H must be >= 1");
+  if (topk < 1 || topk > kMaxTopk) return fail(GCA_ERR_UNSUPPORTED, "topk must be in 1..%d", kMaxTopk);
+  if (dh != 32 && dh != 64) return fail(GCA_ERR_UNSUPPORTED, "dh must be 32 or 64");
+  if (!k_src || !v_src || !idx || !k_dst || !v_dst || !idx_local)
+    return fail(GCA_ERR_INVALID_ARG, "a pointer is NULL");
+  if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(k_dst) || !aligned16(v_dst))
+    return fail(GCA_ERR_INVALID_ARG, "k/v source and destination must be 16-byte aligned");
+  const int64_t per_seq = (int64_t)nC * 64 * H * dh;
+  if (src_batch_stride != 0 && (src_batch_stride < per_seq || src_batch_stride % 8))
+    return fail(GCA_ERR_INVALID_ARG, "src_batch_stride must be 0 or >= nC*64*H*dh and a multiple of 8");
+  if ((int64_t)nQ * topk > 65535 || B > 65535) return fail(GCA_ERR_UNSUPPORTED, "nQ*topk and B must be <= 65535");
+  gca_status st;
+  if ((st = check_ws(ws, ws_bytes, gca_gather_workspace_size())) != GCA_OK) return st;
+  GatherArgs a{};
+  a.k_src = k_src; a.v_src = v_src; a.src_bs = src_batch_stride;
+  a.esize = dtype == GCA_BF16 ? 2 : 4; a.B = B; a.nQ = nQ; a.nC = nC; a.H = H; a.dh = dh; a.topk = topk;
+  a.idx = idx; a.k_dst = k_dst; a.v_dst = v_dst; a.idx_local = idx_local;
+  a.err = reinterpret_cast<ErrWord*>(ws);
+  cudaError_t e = launch_gather(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gca_gather_chunks launch");
+  return GCA_OK;
+}
+
 // ==================================================================== GCA backward
 namespace {
 struct BwdLayout {

@@ -57,6 +57,17 @@ struct FwdArgs {
 };
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 
+// ---- gather of retrieved chunks into a compact buffer (gather.cu)
+struct GatherArgs {
+  const void* k_src; const void* v_src; int64_t src_bs;  // store [B][nC*64][H][dh]; batch stride in elements
+  int esize, B, nQ, nC, H, dh, topk;
+  const int32_t* idx;                                    // [B][nQ][topk]
+  void* k_dst; void* v_dst;                              // [B][nQ*topk*64][H][dh]
+  int32_t* idx_local;                                    // [B][nQ][topk]: slot index r*topk+m, or -1
+  ErrWord* err;
+};
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
 // ---- GCA backward (gca_bwd.cu)
 struct BwdArgs {
   const void* q; const void* k; const void* v;

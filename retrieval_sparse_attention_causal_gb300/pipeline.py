@@ -19,7 +19,8 @@ from __future__ import annotations
 
 import torch
 
-from . import CHUNK, default_workspace, gca_backward, gca_forward, retrieve_topk, scores_backward
+from . import (CHUNK, default_workspace, gather_chunks, gca_backward, gca_forward, retrieve_topk,
+               scores_backward)
 
 
 def landmark_view(o: torch.Tensor) -> torch.Tensor:
@@ -78,3 +79,18 @@ def decode(q_new, k_store, v_store, q_lmk_new, k_lmk_store, topk=8, kv_shared=Fa
     idx, scores = retrieve_topk(q_lmk_new, k_lmk_store, topk, nC, False, ws=ws)
     o, lse = gca_forward(q_new, k_store, v_store, idx, scores, shift=0, kv_shared=kv_shared, ws=ws)
     return dict(idx=idx, scores=scores, o=o, lse=lse)
+
+
+def decode_offload(q_new, k_host, v_host, q_lmk_new, k_lmk_store, topk=8, kv_shared=False, ws=None, bufs=None):
+    """Decode with the K/V store in pinned host memory (the inference offload of the Paper-Notes
+    page, 关键设计 / key design): retrieval over the device-resident landmarks, a GPU gather of
+    the k retrieved chunks from host memory into a compact device buffer, then the GCA forward
+    on that buffer.  Same arguments as decode(), with k_host / v_host pinned host tensors;
+    bufs = (k_dst, v_dst, idx_local) may be passed to reuse the compact buffers."""
+    ws = ws or default_workspace(q_new.device)
+    nC = k_lmk_store.shape[1]
+    idx, scores = retrieve_topk(q_lmk_new, k_lmk_store, topk, nC, False, ws=ws)
+    kd, vd, il = bufs if bufs is not None else (None, None, None)
+    kd, vd, il = gather_chunks(k_host, v_host, idx, kv_shared=kv_shared, ws=ws, k_dst=kd, v_dst=vd, idx_local=il)
+    o, lse = gca_forward(q_new, kd, vd, il, scores, shift=0, ws=ws)
+    return dict(idx=idx, scores=scores, o=o, lse=lse, idx_local=il)

@@ -103,6 +103,28 @@ def test_forward_rejects_bad_arguments(gca):
     assert b"shift" in (_fwd(gca, shift=-1) == gca.GCA_ERR_INVALID_ARG and gca.LIB.gca_last_error_detail())
 
 
+def _gather(gca, **kw):
+    a = dict(k=FAKE, v=FAKE, sbs=0, dt=gca.GCA_BF16, B=16, nQ=1, nC=262144, H=12, dh=64, idx=FAKE, topk=8,
+             kd=FAKE, vd=FAKE, il=FAKE, ws=FAKE, wsb=256)
+    a.update(kw)
+    return gca.LIB.gca_gather_chunks(a["k"], a["v"], a["sbs"], a["dt"], a["B"], a["nQ"], a["nC"], a["H"], a["dh"],
+                                     a["idx"], a["topk"], a["kd"], a["vd"], a["il"], a["ws"], a["wsb"], None)
+
+
+def test_gather_rejects_bad_arguments(gca):
+    assert gca.LIB.gca_gather_workspace_size() == 256
+    assert _gather(gca, k=0) == gca.GCA_ERR_INVALID_ARG
+    assert _gather(gca, il=0) == gca.GCA_ERR_INVALID_ARG
+    assert _gather(gca, v=FAKE + 8) == gca.GCA_ERR_INVALID_ARG
+    assert _gather(gca, dh=128) == gca.GCA_ERR_UNSUPPORTED
+    assert _gather(gca, topk=17) == gca.GCA_ERR_UNSUPPORTED
+    assert _gather(gca, dt=3) == gca.GCA_ERR_INVALID_ARG
+    assert _gather(gca, B=0) == gca.GCA_ERR_INVALID_ARG
+    assert _gather(gca, sbs=100) == gca.GCA_ERR_INVALID_ARG
+    assert _gather(gca, wsb=100) == gca.GCA_ERR_WORKSPACE
+    assert b"workspace" in gca.LIB.gca_last_error_detail()
+
+
 def test_backward_and_scores_backward_reject_bad_arguments(gca):
     L = gca.LIB
     r = L.gca_backward(FAKE, FAKE, FAKE, gca.GCA_BF16, 4, 256, 256, 12, 64, FAKE, FAKE, 8, 1, FAKE, FAKE,
