@@ -25,6 +25,14 @@ What is computed (the definition, written out directly):
   * backward: the chain rule of that definition (dQ, dK, dV, dscores), and the
     gradient of the scaled dot-product scores into both landmark sets.
 
+Also, for the rest of the attention block and the ablation (Notes, training strategy:
+sliding-window self-attention W = 512 beside the top-k retrieval; key design / GCA: the
+chunked cross-attention (CCA) it is contrasted with):
+  * sliding-window causal self-attention: token t attends to tokens t - W + 1 .. t of its
+    own sequence with one softmax, scaled by dh^-1/2;
+  * CCA: the tokens of a query chunk attend to the concatenation of its retrieved chunks
+    with one joint softmax; the retrieval scores take no part.
+
 Readings where the pages are silent (each also listed in the design notes):
   * the next-chunk rule is a shift: query chunk c uses retrieval row c - shift
     (shift = 1 in training, 0 at decode); chunks with no row get O = 0;
@@ -230,6 +238,69 @@ def gca_forward(q, kv_k, kv_v, idx, scores, shift=1, chunk=CHUNK, chunks=None):
             continue
         oc, lc, _ = gca_chunk_forward(q[b, c * chunk:(c + 1) * chunk], kv_k[b], kv_v[b],
                                       idx[b, r], scores[b, r], chunk)
+        o[b, c * chunk:(c + 1) * chunk] = oc
+        lse[b, c] = lc
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window self-attention and CCA (one joint softmax)
+# ---------------------------------------------------------------------------
+
+def swa_forward(q, k, v, window, rows=None):
+    """Sliding-window causal self-attention (Notes, training strategy: W = 512).
+
+    q, k, v [B, L, H, dh] of one sequence each; token t attends to the keys of tokens
+    max(0, t - window + 1) .. t with one softmax of the dh^-1/2-scaled logits.
+    Returns O like q and LSE [B, L, H] (natural log).  `rows` optionally restricts the
+    work to a list of (b, t) pairs (other entries stay zero / -inf).
+    """
+    B, L, H, dh = q.shape
+    o = np.zeros((B, L, H, dh))
+    lse = np.full((B, L, H), -np.inf)
+    pairs = rows if rows is not None else [(b, t) for b in range(B) for t in range(L)]
+    for b, t in pairs:
+        s0 = max(0, t - window + 1)
+        Kh = k[b, s0:t + 1].transpose(1, 0, 2)  # [H, n, dh]
+        Vh = v[b, s0:t + 1].transpose(1, 0, 2)
+        qh = q[b, t][:, None, :]  # [H, 1, dh]
+        S = qh @ Kh.transpose(0, 2, 1) / math.sqrt(dh)  # [H, 1, n]
+        P, l = _softmax_rows(S)
+        o[b, t] = (P @ Vh)[:, 0, :]
+        lse[b, t] = l[:, 0]
+    return o, lse
+
+
+def cca_chunk_forward(qc, kv_k, kv_v, idx_row, chunk=CHUNK):
+    """Chunked cross-attention for one query chunk (Notes, key design / GCA, the variant
+    GCA is contrasted with): the retrieved chunks' keys and values are concatenated (slot
+    order) and attended with one softmax; the retrieval scores are not used.
+    Returns O [S, H, dh] (zero without a valid slot) and LSE [H, S] (-inf then)."""
+    S_, H, dh = qc.shape
+    js = [int(j) for j in idx_row if j >= 0]
+    if not js:
+        return np.zeros((S_, H, dh)), np.full((H, S_), -np.inf)
+    Kc = np.concatenate([kv_k[j * chunk:(j + 1) * chunk] for j in js]).transpose(1, 0, 2)
+    Vc = np.concatenate([kv_v[j * chunk:(j + 1) * chunk] for j in js]).transpose(1, 0, 2)
+    Qh = qc.transpose(1, 0, 2)
+    S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S, n*S]
+    P, l = _softmax_rows(S)
+    return (P @ Vc).transpose(1, 0, 2), l
+
+
+def cca_forward(q, kv_k, kv_v, idx, shift=1, chunk=CHUNK, chunks=None):
+    """CCA over all query chunks; query chunk c uses retrieval row c - shift (as GCA).
+    Returns O like q and LSE [B, nQ, H, S]."""
+    B, L, H, dh = q.shape
+    nQ = L // chunk
+    o = np.zeros_like(q, dtype=np.float64)
+    lse = np.full((B, nQ, H, chunk), -np.inf)
+    pairs = chunks if chunks is not None else [(b, c) for b in range(B) for c in range(nQ)]
+    for b, c in pairs:
+        r = c - shift
+        if r < 0:
+            continue
+        oc, lc = cca_chunk_forward(q[b, c * chunk:(c + 1) * chunk], kv_k[b], kv_v[b], idx[b, r], chunk)
         o[b, c * chunk:(c + 1) * chunk] = oc
         lse[b, c] = lc
     return o, lse

@@ -422,4 +422,105 @@ def pin_two_group_finite_differences(orc):
         _close(g[key], _fd(loss, p[name]))
 
 
+# ----------------------------------------------------------- window attention and CCA
+
+def pin_swa_wide_window_is_causal_sdpa(orc):
+    """A window of at least L tokens is plain causal attention: torch's float64
+    scaled_dot_product_attention with is_causal, and its LSE."""
+    import torch
+    rng = np.random.default_rng(31)
+    B, L, H, dh = 1, 40, 2, 8
+    q, k, v = (rng.standard_normal((B, L, H, dh)) for _ in range(3))
+    o, lse = orc.swa_forward(q, k, v, window=L + 7)
+    Q, K, V = (torch.from_numpy(x[0]).permute(1, 0, 2) for x in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True).permute(1, 0, 2).numpy()
+    assert np.max(np.abs(o[0] - ref)) < 1e-12
+    logits = Q @ K.transpose(1, 2) / math.sqrt(dh)
+    logits = logits.masked_fill(torch.triu(torch.ones(L, L, dtype=torch.bool), 1), float("-inf"))
+    assert np.max(np.abs(lse[0] - torch.logsumexp(logits, -1).numpy().T)) < 1e-12
+
+
+def pin_swa_window_brute_force(orc):
+    """Window 5 by brute force: per token, the softmax over exactly the last 5 keys
+    (fewer at the start), written out with explicit sums."""
+    rng = np.random.default_rng(32)
+    B, L, H, dh, W = 2, 13, 2, 4, 5
+    q, k, v = (rng.standard_normal((B, L, H, dh)) for _ in range(3))
+    o, lse = orc.swa_forward(q, k, v, window=W)
+    for b in range(B):
+        for t in range(L):
+            for h in range(H):
+                keys = list(range(max(0, t - W + 1), t + 1))
+                z = [sum(q[b, t, h, d] * k[b, s, h, d] for d in range(dh)) / math.sqrt(dh) for s in keys]
+                mx = max(z)
+                e = [math.exp(x - mx) for x in z]
+                den = sum(e)
+                for d in range(dh):
+                    want = sum(e[i] * v[b, s, h, d] for i, s in enumerate(keys)) / den
+                    assert abs(o[b, t, h, d] - want) < 1e-12
+                assert abs(lse[b, t, h] - (mx + math.log(den))) < 1e-12
+
+
+def pin_swa_window_one_is_identity(orc):
+    """Window 1: each token attends only to itself, so O = V and LSE = <q, k>/sqrt(dh)."""
+    rng = np.random.default_rng(33)
+    q, k, v = (rng.standard_normal((1, 9, 3, 4)) for _ in range(3))
+    o, lse = orc.swa_forward(q, k, v, window=1)
+    assert np.max(np.abs(o - v)) < 1e-15
+    assert np.max(np.abs(lse - (q * k).sum(-1) / 2.0)) < 1e-12
+
+
+def pin_cca_single_slot_equals_gca(orc):
+    """With one valid slot, CCA and GCA coincide (one softmax over one chunk, weight 1)."""
+    rng = np.random.default_rng(34)
+    q, k, v = _rand_gca(rng, nQ=3, nC=4, chunk=64)
+    idx = np.array([[[2, -1], [0, -1], [3, -1]]], dtype=np.int32)
+    sc = np.array([[[0.3, -np.inf], [1.0, -np.inf], [-2.0, -np.inf]]])
+    og, lg = orc.gca_forward(q, k, v, idx, sc, shift=0)
+    oc, lc = orc.cca_forward(q, k, v, idx, shift=0)
+    assert np.max(np.abs(og - oc)) < 1e-13
+    assert np.max(np.abs(lg[:, :, :, 0, :] - lc)) < 1e-13
+
+
+def pin_cca_joint_softmax_brute_force(orc):
+    """Two slots: one softmax over the 2 x S concatenated keys, by brute force; slot
+    order does not matter; the LSE is the log of the joint normaliser."""
+    rng = np.random.default_rng(35)
+    S, H, dh, nC = 4, 2, 3, 5
+    q = rng.standard_normal((1, S, H, dh))
+    k = rng.standard_normal((1, nC * S, H, dh))
+    v = rng.standard_normal((1, nC * S, H, dh))
+    o, lse = orc.cca_forward(q, k, v, np.array([[[4, 1, -1]]], dtype=np.int32), shift=0, chunk=S)
+    o2, _ = orc.cca_forward(q, k, v, np.array([[[1, -1, 4]]], dtype=np.int32), shift=0, chunk=S)
+    assert np.max(np.abs(o - o2)) < 1e-13
+    keys = list(range(4 * S, 5 * S)) + list(range(1 * S, 2 * S))
+    for t in range(S):
+        for h in range(H):
+            z = [float(q[0, t, h] @ k[0, s, h]) / math.sqrt(dh) for s in keys]
+            mx = max(z)
+            e = [math.exp(x - mx) for x in z]
+            den = sum(e)
+            want = sum(e[i] * v[0, s, h] for i, s in enumerate(keys)) / den
+            assert np.max(np.abs(o[0, t, h] - want)) < 1e-12
+            assert abs(lse[0, 0, h, t] - (mx + math.log(den))) < 1e-12
+
+
+def pin_cca_no_slot_and_shift(orc):
+    """Shift 1: chunk 0 has no row and chunk 2 uses row 1, which has no valid slot; both
+    get O = 0 and LSE = -inf.  Chunk 1 uses row 0 (chunks 1 and 0)."""
+    rng = np.random.default_rng(36)
+    q, k, v = _rand_gca(rng, nQ=3, nC=3, chunk=4)
+    idx = np.array([[[1, 0], [-1, -1], [2, -1]]], dtype=np.int32)
+    o, lse = orc.cca_forward(q, k, v, idx, shift=1, chunk=4)
+    assert np.all(o[0, :4] == 0) and np.all(np.isneginf(lse[0, 0]))
+    assert np.all(o[0, 8:12] == 0) and np.all(np.isneginf(lse[0, 2]))
+    keys = np.concatenate([k[0, 4:8], k[0, 0:4]])  # chunk 1 then chunk 0
+    vals = np.concatenate([v[0, 4:8], v[0, 0:4]])
+    z = np.einsum("thd,shd->hts", q[0, 4:8], keys) / math.sqrt(q.shape[-1])
+    p = np.exp(z - z.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    assert np.max(np.abs(o[0, 4:8] - np.einsum("hts,shd->thd", p, vals))) < 1e-12
+    assert np.all(np.abs(o[0, 4:8]) > 0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -43,6 +43,12 @@ MUTATIONS = {
     "weights_not_softmax": ("e = np.exp(s - s.max())", "e = np.ones_like(s)"),
     "splitmix_shift": ("z = (z ^ (z >> np.uint64(27))) * _M2", "z = (z ^ (z >> np.uint64(28))) * _M2"),
     "chain_wrong_token": ("do1_total[:, chunk - 1::chunk] += dq2_lmk", "do1_total[:, 0::chunk] += dq2_lmk"),
+    "window_one_short": ("s0 = max(0, t - window + 1)", "s0 = max(0, t - window + 2)"),
+    "window_not_causal": ("Kh = k[b, s0:t + 1].transpose(1, 0, 2)  # [H, n, dh]",
+                          "Kh = k[b, s0:t + 2].transpose(1, 0, 2)  # [H, n, dh]"),
+    "cca_softmax_per_chunk": ("S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S, n*S]",
+                              "S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh) / len(js)  # [H, S, n*S]"),
+    "cca_drops_slot": ("js = [int(j) for j in idx_row if j >= 0]", "js = [int(j) for j in idx_row if j > 0]"),
 }
 
 
