@@ -270,6 +270,10 @@ def gpu_arm(args):
                 "peak_source": f"{src} bf16 dense (burst)", "flops_per_launch": dom_flops}
     step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
 
+    # The rest of the attention block at the same shape: sliding-window self-attention
+    # (W = 512) and, as the ablation, chunked cross-attention over the same retrieval.
+    blk = None if args.no_block else block_attn_leg(args, torch, gca, q, k, v, out, timed)
+
     # End to end through the public API from pinned host buffers.
     e2e = None
     if not args.no_e2e:
@@ -292,7 +296,7 @@ def gpu_arm(args):
             "step_tflops_algorithmic": round(step_tflops, 2),
             "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary(),
             "kernels": {n: round(x["avg_ms"], 5) for n, x in kern.items()},
-            "e2e": e2e, "decode": dec, "cpu_baseline": cpu,
+            "e2e": e2e, "decode": dec, "block_attention": blk, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -452,6 +456,40 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
             "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "offload": offload}
 
 
+def block_attn_leg(args, torch, gca, q, k, v, out, timed):
+    """Forward of the sliding-window self-attention (W = 512) beside GCA, accumulated onto
+    GCA's output as in the attention block, and of CCA (one joint softmax over the same
+    retrieved chunks), at the training shape; algorithmic flops count the unmasked
+    (query, key) pairs, 4 dh flops each (QK^T and PV)."""
+    W = 512
+    o = out["o"].clone()
+    lse_w = torch.empty((B, NC, H, 64), dtype=torch.float32, device="cuda")
+    o_c = torch.empty_like(q)
+    lse_c = torch.empty((B, NC, H, 64), dtype=torch.float32, device="cuda")
+
+    def win(i):
+        gca.window_forward(q, k, v, window=W, out=o, lse=lse_w, accumulate=True)
+
+    def cca(i):
+        gca.cca_forward(q, k, v, out["idx"], shift=1, out=o_c, lse=lse_c)
+
+    for i in range(args.warmup):
+        win(i)
+        cca(i)
+    ms_w = timed(win, args.steps) / args.steps
+    ms_c = timed(cca, args.steps) / args.steps
+    t = torch.arange(L, dtype=torch.float64)
+    pairs_w = float(torch.clamp(t + 1, max=W).sum()) * B * H
+    valid = int((out["idx"][:, : NC - 1] >= 0).sum()) * H  # rows 0..nC-2 feed chunks 1..nC-1
+    pairs_c = valid * 64 * 64
+    fl_w, fl_c = pairs_w * 4 * DH, pairs_c * 4 * DH
+    tok = B * L
+    return {"window": {"window": W, "ms": round(ms_w, 4), "tokens_per_s": round(tok / (ms_w / 1e3), 1),
+                       "tflops_algorithmic": round(fl_w / (ms_w / 1e3) / 1e12, 1), "accumulated_onto_gca": True},
+            "cca": {"ms": round(ms_c, 4), "tokens_per_s": round(tok / (ms_c / 1e3), 1),
+                    "tflops_algorithmic": round(fl_c / (ms_c / 1e3) / 1e12, 1)}}
+
+
 def offload_leg(args, torch, gca, kst, vst, qn, ql, kl, ws, o, lse, idx, sc, time_loop):
     """Decode with the K/V store in pinned host memory (the inference offload): the same
     store as the device-resident decode copied to a pinned host buffer (2 x 25.8 GB, shared
@@ -589,6 +627,7 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=DEC_B)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-offload", action="store_true", help="skip the host-memory K/V store decode")
+    ap.add_argument("--no-block", action="store_true", help="skip the window-attention and CCA leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

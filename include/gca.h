@@ -161,6 +161,43 @@ GCA_API gca_status gca_forward(const void* q, const void* k, const void* v, int6
                        void* o, float* lse, void* ws, size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * gca_window_forward - sliding-window causal self-attention.
+ *
+ * Paper-Notes page, 损失函数/训练策略 (training strategy): the attention block runs
+ * sliding-window self-attention (W = 512) beside the top-k retrieval.  Token t attends to
+ * tokens t - window + 1 .. t of its own sequence (fewer at the start) with one softmax of
+ * the dh^-1/2-scaled logits.  With accumulate != 0 the result is added to o (the block's
+ * sum of this sublayer and gca_forward's output); otherwise o is overwritten.
+ *
+ *   q, k, v, o [B][L][H][dh] contiguous, dtype `dtype`; L a multiple of 64.
+ *   lse     [B][L/64][H][64] float32 out: log-sum-exp of each row's scaled logits.
+ *   window  a multiple of 64 in 64..4032.   dh 32 or 64.
+ *   ws      >= gca_forward_workspace_size() bytes (error word only).
+ * ------------------------------------------------------------------------------- */
+GCA_API gca_status gca_window_forward(const void* q, const void* k, const void* v, gca_dtype dtype, int B,
+                              int L, int H, int dh, int window, void* o, float* lse, int accumulate,
+                              void* ws, size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * gca_cca_forward - chunked cross-attention over the retrieved chunks (ablation).
+ *
+ * Paper-Notes page, 关键设计 ("Grouped Cross-Attention"): the variant GCA is contrasted
+ * with.  The valid retrieved chunks of row r = c - shift are concatenated and query chunk
+ * c attends to them with ONE softmax; the retrieval scores take no part.  Chunks without a
+ * valid slot get O = 0 (unchanged when accumulating) and LSE = -inf.
+ *
+ *   q, k, v, kv_batch_stride, idx, topk, shift: as for gca_forward (no scores).
+ *   o       [B][nQ*64][H][dh] out (accumulate != 0: added to).
+ *   lse     [B][nQ][H][64] float32 out.
+ *   ws      >= gca_forward_workspace_size() bytes (error word; idx outside [-1, nC) is
+ *           flagged there and skipped).
+ * ------------------------------------------------------------------------------- */
+GCA_API gca_status gca_cca_forward(const void* q, const void* k, const void* v, int64_t kv_batch_stride,
+                           gca_dtype dtype, int B, int nQ, int nC, int H, int dh, const int32_t* idx,
+                           int topk, int shift, void* o, float* lse, int accumulate, void* ws,
+                           size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * gca_gather_chunks - copy the retrieved chunks' keys and values into a compact buffer.
  *
  * Paper-Notes page, 关键设计 / key design (inference memory offload): the past chunks'

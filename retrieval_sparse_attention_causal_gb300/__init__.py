@@ -49,6 +49,8 @@ def _load():
         "gca_retrieve_topk_noalloc": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P]),
         "gca_forward_workspace_size": (SZ, []),
         "gca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, P, I, I, P, P, P, SZ, P]),
+        "gca_window_forward": (I, [P, P, P, I, I, I, I, I, I, P, P, I, P, SZ, P]),
+        "gca_cca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, I, I, P, P, I, P, SZ, P]),
         "gca_gather_workspace_size": (SZ, []),
         "gca_gather_chunks": (I, [P, P, I64, I, I, I, I, I, I, P, I, P, P, P, P, SZ, P]),
         "gca_backward_workspace_size": (SZ, [I, I, I, I, I]),
@@ -73,7 +75,8 @@ LIB = _load()
 EXPORTS = (
     "gca_status_string", "gca_last_error_detail", "gca_retrieve_workspace_size", "gca_retrieve_topk",
     "gca_retrieve_noalloc_max_scratch", "gca_retrieve_topk_noalloc",
-    "gca_forward_workspace_size", "gca_forward", "gca_gather_workspace_size", "gca_gather_chunks",
+    "gca_forward_workspace_size", "gca_forward", "gca_window_forward", "gca_cca_forward",
+    "gca_gather_workspace_size", "gca_gather_chunks",
     "gca_backward_workspace_size", "gca_backward",
     "gca_scores_backward_workspace_size", "gca_scores_backward", "gca_check_error", "gca_launch_count",
     "gca_profile_begin", "gca_profile_end", "gca_profile_row",
@@ -213,6 +216,60 @@ def gca_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Te
     buf = ws.get(LIB.gca_forward_workspace_size())
     _check(LIB.gca_forward(_ptr(q), _ptr(k), _ptr(v), kv_bs, _dtype(q), B, nQ, nC, H, dh, _ptr(idx),
                            _ptr(scores), topk, shift, _ptr(out), _ptr(lse), _ptr(buf), buf.numel(), _stream()))
+    return out, lse
+
+
+def window_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: int = 512, ws: Workspace = None,
+                   out: torch.Tensor = None, lse: torch.Tensor = None, accumulate: bool = False):
+    """Sliding-window causal self-attention (gca_window_forward).  q, k, v [B, L, H, dh];
+    token t attends to tokens t - window + 1 .. t.  Returns O like q (added to `out` when
+    accumulate) and LSE [B, L/64, H, 64] float32."""
+    _cuda(q, k, v)
+    B, L, H, dh = q.shape
+    _need(L % CHUNK == 0, "sequence length must be a multiple of 64")
+    _need(k.shape == q.shape and v.shape == q.shape and k.dtype == q.dtype == v.dtype, "q/k/v shape or dtype mismatch")
+    _need(q.is_contiguous() and k.is_contiguous() and v.is_contiguous(), "q, k, v must be contiguous")
+    if out is None:
+        _need(not accumulate, "accumulate needs an output buffer")
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, L // CHUNK, H, CHUNK), dtype=torch.float32, device=q.device)
+    ws = ws or default_workspace(q.device)
+    buf = ws.get(LIB.gca_forward_workspace_size())
+    _check(LIB.gca_window_forward(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, L, H, dh, window, _ptr(out), _ptr(lse),
+                                  1 if accumulate else 0, _ptr(buf), buf.numel(), _stream()))
+    return out, lse
+
+
+def cca_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Tensor, shift: int = 1,
+                kv_shared: bool = False, ws: Workspace = None, out: torch.Tensor = None, lse: torch.Tensor = None,
+                accumulate: bool = False):
+    """Chunked cross-attention over the retrieved chunks, one joint softmax
+    (gca_cca_forward).  Shapes as gca_forward (no scores).  Returns O like q and LSE
+    [B, nQ, H, 64] float32."""
+    _cuda(q, k, v, idx)
+    B, L, H, dh = q.shape
+    _need(L % CHUNK == 0, "query length must be a multiple of 64")
+    nQ = L // CHUNK
+    _need(q.is_contiguous() and k.is_contiguous() and v.is_contiguous(), "q, k, v must be contiguous")
+    _need(k.shape == v.shape and k.dtype == q.dtype == v.dtype, "k/v shape or dtype mismatch")
+    if kv_shared:
+        _need(k.dim() == 3 and k.shape[1:] == (H, dh), "shared k/v must be [nC*64, H, dh]")
+        nC, kv_bs = k.shape[0] // CHUNK, 0
+    else:
+        _need(k.dim() == 4 and k.shape[0] == B and k.shape[2:] == (H, dh), "k/v must be [B, nC*64, H, dh]")
+        nC, kv_bs = k.shape[1] // CHUNK, k.stride(0)
+    topk = idx.shape[2]
+    _need(idx.shape == (B, nQ, topk) and idx.dtype == torch.int32 and idx.is_contiguous(), "idx must be int32 [B, nQ, topk]")
+    if out is None:
+        _need(not accumulate, "accumulate needs an output buffer")
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, nQ, H, CHUNK), dtype=torch.float32, device=q.device)
+    ws = ws or default_workspace(q.device)
+    buf = ws.get(LIB.gca_forward_workspace_size())
+    _check(LIB.gca_cca_forward(_ptr(q), _ptr(k), _ptr(v), kv_bs, _dtype(q), B, nQ, nC, H, dh, _ptr(idx), topk, shift,
+                               _ptr(out), _ptr(lse), 1 if accumulate else 0, _ptr(buf), buf.numel(), _stream()))
     return out, lse
 
 

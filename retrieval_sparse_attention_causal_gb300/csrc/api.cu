@@ -205,9 +205,10 @@ extern "C" gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride,
 
 // ==================================================================== GCA forward
 static gca_status check_gca(const void* q, const void* k, const void* v, gca_dtype dt, int B, int nQ, int nC,
-                            int H, int dh, const int32_t* idx, const float* scores, int topk, int shift) {
+                            int H, int dh, const int32_t* idx, const float* scores, int topk, int shift,
+                            bool need_scores = true) {
   if (dt != GCA_F32 && dt != GCA_BF16) return fail(GCA_ERR_INVALID_ARG, "dtype must be GCA_F32 or GCA_BF16");
-  if (!q || !k || !v || !idx || !scores) return fail(GCA_ERR_INVALID_ARG, "input pointer is NULL");
+  if (!q || !k || !v || !idx || (need_scores && !scores)) return fail(GCA_ERR_INVALID_ARG, "input pointer is NULL");
   if (B < 1 || nQ < 1 || nC < 1 || H < 1) return fail(GCA_ERR_INVALID_ARG, "B, nQ, nC, H must be >= 1");
   if (B > 65535 || H > 65535) return fail(GCA_ERR_INVALID_ARG, "B and H must be <= 65535");
   if ((int64_t)nQ * 64 > INT32_MAX || (int64_t)nC * 64 > INT32_MAX)
@@ -240,6 +241,54 @@ extern "C" gca_status gca_forward(const void* q, const void* k, const void* v, i
   a.o = o; a.lse = lse; a.err = reinterpret_cast<ErrWord*>(ws);
   cudaError_t e = launch_forward(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gca_forward launch");
+  return GCA_OK;
+}
+
+// ==================================================================== window attention and CCA
+extern "C" gca_status gca_window_forward(const void* q, const void* k, const void* v, gca_dtype dtype, int B,
+                                         int L, int H, int dh, int window, void* o, float* lse, int accumulate,
+                                         void* ws, size_t ws_bytes, gca_stream_t stream) {
+  if (dtype != GCA_F32 && dtype != GCA_BF16) return fail(GCA_ERR_INVALID_ARG, "dtype must be GCA_F32 or GCA_BF16");
+  if (B < 1 || H < 1 || L < 64 || L % 64) return fail(GCA_ERR_INVALID_ARG, "B, H >= 1 and L a positive multiple of 64");
+  if (dh != 32 && dh != 64) return fail(GCA_ERR_UNSUPPORTED, "dh must be 32 or 64");
+  if (window < 64 || window % 64 || window > 63 * 64)
+    return fail(GCA_ERR_UNSUPPORTED, "window must be a multiple of 64 in 64..4032");
+  if (L / 64 > 65535 || B > 65535 || H > 65535) return fail(GCA_ERR_UNSUPPORTED, "L/64, B and H must be <= 65535");
+  if (!q || !k || !v || !o || !lse) return fail(GCA_ERR_INVALID_ARG, "a pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(GCA_ERR_INVALID_ARG, "q, k, v, o, lse must be 16-byte aligned");
+  gca_status st;
+  if ((st = check_ws(ws, ws_bytes, gca_forward_workspace_size())) != GCA_OK) return st;
+  BlockAttnArgs a{};
+  a.q = q; a.k = k; a.v = v; a.kv_bs = (int64_t)L * H * dh;
+  a.bf16 = dtype == GCA_BF16; a.B = B; a.nQ = L / 64; a.nC = L / 64; a.H = H; a.dh = dh;
+  a.mode = 0; a.window = window; a.o = o; a.lse = lse; a.accumulate = accumulate ? 1 : 0;
+  a.err = reinterpret_cast<ErrWord*>(ws);
+  cudaError_t e = launch_block_attn(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gca_window_forward launch");
+  return GCA_OK;
+}
+
+extern "C" gca_status gca_cca_forward(const void* q, const void* k, const void* v, int64_t kv_batch_stride,
+                                      gca_dtype dtype, int B, int nQ, int nC, int H, int dh, const int32_t* idx,
+                                      int topk, int shift, void* o, float* lse, int accumulate, void* ws,
+                                      size_t ws_bytes, gca_stream_t stream) {
+  gca_status st = check_gca(q, k, v, dtype, B, nQ, nC, H, dh, idx, nullptr, topk, shift, false);
+  if (st != GCA_OK) return st;
+  if (!o || !lse) return fail(GCA_ERR_INVALID_ARG, "o/lse pointer is NULL");
+  if (!aligned16(o) || !aligned16(lse)) return fail(GCA_ERR_INVALID_ARG, "o/lse must be 16-byte aligned");
+  const int64_t per_seq = (int64_t)nC * 64 * H * dh;
+  if (kv_batch_stride != 0 && (kv_batch_stride < per_seq || kv_batch_stride % 8))
+    return fail(GCA_ERR_INVALID_ARG, "kv_batch_stride must be 0 or >= nC*64*H*dh and a multiple of 8");
+  if ((st = check_ws(ws, ws_bytes, gca_forward_workspace_size())) != GCA_OK) return st;
+  BlockAttnArgs a{};
+  a.q = q; a.k = k; a.v = v; a.kv_bs = kv_batch_stride;
+  a.bf16 = dtype == GCA_BF16; a.B = B; a.nQ = nQ; a.nC = nC; a.H = H; a.dh = dh;
+  a.mode = 1; a.idx = idx; a.topk = topk; a.shift = shift;
+  a.o = o; a.lse = lse; a.accumulate = accumulate ? 1 : 0;
+  a.err = reinterpret_cast<ErrWord*>(ws);
+  cudaError_t e = launch_block_attn(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gca_cca_forward launch");
   return GCA_OK;
 }
 

@@ -57,6 +57,19 @@ struct FwdArgs {
 };
 cudaError_t launch_forward(const FwdArgs& a, cudaStream_t s);
 
+// ---- one-softmax attention over a list of key blocks (block_attn.cu):
+// mode 0: sliding-window causal self-attention (K/V of the query's own sequence, nC = nQ);
+// mode 1: chunked cross-attention over the valid retrieved chunks of row c - shift.
+struct BlockAttnArgs {
+  const void* q; const void* k; const void* v; int64_t kv_bs;
+  int bf16, B, nQ, nC, H, dh;
+  int mode, window;                          // window in tokens (mode 0), a multiple of 64
+  const int32_t* idx; int topk, shift;       // mode 1
+  void* o; float* lse; int accumulate;       // lse [B][nQ][H][64]
+  ErrWord* err;
+};
+cudaError_t launch_block_attn(const BlockAttnArgs& a, cudaStream_t s);
+
 // ---- gather of retrieved chunks into a compact buffer (gather.cu)
 struct GatherArgs {
   const void* k_src; const void* v_src; int64_t src_bs;  // store [B][nC*64][H][dh]; batch stride in elements

@@ -160,6 +160,12 @@ __device__ __forceinline__ void st16x128_x4(uint32_t taddr, const uint32_t (&v)[
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
+// Store in the 16x256b fragment layout (the inverse of ld16x256).
+__device__ __forceinline__ void st16x256(uint32_t taddr, const float (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "f"(v[0]), "f"(v[1]),
+               "f"(v[2]), "f"(v[3])
+               : "memory");
+}
 // 16 lanes x 8 columns (registers 0-3 as in the x4 form, columns 0-7).
 __device__ __forceinline__ void st16x128_x2(uint32_t taddr, const uint32_t (&v)[4]) {
   asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
