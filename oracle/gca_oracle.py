@@ -271,6 +271,29 @@ def swa_forward(q, k, v, window, rows=None):
     return o, lse
 
 
+def swa_backward(q, k, v, do, window):
+    """Gradients of swa_forward (the chain rule of its definition, computed directly):
+    per sequence and head, with P the masked row softmax of the scaled logits,
+        dP = dO V^T,  dS = P * (dP - rowsum(P * dP)),
+        dQ = dS K / sqrt(dh),  dK = dS^T Q / sqrt(dh),  dV = P^T dO.
+    Returns dq, dk, dv like q."""
+    B, L, H, dh = q.shape
+    dq, dk, dv = np.zeros((B, L, H, dh)), np.zeros((B, L, H, dh)), np.zeros((B, L, H, dh))
+    t = np.arange(L)
+    allowed = (t[None, :] <= t[:, None]) & (t[None, :] > t[:, None] - window)  # [query, key]
+    for b in range(B):
+        for h in range(H):
+            Q, K, V, dO = q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h]
+            S = np.where(allowed, Q @ K.T / math.sqrt(dh), -np.inf)
+            P, _ = _softmax_rows(S)
+            dP = dO @ V.T
+            dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))
+            dq[b, :, h] = dS @ K / math.sqrt(dh)
+            dk[b, :, h] = dS.T @ Q / math.sqrt(dh)
+            dv[b, :, h] = P.T @ dO
+    return dq, dk, dv
+
+
 def cca_chunk_forward(qc, kv_k, kv_v, idx_row, chunk=CHUNK):
     """Chunked cross-attention for one query chunk (Notes, key design / GCA, the variant
     GCA is contrasted with): the retrieved chunks' keys and values are concatenated (slot

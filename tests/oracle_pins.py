@@ -470,6 +470,41 @@ def pin_swa_window_one_is_identity(orc):
     assert np.max(np.abs(lse - (q * k).sum(-1) / 2.0)) < 1e-12
 
 
+def pin_swa_backward_wide_window_is_torch_autograd(orc):
+    """W >= L: the gradients of causal attention, from torch autograd in float64."""
+    import torch
+    rng = np.random.default_rng(37)
+    B, L, H, dh = 1, 24, 2, 5
+    q, k, v, do = (rng.standard_normal((B, L, H, dh)) for _ in range(4))
+    dq, dk, dv = orc.swa_backward(q, k, v, do, window=L)
+    Q, K, V = (torch.from_numpy(x[0]).permute(1, 0, 2).requires_grad_() for x in (q, k, v))
+    O = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True)
+    O.backward(torch.from_numpy(do[0]).permute(1, 0, 2))
+    for got, ref in ((dq, Q.grad), (dk, K.grad), (dv, V.grad)):
+        assert np.max(np.abs(got[0] - ref.permute(1, 0, 2).numpy())) < 1e-11
+
+
+def pin_swa_backward_finite_differences(orc):
+    """Window 3 on a short sequence: central differences of <dO, O> in float64."""
+    rng = np.random.default_rng(38)
+    B, L, H, dh, W = 1, 7, 1, 3, 3
+    q, k, v, do = (rng.standard_normal((B, L, H, dh)) for _ in range(4))
+    dq, dk, dv = orc.swa_backward(q, k, v, do, W)
+
+    def loss(qq, kk, vv):
+        return float(np.sum(orc.swa_forward(qq, kk, vv, W)[0] * do))
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for ix in [(0, 0, 0, 1), (0, 3, 0, 0), (0, 6, 0, 2), (0, 4, 0, 1)]:
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += 1e-6
+            xm[ix] -= 1e-6
+            args = {"q": q, "k": k, "v": v}
+            fp = loss(*[xp if n == name else args[n] for n in ("q", "k", "v")])
+            fm = loss(*[xm if n == name else args[n] for n in ("q", "k", "v")])
+            fd = (fp - fm) / 2e-6
+            assert abs(fd - g[ix]) <= 1e-6 * max(1.0, abs(fd)), (name, ix, fd, g[ix])
+
+
 def pin_cca_single_slot_equals_gca(orc):
     """With one valid slot, CCA and GCA coincide (one softmax over one chunk, weight 1)."""
     rng = np.random.default_rng(34)

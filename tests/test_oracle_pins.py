@@ -49,6 +49,10 @@ MUTATIONS = {
     "cca_softmax_per_chunk": ("S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S, n*S]",
                               "S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh) / len(js)  # [H, S, n*S]"),
     "cca_drops_slot": ("js = [int(j) for j in idx_row if j >= 0]", "js = [int(j) for j in idx_row if j > 0]"),
+    "swa_bwd_window_mask": ("allowed = (t[None, :] <= t[:, None]) & (t[None, :] > t[:, None] - window)  # [query, key]",
+                            "allowed = (t[None, :] <= t[:, None]) & (t[None, :] >= t[:, None] - window)  # [query, key]"),
+    "swa_bwd_dk_scale": ("dk[b, :, h] = dS.T @ Q / math.sqrt(dh)", "dk[b, :, h] = dS.T @ Q"),
+    "swa_bwd_rowsum": ("dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))", "dS = P * (dP - np.sum(dP, axis=1, keepdims=True))"),
 }
 
 
