@@ -457,25 +457,36 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
 
 
 def block_attn_leg(args, torch, gca, q, k, v, out, timed):
-    """Forward of the sliding-window self-attention (W = 512) beside GCA, accumulated onto
-    GCA's output as in the attention block, and of CCA (one joint softmax over the same
-    retrieved chunks), at the training shape; algorithmic flops count the unmasked
-    (query, key) pairs, 4 dh flops each (QK^T and PV)."""
+    """Forward and backward of the sliding-window self-attention (W = 512) beside GCA (the
+    forward accumulated onto GCA's output as in the attention block), and the forward of
+    CCA (one joint softmax over the same retrieved chunks), at the training shape.
+    Algorithmic flops count the unmasked (query, key) pairs: 4 dh flops each forward (QK^T,
+    PV) and 2.5 times that backward (S recompute, dO V^T, dQ, dK, dV)."""
     W = 512
     o = out["o"].clone()
     lse_w = torch.empty((B, NC, H, 64), dtype=torch.float32, device="cuda")
     o_c = torch.empty_like(q)
     lse_c = torch.empty((B, NC, H, 64), dtype=torch.float32, device="cuda")
 
+    o_w = torch.empty_like(q)
+    do = torch.empty_like(q).normal_(0.0, 0.125)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
     def win(i):
         gca.window_forward(q, k, v, window=W, out=o, lse=lse_w, accumulate=True)
+
+    def win_bwd(i):
+        gca.window_backward(q, k, v, o_w, do, lse_w, window=W, dq=dq, dk=dk, dv=dv)
 
     def cca(i):
         gca.cca_forward(q, k, v, out["idx"], shift=1, out=o_c, lse=lse_c)
 
+    gca.window_forward(q, k, v, window=W, out=o_w, lse=lse_w)  # the window attention's own output
     for i in range(args.warmup):
+        win_bwd(i)
         win(i)
         cca(i)
+    ms_wb = timed(win_bwd, args.steps) / args.steps
     ms_w = timed(win, args.steps) / args.steps
     ms_c = timed(cca, args.steps) / args.steps
     t = torch.arange(L, dtype=torch.float64)
@@ -485,7 +496,10 @@ def block_attn_leg(args, torch, gca, q, k, v, out, timed):
     fl_w, fl_c = pairs_w * 4 * DH, pairs_c * 4 * DH
     tok = B * L
     return {"window": {"window": W, "ms": round(ms_w, 4), "tokens_per_s": round(tok / (ms_w / 1e3), 1),
-                       "tflops_algorithmic": round(fl_w / (ms_w / 1e3) / 1e12, 1), "accumulated_onto_gca": True},
+                       "tflops_algorithmic": round(fl_w / (ms_w / 1e3) / 1e12, 1), "accumulated_onto_gca": True,
+                       "backward_ms": round(ms_wb, 4),
+                       "backward_tflops_algorithmic": round(2.5 * fl_w / (ms_wb / 1e3) / 1e12, 1),
+                       "fwd_bwd_tokens_per_s": round(tok / ((ms_w + ms_wb) / 1e3), 1)},
             "cca": {"ms": round(ms_c, 4), "tokens_per_s": round(tok / (ms_c / 1e3), 1),
                     "tflops_algorithmic": round(fl_c / (ms_c / 1e3) / 1e12, 1)}}
 

@@ -179,6 +179,26 @@ GCA_API gca_status gca_window_forward(const void* q, const void* k, const void* 
                               void* ws, size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * gca_window_backward - gradients of gca_window_forward.
+ *
+ * With P the masked row softmax (from the saved LSE) and D = rowsum(dO * O):
+ *     dS = P * (dO V^T - D),  dQ = dS K / sqrt(dh),  dK = dS^T Q / sqrt(dh),  dV = P^T dO.
+ * Deterministic (no atomics): a query-side and a key-side pass.
+ *
+ *   q, k, v, lse, window: as passed to / produced by gca_window_forward.
+ *   o       [B][L][H][dh] the window attention's own output (before any accumulation
+ *           onto another sublayer's output; that sum is linear, so dout is the same).
+ *   dout    [B][L][H][dh] gradient of o.
+ *   dq, dk, dv [B][L][H][dh] out (accumulate != 0: added to).
+ *   ws      >= gca_window_backward_workspace_size(B, L, H) bytes.
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_window_backward_workspace_size(int B, int L, int H);
+GCA_API gca_status gca_window_backward(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, gca_dtype dtype, int B, int L,
+                               int H, int dh, int window, void* dq, void* dk, void* dv,
+                               int accumulate, void* ws, size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * gca_cca_forward - chunked cross-attention over the retrieved chunks (ablation).
  *
  * Paper-Notes page, 关键设计 ("Grouped Cross-Attention"): the variant GCA is contrasted

@@ -51,6 +51,8 @@ def _load():
         "gca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, P, I, I, P, P, P, SZ, P]),
         "gca_window_forward": (I, [P, P, P, I, I, I, I, I, I, P, P, I, P, SZ, P]),
         "gca_cca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, I, I, P, P, I, P, SZ, P]),
+        "gca_window_backward_workspace_size": (SZ, [I, I, I]),
+        "gca_window_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, I, P, SZ, P]),
         "gca_gather_workspace_size": (SZ, []),
         "gca_gather_chunks": (I, [P, P, I64, I, I, I, I, I, I, P, I, P, P, P, P, SZ, P]),
         "gca_backward_workspace_size": (SZ, [I, I, I, I, I]),
@@ -76,6 +78,7 @@ EXPORTS = (
     "gca_status_string", "gca_last_error_detail", "gca_retrieve_workspace_size", "gca_retrieve_topk",
     "gca_retrieve_noalloc_max_scratch", "gca_retrieve_topk_noalloc",
     "gca_forward_workspace_size", "gca_forward", "gca_window_forward", "gca_cca_forward",
+    "gca_window_backward_workspace_size", "gca_window_backward",
     "gca_gather_workspace_size", "gca_gather_chunks",
     "gca_backward_workspace_size", "gca_backward",
     "gca_scores_backward_workspace_size", "gca_scores_backward", "gca_check_error", "gca_launch_count",
@@ -239,6 +242,28 @@ def window_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, window: in
     _check(LIB.gca_window_forward(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, L, H, dh, window, _ptr(out), _ptr(lse),
                                   1 if accumulate else 0, _ptr(buf), buf.numel(), _stream()))
     return out, lse
+
+
+def window_backward(q, k, v, o, dout, lse, window: int = 512, ws: Workspace = None, dq=None, dk=None, dv=None,
+                    accumulate: bool = False):
+    """Gradients of window_forward (gca_window_backward).  o is the window attention's own
+    output; returns dq, dk, dv like q (added to the given buffers when accumulate)."""
+    _cuda(q, k, v, o, dout, lse)
+    B, L, H, dh = q.shape
+    for t in (k, v, o, dout):
+        _need(t.shape == q.shape and t.dtype == q.dtype and t.is_contiguous(), "q/k/v/o/dout shape or dtype mismatch")
+    _need(lse.shape == (B, L // CHUNK, H, CHUNK) and lse.dtype == torch.float32, "lse must be [B, L/64, H, 64] float32")
+    if accumulate:
+        _need(dq is not None and dk is not None and dv is not None, "accumulate needs dq, dk and dv buffers")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = ws or default_workspace(q.device)
+    buf = ws.get(LIB.gca_window_backward_workspace_size(B, L, H))
+    _check(LIB.gca_window_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _dtype(q), B, L, H, dh,
+                                   window, _ptr(dq), _ptr(dk), _ptr(dv), 1 if accumulate else 0, _ptr(buf), buf.numel(),
+                                   _stream()))
+    return dq, dk, dv
 
 
 def cca_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Tensor, shift: int = 1,

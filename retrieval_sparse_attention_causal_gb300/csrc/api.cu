@@ -269,6 +269,39 @@ extern "C" gca_status gca_window_forward(const void* q, const void* k, const voi
   return GCA_OK;
 }
 
+extern "C" size_t gca_window_backward_workspace_size(int B, int L, int H) {
+  if (B < 1 || L < 64 || H < 1) return kErrBytes;
+  return kErrBytes + align256((size_t)B * (L / 64) * H * 64 * 4);
+}
+
+extern "C" gca_status gca_window_backward(const void* q, const void* k, const void* v, const void* o,
+                                          const void* dout, const float* lse, gca_dtype dtype, int B, int L, int H,
+                                          int dh, int window, void* dq, void* dk, void* dv, int accumulate,
+                                          void* ws, size_t ws_bytes, gca_stream_t stream) {
+  if (dtype != GCA_F32 && dtype != GCA_BF16) return fail(GCA_ERR_INVALID_ARG, "dtype must be GCA_F32 or GCA_BF16");
+  if (B < 1 || H < 1 || L < 64 || L % 64) return fail(GCA_ERR_INVALID_ARG, "B, H >= 1 and L a positive multiple of 64");
+  if (dh != 32 && dh != 64) return fail(GCA_ERR_UNSUPPORTED, "dh must be 32 or 64");
+  if (window < 64 || window % 64 || window > 63 * 64)
+    return fail(GCA_ERR_UNSUPPORTED, "window must be a multiple of 64 in 64..4032");
+  if (L / 64 > 65535 || B > 65535 || H > 65535) return fail(GCA_ERR_UNSUPPORTED, "L/64, B and H must be <= 65535");
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return fail(GCA_ERR_INVALID_ARG, "a pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(GCA_ERR_INVALID_ARG, "all tensors must be 16-byte aligned");
+  gca_status st;
+  if ((st = check_ws(ws, ws_bytes, gca_window_backward_workspace_size(B, L, H))) != GCA_OK) return st;
+  WindowBwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse = lse;
+  a.Dbuf = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kErrBytes);
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.bf16 = dtype == GCA_BF16; a.B = B; a.nQ = L / 64; a.H = H; a.dh = dh; a.window = window;
+  a.accumulate = accumulate ? 1 : 0;
+  a.err = reinterpret_cast<ErrWord*>(ws);
+  cudaError_t e = launch_window_backward(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gca_window_backward launch");
+  return GCA_OK;
+}
+
 extern "C" gca_status gca_cca_forward(const void* q, const void* k, const void* v, int64_t kv_batch_stride,
                                       gca_dtype dtype, int B, int nQ, int nC, int H, int dh, const int32_t* idx,
                                       int topk, int shift, void* o, float* lse, int accumulate, void* ws,

@@ -70,6 +70,18 @@ struct BlockAttnArgs {
 };
 cudaError_t launch_block_attn(const BlockAttnArgs& a, cudaStream_t s);
 
+// ---- backward of the sliding-window attention (window_bwd.cu)
+struct WindowBwdArgs {
+  const void* q; const void* k; const void* v;  // [B][nQ*64][H][dh]
+  const void* o; const void* dout;               // window output (not accumulated) and its gradient
+  const float* lse;                              // [B][nQ][H][64] from the forward
+  float* Dbuf;                                   // [B][nQ][H][64] workspace: rowsum(dO * O)
+  void* dq; void* dk; void* dv;
+  int bf16, B, nQ, H, dh, window, accumulate;
+  ErrWord* err;
+};
+cudaError_t launch_window_backward(const WindowBwdArgs& a, cudaStream_t s);
+
 // ---- gather of retrieved chunks into a compact buffer (gather.cu)
 struct GatherArgs {
   const void* k_src; const void* v_src; int64_t src_bs;  // store [B][nC*64][H][dh]; batch stride in elements

@@ -1,0 +1,561 @@
+// Backward of the sliding-window causal self-attention (block_attn.cu, window mode).
+//
+// Paper-Notes page on "Efficient Length-Generalizable Attention via Causal Retrieval for
+// Long-Context Language Modeling", 损失函数/训练策略 (training strategy: sliding-window
+// self-attention, W = 512, trained beside the top-k retrieval).  With P the masked row
+// softmax (recomputed from the saved LSE), per sequence and head:
+//     D = rowsum(dO * O),  dS = P * (dO V^T - D),
+//     dQ = dS K / sqrt(dh),  dK = dS^T Q / sqrt(dh),  dV = P^T dO.
+// Three kernels: D per row; a query-side pass (per query chunk over its window blocks,
+// dQ); a key-side pass (per key chunk over the query chunks whose window covers it, dK and
+// dV).  Neither needs atomics, so the result is deterministic.  Both tensor-core passes
+// follow the GCA backward's layout: a control warp issues TMA loads and tcgen05.mma, eight
+// element warps (TMEM lane quarter w % 4, column half w / 4) do the arithmetic and store
+// the bf16 A operand of the next product into TMEM over the columns they read.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace gca {
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kEW = 8, kThreads = 32 * (kEW + 1), kCtl = kEW;
+constexpr int TILE = 8192, ROWB = 128, UPR = 8, DH = 64;
+enum { kBarOpReady = 2, kBarEW = 3 };
+
+// ------------------------------------------------------------------ D = rowsum(dO * O)
+// One thread per (token, head) row; D [B][L/64][H][64] like the LSE.
+template <typename T, int DHT>
+__global__ void __launch_bounds__(256) window_d_kernel(WindowBwdArgs a) {
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // token * H + h
+  const int64_t nrows = (int64_t)a.B * a.nQ * 64 * a.H;
+  if (row >= nrows) return;
+  const int64_t tok = row / a.H;
+  const int h = (int)(row % a.H);
+  const T* o = reinterpret_cast<const T*>(a.o) + row * DHT;
+  const T* d = reinterpret_cast<const T*>(a.dout) + row * DHT;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int x = 0; x < DHT; ++x) acc = fmaf(Elem<T>::ld(o + x), Elem<T>::ld(d + x), acc);
+  const int64_t bc = tok / 64;  // b * nQ + c
+  a.Dbuf[(bc * a.H + h) * 64 + tok % 64] = acc;
+}
+
+// Mask of key column kc against query row qr inside a block pair: kind 1 (tail block of
+// the window) keeps kc > qr, kind 2 (diagonal block) keeps kc <= qr.
+__device__ __forceinline__ bool dropped(int kind, int kc, int qr) {
+  return kind == 1 ? kc <= qr : (kind == 2 ? kc > qr : false);
+}
+
+// ------------------------------------------------------------------ query side (bf16, dh = 64)
+constexpr int kQStages = 4;
+constexpr int kQSmem = TILE * (2 + 2 * kQStages) + 1024;  // Q, dO, ring of (K, V)
+
+__global__ void __launch_bounds__(kThreads, 2)
+window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  constexpr int NST = kQStages, NT = kThreads;
+  constexpr uint32_t kIdKm = tc::idesc_bf16(64, 64, false);
+  constexpr uint32_t kIdMn = tc::idesc_bf16(64, 64, true);
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  unsigned char* Qs = sm;
+  unsigned char* dOs = sm + TILE;
+  unsigned char* ring = sm + 2 * TILE;
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bar_q, bar_kv[NST], bar_s, bar_o;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t ts = (int64_t)a.H * DH;
+  const int64_t tok0 = ((int64_t)b * a.nQ * 64 + (int64_t)c * 64) * ts + h * DH;
+  bf16* dqg = reinterpret_cast<bf16*>(a.dq) + tok0;
+  const int64_t rowbase = (((int64_t)b * a.nQ + c) * a.H + h) * 64;
+  const int wb = a.window / 64;
+  const int j0 = c - wb < 0 ? 0 : c - wb;  // key blocks j0 .. c
+  const int nb = c - j0 + 1;
+  auto kind_of = [&](int n) { const int j = j0 + n; return j == c ? 2 : (j == c - wb ? 1 : 0); };
+
+  if (tid == 0) {
+    tc::mbar_init(&bar_q, 1);
+    for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_kv[st], 1);
+    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_o, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tQ = tmem_slot + 128;
+
+  if (warp == kCtl) {
+    // ------------------------------------------------------------ control warp
+    bool ok = true;
+    auto load_block = [&](int x) {  // lane 0
+      const int st = x % NST;
+      unsigned char* Ks = ring + 2 * st * TILE;
+      tc::mbar_expect_tx(&bar_kv[st], 2 * TILE);
+      tc::tma_load_4d(Ks, &tmK, 0, h, (j0 + x) * 64, b, &bar_kv[st]);
+      tc::tma_load_4d(Ks + TILE, &tmV, 0, h, (j0 + x) * 64, b, &bar_kv[st]);
+    };
+    const uint64_t dQd = tc::desc_km(tc::su32(Qs)), dOd = tc::desc_km(tc::su32(dOs));
+    const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
+    constexpr uint64_t kStage = (2 * TILE) >> 4, kTileStep = TILE >> 4;
+    auto issue_s = [&](int x) {  // S = Q K^T and dPo = dO V^T of block x (whole warp)
+      const uint64_t dk = dRingKm + (x % NST) * kStage, dv = dk + kTileStep;
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks) {
+        tc::mma_warp(tS, dQd + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+        tc::mma_warp(tP, dOd + ks * tc::kKStepKm, dv + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+      }
+      tc::commit_warp(&bar_s);
+    };
+    if (lane == 0) {
+      tc::mbar_expect_tx(&bar_q, 2 * TILE);
+      tc::tma_load_4d(Qs, &tmQ, 0, h, c * 64, b, &bar_q);
+      tc::tma_load_4d(dOs, &tmdO, 0, h, c * 64, b, &bar_q);
+      for (int x = 0; x < NST && x < nb; ++x) load_block(x);
+    }
+    __syncwarp();
+    ok = tc::mbar_wait(&bar_q, 0) && ok;
+    ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
+    issue_s(0);
+    for (int n = 0; n < nb; ++n) {
+      tc::named_sync(kBarOpReady, NT);  // dS(n) is in TMEM columns 0-31
+      tc::fence_after();
+      const uint64_t dk = dRingMn + (n % NST) * kStage;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
+        tc::mma_ts_warp(tQ, tS + 8 * kk, dk + kk * tc::kKStepMn, kIdMn, (n > 0 || kk > 0) ? 1u : 0u);
+      tc::commit_warp(&bar_o);
+      if (n + 1 < nb) {
+        ok = tc::mbar_wait(&bar_kv[(n + 1) % NST], ((n + 1) / NST) & 1) && ok;
+        issue_s(n + 1);
+      }
+      ok = tc::mbar_wait(&bar_o, n & 1) && ok;  // ring stage n % NST is free
+      if (lane == 0) {
+        if (n + NST < nb) load_block(n + NST);
+        if (!ok) flag_timeout(a.err);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise warps
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const int row0 = 16 * quarter + g;
+    const uint32_t lane_q = (uint32_t)(32 * quarter) << 16;
+    const uint32_t lane_base = lane_q + 32 * hc;
+    const float scale = 1.0f / sqrtf((float)DH);
+    const float sl2 = scale * kLog2e;
+    const float lse0 = a.lse[rowbase + row0] * kLog2e, lse1 = a.lse[rowbase + row0 + 8] * kLog2e;
+    const float D0 = a.Dbuf[rowbase + row0], D1 = a.Dbuf[rowbase + row0 + 8];
+    for (int n = 0; n < nb; ++n) {
+      if (!tc::mbar_wait(&bar_s, n & 1)) flag_timeout(a.err);  // S(n), dPo(n)
+      float s[4][4], dp[4][4];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
+      tc::ld_wait(s);
+      tc::ld_wait(dp);
+      const int kind = kind_of(n);
+      uint32_t dv[8];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {  // key columns 32hc + 8cb + 2cq (+1)
+        float ds[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kc = 32 * hc + 8 * cb + 2 * cq + (e & 1), qr = row0 + 8 * (e >> 1);
+          const float l = e < 2 ? lse0 : lse1, dd = e < 2 ? D0 : D1;
+          const float p = dropped(kind, kc, qr) ? 0.f : tc::ex2(fmaf(s[cb][e], sl2, -l));
+          ds[e] = p * (dp[cb][e] - dd) * scale;
+        }
+        dv[2 * cb] = pack_bf16(ds[0], ds[1]);
+        dv[2 * cb + 1] = pack_bf16(ds[2], ds[3]);
+      }
+      tc::named_sync(kBarEW, 32 * kEW);  // both column halves have read S before stores over it
+      tc::st16x128_x4(tS + lane_q + 16 * hc, dv);
+      tc::st_wait();
+      tc::fence_before();
+      tc::named_arrive(kBarOpReady, NT);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp < kEW) {  // dQ from TMEM, staged through the Q tile
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    float o[4][4];
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tQ + lane_base + cb * 8, o[cb]);
+    tc::ld_wait(o);
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int r0 = 16 * quarter + g;
+      *reinterpret_cast<uint32_t*>(Qs + swz<ROWB>(r0, 4 * hc + n) + cq * 4) = pack_bf16(o[n][0], o[n][1]);
+      *reinterpret_cast<uint32_t*>(Qs + swz<ROWB>(r0 + 8, 4 * hc + n) + cq * 4) = pack_bf16(o[n][2], o[n][3]);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem_slot, 256);
+  }
+  for (int u = tid; u < 64 * UPR; u += NT) {
+    const int row = u / UPR, w = u % UPR;
+    uint4 val = *reinterpret_cast<const uint4*>(Qs + swz<ROWB>(row, w));
+    if (a.accumulate) {
+      const uint4 old = *reinterpret_cast<const uint4*>(dqg + row * ts + w * 8);
+      float fo[8], fn[8];
+      unpack16(old, fo, (const bf16*)nullptr);
+      unpack16(val, fn, (const bf16*)nullptr);
+      val.x = pack_bf16(fo[0] + fn[0], fo[1] + fn[1]); val.y = pack_bf16(fo[2] + fn[2], fo[3] + fn[3]);
+      val.z = pack_bf16(fo[4] + fn[4], fo[5] + fn[5]); val.w = pack_bf16(fo[6] + fn[6], fo[7] + fn[7]);
+    }
+    *reinterpret_cast<uint4*>(dqg + row * ts + w * 8) = val;
+  }
+}
+
+// ------------------------------------------------------------------ key side (bf16, dh = 64)
+constexpr int kKVStages = 4;
+constexpr int kKVStageBytes = 2 * TILE + 1024;  // Q, dO tiles + LSE and D rows
+constexpr int kKVSmem = TILE * 2 + kKVStages * kKVStageBytes + 1024;
+
+__global__ void __launch_bounds__(kThreads, 2)
+window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  constexpr int NST = kKVStages, NT = kThreads;
+  constexpr uint32_t kIdKm = tc::idesc_bf16(64, 64, false);
+  constexpr uint32_t kIdMn = tc::idesc_bf16(64, 64, true);
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
+  unsigned char* Ks = sm;
+  unsigned char* Vs = sm + TILE;
+  unsigned char* ring = sm + 2 * TILE;  // stage st: Q, dO, lse[64], D[64]
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bar_k, bar_c[NST], bar_s, bar_o;
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t ts = (int64_t)a.H * DH;
+  const int64_t ktok0 = ((int64_t)b * a.nQ * 64 + (int64_t)j * 64) * ts + h * DH;
+  bf16* dkg = reinterpret_cast<bf16*>(a.dk) + ktok0;
+  bf16* dvg = reinterpret_cast<bf16*>(a.dv) + ktok0;
+  const int wb = a.window / 64;
+  const int c1 = j + wb < a.nQ - 1 ? j + wb : a.nQ - 1;  // query chunks j .. c1 see key chunk j
+  const int ncons = c1 - j + 1;
+  // Consumer x is query chunk j + x: x = 0 the diagonal block (keep key <= query), x = wb the
+  // block where the window starts (keep key > query).
+  auto kind_of = [&](int x) { return x == 0 ? 2 : (x == wb ? 1 : 0); };
+
+  if (warp == kCtl && lane == 0) {
+    tc::mbar_init(&bar_k, 1);
+    for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_c[st], 1);
+    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_o, 1);
+    tc::fence_mbar_init();
+    tc::mbar_expect_tx(&bar_k, 2 * TILE);
+    tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, b, &bar_k);
+    tc::tma_load_4d(Vs, &tmV, 0, h, j * 64, b, &bar_k);
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tdV = tmem_slot + 128, tdK = tmem_slot + 192;
+
+  if (warp == kCtl) {
+    // ------------------------------------------------------------ control warp
+    bool ok = true;
+    auto load_cons = [&](int x) {  // lane 0: query chunk j + x's Q, dO tiles, LSE and D rows
+      const int st = x % NST;
+      const int c = j + x;
+      unsigned char* base = ring + st * kKVStageBytes;
+      const int64_t rb = (((int64_t)b * a.nQ + c) * a.H + h) * 64;
+      tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
+      tc::tma_load_4d(base, &tmQ, 0, h, c * 64, b, &bar_c[st]);
+      tc::tma_load_4d(base + TILE, &tmdO, 0, h, c * 64, b, &bar_c[st]);
+      tc::bulk_load(base + 2 * TILE, a.lse + rb, 256, &bar_c[st]);
+      tc::bulk_load(base + 2 * TILE + 256, a.Dbuf + rb, 256, &bar_c[st]);
+    };
+    const uint64_t dKd = tc::desc_km(tc::su32(Ks)), dVd = tc::desc_km(tc::su32(Vs));
+    const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
+    constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
+    auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x (whole warp)
+      const uint64_t dq = dRingKm + (x % NST) * kStage, ddo = dq + kTileStep;
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks) {
+        tc::mma_warp(tS, dKd + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+        tc::mma_warp(tP, dVd + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+      }
+      tc::commit_warp(&bar_s);
+    };
+    if (lane == 0)
+      for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
+    __syncwarp();
+    ok = tc::mbar_wait(&bar_k, 0) && ok;
+    ok = tc::mbar_wait(&bar_c[0], 0) && ok;
+    issue_s(0);
+    for (int ci = 0; ci < ncons; ++ci) {
+      tc::named_sync(kBarOpReady, NT);  // P^T and dS^T are in TMEM columns 0-31, 64-95
+      tc::fence_after();
+      const uint64_t bq = dRingMn + (ci % NST) * kStage, bdo = bq + kTileStep;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
+        tc::mma_ts_warp(tdV, tS + 8 * kk, bdo + kk * tc::kKStepMn, kIdMn, acc);
+        tc::mma_ts_warp(tdK, tP + 8 * kk, bq + kk * tc::kKStepMn, kIdMn, acc);
+      }
+      tc::commit_warp(&bar_o);
+      if (ci + 1 < ncons) {
+        ok = tc::mbar_wait(&bar_c[(ci + 1) % NST], ((ci + 1) / NST) & 1) && ok;
+        issue_s(ci + 1);
+      }
+      ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // ring stage ci % NST is free
+      if (lane == 0) {
+        if (ci + NST < ncons) load_cons(ci + NST);
+        if (!ok) flag_timeout(a.err);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise warps
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const int key0 = 16 * quarter + g;  // key rows key0, key0 + 8
+    const uint32_t lane_q = (uint32_t)(32 * quarter) << 16;
+    const uint32_t lane_base = lane_q + 32 * hc;
+    const float scale = 1.0f / sqrtf((float)DH);
+    const float sl2 = scale * kLog2e;
+    for (int ci = 0; ci < ncons; ++ci) {
+      if (!tc::mbar_wait(&bar_s, ci & 1)) flag_timeout(a.err);  // S^T(ci), dPo^T(ci)
+      const int st = ci % NST;
+      tc::mbar_wait(&bar_c[st], (ci / NST) & 1);  // observe the rows' phase (complete)
+      const float* lrow = reinterpret_cast<const float*>(ring + st * kKVStageBytes + 2 * TILE) + 32 * hc;
+      const float* drow = lrow + 64;
+      float s[4][4], dp[4][4];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
+      tc::ld_wait(s);
+      tc::ld_wait(dp);
+      const int kind = kind_of(ci);
+      uint32_t pv[8], dv[8];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {  // query columns 32hc + 8n + 2cq (+1)
+        const float2 l2 = *reinterpret_cast<const float2*>(lrow + 8 * n + 2 * cq);
+        const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
+        float p[4], ds[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int qc = 32 * hc + 8 * n + 2 * cq + (e & 1), kr = key0 + 8 * (e >> 1);
+          const float l = (e & 1) ? l2.y : l2.x, dd = (e & 1) ? d2.y : d2.x;
+          p[e] = dropped(kind, kr, qc) ? 0.f : tc::ex2(fmaf(s[n][e], sl2, -l * kLog2e));
+          ds[e] = p[e] * (dp[n][e] - dd) * scale;
+        }
+        pv[2 * n] = pack_bf16(p[0], p[1]);
+        pv[2 * n + 1] = pack_bf16(p[2], p[3]);
+        dv[2 * n] = pack_bf16(ds[0], ds[1]);
+        dv[2 * n + 1] = pack_bf16(ds[2], ds[3]);
+      }
+      tc::named_sync(kBarEW, 32 * kEW);  // both column halves have read before stores over it
+      tc::st16x128_x4(tS + lane_q + 16 * hc, pv);
+      tc::st16x128_x4(tP + lane_q + 16 * hc, dv);
+      tc::st_wait();
+      tc::fence_before();
+      tc::named_arrive(kBarOpReady, NT);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp < kEW) {  // dK (TMEM 192-255) into the K tile, dV (128-191) into the V tile
+    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
+    float o[4][4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      unsigned char* dst = half ? Vs : Ks;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256((half ? tdV : tdK) + lane_base + cb * 8, o[cb]);
+      tc::ld_wait(o);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const int r0 = 16 * quarter + g;
+        *reinterpret_cast<uint32_t*>(dst + swz<ROWB>(r0, 4 * hc + n) + cq * 4) = pack_bf16(o[n][0], o[n][1]);
+        *reinterpret_cast<uint32_t*>(dst + swz<ROWB>(r0 + 8, 4 * hc + n) + cq * 4) = pack_bf16(o[n][2], o[n][3]);
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::tmem_dealloc(tmem_slot, 256);
+  }
+  for (int u = tid; u < 64 * UPR; u += NT) {
+    const int row = u / UPR, w = u % UPR;
+    uint4 vk = *reinterpret_cast<const uint4*>(Ks + swz<ROWB>(row, w));
+    uint4 vv = *reinterpret_cast<const uint4*>(Vs + swz<ROWB>(row, w));
+    if (a.accumulate) {
+      const uint4 ok = *reinterpret_cast<const uint4*>(dkg + row * ts + w * 8);
+      const uint4 ov = *reinterpret_cast<const uint4*>(dvg + row * ts + w * 8);
+      float fk[8], fv[8], nk[8], nv[8];
+      unpack16(ok, fk, (const bf16*)nullptr);
+      unpack16(ov, fv, (const bf16*)nullptr);
+      unpack16(vk, nk, (const bf16*)nullptr);
+      unpack16(vv, nv, (const bf16*)nullptr);
+      vk.x = pack_bf16(nk[0] + fk[0], nk[1] + fk[1]); vk.y = pack_bf16(nk[2] + fk[2], nk[3] + fk[3]);
+      vk.z = pack_bf16(nk[4] + fk[4], nk[5] + fk[5]); vk.w = pack_bf16(nk[6] + fk[6], nk[7] + fk[7]);
+      vv.x = pack_bf16(nv[0] + fv[0], nv[1] + fv[1]); vv.y = pack_bf16(nv[2] + fv[2], nv[3] + fv[3]);
+      vv.z = pack_bf16(nv[4] + fv[4], nv[5] + fv[5]); vv.w = pack_bf16(nv[6] + fv[6], nv[7] + fv[7]);
+    }
+    *reinterpret_cast<uint4*>(dkg + row * ts + w * 8) = vk;
+    *reinterpret_cast<uint4*>(dvg + row * ts + w * 8) = vv;
+  }
+}
+
+// ------------------------------------------------------------------ SIMT path (f32, or dh = 32)
+// One thread per query row (dQ) and per key row (dK, dV), two passes over the blocks.
+template <typename T, int DHT>
+__global__ void __launch_bounds__(64) window_bwd_q_simt_kernel(WindowBwdArgs a) {
+  __shared__ float Ks[64][DHT + 1], Vs[64][DHT + 1];
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
+  const int64_t ts = (int64_t)a.H * DHT;
+  const int64_t tok = ((int64_t)b * a.nQ * 64 + (int64_t)c * 64 + t) * ts + h * DHT;
+  const int64_t rb = (((int64_t)b * a.nQ + c) * a.H + h) * 64 + t;
+  const float scale = 1.0f / sqrtf((float)DHT), lse = a.lse[rb], D = a.Dbuf[rb];
+  float qv[DHT], dov[DHT], dq[DHT];
+  for (int d = 0; d < DHT; ++d) {
+    qv[d] = Elem<T>::ld(reinterpret_cast<const T*>(a.q) + tok + d);
+    dov[d] = Elem<T>::ld(reinterpret_cast<const T*>(a.dout) + tok + d);
+    dq[d] = 0.f;
+  }
+  const int wb = a.window / 64, j0 = c - wb < 0 ? 0 : c - wb;
+  for (int jb = j0; jb <= c; ++jb) {
+    __syncthreads();
+    const int64_t kb = ((int64_t)b * a.nQ * 64 + (int64_t)jb * 64) * ts + h * DHT;
+    for (int x = t; x < 64 * DHT; x += 64) {
+      const int row = x / DHT, d = x % DHT;
+      Ks[row][d] = Elem<T>::ld(reinterpret_cast<const T*>(a.k) + kb + row * ts + d);
+      Vs[row][d] = Elem<T>::ld(reinterpret_cast<const T*>(a.v) + kb + row * ts + d);
+    }
+    __syncthreads();
+    const int kind = jb == c ? 2 : (jb == c - wb ? 1 : 0);
+    for (int key = 0; key < 64; ++key) {
+      if (dropped(kind, key, t)) continue;
+      float s = 0.f, dp = 0.f;
+      for (int d = 0; d < DHT; ++d) {
+        s = fmaf(qv[d], Ks[key][d], s);
+        dp = fmaf(dov[d], Vs[key][d], dp);
+      }
+      const float ds = expf(s * scale - lse) * (dp - D) * scale;
+      for (int d = 0; d < DHT; ++d) dq[d] = fmaf(ds, Ks[key][d], dq[d]);
+    }
+  }
+  for (int d = 0; d < DHT; ++d) {
+    T* p = reinterpret_cast<T*>(a.dq) + tok + d;
+    Elem<T>::st(p, a.accumulate ? Elem<T>::ld(p) + dq[d] : dq[d]);
+  }
+}
+
+template <typename T, int DHT>
+__global__ void __launch_bounds__(64) window_bwd_kv_simt_kernel(WindowBwdArgs a) {
+  __shared__ float Qs[64][DHT + 1], dOs[64][DHT + 1], ls[64], Ds[64];
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
+  const int64_t ts = (int64_t)a.H * DHT;
+  const int64_t tok = ((int64_t)b * a.nQ * 64 + (int64_t)j * 64 + t) * ts + h * DHT;
+  const float scale = 1.0f / sqrtf((float)DHT);
+  float kv[DHT], vv[DHT], dk[DHT], dv[DHT];
+  for (int d = 0; d < DHT; ++d) {
+    kv[d] = Elem<T>::ld(reinterpret_cast<const T*>(a.k) + tok + d);
+    vv[d] = Elem<T>::ld(reinterpret_cast<const T*>(a.v) + tok + d);
+    dk[d] = dv[d] = 0.f;
+  }
+  const int wb = a.window / 64;
+  const int c1 = j + wb < a.nQ - 1 ? j + wb : a.nQ - 1;
+  for (int c = j; c <= c1; ++c) {
+    __syncthreads();
+    const int64_t qb = ((int64_t)b * a.nQ * 64 + (int64_t)c * 64) * ts + h * DHT;
+    for (int x = t; x < 64 * DHT; x += 64) {
+      const int row = x / DHT, d = x % DHT;
+      Qs[row][d] = Elem<T>::ld(reinterpret_cast<const T*>(a.q) + qb + row * ts + d);
+      dOs[row][d] = Elem<T>::ld(reinterpret_cast<const T*>(a.dout) + qb + row * ts + d);
+    }
+    const int64_t rb = (((int64_t)b * a.nQ + c) * a.H + h) * 64;
+    ls[t] = a.lse[rb + t];
+    Ds[t] = a.Dbuf[rb + t];
+    __syncthreads();
+    const int kind = c == j ? 2 : (c == j + wb ? 1 : 0);
+    for (int qr = 0; qr < 64; ++qr) {
+      if (dropped(kind, t, qr)) continue;  // this thread's key t against query row qr
+      float s = 0.f, dp = 0.f;
+      for (int d = 0; d < DHT; ++d) {
+        s = fmaf(Qs[qr][d], kv[d], s);
+        dp = fmaf(dOs[qr][d], vv[d], dp);
+      }
+      const float p = expf(s * scale - ls[qr]);
+      const float ds = p * (dp - Ds[qr]) * scale;
+      for (int d = 0; d < DHT; ++d) {
+        dv[d] = fmaf(p, dOs[qr][d], dv[d]);
+        dk[d] = fmaf(ds, Qs[qr][d], dk[d]);
+      }
+    }
+  }
+  for (int d = 0; d < DHT; ++d) {
+    T* pk = reinterpret_cast<T*>(a.dk) + tok + d;
+    T* pv = reinterpret_cast<T*>(a.dv) + tok + d;
+    Elem<T>::st(pk, a.accumulate ? Elem<T>::ld(pk) + dk[d] : dk[d]);
+    Elem<T>::st(pv, a.accumulate ? Elem<T>::ld(pv) + dv[d] : dv[d]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_window_backward(const WindowBwdArgs& a, cudaStream_t s) {
+  const int64_t nrows = (int64_t)a.B * a.nQ * 64 * a.H;
+  const unsigned dgrid = (unsigned)((nrows + 255) / 256);
+  launch_begin("window_d", s);
+  if (a.bf16) {
+    if (a.dh == 64) window_d_kernel<bf16, 64><<<dgrid, 256, 0, s>>>(a);
+    else window_d_kernel<bf16, 32><<<dgrid, 256, 0, s>>>(a);
+  } else {
+    if (a.dh == 64) window_d_kernel<float, 64><<<dgrid, 256, 0, s>>>(a);
+    else window_d_kernel<float, 32><<<dgrid, 256, 0, s>>>(a);
+  }
+  cudaError_t e = launch_end("window_d", s);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.nQ, a.H, a.B);
+  if (a.bf16 && a.dh == 64) {
+    CUtensorMap tq, tdo, tk, tv;
+    const int64_t bs = (int64_t)a.nQ * 64 * a.H * 64, rows = (int64_t)a.nQ * 64;
+    e = make_head_tmap(&tq, a.q, 64, a.H, rows, a.B, bs);
+    if (e == cudaSuccess) e = make_head_tmap(&tdo, a.dout, 64, a.H, rows, a.B, bs);
+    if (e == cudaSuccess) e = make_head_tmap(&tk, a.k, 64, a.H, rows, a.B, bs);
+    if (e == cudaSuccess) e = make_head_tmap(&tv, a.v, 64, a.H, rows, a.B, bs);
+    if (e == cudaSuccess) e = allow_smem((const void*)window_bwd_q_tc_kernel, kQSmem);
+    if (e == cudaSuccess) e = allow_smem((const void*)window_bwd_kv_tc_kernel, kKVSmem);
+    if (e != cudaSuccess) return e;
+    launch_begin("window_bwd_q", s);
+    window_bwd_q_tc_kernel<<<grid, kThreads, kQSmem, s>>>(a, tq, tdo, tk, tv);
+    if ((e = launch_end("window_bwd_q", s)) != cudaSuccess) return e;
+    launch_begin("window_bwd_kv", s);
+    window_bwd_kv_tc_kernel<<<grid, kThreads, kKVSmem, s>>>(a, tq, tdo, tk, tv);
+    return launch_end("window_bwd_kv", s);
+  }
+  launch_begin("window_bwd_q", s);
+  if (a.bf16) window_bwd_q_simt_kernel<bf16, 32><<<grid, 64, 0, s>>>(a);
+  else if (a.dh == 64) window_bwd_q_simt_kernel<float, 64><<<grid, 64, 0, s>>>(a);
+  else window_bwd_q_simt_kernel<float, 32><<<grid, 64, 0, s>>>(a);
+  if ((e = launch_end("window_bwd_q", s)) != cudaSuccess) return e;
+  launch_begin("window_bwd_kv", s);
+  if (a.bf16) window_bwd_kv_simt_kernel<bf16, 32><<<grid, 64, 0, s>>>(a);
+  else if (a.dh == 64) window_bwd_kv_simt_kernel<float, 64><<<grid, 64, 0, s>>>(a);
+  else window_bwd_kv_simt_kernel<float, 32><<<grid, 64, 0, s>>>(a);
+  return launch_end("window_bwd_kv", s);
+}
+
+}  // namespace gca

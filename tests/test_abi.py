@@ -125,6 +125,35 @@ def test_gather_rejects_bad_arguments(gca):
     assert b"workspace" in gca.LIB.gca_last_error_detail()
 
 
+def test_window_and_cca_reject_bad_arguments(gca):
+    L = gca.LIB
+    def win(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, dt=gca.GCA_BF16, B=4, L=16384, H=12, dh=64, W=512, o=FAKE, lse=FAKE, acc=0,
+                 ws=FAKE, wsb=256)
+        a.update(kw)
+        return L.gca_window_forward(a["q"], a["k"], a["v"], a["dt"], a["B"], a["L"], a["H"], a["dh"], a["W"], a["o"],
+                                    a["lse"], a["acc"], a["ws"], a["wsb"], None)
+    assert win(W=500) == gca.GCA_ERR_UNSUPPORTED
+    assert win(W=0) == gca.GCA_ERR_UNSUPPORTED
+    assert win(W=64 * 64) == gca.GCA_ERR_UNSUPPORTED
+    assert win(L=100) == gca.GCA_ERR_INVALID_ARG
+    assert win(dh=48) == gca.GCA_ERR_UNSUPPORTED
+    assert win(o=0) == gca.GCA_ERR_INVALID_ARG
+    assert win(k=FAKE + 4) == gca.GCA_ERR_INVALID_ARG
+    assert win(wsb=16) == gca.GCA_ERR_WORKSPACE
+    assert L.gca_window_backward_workspace_size(4, 16384, 12) >= 256 + 4 * 256 * 12 * 64 * 4
+    assert L.gca_window_backward(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, gca.GCA_BF16, 4, 16384, 12, 64, 512, FAKE, FAKE,
+                                 FAKE, 0, FAKE, 256, None) == gca.GCA_ERR_WORKSPACE
+    assert L.gca_window_backward(FAKE, FAKE, FAKE, 0, FAKE, FAKE, gca.GCA_BF16, 4, 16384, 12, 64, 512, FAKE, FAKE,
+                                 FAKE, 0, FAKE, 1 << 30, None) == gca.GCA_ERR_INVALID_ARG
+    assert L.gca_cca_forward(FAKE, FAKE, FAKE, 0, gca.GCA_BF16, 4, 256, 256, 12, 64, FAKE, 17, 1, FAKE, FAKE, 0, FAKE,
+                             256, None) == gca.GCA_ERR_UNSUPPORTED
+    assert L.gca_cca_forward(FAKE, FAKE, FAKE, 0, gca.GCA_BF16, 4, 256, 256, 12, 64, 0, 8, 1, FAKE, FAKE, 0, FAKE,
+                             256, None) == gca.GCA_ERR_INVALID_ARG
+    assert L.gca_cca_forward(FAKE, FAKE, FAKE, 0, gca.GCA_BF16, 4, 256, 256, 12, 64, FAKE, 8, 2, FAKE, FAKE, 0, FAKE,
+                             256, None) == gca.GCA_ERR_INVALID_ARG
+
+
 def test_backward_and_scores_backward_reject_bad_arguments(gca):
     L = gca.LIB
     r = L.gca_backward(FAKE, FAKE, FAKE, gca.GCA_BF16, 4, 256, 256, 12, 64, FAKE, FAKE, 8, 1, FAKE, FAKE,

@@ -73,6 +73,39 @@ def test_window_full_size_sampled():
         assert_close(host(lse[b, t // 64, :, t % 64]), lo[0, t - s0], TOL["bf16"], f"LSE[{b},{t}]")
 
 
+@pytest.mark.parametrize("dtype,dh,L,W", [("bf16", 64, 1024, 512), ("bf16", 64, 384, 64), ("bf16", 64, 256, 1024),
+                                          ("f32", 32, 320, 128), ("f32", 64, 192, 128), ("bf16", 32, 256, 192)])
+def test_window_backward_against_oracle(dtype, dh, L, W):
+    g = _g()
+    B, H = 2, 2
+    q, k, v = _qkv(36, B, L, H, dh, dtype)
+    do = synth.normal(36, synth.S_DO, (B, L, H, dh), 1.0, dtype)
+    qd, kd, vd, dod = (dev(x, dtype) for x in (q, k, v, do))
+    o, lse = g.window_forward(qd, kd, vd, window=W)
+    dq, dk, dv = g.window_backward(qd, kd, vd, o, dod, lse, window=W)
+    torch.cuda.synchronize()
+    rq, rk, rv = orc.swa_backward(q, k, v, do, W)
+    assert_close(host(dq), rq, TOL[dtype], "dQ")
+    assert_close(host(dk), rk, TOL[dtype], "dK")
+    assert_close(host(dv), rv, TOL[dtype], "dV")
+
+
+def test_window_backward_accumulates():
+    g = _g()
+    B, L, H, dh, W = 1, 256, 2, 64, 128
+    q, k, v = _qkv(37, B, L, H, dh, "bf16")
+    do = synth.normal(37, synth.S_DO, (B, L, H, dh), 1.0, "bf16")
+    qd, kd, vd, dod = (dev(x, "bf16") for x in (q, k, v, do))
+    o, lse = g.window_forward(qd, kd, vd, window=W)
+    base = [torch.full_like(qd, 0.5) for _ in range(3)]
+    dq, dk, dv = g.window_backward(qd, kd, vd, o, dod, lse, window=W, dq=base[0], dk=base[1], dv=base[2],
+                                   accumulate=True)
+    torch.cuda.synchronize()
+    rq, rk, rv = orc.swa_backward(q, k, v, do, W)
+    for got, ref, n in ((dq, rq, "dQ"), (dk, rk, "dK"), (dv, rv, "dV")):
+        assert_close(host(got), ref + 0.5, 3e-2, n)
+
+
 def _cca_case(seed, B, nC, H, dh, K, dtype):
     x = synth.gca_inputs(seed, B, nC, nC, H, dh, 1.0, dtype)
     lm = synth.landmark_inputs(seed, B, nC, nC, 128, dtype)
