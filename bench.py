@@ -152,9 +152,9 @@ KERNEL_SOURCES = {
     "retrieve_stream": ("retrieve.cu", "common.cuh"),
 }
 KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
-    "gca_fwd": (382.8e6, "55be0ffd024a817d"),
-    "gca_bwd_q": (514.6e6, "dcb2b906194b5e0b"),
-    "gca_bwd_kv": (606.5e6, "dcb2b906194b5e0b"),
+    "gca_fwd": (382.37e6, "7e6df2385ac4ce02"),
+    "gca_bwd_q": (510.45e6, "5c4fccd2ea985839"),
+    "gca_bwd_kv": (603.0e6, "5c4fccd2ea985839"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
 STREAM_TRAFFIC_PER_SEQ = (808.35e6 / 2, "74df39448ea668d2")

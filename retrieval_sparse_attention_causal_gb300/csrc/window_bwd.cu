@@ -26,21 +26,34 @@ constexpr int TILE = 8192, ROWB = 128, UPR = 8, DH = 64;
 enum { kBarOpReady = 2, kBarEW = 3 };
 
 // ------------------------------------------------------------------ D = rowsum(dO * O)
-// One thread per (token, head) row; D [B][L/64][H][64] like the LSE.
+// LPR consecutive lanes per (token, head) row, one 16-byte vector of O and of dO each, so a
+// warp reads 32 contiguous vectors; the partial dot products meet by shuffles.
+// D [B][L/64][H][64] like the LSE.
 template <typename T, int DHT>
 __global__ void __launch_bounds__(256) window_d_kernel(WindowBwdArgs a) {
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // token * H + h
+  constexpr int EPV = Elem<T>::kVec, LPR = DHT / EPV;
+  static_assert(32 % LPR == 0, "a row's lanes stay inside one warp");
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = g / LPR;  // token * H + h
+  const int part = (int)(g % LPR);
   const int64_t nrows = (int64_t)a.B * a.nQ * 64 * a.H;
-  if (row >= nrows) return;
-  const int64_t tok = row / a.H;
-  const int h = (int)(row % a.H);
-  const T* o = reinterpret_cast<const T*>(a.o) + row * DHT;
-  const T* d = reinterpret_cast<const T*>(a.dout) + row * DHT;
   float acc = 0.f;
-#pragma unroll 8
-  for (int x = 0; x < DHT; ++x) acc = fmaf(Elem<T>::ld(o + x), Elem<T>::ld(d + x), acc);
-  const int64_t bc = tok / 64;  // b * nQ + c
-  a.Dbuf[(bc * a.H + h) * 64 + tok % 64] = acc;
+  if (row < nrows) {
+    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.o) + row * DHT) + part);
+    const uint4 dv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.dout) + row * DHT) + part);
+    float of[EPV], df[EPV];
+    unpack16(ov, of, static_cast<const T*>(nullptr));
+    unpack16(dv, df, static_cast<const T*>(nullptr));
+#pragma unroll
+    for (int x = 0; x < EPV; ++x) acc = fmaf(of[x], df[x], acc);
+  }
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < nrows && part == 0) {
+    const int64_t tok = row / a.H;
+    const int h = (int)(row % a.H);
+    a.Dbuf[((tok / 64) * a.H + h) * 64 + tok % 64] = acc;  // tok / 64 = b * nQ + c
+  }
 }
 
 // Mask of key column kc against query row qr inside a block pair: kind 1 (tail block of
@@ -517,7 +530,8 @@ __global__ void __launch_bounds__(64) window_bwd_kv_simt_kernel(WindowBwdArgs a)
 
 cudaError_t launch_window_backward(const WindowBwdArgs& a, cudaStream_t s) {
   const int64_t nrows = (int64_t)a.B * a.nQ * 64 * a.H;
-  const unsigned dgrid = (unsigned)((nrows + 255) / 256);
+  const int lpr = a.dh * (a.bf16 ? 2 : 4) / 16;  // lanes per row in window_d_kernel
+  const unsigned dgrid = (unsigned)((nrows * lpr + 255) / 256);
   launch_begin("window_d", s);
   if (a.bf16) {
     if (a.dh == 64) window_d_kernel<bf16, 64><<<dgrid, 256, 0, s>>>(a);
