@@ -33,6 +33,14 @@ chunked cross-attention (CCA) it is contrasted with):
   * CCA: the tokens of a query chunk attend to the concatenation of its retrieved chunks
     with one joint softmax; the retrieval scores take no part.
 
+And the encoder in front of the upper layers (Notes, framework): every chunk's 64 tokens
+plus its LMK token go through a bidirectional Transformer encoder; its token outputs,
+through one shared K/V transform, are GCA's K and V, and its LMK output is the chunk's
+landmark (k_lmk).  The pages give neither the depth nor the layer's form; the reading
+here is one pre-LN layer (multi-head attention over the chunk's 65 rows with no mask,
+then a d -> 4d -> d MLP with the erf GELU, each with a residual), LayerNorm eps 1e-5,
+and a bias-free K/V transform.
+
 Readings where the pages are silent (each also listed in the design notes):
   * the next-chunk rule is a shift: query chunk c uses retrieval row c - shift
     (shift = 1 in training, 0 at decode); chunks with no row get O = 0;
@@ -531,3 +539,61 @@ def _scores_at(q_lmk, k_lmk, idx):
 
 
 scores_at = _scores_at
+
+
+# ---------------------------------------------------------------------------
+# Chunk / landmark encoder (Notes, framework): the lower layers' output, with a
+# landmark (LMK) token at the end of every 64-token chunk, passes through a
+# bidirectional Transformer encoder that yields the chunk representations (source of
+# GCA's K and V, one K/V transform shared by all upper layers: Notes, key design / GCA)
+# and the landmark representations (the k_lmk of retrieval).
+# ---------------------------------------------------------------------------
+
+ENC_CHUNK = CHUNK + 1  # a chunk's 64 tokens followed by its LMK token
+
+
+def layer_norm(x, g, b, eps=1e-5):
+    """Each row over its last axis: (x - mean) / sqrt(var + eps) * g + b, with the
+    population variance."""
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps) * g + b
+
+
+def gelu(x):
+    """x * Phi(x), Phi the standard normal distribution function (the erf form)."""
+    from scipy.special import erf
+    return 0.5 * x * (1.0 + erf(x / math.sqrt(2.0)))
+
+
+def chunk_encoder_forward(x, p, H):
+    """One pre-LN bidirectional encoder layer applied to every chunk on its own, then
+    the shared K/V transform of the chunk representations.
+
+    x [B, nC * 65, d]: per chunk its 64 token rows, then its LMK row.  p holds
+    ln1_g, ln1_b, w_qkv [3d, d], b_qkv, w_o [d, d], b_o, ln2_g, ln2_b, w_1 [4d, d], b_1,
+    w_2 [d, 4d], b_2 and w_kv [2d, d] (K rows first).  With dh = d / H:
+        u = x + MHA(LN1(x)) W_o^T + b_o,  attention over the 65 rows of the chunk, no mask,
+            logits scaled by dh^-1/2;
+        y = u + GELU(LN2(u) W_1^T + b_1) W_2^T + b_2;
+        k_lmk = y at the LMK rows [B, nC, d];
+        K, V = (y at the token rows) W_K^T, W_V^T, as [B, nC * 64, H, dh].
+    """
+    B, M, d = x.shape
+    assert M % ENC_CHUNK == 0 and d % H == 0
+    nC, dh = M // ENC_CHUNK, d // H
+    xn = layer_norm(x, p["ln1_g"], p["ln1_b"])
+    qkv = xn @ p["w_qkv"].T + p["b_qkv"]  # [B, M, 3d]
+    heads = [qkv[..., i * d:(i + 1) * d].reshape(B, nC, ENC_CHUNK, H, dh).transpose(0, 1, 3, 2, 4)
+             for i in range(3)]  # q, k, v [B, nC, H, 65, dh]
+    S = heads[0] @ heads[1].transpose(0, 1, 2, 4, 3) / math.sqrt(dh)  # [B, nC, H, 65(query), 65(key)]
+    P, _ = _softmax_rows(S)
+    a = (P @ heads[2]).transpose(0, 1, 3, 2, 4).reshape(B, M, d)
+    u = x + a @ p["w_o"].T + p["b_o"]
+    f = gelu(layer_norm(u, p["ln2_g"], p["ln2_b"]) @ p["w_1"].T + p["b_1"])
+    y = u + f @ p["w_2"].T + p["b_2"]
+    yc = y.reshape(B, nC, ENC_CHUNK, d)
+    tok = yc[:, :, :CHUNK].reshape(B, nC * CHUNK, d)
+    kk = (tok @ p["w_kv"][:d].T).reshape(B, nC * CHUNK, H, dh)
+    vv = (tok @ p["w_kv"][d:].T).reshape(B, nC * CHUNK, H, dh)
+    return {"u": u, "y": y, "k_lmk": yc[:, :, CHUNK].copy(), "k": kk, "v": vv}

@@ -90,6 +90,34 @@ def planted_landmarks(seed, B, nC, D, dtype):
 
 
 # ---------------------------------------------------------------------------
+# Chunk encoder: input rows and synthetic weights.
+# ---------------------------------------------------------------------------
+
+S_ENC_X = 30  # stream ids 30.. belong to the encoder
+ENC_MATRICES = {"w_qkv": (3, 1), "w_o": (1, 1), "w_1": (4, 1), "w_2": (1, 4), "w_kv": (2, 1)}  # (rows, cols) in units of d
+ENC_VECTORS = {"ln1_g": 1, "ln1_b": 1, "b_qkv": 3, "b_o": 1, "ln2_g": 1, "ln2_b": 1, "b_1": 4, "b_2": 1}  # length in units of d
+
+
+def encoder_inputs(seed, B, nC, d, dtype, std=1.0):
+    """Encoder input x [B, nC * 65, d]: per chunk its 64 token rows, then its LMK row."""
+    return normal(seed, S_ENC_X, (B, nC * (CHUNK + 1), d), std, dtype)
+
+
+def encoder_params(seed, d, dtype, w_scale=1.0):
+    """Synthetic encoder weights (float64 values).  Matrices are N(0, w_scale^2 / fan_in)
+    rounded to `dtype`, so that every projection keeps its input's scale; biases are
+    N(0, 0.02^2) and LayerNorm gains 1 + N(0, 0.1^2), shifts N(0, 0.1^2), all float32."""
+    p = {}
+    for n, (name, (r, c)) in enumerate(sorted(ENC_MATRICES.items())):
+        p[name] = normal(seed, S_ENC_X + 1 + n, (r * d, c * d), w_scale / (c * d) ** 0.5, dtype)
+    for n, (name, r) in enumerate(sorted(ENC_VECTORS.items())):
+        std = 0.02 if name.startswith("b_") else 0.1
+        v = normal(seed, S_ENC_X + 10 + n, (r * d,), std, "f32")
+        p[name] = quantize(1.0 + v, "f32") if name.endswith("_g") else v
+    return p
+
+
+# ---------------------------------------------------------------------------
 # Device-side draws for the full-size workloads (hundreds of MB to tens of GB).
 # ---------------------------------------------------------------------------
 

@@ -558,4 +558,100 @@ def pin_cca_no_slot_and_shift(orc):
     assert np.all(np.abs(o[0, 4:8]) > 0)
 
 
+# ------------------------------------------------------------------------ chunk encoder
+
+def _enc_params(rng, d):
+    f = lambda *sh: rng.standard_normal(sh)
+    return {"ln1_g": 1 + 0.2 * f(d), "ln1_b": 0.2 * f(d), "w_qkv": f(3 * d, d) / math.sqrt(d),
+            "b_qkv": 0.1 * f(3 * d), "w_o": f(d, d) / math.sqrt(d), "b_o": 0.1 * f(d),
+            "ln2_g": 1 + 0.2 * f(d), "ln2_b": 0.2 * f(d), "w_1": f(4 * d, d) / math.sqrt(d),
+            "b_1": 0.1 * f(4 * d), "w_2": f(d, 4 * d) / math.sqrt(4 * d), "b_2": 0.1 * f(d),
+            "w_kv": f(2 * d, d) / math.sqrt(d)}
+
+
+def _torch_encoder_layer(p, d, H):
+    """torch's own pre-LN encoder layer (float64, no dropout) holding the weights p."""
+    import torch
+    layer = torch.nn.TransformerEncoderLayer(d, H, 4 * d, dropout=0.0, activation="gelu", layer_norm_eps=1e-5,
+                                             batch_first=True, norm_first=True, dtype=torch.float64)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    with torch.no_grad():
+        for mod, w, b in ((layer.self_attn, "w_qkv", "b_qkv"),):
+            mod.in_proj_weight.copy_(t(p[w]))
+            mod.in_proj_bias.copy_(t(p[b]))
+        for mod, w, b in ((layer.self_attn.out_proj, "w_o", "b_o"), (layer.linear1, "w_1", "b_1"),
+                          (layer.linear2, "w_2", "b_2"), (layer.norm1, "ln1_g", "ln1_b"),
+                          (layer.norm2, "ln2_g", "ln2_b")):
+            mod.weight.copy_(t(p[w]))
+            mod.bias.copy_(t(p[b]))
+    return layer.train(False)
+
+
+def pin_encoder_is_torch_encoder_layer(orc):
+    """Each 65-row chunk through torch.nn.TransformerEncoderLayer (pre-LN, erf GELU,
+    eps 1e-5, float64) with the same weights gives y; the LMK rows of y are k_lmk."""
+    import torch
+    rng = np.random.default_rng(41)
+    B, nC, d, H = 2, 3, 16, 2
+    x = rng.standard_normal((B, nC * 65, d))
+    p = _enc_params(rng, d)
+    r = orc.chunk_encoder_forward(x, p, H)
+    layer = _torch_encoder_layer(p, d, H)
+    with torch.no_grad():
+        ref = layer(torch.from_numpy(x.reshape(B * nC, 65, d))).numpy().reshape(B, nC * 65, d)
+    assert np.max(np.abs(r["y"] - ref)) < 1e-11
+    assert np.max(np.abs(r["k_lmk"] - ref.reshape(B, nC, 65, d)[:, :, 64])) < 1e-11
+
+
+def pin_encoder_kv_transform_layout(orc):
+    """W_K = I and W_V = 2 I: K and V are the token rows of y (the LMK rows left out),
+    split into heads in order, so K[b, 64 c + t, h] = y[b, 65 c + t, h dh : (h + 1) dh]."""
+    rng = np.random.default_rng(42)
+    B, nC, d, H = 1, 3, 12, 3
+    x = rng.standard_normal((B, nC * 65, d))
+    p = _enc_params(rng, d)
+    p["w_kv"] = np.concatenate([np.eye(d), 2 * np.eye(d)])
+    r = orc.chunk_encoder_forward(x, p, H)
+    y = r["y"]
+    for c in range(nC):
+        for t in (0, 17, 63):
+            for h in range(H):
+                want = y[0, 65 * c + t, 4 * h:4 * (h + 1)]
+                assert np.array_equal(r["k"][0, 64 * c + t, h], want)
+                assert np.array_equal(r["v"][0, 64 * c + t, h], 2 * want)
+
+
+def pin_encoder_chunks_independent_and_bidirectional(orc):
+    """Changing the last token of chunk 1 changes every row of chunk 1, its first token
+    and its LMK included (no causal mask), and no row of chunks 0 and 2.  Permuting the
+    64 tokens of a chunk permutes their outputs and leaves the LMK output as it was."""
+    rng = np.random.default_rng(43)
+    B, nC, d, H = 1, 3, 8, 2
+    x = rng.standard_normal((B, nC * 65, d))
+    p = _enc_params(rng, d)
+    y0 = orc.chunk_encoder_forward(x, p, H)["y"]
+    x1 = x.copy()
+    x1[0, 65 + 63] += rng.standard_normal(d)  # not a constant: LayerNorm would remove that
+    y1 = orc.chunk_encoder_forward(x1, p, H)["y"]
+    assert np.array_equal(y0[0, :65], y1[0, :65]) and np.array_equal(y0[0, 130:], y1[0, 130:])
+    assert np.all(np.abs(y0[0, 65:130] - y1[0, 65:130]).max(-1) > 1e-9)
+    perm = rng.permutation(64)
+    x2 = x.copy()
+    x2[0, 65:129] = x[0, 65 + perm]
+    y2 = orc.chunk_encoder_forward(x2, p, H)["y"]
+    assert np.max(np.abs(y2[0, 65:129] - y0[0, 65 + perm])) < 1e-12
+    assert np.max(np.abs(y2[0, 129] - y0[0, 129])) < 1e-12
+
+
+def pin_gelu_and_layer_norm_closed_forms(orc):
+    """GELU(x) = x Phi(x): Phi(1) = 0.841344746068543, Phi(-1) = 0.158655253931457,
+    GELU(0) = 0.  LayerNorm of (1, 2, 3, 4) with gain 1, shift 0 and eps 0: mean 5/2,
+    population variance 5/4, so (x - 5/2) * 2/sqrt(5)."""
+    g = orc.gelu(np.array([1.0, -1.0, 0.0, 2.0]))
+    want = [0.841344746068543, -0.158655253931457, 0.0, 2 * 0.977249868051821]
+    assert np.max(np.abs(g - want)) < 1e-14
+    ln = orc.layer_norm(np.array([1.0, 2.0, 3.0, 4.0]), 1.0, 0.0, eps=0.0)
+    assert np.max(np.abs(ln - (np.array([1, 2, 3, 4]) - 2.5) * 2 / math.sqrt(5))) < 1e-15
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -52,6 +52,20 @@ MUTATIONS = {
     "swa_bwd_window_mask": ("allowed = (t[None, :] <= t[:, None]) & (t[None, :] > t[:, None] - window)  # [query, key]",
                             "allowed = (t[None, :] <= t[:, None]) & (t[None, :] >= t[:, None] - window)  # [query, key]"),
     "swa_bwd_dk_scale": ("dk[b, :, h] = dS.T @ Q / math.sqrt(dh)", "dk[b, :, h] = dS.T @ Q"),
+    "encoder_causal": ("P, _ = _softmax_rows(S)\n    a = (P @ heads[2])",
+                       "P, _ = _softmax_rows(np.where(np.tri(ENC_CHUNK, dtype=bool), S, -np.inf))\n    a = (P @ heads[2])"),
+    "encoder_lmk_not_a_key": ("P, _ = _softmax_rows(S)\n    a = (P @ heads[2])",
+                              "P, _ = _softmax_rows(np.where(np.arange(ENC_CHUNK) < CHUNK, S, -np.inf))\n    a = (P @ heads[2])"),
+    "encoder_post_ln": ("u = x + a @ p[\"w_o\"].T + p[\"b_o\"]",
+                        "u = layer_norm(x + a @ p[\"w_o\"].T + p[\"b_o\"], p[\"ln1_g\"], p[\"ln1_b\"])"),
+    "encoder_gelu_tanh": ("return 0.5 * x * (1.0 + erf(x / math.sqrt(2.0)))",
+                          "return 0.5 * x * (1.0 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))"),
+    "encoder_ln_sample_variance": ("var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)",
+                                   "var = ((x - mu) ** 2).sum(axis=-1, keepdims=True) / (x.shape[-1] - 1)"),
+    "encoder_kv_rows_shifted": ("tok = yc[:, :, :CHUNK].reshape(B, nC * CHUNK, d)",
+                                "tok = yc[:, :, 1:].reshape(B, nC * CHUNK, d)"),
+    "encoder_heads_interleaved": ("for i in range(3)]  # q, k, v [B, nC, H, 65, dh]",
+                                  "for i in range(3)]  # q, k, v [B, nC, H, 65, dh]\n    heads = [h.reshape(B, nC, dh, ENC_CHUNK, H).transpose(0, 1, 4, 3, 2) for h in heads]"),
     "swa_bwd_rowsum": ("dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))", "dS = P * (dP - np.sum(dP, axis=1, keepdims=True))"),
 }
 
