@@ -273,6 +273,8 @@ def gpu_arm(args):
     # The rest of the attention block at the same shape: sliding-window self-attention
     # (W = 512) and, as the ablation, chunked cross-attention over the same retrieval.
     blk = None if args.no_block else block_attn_leg(args, torch, gca, q, k, v, out, timed)
+    # The chunk / landmark encoder that produces K, V and the key landmarks.
+    enc = None if args.no_encoder else encoder_leg(args, torch, gca, synth, timed, pk)
 
     # End to end through the public API from pinned host buffers.
     e2e = None
@@ -296,7 +298,7 @@ def gpu_arm(args):
             "step_tflops_algorithmic": round(step_tflops, 2),
             "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary(),
             "kernels": {n: round(x["avg_ms"], 5) for n, x in kern.items()},
-            "e2e": e2e, "decode": dec, "block_attention": blk, "cpu_baseline": cpu,
+            "e2e": e2e, "decode": dec, "block_attention": blk, "encoder": enc, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -504,6 +506,67 @@ def block_attn_leg(args, torch, gca, q, k, v, out, timed):
                     "tflops_algorithmic": round(fl_c / (ms_c / 1e3) / 1e12, 1)}}
 
 
+ENC_D, ENC_H = 768, 12  # the 128M model's width: the encoder's rows have d = H * 64 = 768
+
+
+def encoder_flops(nb, nc, d, h):
+    """Algorithmic flops of one encoder pass, per kernel: 2 m n k for each GEMM over the
+    rows it needs (every row of the layer; token rows only for the K/V transform) and
+    4 * 65^2 * 64 per (chunk, head) for the in-chunk attention (QK^T and PV)."""
+    m, mt = nb * nc * 65, nb * nc * 64
+    return {"enc_qkv": 2 * m * d * 3 * d, "enc_attn": 4 * 65 * 65 * 64 * nb * nc * h, "enc_out": 2 * m * d * d,
+            "enc_mlp1": 2 * m * d * 4 * d, "enc_mlp2": 2 * m * 4 * d * d, "enc_kv": 2 * mt * d * 2 * d}
+
+
+def encoder_leg(args, torch, gca, synth, timed, pk):
+    """The chunk / landmark encoder at the training shape (B = 4, 256 chunks of 64 tokens
+    plus their LMK rows, d = 768, 12 heads): one pre-LN encoder layer over every chunk and
+    the shared K/V transform, with synthetic weights (matrices N(0, 1/fan_in) in bf16,
+    biases N(0, 0.02^2), LayerNorm gains 1).  Reports the pass time, tokens/s and per-kernel
+    algorithmic TFLOP/s against the measured bf16 peak."""
+    d, h = ENC_D, ENC_H
+    x = synth.device_normal(args.seed, synth.S_ENC_X, (B, NC * 65, d), 1.0, torch.bfloat16)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(args.seed + 17)
+    w = {}
+    for n in gca.ENCODER_WEIGHTS:
+        if n.startswith("w_"):
+            rows, cols = {"w_qkv": (3 * d, d), "w_o": (d, d), "w_1": (4 * d, d), "w_2": (d, 4 * d), "w_kv": (2 * d, d)}[n]
+            w[n] = (torch.randn((rows, cols), device="cuda", generator=gen) / cols ** 0.5).to(torch.bfloat16)
+        else:
+            size = {"b_qkv": 3 * d, "b_1": 4 * d}.get(n, d)
+            w[n] = torch.ones(size, device="cuda") if n.endswith("_g") else 0.02 * torch.randn(size, device="cuda", generator=gen)
+    ws = gca.Workspace()
+    y = torch.empty_like(x)
+    kk = torch.empty((B, NC * 64, d), dtype=torch.bfloat16, device="cuda")
+    vv = torch.empty_like(kk)
+    kl = torch.empty((B, NC, d), dtype=torch.bfloat16, device="cuda")
+
+    def enc(i):
+        gca.chunk_encoder(x, w, h, ws=ws, y=y, k=kk, v=vv, k_lmk=kl)
+
+    for i in range(args.warmup):
+        enc(i)
+    ws.check()
+    ms = timed(enc, args.steps) / args.steps
+    gca.profile_begin()
+    timed(enc, args.steps)
+    prof = gca.profile_end()
+    fl = encoder_flops(B, NC, d, h)
+    kern = {}
+    for n, (c, t) in prof.items():
+        avg = t / c
+        row = {"avg_ms": round(avg, 5)}
+        if n in fl:
+            row["tflops"] = round(fl[n] / (avg / 1e3) / 1e12, 1)
+            row["frac_of_bf16_peak"] = round(fl[n] / (avg / 1e3) / 1e12 / pk["bf16_tflops"], 3)
+        kern[n] = row
+    total = sum(fl.values())
+    return {"B": B, "chunks": NC, "d": d, "heads": h, "ms": round(ms, 4),
+            "tokens_per_s": round(B * NC * 64 / (ms / 1e3), 1),
+            "tflops_algorithmic": round(total / (ms / 1e3) / 1e12, 1), "kernels": kern}
+
+
 def offload_leg(args, torch, gca, kst, vst, qn, ql, kl, ws, o, lse, idx, sc, time_loop):
     """Decode with the K/V store in pinned host memory (the inference offload): the same
     store as the device-resident decode copied to a pinned host buffer (2 x 25.8 GB, shared
@@ -642,6 +705,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-offload", action="store_true", help="skip the host-memory K/V store decode")
     ap.add_argument("--no-block", action="store_true", help="skip the window-attention and CCA leg")
+    ap.add_argument("--no-encoder", action="store_true", help="skip the chunk / landmark encoder leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -218,6 +218,48 @@ GCA_API gca_status gca_cca_forward(const void* q, const void* k, const void* v, 
                            size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * gca_chunk_encoder_forward - the chunk / landmark encoder and the shared K/V transform.
+ *
+ * Paper-Notes page, 整体框架 (framework): the lower layers' output, with an LMK token
+ * closing every 64-token chunk, passes a bidirectional Transformer encoder that yields
+ * the chunk representations and the landmark representations shared by the upper
+ * layers; 关键设计 / GCA: one K/V transform serves all of them.  Read as one pre-LN
+ * encoder layer applied to every chunk on its own (the pages give neither depth nor
+ * form), with dh = d / H:
+ *     u = x + MHA(LN1(x)) W_o^T + b_o     attention over the chunk's 65 rows, no mask,
+ *                                         logits scaled by dh^-1/2;
+ *     y = u + GELU(LN2(u) W_1^T + b_1) W_2^T + b_2      (erf GELU, LayerNorm eps 1e-5);
+ *     k_lmk = y at the LMK rows;   K, V = (y at the token rows) W_K^T, W_V^T.
+ *
+ *   x       [B][nC*65][d] bf16: per chunk its 64 token rows, then its LMK row.
+ *   w       weights: matrices bf16 [out][in] row-major (w_qkv [3d][d] with the Q, K, V
+ *           blocks in that order and heads contiguous inside each; w_o [d][d]; w_1 [4d][d];
+ *           w_2 [d][4d]; w_kv [2d][d], K rows first); biases and LayerNorm gains/shifts
+ *           float32 ([3d], [d], [4d], [d]; [d]).  Caller-owned device memory.
+ *   y       [B][nC*65][d] bf16 out: the encoder's output rows.
+ *   k, v    [B][nC*64][d] bf16 out: GCA's keys and values, i.e. [B][L][H'][dh'] for any
+ *           head split H' dh' = d of the upper layers.
+ *   k_lmk   [B][nC][d] bf16 out: the landmark representations (retrieval's k_lmk, D = d).
+ *   dtype   GCA_BF16 (GCA_ERR_UNSUPPORTED otherwise).   d a multiple of 128 in 128..1024,
+ *           H = d / 64 (encoder head dim 64).  All pointers 16-byte aligned.
+ *   ws      >= gca_chunk_encoder_workspace_size(B, nC, d) bytes: the error word and the
+ *           intermediate rows (B*nC*65 x 6d bf16).
+ * ------------------------------------------------------------------------------- */
+typedef struct {
+  const float* ln1_g; const float* ln1_b;
+  const void* w_qkv;  const float* b_qkv;
+  const void* w_o;    const float* b_o;
+  const float* ln2_g; const float* ln2_b;
+  const void* w_1;    const float* b_1;
+  const void* w_2;    const float* b_2;
+  const void* w_kv;
+} gca_encoder_weights;
+GCA_API size_t gca_chunk_encoder_workspace_size(int B, int nC, int d);
+GCA_API gca_status gca_chunk_encoder_forward(const void* x, gca_dtype dtype, int B, int nC, int d, int H,
+                                     const gca_encoder_weights* w, void* y, void* k, void* v, void* k_lmk,
+                                     void* ws, size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * gca_gather_chunks - copy the retrieved chunks' keys and values into a compact buffer.
  *
  * Paper-Notes page, 关键设计 / key design (inference memory offload): the past chunks'

@@ -33,6 +33,15 @@ class GCAError(RuntimeError):
         self.detail = detail
 
 
+ENCODER_WEIGHTS = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_1", "b_1", "w_2", "b_2",
+                   "w_kv")
+
+
+class EncoderWeights(ctypes.Structure):
+    """gca_encoder_weights: one device pointer per weight, in the header's order."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ENCODER_WEIGHTS]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -53,6 +62,8 @@ def _load():
         "gca_cca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, I, I, P, P, I, P, SZ, P]),
         "gca_window_backward_workspace_size": (SZ, [I, I, I]),
         "gca_window_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, I, P, SZ, P]),
+        "gca_chunk_encoder_workspace_size": (SZ, [I, I, I]),
+        "gca_chunk_encoder_forward": (I, [P, I, I, I, I, I, ctypes.POINTER(EncoderWeights), P, P, P, P, P, SZ, P]),
         "gca_gather_workspace_size": (SZ, []),
         "gca_gather_chunks": (I, [P, P, I64, I, I, I, I, I, I, P, I, P, P, P, P, SZ, P]),
         "gca_backward_workspace_size": (SZ, [I, I, I, I, I]),
@@ -80,6 +91,7 @@ EXPORTS = (
     "gca_forward_workspace_size", "gca_forward", "gca_window_forward", "gca_cca_forward",
     "gca_window_backward_workspace_size", "gca_window_backward",
     "gca_gather_workspace_size", "gca_gather_chunks",
+    "gca_chunk_encoder_workspace_size", "gca_chunk_encoder_forward",
     "gca_backward_workspace_size", "gca_backward",
     "gca_scores_backward_workspace_size", "gca_scores_backward", "gca_check_error", "gca_launch_count",
     "gca_profile_begin", "gca_profile_end", "gca_profile_row",
@@ -264,6 +276,39 @@ def window_backward(q, k, v, o, dout, lse, window: int = 512, ws: Workspace = No
                                    window, _ptr(dq), _ptr(dk), _ptr(dv), 1 if accumulate else 0, _ptr(buf), buf.numel(),
                                    _stream()))
     return dq, dk, dv
+
+
+def chunk_encoder(x: torch.Tensor, weights: dict, H: int, ws: Workspace = None, y: torch.Tensor = None,
+                  k: torch.Tensor = None, v: torch.Tensor = None, k_lmk: torch.Tensor = None):
+    """Chunk / landmark encoder and the shared K/V transform (gca_chunk_encoder_forward).
+
+    x [B, nC*65, d] bf16 (per chunk 64 token rows, then the LMK row); weights maps the
+    names in ENCODER_WEIGHTS to device tensors (matrices bf16 [out, in], vectors float32).
+    Returns y [B, nC*65, d], k and v [B, nC*64, d] and k_lmk [B, nC, d], all bf16."""
+    _cuda(x)
+    _need(x.dim() == 3 and x.shape[1] % (CHUNK + 1) == 0, "x must be [B, nC*65, d]")
+    _need(x.dtype == torch.bfloat16 and x.is_contiguous(), "x must be contiguous bfloat16")
+    B, M, d = x.shape
+    nC = M // (CHUNK + 1)
+    shapes = {"w_qkv": (3 * d, d), "w_o": (d, d), "w_1": (4 * d, d), "w_2": (d, 4 * d), "w_kv": (2 * d, d),
+              "b_qkv": (3 * d,), "b_1": (4 * d,)}
+    w = EncoderWeights()
+    for n in ENCODER_WEIGHTS:
+        t = weights[n]
+        _cuda(t)
+        want = shapes.get(n, (d,))
+        _need(tuple(t.shape) == want and t.is_contiguous(), f"{n} must be a contiguous {list(want)} tensor")
+        _need(t.dtype == (torch.bfloat16 if n.startswith("w_") else torch.float32), f"{n} has the wrong dtype")
+        setattr(w, n, t.data_ptr())
+    y = torch.empty_like(x) if y is None else y
+    k = torch.empty((B, nC * CHUNK, d), dtype=x.dtype, device=x.device) if k is None else k
+    v = torch.empty((B, nC * CHUNK, d), dtype=x.dtype, device=x.device) if v is None else v
+    k_lmk = torch.empty((B, nC, d), dtype=x.dtype, device=x.device) if k_lmk is None else k_lmk
+    ws = ws or default_workspace(x.device)
+    buf = ws.get(LIB.gca_chunk_encoder_workspace_size(B, nC, d))
+    _check(LIB.gca_chunk_encoder_forward(_ptr(x), GCA_BF16, B, nC, d, H, ctypes.byref(w), _ptr(y), _ptr(k), _ptr(v),
+                                         _ptr(k_lmk), _ptr(buf), buf.numel(), _stream()))
+    return y, k, v, k_lmk
 
 
 def cca_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, idx: torch.Tensor, shift: int = 1,

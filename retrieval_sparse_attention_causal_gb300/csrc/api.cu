@@ -325,6 +325,48 @@ extern "C" gca_status gca_cca_forward(const void* q, const void* k, const void* 
   return GCA_OK;
 }
 
+// ==================================================================== chunk encoder
+extern "C" size_t gca_chunk_encoder_workspace_size(int B, int nC, int d) {
+  if (B < 1 || nC < 1 || d < 1) return kErrBytes;
+  const size_t M = (size_t)B * nC * 65;
+  return kErrBytes + 2 * align256(M * d * 2) + align256(M * 4 * d * 2);
+}
+
+extern "C" gca_status gca_chunk_encoder_forward(const void* x, gca_dtype dtype, int B, int nC, int d, int H,
+                                                const gca_encoder_weights* w, void* y, void* k, void* v,
+                                                void* k_lmk, void* ws, size_t ws_bytes, gca_stream_t stream) {
+  if (dtype != GCA_F32 && dtype != GCA_BF16) return fail(GCA_ERR_INVALID_ARG, "dtype must be GCA_F32 or GCA_BF16");
+  if (dtype != GCA_BF16) return fail(GCA_ERR_UNSUPPORTED, "the encoder runs in bf16 only");
+  if (B < 1 || nC < 1 || H < 1) return fail(GCA_ERR_INVALID_ARG, "B, nC, H must be >= 1");
+  if (d % 128 || d < 128 || d > 1024) return fail(GCA_ERR_UNSUPPORTED, "d must be a multiple of 128 in 128..1024");
+  if (d != 64 * H) return fail(GCA_ERR_UNSUPPORTED, "the encoder's head dim d / H must be 64");
+  if ((int64_t)B * nC > (int64_t)INT32_MAX / 65) return fail(GCA_ERR_UNSUPPORTED, "B * nC * 65 must fit in int32");
+  if (!w) return fail(GCA_ERR_INVALID_ARG, "weights pointer is NULL");
+  const void* ptrs[] = {x, y, k, v, k_lmk, w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o, w->b_o,
+                        w->ln2_g, w->ln2_b, w->w_1, w->b_1, w->w_2, w->b_2, w->w_kv};
+  for (const void* p : ptrs) {
+    if (!p) return fail(GCA_ERR_INVALID_ARG, "a pointer is NULL");
+    if (!aligned16(p)) return fail(GCA_ERR_INVALID_ARG, "all tensors must be 16-byte aligned");
+  }
+  gca_status st;
+  if ((st = check_ws(ws, ws_bytes, gca_chunk_encoder_workspace_size(B, nC, d))) != GCA_OK) return st;
+  const size_t M = (size_t)B * nC * 65;
+  unsigned char* base = static_cast<unsigned char*>(ws) + kErrBytes;
+  EncoderArgs a{};
+  a.x = x; a.B = B; a.nC = nC; a.d = d; a.H = H;
+  a.ln1_g = w->ln1_g; a.ln1_b = w->ln1_b; a.b_qkv = w->b_qkv; a.b_o = w->b_o;
+  a.ln2_g = w->ln2_g; a.ln2_b = w->ln2_b; a.b_1 = w->b_1; a.b_2 = w->b_2;
+  a.w_qkv = w->w_qkv; a.w_o = w->w_o; a.w_1 = w->w_1; a.w_2 = w->w_2; a.w_kv = w->w_kv;
+  a.y = y; a.k = k; a.v = v; a.k_lmk = k_lmk;
+  a.bufA = base;
+  a.bufU = base + align256(M * d * 2);
+  a.bufF = base + 2 * align256(M * d * 2);
+  a.err = reinterpret_cast<ErrWord*>(ws);
+  cudaError_t e = launch_chunk_encoder(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gca_chunk_encoder_forward launch");
+  return GCA_OK;
+}
+
 // ==================================================================== chunk gather
 extern "C" size_t gca_gather_workspace_size(void) { return kErrBytes; }
 

@@ -27,6 +27,10 @@ cudaError_t allow_smem(const void* fn, int bytes);
 cudaError_t make_head_tmap(CUtensorMap* out, const void* base, int dh, int H, int64_t rows, int B,
                            int64_t batch_stride_elems);
 
+// TMA tensor map of a row-major [rows][cols] bf16 matrix whose box is 64 columns by
+// box_rows rows, 128-byte swizzled (tmap.cu).
+cudaError_t make_rows_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows, int box_rows);
+
 // ---- retrieval (retrieve.cu)
 struct RetrieveArgs {
   const void* q; int64_t q_rs, q_bs;
@@ -112,6 +116,23 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s);
 // Tensor-core (tcgen05) query-side and key-side passes, bf16 with dh = 64 (gca_bwd_tc.cu).
 cudaError_t launch_bwd_q_tc(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t s);
+
+// ---- chunk / landmark encoder (encoder.cu), bf16, encoder head dim 64
+struct EncoderArgs {
+  const void* x;  // [B][nC*65][d]: per chunk 64 token rows, then the LMK row
+  int B, nC, d, H;
+  const float *ln1_g, *ln1_b, *b_qkv, *b_o, *ln2_g, *ln2_b, *b_1, *b_2;
+  const void *w_qkv, *w_o, *w_1, *w_2, *w_kv;  // [N][K] row-major
+  void* y;      // [B][nC*65][d]
+  void* k;      // [B][nC*64][d]
+  void* v;      // [B][nC*64][d]
+  void* k_lmk;  // [B][nC][d]
+  void* bufA;   // workspace [M][d]
+  void* bufU;   // workspace [M][d]
+  void* bufF;   // workspace [M][4d]
+  ErrWord* err;
+};
+cudaError_t launch_chunk_encoder(const EncoderArgs& a, cudaStream_t s);
 
 // ---- CSR of consumers per key chunk (gca_bwd.cu), also used by the score backward.
 // Rows r in [0, nrows) of idx [B][ld_rows][topk] are entries e = r*topk + m.

@@ -165,3 +165,29 @@ def test_backward_and_scores_backward_reject_bad_arguments(gca):
     r = L.gca_scores_backward(FAKE, 768, 256 * 768, FAKE, 0, gca.GCA_BF16, 4, 256, 256, 768, FAKE, FAKE, 8,
                               FAKE, gca.GCA_F32, 768, 256 * 768, 0, FAKE, FAKE, 1 << 30, None)
     assert r == gca.GCA_ERR_INVALID_ARG  # shared k_lmk not allowed here
+
+
+def test_chunk_encoder_rejects_bad_arguments(gca):
+    L = gca.LIB
+    w = gca.EncoderWeights(*([FAKE] * len(gca.ENCODER_WEIGHTS)))
+
+    def enc(**kw):
+        a = dict(x=FAKE, dt=gca.GCA_BF16, B=4, nC=256, d=768, H=12, w=ctypes.byref(w), y=FAKE, k=FAKE, v=FAKE,
+                 lmk=FAKE, ws=FAKE, wsb=1 << 40)
+        a.update(kw)
+        return L.gca_chunk_encoder_forward(a["x"], a["dt"], a["B"], a["nC"], a["d"], a["H"], a["w"], a["y"], a["k"],
+                                           a["v"], a["lmk"], a["ws"], a["wsb"], None)
+    assert enc(dt=gca.GCA_F32) == gca.GCA_ERR_UNSUPPORTED
+    assert enc(d=704, H=11) == gca.GCA_ERR_UNSUPPORTED  # not a multiple of 128
+    assert enc(d=1152, H=18) == gca.GCA_ERR_UNSUPPORTED  # above 1024
+    assert enc(H=6) == gca.GCA_ERR_UNSUPPORTED  # head dim 128
+    assert enc(B=0) == gca.GCA_ERR_INVALID_ARG
+    assert enc(w=None) == gca.GCA_ERR_INVALID_ARG
+    assert enc(lmk=0) == gca.GCA_ERR_INVALID_ARG
+    assert enc(y=FAKE + 8) == gca.GCA_ERR_INVALID_ARG
+    bad = gca.EncoderWeights(*([FAKE] * len(gca.ENCODER_WEIGHTS)))
+    bad.w_2 = 0
+    assert enc(w=ctypes.byref(bad)) == gca.GCA_ERR_INVALID_ARG
+    need = L.gca_chunk_encoder_workspace_size(4, 256, 768)
+    assert need >= 256 + 4 * 256 * 65 * 768 * 2 * 6
+    assert enc(wsb=need - 1) == gca.GCA_ERR_WORKSPACE
