@@ -99,8 +99,11 @@ __global__ void __launch_bounds__(256) enc_layernorm_kernel(const bf16* __restri
 // 64 through a 4-stage TMA ring, tcgen05.mma M = 128, N = BN, K = 16 into one of two TMEM
 // accumulators, so that the epilogue of a tile overlaps the products of the next.  One
 // CTA per SM, persistent over the tiles; consecutive tiles share their rows of A.
-// Warp 0 loads, warp 1 issues the products, warps 2-5 (TMEM lane quarters 2, 3, 0, 1)
-// read the accumulator a row per thread and apply the epilogue.
+// Warp 0 loads, warp 1 issues the products, warps 2-9 run the epilogue: warp w reads
+// TMEM lane quarter w % 4 (a row per thread) over half of the tile's columns, one 32-column
+// chunk at a time with the next chunk's load in flight, applies the step's epilogue and
+// writes the chunk (32 rows x 64 bytes) through its own swizzled staging buffer with a TMA
+// store, so that global writes go out as whole lines.
 enum Epi { kEpiBias = 0, kEpiGelu = 1, kEpiResid = 2, kEpiKV = 3 };
 
 struct GemmArgs {
@@ -113,10 +116,11 @@ struct GemmArgs {
   ErrWord* err;
 };
 
-constexpr int kGemmStages = 4, kGemmThreads = 192;
+constexpr int kGemmStages = 4, kGemmEpiWarps = 8, kGemmThreads = 32 * (2 + kGemmEpiWarps);
+constexpr int kStageBufBytes = 2 * 32 * 64;  // per epilogue warp: two 32 x 32 bf16 chunks
 template <int BN>
 constexpr int gemm_smem() {
-  return kGemmStages * (128 + BN) * 128 + 1024;
+  return kGemmStages * (128 + BN) * 128 + kGemmEpiWarps * kStageBufBytes + 1024;
 }
 
 // Bounded wait for phase `parity` of `bar` that gives up early once the CTA's abort flag
@@ -143,8 +147,9 @@ __device__ __forceinline__ void store32(bf16* dst, const float (&v)[32]) {
                        pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
 }
 
+// Math of the step's epilogue on a 32-column chunk (everything but the store).
 template <int EPI>
-__device__ __forceinline__ void epilogue(const GemmArgs& a, int row, int col, float (&v)[32]) {
+__device__ __forceinline__ void epilogue_math(const GemmArgs& a, int row, int col, float (&v)[32]) {
   if (EPI != kEpiKV) {
     const float4* b4 = reinterpret_cast<const float4*>(a.bias + col);
 #pragma unroll
@@ -160,7 +165,7 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, int row, int col, fl
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
   }
-  if (EPI == kEpiResid) {
+  if (EPI == kEpiResid && row < a.M) {
     const uint4* r4 = reinterpret_cast<const uint4*>(a.resid + (size_t)row * a.N + col);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -170,22 +175,22 @@ __device__ __forceinline__ void epilogue(const GemmArgs& a, int row, int col, fl
       for (int e = 0; e < 8; ++e) v[8 * q + e] += f[e];
     }
   }
-  if (EPI == kEpiKV) {
-    const int t = row % kRows;
-    if (t == kRows - 1) return;  // LMK rows have no K/V
-    const size_t tok = (size_t)(row / kRows) * 64 + t;
-    bf16* dst = col < a.d ? a.out + tok * a.d + col : a.out2 + tok * a.d + (col - a.d);
-    store32(dst, v);
-    return;
-  }
-  store32(a.out + (size_t)row * a.N + col, v);
-  if (EPI == kEpiResid && a.out2 != nullptr && row % kRows == kRows - 1)
-    store32(a.out2 + (size_t)(row / kRows) * a.N + col, v);
+}
+
+// Row `lane` of a 32 x 32 bf16 chunk into the 64-byte-swizzled staging buffer.
+__device__ __forceinline__ void stage_row(unsigned char* buf, int lane, const float (&v)[32]) {
+  uint4* row = reinterpret_cast<uint4*>(buf + lane * 64);
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    row[u ^ sw] = make_uint4(pack_bf16(v[8 * u], v[8 * u + 1]), pack_bf16(v[8 * u + 2], v[8 * u + 3]),
+                             pack_bf16(v[8 * u + 4], v[8 * u + 5]), pack_bf16(v[8 * u + 6], v[8 * u + 7]));
 }
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB) {
+enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC) {
   constexpr int NST = kGemmStages;
   constexpr uint32_t kABytes = 128 * 128, kStage = (128 + BN) * 128;
   constexpr uint32_t kId = tc::idesc_bf16(128, BN, false);
@@ -205,13 +210,14 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&acc_full[b], 1);
-      tc::mbar_init(&acc_empty[b], 4);
+      tc::mbar_init(&acc_empty[b], kGemmEpiWarps);
     }
     tc::mbar_init(&drain, 1);
     tc::fence_mbar_init();
     abort_s = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    if (EPI != kEpiKV) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
   }
   if (warp == 1) tc::tmem_alloc(&tmem_slot, 2 * BN);
   tc::fence_before();
@@ -277,25 +283,58 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
     }
   } else {
     // ------------------------------------------------------------ epilogue warps
-    const int q = warp & 3;
+    constexpr int HALF = BN / 2, NCH = HALF / 32;
+    const int ew = warp - 2, q = warp & 3, hf = ew >> 2;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    unsigned char* stg = sm + NST * kStage + ew * kStageBufBytes;
+    int sb = 0;  // staging buffer to fill next
     int i = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int buf = i & 1;
       if (!wait_or_abort(&acc_full[buf], (uint32_t)(i >> 1) & 1, &abort_s, a.err, 24, t)) break;
       tc::fence_after();
-      const int row = (t / nt) * 128 + 32 * q + lane, n0 = (t % nt) * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tc::ld32x32b_x32(tmem + lane_base + buf * BN + 32 * c, v);
-        tc::ld_wait_row(v);
-        if (row < a.M) epilogue<EPI>(a, row, n0 + 32 * c, v);
+      const int row0 = (t / nt) * 128 + 32 * q, row = row0 + lane;
+      const int col0 = (t % nt) * BN + hf * HALF;
+      const uint32_t tcol = tmem + lane_base + buf * BN + hf * HALF;
+      float v[2][32];
+      tc::ld32x32b_x32(tcol, v[0]);
+      tc::ld_wait_row(v[0]);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        if (c + 1 < NCH) tc::ld32x32b_x32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
+        float(&cur)[32] = v[c & 1];
+        const int col = col0 + 32 * c;
+        epilogue_math<EPI>(a, row, col, cur);
+        if (EPI == kEpiKV) {
+          if (row < a.M) {
+            const int tr = row % kRows;
+            if (tr != kRows - 1) {  // LMK rows have no K/V
+              const size_t tok = (size_t)(row / kRows) * 64 + tr;
+              store32(col < a.d ? a.out + tok * a.d + col : a.out2 + tok * a.d + (col - a.d), cur);
+            }
+          }
+        } else {
+          unsigned char* sbuf = stg + sb * (kStageBufBytes / 2);
+          if (lane == 0) tc::bulk_wait_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
+          stage_row(sbuf, lane, cur);
+          tc::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc::tma_store_2d(&tmC, col, row0, sbuf);
+            tc::bulk_commit();
+          }
+          sb ^= 1;
+          if (EPI == kEpiResid && a.out2 != nullptr && row < a.M && row % kRows == kRows - 1)
+            store32(a.out2 + (size_t)(row / kRows) * a.N + col, cur);
+        }
+        if (c + 1 < NCH) tc::ld_wait_row(v[(c + 1) & 1]);
       }
       tc::fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
     }
+    if (EPI != kEpiKV && lane == 0) tc::bulk_wait_all();
   }
   tc::fence_before();
   __syncthreads();
@@ -437,14 +476,16 @@ __global__ void __launch_bounds__(kAttnThreads) enc_attn_tc_kernel(int M, int d,
 // ------------------------------------------------------------------ host side
 template <int BN, int EPI>
 cudaError_t run_gemm(const GemmArgs& g, const void* A, const void* W, int sms, cudaStream_t s, const char* name) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc_;
   cudaError_t e = make_rows_tmap(&ta, A, g.K, g.M, 128);
   if (e == cudaSuccess) e = make_rows_tmap(&tb, W, g.K, g.N, BN);
+  if (e == cudaSuccess) e = EPI == kEpiKV ? make_rows_tmap(&tc_, A, g.K, g.M, 128)  // unused
+                                          : make_store_tmap(&tc_, g.out, g.N, g.M);
   if (e == cudaSuccess) e = allow_smem((const void*)enc_gemm_kernel<BN, EPI>, gemm_smem<BN>());
   if (e != cudaSuccess) return e;
   const int tiles = ((g.M + 127) / 128) * (g.N / BN);
   launch_begin(name, s);
-  enc_gemm_kernel<BN, EPI><<<std::min(tiles, sms), kGemmThreads, gemm_smem<BN>(), s>>>(g, ta, tb);
+  enc_gemm_kernel<BN, EPI><<<std::min(tiles, sms), kGemmThreads, gemm_smem<BN>(), s>>>(g, ta, tb, tc_);
   return launch_end(name, s);
 }
 

@@ -30,6 +30,8 @@ cudaError_t make_head_tmap(CUtensorMap* out, const void* base, int dh, int H, in
 // TMA tensor map of a row-major [rows][cols] bf16 matrix whose box is 64 columns by
 // box_rows rows, 128-byte swizzled (tmap.cu).
 cudaError_t make_rows_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows, int box_rows);
+// The same matrix as a TMA store target: 32 x 32 boxes, 64-byte swizzle (tmap.cu).
+cudaError_t make_store_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows);
 
 // ---- retrieval (retrieve.cu)
 struct RetrieveArgs {

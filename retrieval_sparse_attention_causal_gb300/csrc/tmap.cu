@@ -60,4 +60,19 @@ cudaError_t make_rows_tmap(CUtensorMap* out, const void* base, int64_t cols, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_store_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows) {
+  std::call_once(g_once, load_encode);
+  if (g_encode_err != cudaSuccess) return g_encode_err;
+  // Box of 32 columns (64 bytes) by 32 rows, 64-byte swizzle: in shared memory 16-byte
+  // unit u of row r sits at unit u ^ ((r >> 1) & 3) of the row's 64 bytes.
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace gca
