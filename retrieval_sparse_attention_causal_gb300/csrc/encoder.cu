@@ -110,7 +110,7 @@ struct GemmArgs {
   int M, N, K;
   const float* bias;  // [N]
   const bf16* resid;  // [M][N] (kEpiResid)
-  bf16* out;          // [M][N]; kEpiKV: K [M / 65 * 64][d]
+  bf16* out;          // [M][N]; kEpiKV: K [M][d] (M counts token rows there)
   bf16* out2;         // kEpiResid: the LMK rows [M / 65][N] (or null); kEpiKV: V
   int d;              // kEpiKV: columns of K and of V
   ErrWord* err;
@@ -190,7 +190,7 @@ __device__ __forceinline__ void stage_row(unsigned char* buf, int lane, const fl
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmC2) {
   constexpr int NST = kGemmStages;
   constexpr uint32_t kABytes = 128 * 128, kStage = (128 + BN) * 128;
   constexpr uint32_t kId = tc::idesc_bf16(128, BN, false);
@@ -217,7 +217,8 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
     abort_s = 0;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
-    if (EPI != kEpiKV) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC)) : "memory");
+    if (EPI == kEpiKV) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmC2)) : "memory");
   }
   if (warp == 1) tc::tmem_alloc(&tmem_slot, 2 * BN);
   tc::fence_before();
@@ -240,7 +241,8 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
           }
           unsigned char* st = sm + s * kStage;
           tc::mbar_expect_tx(&full[s], kStage);
-          tc::tma_load_2d(st, &tmA, kb * 64, m0, &full[s]);
+          if (EPI == kEpiKV) tc::tma_load_3d(st, &tmA, kb * 64, 0, m0 / 64, &full[s]);  // two chunks' token rows
+          else tc::tma_load_2d(st, &tmA, kb * 64, m0, &full[s]);
           tc::tma_load_2d(st + kABytes, &tmB, kb * 64, n0, &full[s]);
           ++it;
         }
@@ -305,15 +307,7 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
         float(&cur)[32] = v[c & 1];
         const int col = col0 + 32 * c;
         epilogue_math<EPI>(a, row, col, cur);
-        if (EPI == kEpiKV) {
-          if (row < a.M) {
-            const int tr = row % kRows;
-            if (tr != kRows - 1) {  // LMK rows have no K/V
-              const size_t tok = (size_t)(row / kRows) * 64 + tr;
-              store32(col < a.d ? a.out + tok * a.d + col : a.out2 + tok * a.d + (col - a.d), cur);
-            }
-          }
-        } else {
+        {
           unsigned char* sbuf = stg + sb * (kStageBufBytes / 2);
           if (lane == 0) tc::bulk_wait_read<1>();  // this buffer's previous store has read it
           __syncwarp();
@@ -321,7 +315,9 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
           tc::fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tc::tma_store_2d(&tmC, col, row0, sbuf);
+            // K/V transform: rows are token rows; columns below d go to K, the rest to V.
+            if (EPI == kEpiKV && col >= a.d) tc::tma_store_2d(&tmC2, col - a.d, row0, sbuf);
+            else tc::tma_store_2d(&tmC, col, row0, sbuf);
             tc::bulk_commit();
           }
           sb ^= 1;
@@ -334,7 +330,7 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
     }
-    if (EPI != kEpiKV && lane == 0) tc::bulk_wait_all();
+    if (lane == 0) tc::bulk_wait_all();
   }
   tc::fence_before();
   __syncthreads();
@@ -476,16 +472,18 @@ __global__ void __launch_bounds__(kAttnThreads) enc_attn_tc_kernel(int M, int d,
 // ------------------------------------------------------------------ host side
 template <int BN, int EPI>
 cudaError_t run_gemm(const GemmArgs& g, const void* A, const void* W, int sms, cudaStream_t s, const char* name) {
-  CUtensorMap ta, tb, tc_;
-  cudaError_t e = make_rows_tmap(&ta, A, g.K, g.M, 128);
+  // kEpiKV: g.M counts token rows; A is [M / 64][65][K] (the LMK rows are skipped by the
+  // load) and the outputs are K and V, [M][d] each.
+  CUtensorMap ta, tb, tc_, tc2;
+  cudaError_t e = EPI == kEpiKV ? make_chunk_token_tmap(&ta, A, g.K, g.M / 64) : make_rows_tmap(&ta, A, g.K, g.M, 128);
   if (e == cudaSuccess) e = make_rows_tmap(&tb, W, g.K, g.N, BN);
-  if (e == cudaSuccess) e = EPI == kEpiKV ? make_rows_tmap(&tc_, A, g.K, g.M, 128)  // unused
-                                          : make_store_tmap(&tc_, g.out, g.N, g.M);
+  if (e == cudaSuccess) e = make_store_tmap(&tc_, g.out, EPI == kEpiKV ? g.d : g.N, g.M);
+  if (e == cudaSuccess) e = make_store_tmap(&tc2, EPI == kEpiKV ? g.out2 : g.out, EPI == kEpiKV ? g.d : g.N, g.M);
   if (e == cudaSuccess) e = allow_smem((const void*)enc_gemm_kernel<BN, EPI>, gemm_smem<BN>());
   if (e != cudaSuccess) return e;
   const int tiles = ((g.M + 127) / 128) * (g.N / BN);
   launch_begin(name, s);
-  enc_gemm_kernel<BN, EPI><<<std::min(tiles, sms), kGemmThreads, gemm_smem<BN>(), s>>>(g, ta, tb, tc_);
+  enc_gemm_kernel<BN, EPI><<<std::min(tiles, sms), kGemmThreads, gemm_smem<BN>(), s>>>(g, ta, tb, tc_, tc2);
   return launch_end(name, s);
 }
 
@@ -536,7 +534,7 @@ cudaError_t run_encoder(const EncoderArgs& a, int sms, cudaStream_t s) {
     e = run_gemm<BN, kEpiResid>(g, F, a.w_2, sms, s, "enc_mlp2");
   }
   if (e == cudaSuccess) {
-    g.N = 2 * d; g.K = d; g.bias = nullptr; g.resid = nullptr; g.d = d;
+    g.M = a.B * a.nC * 64; g.N = 2 * d; g.K = d; g.bias = nullptr; g.resid = nullptr; g.d = d;
     g.out = static_cast<bf16*>(a.k); g.out2 = static_cast<bf16*>(a.v);
     e = run_gemm<BN, kEpiKV>(g, a.y, a.w_kv, sms, s, "enc_kv");
   }

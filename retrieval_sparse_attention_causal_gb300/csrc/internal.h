@@ -30,6 +30,9 @@ cudaError_t make_head_tmap(CUtensorMap* out, const void* base, int dh, int H, in
 // TMA tensor map of a row-major [rows][cols] bf16 matrix whose box is 64 columns by
 // box_rows rows, 128-byte swizzled (tmap.cu).
 cudaError_t make_rows_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows, int box_rows);
+// Token rows of a [chunks][65][cols] bf16 tensor (64 tokens and an LMK row per chunk) as
+// 128-row boxes of two chunks' tokens, 64 columns wide, 128-byte swizzled (tmap.cu).
+cudaError_t make_chunk_token_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t chunks);
 // The same matrix as a TMA store target: 32 x 32 boxes, 64-byte swizzle (tmap.cu).
 cudaError_t make_store_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows);
 

@@ -66,6 +66,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       : "memory");
 }
 
+// TMA tile load of a 3-D tensor map (x innermost, same alignment rule), completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(su32(bar))
+      : "memory");
+}
+
 // TMA tile store of a 2-D tensor map from shared memory (bulk-group completion); rows or
 // columns outside the tensor are not written.  x and y must not be negative.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, const void* src) {

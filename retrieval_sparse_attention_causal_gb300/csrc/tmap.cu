@@ -60,6 +60,21 @@ cudaError_t make_rows_tmap(CUtensorMap* out, const void* base, int64_t cols, int
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_chunk_token_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t chunks) {
+  std::call_once(g_once, load_encode);
+  if (g_encode_err != cudaSuccess) return g_encode_err;
+  // [chunks][65][cols] viewed with a box of 64 columns x the first 64 rows x 2 chunks: the
+  // token rows of two consecutive chunks, without their LMK rows, as one 128-row tile.
+  cuuint64_t dims[3] = {(cuuint64_t)cols, 65, (cuuint64_t)chunks};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)cols * 2 * 65};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_store_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows) {
   std::call_once(g_once, load_encode);
   if (g_encode_err != cudaSuccess) return g_encode_err;
