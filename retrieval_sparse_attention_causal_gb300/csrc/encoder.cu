@@ -43,53 +43,64 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------------ LayerNorm
-// One warp per row, the row held in registers: mean, then the population variance of the
-// centred values, y = (x - mean) / sqrt(var + 1e-5) * g + b.  NV 16-byte vectors per lane
-// cover d <= 256 NV.
-template <int NV>
+// One warp per RPW rows, held in registers (every load issued before the first
+// reduction, so that a warp keeps RPW rows in flight): mean, then the population variance
+// of the centred values, y = (x - mean) / sqrt(var + 1e-5) * g + b.  NV 16-byte vectors per
+// lane cover d <= 256 NV.
+template <int NV, int RPW>
 __global__ void __launch_bounds__(256) enc_layernorm_kernel(const bf16* __restrict__ x, const float* __restrict__ g,
                                                             const float* __restrict__ b, bf16* __restrict__ y,
                                                             int64_t M, int d) {
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW;
   const int lane = threadIdx.x & 31;
-  if (row >= M) return;  // uniform across the warp
   const int nv = d / 8;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
-  float f[NV][8];
-  float s = 0.f;
+  float f[RPW][NV][8];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int v = lane + 32 * i;
-    if (v < nv) {
-      unpack16(__ldg(xr + v), f[i], static_cast<const bf16*>(nullptr));
+  for (int r = 0; r < RPW; ++r)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s += f[i][e];
+    for (int i = 0; i < NV; ++i) {
+      const int v = lane + 32 * i;
+      if (row0 + r < M && v < nv)
+        unpack16(__ldg(reinterpret_cast<const uint4*>(x + (row0 + r) * d) + v), f[r][i], static_cast<const bf16*>(nullptr));
+      else
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[r][i][e] = 0.f;
     }
-  }
-  const float mean = warp_sum(s) / (float)d;
-  float q = 0.f;
 #pragma unroll
-  for (int i = 0; i < NV; ++i)
-    if (lane + 32 * i < nv)
+  for (int r = 0; r < RPW; ++r) {
+    if (row0 + r >= M) break;  // uniform across the warp
+    float s = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float t = f[i][e] - mean;
-        q += t * t;
+    for (int i = 0; i < NV; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += f[r][i][e];
+    const float mean = warp_sum(s) / (float)d;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (lane + 32 * i < nv)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float t = f[r][i][e] - mean;
+          q += t * t;
+        }
+    const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
+    uint4* yr = reinterpret_cast<uint4*>(y + (row0 + r) * d);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int v = lane + 32 * i;
+      if (v < nv) {
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(g) + 2 * v);
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(g) + 2 * v + 1);
+        const float4 b0 = __ldg(reinterpret_cast<const float4*>(b) + 2 * v);
+        const float4 b1 = __ldg(reinterpret_cast<const float4*>(b) + 2 * v + 1);
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (f[r][i][e] - mean) * rstd * gg[e] + bb[e];
+        yr[v] = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
       }
-  const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
-  uint4* yr = reinterpret_cast<uint4*>(y + row * d);
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int v = lane + 32 * i;
-    if (v < nv) {
-      const float4 g0 = __ldg(reinterpret_cast<const float4*>(g) + 2 * v), g1 = __ldg(reinterpret_cast<const float4*>(g) + 2 * v + 1);
-      const float4 b0 = __ldg(reinterpret_cast<const float4*>(b) + 2 * v), b1 = __ldg(reinterpret_cast<const float4*>(b) + 2 * v + 1);
-      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-      float o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = (f[i][e] - mean) * rstd * gg[e] + bb[e];
-      yr[v] = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
     }
   }
 }
@@ -136,7 +147,22 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
   return false;
 }
 
-__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+// GELU(x) = x Phi(x) = x (1 + erf(x / sqrt 2)) / 2, with erf from Abramowitz & Stegun,
+// Handbook of Mathematical Functions, 7.1.26 (Hastings' rational approximation, absolute
+// error <= 1.5e-7): for z = |x| / sqrt 2 and t = 1 / (1 + p z),
+//     q = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2) = 1 - erf(z),
+// so 1 + erf(x / sqrt 2) is 2 - q for x >= 0 and q for x < 0 (no cancellation for x < 0).
+// Branch-free: one reciprocal and one exp2 on the special-function unit; the error of the
+// result stays near 2e-7 max(1, |GELU(x)|), far below the bf16 output's rounding.
+__device__ __forceinline__ float gelu(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  float t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, z, 1.0f)));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+  const float q = poly * tc::ex2(-(z * z) * kLog2e);
+  return 0.5f * x * (x >= 0.f ? 2.0f - q : q);
+}
 
 // 32 consecutive columns as bf16: four 16-byte stores.
 __device__ __forceinline__ void store32(bf16* dst, const float (&v)[32]) {
@@ -163,7 +189,7 @@ __device__ __forceinline__ void epilogue_math(const GemmArgs& a, int row, int co
   }
   if (EPI == kEpiGelu) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+    for (int j = 0; j < 32; ++j) v[j] = gelu(v[j]);
   }
   if (EPI == kEpiResid && row < a.M) {
     const uint4* r4 = reinterpret_cast<const uint4*>(a.resid + (size_t)row * a.N + col);
@@ -341,32 +367,52 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
 }
 
 // ------------------------------------------------------------------ attention inside a chunk
-// One CTA per (chunk, head): the chunk's 65 rows of Q, K and V (head dim 64) arrive by TMA
-// as 80-row boxes (the MMA's N granularity is 16; keys 65..79 are masked, rows past the
-// end of the tensor read as zeros).  S = Q K^T (M = 128, N = 80) goes to TMEM columns
-// 0-79; thread r owns row r: it takes the row's softmax over the 65 keys without a mask
-// otherwise, writes the bf16 P over the first 40 columns as the A operand of O = P V
-// (M = 128, N = 64, K = 80, into columns 64-127), and scales O's row by 1 / sum.
-constexpr int kAttnThreads = 128, kAttnKeys = 80;
-constexpr int kAttnSmem = 46 * 1024 + 1024;  // Q 16 KB + K, V 10 KB each; padded so that at most 4 CTAs share an SM
+// One CTA per (chunk, group of kAttnHpc heads), the heads in turn with the next head's
+// operands loading meanwhile (two stages).  The chunk's 65 rows of Q, K and V (head dim
+// 64) arrive by TMA as 80-row boxes (the MMA's N granularity is 16; keys 65..79 are
+// masked, rows past the end of the tensor read as zeros).  Per head: S = Q K^T (M = 128,
+// N = 80; A rows 80..127 read the neighbouring tile and are never used) into TMEM columns
+// 0-79; thread r owns row r: the softmax over the 65 keys, the bf16 P over the first 40
+// columns as the A operand of O = P V (M = 128, N = 64, K = 80, into columns 64-127),
+// then O's row scaled by 1 / sum.
+constexpr int kAttnThreads = 128, kAttnKeys = 80, kAttnHpc = 4;
+constexpr uint32_t kAttnBox = kAttnKeys * 128;  // 10 KB: one operand of one head
+constexpr uint32_t kAttnStage = 3 * kAttnBox;    // Q, K, V
+constexpr int kAttnSmem = 2 * kAttnStage + 1024;  // 61 KB: three CTAs per SM (TMEM: 128 columns each)
 
-__global__ void __launch_bounds__(kAttnThreads) enc_attn_tc_kernel(int M, int d, const __grid_constant__ CUtensorMap tm,
+__global__ void __launch_bounds__(kAttnThreads) enc_attn_tc_kernel(int M, int d, int H,
+                                                                   const __grid_constant__ CUtensorMap tm,
                                                                    bf16* __restrict__ out, ErrWord* err) {
   constexpr uint32_t kIdS = tc::idesc_bf16(128, kAttnKeys, false);
   constexpr uint32_t kIdO = tc::idesc_bf16(128, 64, true);
-  constexpr uint32_t kBox = kAttnKeys * 128;
   extern __shared__ __align__(1024) unsigned char dsm[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
-  unsigned char *sQ = sm, *sK = sm + 16384, *sV = sK + kBox;  // Q's tile has 128 rows for the M = 128 product
-  __shared__ __align__(8) uint64_t bar_ld, bar_mma;
+  // bar_ld[st] per load into stage st; bar_mma twice per head (S, then O); drain at exit.
+  __shared__ __align__(8) uint64_t bar_ld[2], bar_mma, drain;
   __shared__ uint32_t tmem_slot;
+  __shared__ int abort_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, r = threadIdx.x;
-  const int bc = blockIdx.x, h = blockIdx.y;
+  const int bc = blockIdx.x, h0 = blockIdx.y * kAttnHpc, nh = min(kAttnHpc, H - h0);
   const int row0 = bc * kRows;
+  int nld[2] = {0, 0};  // loads issued per stage (thread 0)
+  auto issue_load = [&](int i) {
+    const int st = i & 1, h = h0 + i;
+    unsigned char* b = sm + st * kAttnStage;
+    tc::mbar_expect_tx(&bar_ld[st], kAttnStage);
+    tc::tma_load_2d(b, &tm, h * 64, row0, &bar_ld[st]);
+    tc::tma_load_2d(b + kAttnBox, &tm, d + h * 64, row0, &bar_ld[st]);
+    tc::tma_load_2d(b + 2 * kAttnBox, &tm, 2 * d + h * 64, row0, &bar_ld[st]);
+    ++nld[st];
+  };
   if (threadIdx.x == 0) {
-    tc::mbar_init(&bar_ld, 1);
+    tc::mbar_init(&bar_ld[0], 1);
+    tc::mbar_init(&bar_ld[1], 1);
     tc::mbar_init(&bar_mma, 1);
+    tc::mbar_init(&drain, 1);
     tc::fence_mbar_init();
+    abort_s = 0;
+    issue_load(0);
+    if (nh > 1) issue_load(1);
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
   tc::fence_before();
@@ -374,93 +420,101 @@ __global__ void __launch_bounds__(kAttnThreads) enc_attn_tc_kernel(int M, int d,
   tc::fence_after();
   const uint32_t tS = tmem_slot, tO = tmem_slot + 64;
   const uint32_t lb = (uint32_t)(32 * warp) << 16;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      tc::mbar_expect_tx(&bar_ld, 3 * kBox);
-      tc::tma_load_2d(sQ, &tm, h * 64, row0, &bar_ld);
-      tc::tma_load_2d(sK, &tm, d + h * 64, row0, &bar_ld);
-      tc::tma_load_2d(sV, &tm, 2 * d + h * 64, row0, &bar_ld);
-    }
-    __syncwarp();
-    if (tc::mbar_wait(&bar_ld, 0, kWaitLimit)) {
-      tc::fence_after();
-      const uint64_t dq = tc::desc_km(tc::su32(sQ)), dk = tc::desc_km(tc::su32(sK));
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) tc::mma_warp(tS, dq + kk * tc::kKStepKm, dk + kk * tc::kKStepKm, kIdS, kk > 0);
-      tc::commit_warp(&bar_mma);
-    } else if (lane == 0) {
-      flag_timeout(err, 25, bc, h);
-    }
-  }
-  bool ok = tc::mbar_wait(&bar_mma, 0, kWaitLimit);
-  if (!ok && lane == 0) flag_timeout(err, 26, bc, h);
-  tc::fence_after();
-  float s0[32], s1[32], s2[16];
-  tc::ld32x32b_x32(tS + lb, s0);
-  tc::ld32x32b_x32(tS + lb + 32, s1);
-  tc::ld32x32b_x16(tS + lb + 64, s2);
-  tc::ld_wait_row(s0);
-  tc::ld_wait_row(s1);
-  tc::ld_wait_row(s2);
+  const bool live = r < kRows && row0 + r < M;
   const float sl2 = 0.125f * kLog2e;  // dh^-1/2 with dh = 64, in base 2
-  float mx = s2[0];                    // key 64, the LMK token
+  bool issued = false;
+
+  for (int i = 0; i < nh; ++i) {
+    const int st = i & 1, h = h0 + i;
+    unsigned char* b = sm + st * kAttnStage;
+    if (warp == 0) {
+      if (wait_or_abort(&bar_ld[st], (uint32_t)(i >> 1) & 1, &abort_s, err, 25, bc)) {
+        tc::fence_after();
+        const uint64_t dq = tc::desc_km(tc::su32(b)), dk = tc::desc_km(tc::su32(b + kAttnBox));
 #pragma unroll
-  for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(s0[j], s1[j]));
-  const bool live = r < kRows;
-  float sum = 0.f;
-  uint32_t p[40];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float a0 = tc::ex2((s0[2 * j] - mx) * sl2), a1 = tc::ex2((s0[2 * j + 1] - mx) * sl2);
-    const float b0 = tc::ex2((s1[2 * j] - mx) * sl2), b1 = tc::ex2((s1[2 * j + 1] - mx) * sl2);
-    sum += (a0 + a1) + (b0 + b1);
-    p[j] = live ? pack_bf16(a0, a1) : 0u;
-    p[16 + j] = live ? pack_bf16(b0, b1) : 0u;
-  }
-  const float c64 = tc::ex2((s2[0] - mx) * sl2);  // = 1 when the LMK key holds the maximum
-  sum += c64;
-  p[32] = live ? pack_bf16(c64, 0.f) : 0u;  // keys 65..79 are masked
-#pragma unroll
-  for (int j = 33; j < 40; ++j) p[j] = 0u;
-#pragma unroll
-  for (int c = 0; c < 5; ++c) {
-    uint32_t w[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) w[e] = p[8 * c + e];
-    tc::st32x32b_x8(tS + lb + 8 * c, w);
-  }
-  tc::st_wait();
-  tc::fence_before();
-  __syncthreads();
-  if (warp == 0 && ok) {
-    tc::fence_after();
-    const uint64_t dv = tc::desc_mn(tc::su32(sV));
-#pragma unroll
-    for (int kk = 0; kk < 5; ++kk) tc::mma_ts_warp(tO, tS + 8 * kk, dv + kk * tc::kKStepMn, kIdO, kk > 0);
-    tc::commit_warp(&bar_mma);
-  }
-  if (ok && !tc::mbar_wait(&bar_mma, 1, kWaitLimit)) {
-    if (lane == 0) flag_timeout(err, 27, bc, h);
-    ok = false;
-  }
-  tc::fence_after();
-  float o0[32], o1[32];
-  tc::ld32x32b_x32(tO + lb, o0);
-  tc::ld32x32b_x32(tO + lb + 32, o1);
-  tc::ld_wait_row(o0);
-  tc::ld_wait_row(o1);
-  if (live && ok && row0 + r < M) {
-    const float inv = 1.0f / sum;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      o0[j] *= inv;
-      o1[j] *= inv;
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_warp(tS, dq + kk * tc::kKStepKm, dk + kk * tc::kKStepKm, kIdS, kk > 0);
+        tc::commit_warp(&bar_mma);
+        issued = true;
+      }
     }
-    bf16* dst = out + (size_t)(row0 + r) * d + h * 64;
-    store32(dst, o0);
-    store32(dst + 32, o1);
+    wait_or_abort(&bar_mma, 0, &abort_s, err, 26, bc);
+    tc::fence_after();
+    float s0[32], s1[32], s2[16];
+    tc::ld32x32b_x32(tS + lb, s0);
+    tc::ld32x32b_x32(tS + lb + 32, s1);
+    tc::ld32x32b_x16(tS + lb + 64, s2);
+    tc::ld_wait_row(s0);
+    tc::ld_wait_row(s1);
+    tc::ld_wait_row(s2);
+    float mx = s2[0];  // key 64, the LMK token
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(s0[j], s1[j]));
+    float sum = 0.f;
+    uint32_t p[40];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float a0 = tc::ex2((s0[2 * j] - mx) * sl2), a1 = tc::ex2((s0[2 * j + 1] - mx) * sl2);
+      const float b0 = tc::ex2((s1[2 * j] - mx) * sl2), b1 = tc::ex2((s1[2 * j + 1] - mx) * sl2);
+      sum += (a0 + a1) + (b0 + b1);
+      p[j] = live ? pack_bf16(a0, a1) : 0u;
+      p[16 + j] = live ? pack_bf16(b0, b1) : 0u;
+    }
+    const float c64 = tc::ex2((s2[0] - mx) * sl2);
+    sum += c64;
+    p[32] = live ? pack_bf16(c64, 0.f) : 0u;  // keys 65..79 are masked
+#pragma unroll
+    for (int j = 33; j < 40; ++j) p[j] = 0u;
+#pragma unroll
+    for (int c = 0; c < 5; ++c) {
+      uint32_t w[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = p[8 * c + e];
+      tc::st32x32b_x8(tS + lb + 8 * c, w);
+    }
+    tc::st_wait();
+    tc::fence_before();
+    __syncthreads();  // every row's P is in TMEM
+    if (*reinterpret_cast<volatile int*>(&abort_s)) break;
+    if (warp == 0) {
+      tc::fence_after();
+      const uint64_t dv = tc::desc_mn(tc::su32(b + 2 * kAttnBox));
+#pragma unroll
+      for (int kk = 0; kk < 5; ++kk) tc::mma_ts_warp(tO, tS + 8 * kk, dv + kk * tc::kKStepMn, kIdO, kk > 0);
+      tc::commit_warp(&bar_mma);
+    }
+    wait_or_abort(&bar_mma, 1, &abort_s, err, 27, bc);
+    tc::fence_after();
+    float o0[32], o1[32];
+    tc::ld32x32b_x32(tO + lb, o0);
+    tc::ld32x32b_x32(tO + lb + 32, o1);
+    tc::ld_wait_row(o0);
+    tc::ld_wait_row(o1);
+    tc::fence_before();
+    __syncthreads();  // O read by every row (the next S overwrites columns 64-79); stage st is free
+    if (*reinterpret_cast<volatile int*>(&abort_s)) break;
+    if (threadIdx.x == 0 && i + 2 < nh) issue_load(i + 2);
+    if (live) {
+      const float inv = 1.0f / sum;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        o0[j] *= inv;
+        o1[j] *= inv;
+      }
+      bf16* dst = out + (size_t)(row0 + r) * d + h * 64;
+      store32(dst, o0);
+      store32(dst + 32, o1);
+    }
   }
+  // After an abort: no product may still run when TMEM is released, and no copy may
+  // still land in shared memory when the CTA exits.
+  if (warp == 0 && issued) {
+    tc::commit_warp(&drain);
+    if (!tc::mbar_wait(&drain, 0) && lane == 0) flag_timeout(err, 28, bc);
+  }
+  if (threadIdx.x == 0 && *reinterpret_cast<volatile int*>(&abort_s))
+    for (int st = 0; st < 2; ++st)
+      if (nld[st] > 0) tc::mbar_wait(&bar_ld[st], (uint32_t)(nld[st] - 1) & 1);
   tc::fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -489,11 +543,13 @@ cudaError_t run_gemm(const GemmArgs& g, const void* A, const void* W, int sms, c
 
 cudaError_t run_layernorm(const bf16* x, const float* g, const float* b, bf16* y, int64_t M, int d, cudaStream_t s,
                           const char* name) {
-  const unsigned grid = (unsigned)((M + 7) / 8);
+  constexpr int RPW = 2;
+  const unsigned grid = (unsigned)((M + 8 * RPW - 1) / (8 * RPW));
   launch_begin(name, s);
-  if (d <= 256) enc_layernorm_kernel<1><<<grid, 256, 0, s>>>(x, g, b, y, M, d);
-  else if (d <= 512) enc_layernorm_kernel<2><<<grid, 256, 0, s>>>(x, g, b, y, M, d);
-  else enc_layernorm_kernel<4><<<grid, 256, 0, s>>>(x, g, b, y, M, d);
+  if (d <= 256) enc_layernorm_kernel<1, RPW><<<grid, 256, 0, s>>>(x, g, b, y, M, d);
+  else if (d <= 512) enc_layernorm_kernel<2, RPW><<<grid, 256, 0, s>>>(x, g, b, y, M, d);
+  else if (d <= 768) enc_layernorm_kernel<3, RPW><<<grid, 256, 0, s>>>(x, g, b, y, M, d);
+  else enc_layernorm_kernel<4, RPW><<<grid, 256, 0, s>>>(x, g, b, y, M, d);
   return launch_end(name, s);
 }
 
@@ -516,7 +572,8 @@ cudaError_t run_encoder(const EncoderArgs& a, int sms, cudaStream_t s) {
     if (e == cudaSuccess) e = allow_smem((const void*)enc_attn_tc_kernel, kAttnSmem);
     if (e != cudaSuccess) return e;
     launch_begin("enc_attn", s);
-    enc_attn_tc_kernel<<<dim3(a.B * a.nC, a.H), kAttnThreads, kAttnSmem, s>>>(M, d, tm, A, a.err);
+    enc_attn_tc_kernel<<<dim3(a.B * a.nC, (a.H + kAttnHpc - 1) / kAttnHpc), kAttnThreads, kAttnSmem, s>>>(M, d, a.H, tm,
+                                                                                                       A, a.err);
     e = launch_end("enc_attn", s);
   }
   if (e == cudaSuccess) {
