@@ -43,10 +43,10 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------------ LayerNorm
-// One warp per RPW rows, held in registers (every load issued before the first
-// reduction, so that a warp keeps RPW rows in flight): mean, then the population variance
-// of the centred values, y = (x - mean) / sqrt(var + 1e-5) * g + b.  NV 16-byte vectors per
-// lane cover d <= 256 NV.
+// One warp per RPW rows, held in registers as packed bf16 (every load issued before the
+// first reduction, so that a warp keeps RPW rows in flight with few registers): mean, then
+// the population variance of the centred values, y = (x - mean) / sqrt(var + 1e-5) * g + b.
+// NV 16-byte vectors per lane cover d <= 256 NV.
 template <int NV, int RPW>
 __global__ void __launch_bounds__(256) enc_layernorm_kernel(const bf16* __restrict__ x, const float* __restrict__ g,
                                                             const float* __restrict__ b, bf16* __restrict__ y,
@@ -54,42 +54,47 @@ __global__ void __launch_bounds__(256) enc_layernorm_kernel(const bf16* __restri
   const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW;
   const int lane = threadIdx.x & 31;
   const int nv = d / 8;
-  float f[RPW][NV][8];
+  uint4 raw[RPW][NV];
 #pragma unroll
   for (int r = 0; r < RPW; ++r)
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int v = lane + 32 * i;
-      if (row0 + r < M && v < nv)
-        unpack16(__ldg(reinterpret_cast<const uint4*>(x + (row0 + r) * d) + v), f[r][i], static_cast<const bf16*>(nullptr));
-      else
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[r][i][e] = 0.f;
+      raw[r][i] = (row0 + r < M && v < nv) ? __ldg(reinterpret_cast<const uint4*>(x + (row0 + r) * d) + v)
+                                           : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
   for (int r = 0; r < RPW; ++r) {
     if (row0 + r >= M) break;  // uniform across the warp
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < NV; ++i)
+    for (int i = 0; i < NV; ++i) {
+      float f[8];
+      unpack16(raw[r][i], f, static_cast<const bf16*>(nullptr));
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s += f[r][i][e];
+      for (int e = 0; e < 8; ++e) s += f[e];
+    }
     const float mean = warp_sum(s) / (float)d;
     float q = 0.f;
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (lane + 32 * i < nv)
+      if (lane + 32 * i < nv) {
+        float f[8];
+        unpack16(raw[r][i], f, static_cast<const bf16*>(nullptr));
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float t = f[r][i][e] - mean;
+          const float t = f[e] - mean;
           q += t * t;
         }
+      }
     const float rstd = rsqrtf(warp_sum(q) / (float)d + 1e-5f);
     uint4* yr = reinterpret_cast<uint4*>(y + (row0 + r) * d);
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int v = lane + 32 * i;
       if (v < nv) {
+        float f[8];
+        unpack16(raw[r][i], f, static_cast<const bf16*>(nullptr));
         const float4 g0 = __ldg(reinterpret_cast<const float4*>(g) + 2 * v);
         const float4 g1 = __ldg(reinterpret_cast<const float4*>(g) + 2 * v + 1);
         const float4 b0 = __ldg(reinterpret_cast<const float4*>(b) + 2 * v);
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(256) enc_layernorm_kernel(const bf16* __restri
         const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
         float o[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = (f[r][i][e] - mean) * rstd * gg[e] + bb[e];
+        for (int e = 0; e < 8; ++e) o[e] = (f[e] - mean) * rstd * gg[e] + bb[e];
         yr[v] = make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]), pack_bf16(o[6], o[7]));
       }
     }
@@ -175,7 +180,7 @@ __device__ __forceinline__ void store32(bf16* dst, const float (&v)[32]) {
 
 // Math of the step's epilogue on a 32-column chunk (everything but the store).
 template <int EPI>
-__device__ __forceinline__ void epilogue_math(const GemmArgs& a, int row, int col, float (&v)[32]) {
+__device__ __forceinline__ void epilogue_math(const GemmArgs& a, int col, const uint4 (&res)[4], float (&v)[32]) {
   if (EPI != kEpiKV) {
     const float4* b4 = reinterpret_cast<const float4*>(a.bias + col);
 #pragma unroll
@@ -191,12 +196,11 @@ __device__ __forceinline__ void epilogue_math(const GemmArgs& a, int row, int co
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = gelu(v[j]);
   }
-  if (EPI == kEpiResid && row < a.M) {
-    const uint4* r4 = reinterpret_cast<const uint4*>(a.resid + (size_t)row * a.N + col);
+  if (EPI == kEpiResid) {  // the residual's 32 values, loaded before the accumulator was ready
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       float f[8];
-      unpack16(__ldg(r4 + q), f, static_cast<const bf16*>(nullptr));
+      unpack16(res[q], f, static_cast<const bf16*>(nullptr));
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[8 * q + e] += f[e];
     }
@@ -319,10 +323,20 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
     int i = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int buf = i & 1;
-      if (!wait_or_abort(&acc_full[buf], (uint32_t)(i >> 1) & 1, &abort_s, a.err, 24, t)) break;
-      tc::fence_after();
       const int row0 = (t / nt) * 128 + 32 * q, row = row0 + lane;
       const int col0 = (t % nt) * BN + hf * HALF;
+      // The residual does not depend on the products: fetch the warp's part of the tile
+      // (its row, HALF columns) now, so that the loads overlap the wait below.
+      uint4 res[NCH][4];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          res[c][u] = (EPI == kEpiResid && row < a.M)
+                          ? __ldg(reinterpret_cast<const uint4*>(a.resid + (size_t)row * a.N + col0 + 32 * c) + u)
+                          : make_uint4(0u, 0u, 0u, 0u);
+      if (!wait_or_abort(&acc_full[buf], (uint32_t)(i >> 1) & 1, &abort_s, a.err, 24, t)) break;
+      tc::fence_after();
       const uint32_t tcol = tmem + lane_base + buf * BN + hf * HALF;
       float v[2][32];
       tc::ld32x32b_x32(tcol, v[0]);
@@ -332,7 +346,7 @@ enc_gemm_kernel(GemmArgs a, const __grid_constant__ CUtensorMap tmA, const __gri
         if (c + 1 < NCH) tc::ld32x32b_x32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
         float(&cur)[32] = v[c & 1];
         const int col = col0 + 32 * c;
-        epilogue_math<EPI>(a, row, col, cur);
+        epilogue_math<EPI>(a, col, res[c], cur);
         {
           unsigned char* sbuf = stg + sb * (kStageBufBytes / 2);
           if (lane == 0) tc::bulk_wait_read<1>();  // this buffer's previous store has read it
