@@ -272,7 +272,7 @@ def gpu_arm(args):
 
     # The rest of the attention block at the same shape: sliding-window self-attention
     # (W = 512) and, as the ablation, chunked cross-attention over the same retrieval.
-    blk = None if args.no_block else block_attn_leg(args, torch, gca, q, k, v, out, timed)
+    blk = None if args.no_block else block_attn_leg(args, torch, gca, q, k, v, out, timed, pk)
     # The chunk / landmark encoder that produces K, V and the key landmarks.
     enc = None if args.no_encoder else encoder_leg(args, torch, gca, synth, timed, pk)
 
@@ -287,6 +287,14 @@ def gpu_arm(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.seed, budget_s=args.cpu_seconds)
+        side = next_rows_cpu(args.seed)
+        if dec is not None and dec.get("offload") is not None:
+            dec["offload"]["cpu_baseline"] = side["decode"]
+        if blk is not None:
+            blk["window"]["cpu_baseline"] = side["window"]
+            blk["cca"]["cpu_baseline"] = side["cca"]
+        if enc is not None:
+            enc["cpu_baseline"] = side["encoder"]
 
     if rank == 0:
         line = {
@@ -458,7 +466,7 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
             "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "offload": offload}
 
 
-def block_attn_leg(args, torch, gca, q, k, v, out, timed):
+def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):
     """Forward and backward of the sliding-window self-attention (W = 512) beside GCA (the
     forward accumulated onto GCA's output as in the attention block), and the forward of
     CCA (one joint softmax over the same retrieved chunks), at the training shape.
@@ -497,13 +505,16 @@ def block_attn_leg(args, torch, gca, q, k, v, out, timed):
     pairs_c = valid * 64 * 64
     fl_w, fl_c = pairs_w * 4 * DH, pairs_c * 4 * DH
     tok = B * L
+    tf = lambda f, ms: f / (ms / 1e3) / 1e12
+    peak = pk["bf16_tflops"]
     return {"window": {"window": W, "ms": round(ms_w, 4), "tokens_per_s": round(tok / (ms_w / 1e3), 1),
-                       "tflops_algorithmic": round(fl_w / (ms_w / 1e3) / 1e12, 1), "accumulated_onto_gca": True,
-                       "backward_ms": round(ms_wb, 4),
-                       "backward_tflops_algorithmic": round(2.5 * fl_w / (ms_wb / 1e3) / 1e12, 1),
+                       "tflops_algorithmic": round(tf(fl_w, ms_w), 1), "frac_of_bf16_peak": round(tf(fl_w, ms_w) / peak, 3),
+                       "accumulated_onto_gca": True, "backward_ms": round(ms_wb, 4),
+                       "backward_tflops_algorithmic": round(tf(2.5 * fl_w, ms_wb), 1),
+                       "backward_frac_of_bf16_peak": round(tf(2.5 * fl_w, ms_wb) / peak, 3),
                        "fwd_bwd_tokens_per_s": round(tok / ((ms_w + ms_wb) / 1e3), 1)},
             "cca": {"ms": round(ms_c, 4), "tokens_per_s": round(tok / (ms_c / 1e3), 1),
-                    "tflops_algorithmic": round(fl_c / (ms_c / 1e3) / 1e12, 1)}}
+                    "tflops_algorithmic": round(tf(fl_c, ms_c), 1), "frac_of_bf16_peak": round(tf(fl_c, ms_c) / peak, 3)}}
 
 
 ENC_D, ENC_H = 768, 12  # the 128M model's width: the encoder's rows have d = H * 64 = 768
@@ -656,6 +667,73 @@ def cpu_sample(seed, rows, budget_s=None):
     r1 = resource.getrusage(resource.RUSAGE_SELF)
     cpu_s = (r1.ru_utime + r1.ru_stime) - (r0.ru_utime + r0.ru_stime)
     return done * 64, dt, cpu_s
+
+
+def _cpu_timed(fn, min_s=1.5):
+    """fn() repeated until min_s seconds have passed: (wall seconds per call, process CPU
+    seconds per call, calls)."""
+    r0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    n = 0
+    while n == 0 or time.perf_counter() - t0 < min_s:
+        fn()
+        n += 1
+    dt = time.perf_counter() - t0
+    r1 = resource.getrusage(resource.RUSAGE_SELF)
+    return dt / n, ((r1.ru_utime + r1.ru_stime) - (r0.ru_utime + r0.ru_stime)) / n, n
+
+
+def next_rows_cpu(seed):
+    """The oracle timed beside each leg of the rest of the method, on a bounded sample of
+    that leg's workload (a few seconds each), in the leg's own unit."""
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    import oracle.gca_oracle as orc
+    from retrieval_sparse_attention_causal_gb300 import synth
+
+    cores = len(os.sched_getaffinity(0))
+    out = {}
+
+    def entry(value, unit, t, sample):
+        dt, cpu_s, n = t
+        return {"value": round(value, 3), "unit": unit, "cores": cores, "threads_busy": round(cpu_s / dt, 2),
+                "kind": "oracle", "sample": f"{sample}; float64 numpy; {dt:.3f} s wall per call, {n} calls"}
+
+    # Decode at long context: retrieval over 32768 of one sequence's landmarks (1/8 of the
+    # 16M-context row) and the forward over the 8 retrieved chunks.
+    nk = DEC_NC // 8
+    ql = synth.normal(seed, synth.S_QL, (1, 1, D), 1.0, "bf16")
+    kl = synth.normal(seed, synth.S_KL, (1, nk, D), 1.0, "bf16")
+    qn = synth.normal(seed, synth.S_Q, (64, H, DH), 1 / 8, "bf16")
+    kc = synth.normal(seed, synth.S_K, (K * 64, H, DH), 1 / 8, "bf16")
+    vc = synth.normal(seed, synth.S_V, (K * 64, H, DH), 1 / 8, "bf16")
+
+    def dec():
+        idx, sc, _ = orc.retrieve_topk(ql, kl, K, nk, False, 0)
+        orc.gca_chunk_forward(qn, kc, vc, np.arange(K), sc[0, 0])  # on the compact buffer of the 8 chunks
+    t = _cpu_timed(dec)
+    out["decode"] = entry(nk * D * 2 / t[0] / 1e9, "GB/s", t,
+                          f"one sequence: retrieval over {nk} landmarks x {D} (1/8 of the 16M-context row), "
+                          f"forward over the {K} retrieved chunks")
+    # Window attention W = 512, forward and backward, one sequence of 1024 tokens.
+    lw = 1024
+    q, k, v, do = (synth.normal(seed, st, (1, lw, H, DH), 1 / 8, "bf16")
+                   for st in (synth.S_Q, synth.S_K, synth.S_V, synth.S_DO))
+    t = _cpu_timed(lambda: (orc.swa_forward(q, k, v, 512), orc.swa_backward(q, k, v, do, 512)))
+    out["window"] = entry(lw / t[0], "tokens/s", t, f"one sequence of {lw} tokens, 12 heads: forward + backward")
+    # CCA forward: 16 query chunks of one sequence over its 256 chunks, 8 retrieved each.
+    x = synth.gca_inputs(seed, 1, NC, NC, H, DH, 1 / 8, "bf16", with_grad=False)
+    idx = np.stack([np.sort(synth.integers(seed, 40 + r, 0, max(r, 1), (K,))) if r >= K else
+                    np.concatenate([np.arange(r), -np.ones(K - r, dtype=np.int64)]) for r in range(NC)])[None]
+    nq = 16
+    t = _cpu_timed(lambda: orc.cca_forward(x["q"], x["k"], x["v"], idx, 1, chunks=[(0, r) for r in range(1, nq + 1)]))
+    out["cca"] = entry(nq * 64 / t[0], "tokens/s", t, f"{nq} query chunks of one sequence, {K} retrieved chunks each")
+    # Chunk encoder: 8 chunks (520 rows) of one sequence at d = 768.
+    ne = 8
+    xe = synth.encoder_inputs(seed, 1, ne, ENC_D, "bf16")
+    pe = synth.encoder_params(seed, ENC_D, "bf16")
+    t = _cpu_timed(lambda: orc.chunk_encoder_forward(xe, pe, ENC_H))
+    out["encoder"] = entry(ne * 64 / t[0], "tokens/s", t, f"{ne} chunks of one sequence (their {ne * 65} rows), d = {ENC_D}")
+    return out
 
 
 def cpu_baseline(seed, budget_s=20.0):
