@@ -625,12 +625,99 @@ __global__ void __launch_bounds__(256) gca_dscores_kernel(BwdArgs a) {
 }
 
 // ------------------------------------------------------------------ CSR of consumers
+// One CTA per sequence: per-chunk counts, an exclusive scan into the offsets, then a fill
+// by one warp, 32 entries at a time in entry order (ranks inside a step from
+// __match_any_sync), so that every chunk's list is in increasing entry order.  kSmem keeps
+// the counters and fill cursors in shared memory (nC <= kCsrSmemChunks), so that the
+// fill's step-to-step dependence goes through shared memory; the entries of the next step
+// are loaded while the current one is placed.
+constexpr int kCsrSmemChunks = 16384;
+constexpr int kCsrParChunks = 8192, kCsrParEntries = 8192;  // the parallel fill's shared-memory limits
+
+// The same CSR with a parallel fill (nC <= kCsrParChunks, entries <= kCsrParEntries):
+// counts and cursors in shared memory; every entry takes a slot of its chunk's segment by
+// a shared atomic (in any order), then one warp per chunk writes each of the segment's
+// entries at its rank, the number of smaller entry indices in the segment, which is the
+// entry-order position.
+__global__ void __launch_bounds__(1024) csr_par_kernel(const int32_t* idx, int ld_rows, int nrows, int topk, int nC,
+                                                       int32_t* off, int32_t* ent, ErrWord* err) {
+  extern __shared__ int32_t sh[];
+  int32_t* cnt = sh;         // [nC]: counts, then offsets, then fill cursors
+  int32_t* beg = sh + nC;    // [nC + 1]: offsets
+  int32_t* tmp = beg + nC + 1;  // [n]: entries, unordered within each segment
+  __shared__ int wsum[32];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t* ib = idx + (int64_t)b * ld_rows * topk;
+  int32_t* ob = off + (int64_t)b * (nC + 1);
+  int32_t* eb = ent + (int64_t)b * ld_rows * topk;
+  const int n = nrows * topk;
+  for (int j = tid; j < nC; j += 1024) cnt[j] = 0;
+  __syncthreads();
+  for (int e = tid; e < n; e += 1024) {
+    const int j = ib[e];
+    if (j >= 0 && j < nC) atomicAdd(&cnt[j], 1);
+    else if (j != -1) flag_bad_index(err, j);
+  }
+  __syncthreads();
+  const int per = (nC + 1023) / 1024;
+  const int lo = min(nC, tid * per), hi = min(nC, lo + per);
+  int mine = 0;
+  for (int j = lo; j < hi; ++j) mine += cnt[j];
+  int incl = mine;
+#pragma unroll
+  for (int k = 1; k < 32; k <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, k);
+    if (lane >= k) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = wsum[lane];
+#pragma unroll
+    for (int k = 1; k < 32; k <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, k);
+      if (lane >= k) v += u;
+    }
+    wsum[lane] = v;
+  }
+  __syncthreads();
+  int run = incl - mine + (warp > 0 ? wsum[warp - 1] : 0);
+  for (int j = lo; j < hi; ++j) {
+    const int cj = cnt[j];
+    beg[j] = run;
+    ob[j] = run;
+    cnt[j] = run;
+    run += cj;
+  }
+  if (tid == 1023) {
+    beg[nC] = wsum[31];
+    ob[nC] = wsum[31];
+  }
+  __syncthreads();
+  for (int e = tid; e < n; e += 1024) {
+    const int j = ib[e];
+    if (j >= 0 && j < nC) tmp[atomicAdd(&cnt[j], 1)] = e;
+  }
+  __syncthreads();
+  for (int j = warp; j < nC; j += 32) {
+    const int s0 = beg[j], len = beg[j + 1] - s0;
+    for (int x = lane; x < len; x += 32) {
+      const int v = tmp[s0 + x];
+      int rank = 0;
+      for (int y = 0; y < len; ++y) rank += tmp[s0 + y] < v;
+      eb[s0 + rank] = v;
+    }
+  }
+}
+
+template <bool kSmem>
 __global__ void __launch_bounds__(1024) csr_kernel(const int32_t* idx, int ld_rows, int nrows, int topk,
                                                     int nC, int32_t* off, int32_t* ent, int32_t* cur,
                                                     ErrWord* err) {
+  extern __shared__ int32_t cnt_s[];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t* ib = idx + (int64_t)b * ld_rows * topk;
-  int32_t* cnt = cur + (int64_t)b * nC;
+  int32_t* cnt = kSmem ? cnt_s : cur + (int64_t)b * nC;
   int32_t* ob = off + (int64_t)b * (nC + 1);
   int32_t* eb = ent + (int64_t)b * ld_rows * topk;
   const int n = nrows * topk;
@@ -677,10 +764,12 @@ __global__ void __launch_bounds__(1024) csr_kernel(const int32_t* idx, int ld_ro
   __syncthreads();
   // Stable fill by one warp, 32 entries at a time, in entry order.
   if (warp == 0) {
+    int jn = lane < n ? ib[lane] : -1;
     for (int base = 0; base < n; base += 32) {
       const int e = base + lane;
-      int j = (e < n) ? ib[e] : -1;
-      const bool valid = j >= 0 && j < nC;
+      int j = jn;
+      jn = (e + 32 < n) ? ib[e + 32] : -1;  // next step's entry, in flight meanwhile
+      const bool valid = e < n && j >= 0 && j < nC;
       if (!valid) j = -1;
       const unsigned grp = __match_any_sync(0xffffffffu, j);
       const int rank = __popc(grp & ((1u << lane) - 1));
@@ -703,8 +792,25 @@ size_t bwd_kv_smem(int dh) { return (size_t)64 * dh * 2 * 6 + 1024; }
 
 cudaError_t launch_csr(const int32_t* idx, int B, int ld_rows, int nrows, int topk, int nC,
                        int32_t* off, int32_t* ent, int32_t* cur, ErrWord* err, cudaStream_t s) {
+  const int n = nrows * topk;
+  if (nC <= kCsrParChunks && n <= kCsrParEntries) {
+    const int sm = (2 * nC + 1 + n) * (int)sizeof(int32_t);
+    cudaError_t e = allow_smem((const void*)csr_par_kernel, sm);
+    if (e != cudaSuccess) return e;
+    launch_begin("gca_csr", s);
+    csr_par_kernel<<<B, 1024, sm, s>>>(idx, ld_rows, nrows, topk, nC, off, ent, err);
+    return launch_end("gca_csr", s);
+  }
+  if (nC <= kCsrSmemChunks) {
+    const int sm = nC * (int)sizeof(int32_t);
+    cudaError_t e = allow_smem((const void*)csr_kernel<true>, sm);
+    if (e != cudaSuccess) return e;
+    launch_begin("gca_csr", s);
+    csr_kernel<true><<<B, 1024, sm, s>>>(idx, ld_rows, nrows, topk, nC, off, ent, cur, err);
+    return launch_end("gca_csr", s);
+  }
   launch_begin("gca_csr", s);
-  csr_kernel<<<B, 1024, 0, s>>>(idx, ld_rows, nrows, topk, nC, off, ent, cur, err);
+  csr_kernel<false><<<B, 1024, 0, s>>>(idx, ld_rows, nrows, topk, nC, off, ent, cur, err);
   return launch_end("gca_csr", s);
 }
 

@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(256) dq_lmk_kernel(ScoresBwdArgs a) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) dk_lmk_kernel(ScoresBwdArgs a) {
+  __shared__ int row_s[256];
+  __shared__ float ds_s[256];
   const int j = blockIdx.x, b = blockIdx.y;
   const int e0 = a.csr_off[(int64_t)b * (a.nC + 1) + j];
   const int e1 = a.csr_off[(int64_t)b * (a.nC + 1) + j + 1];
@@ -53,15 +55,44 @@ __global__ void __launch_bounds__(256) dk_lmk_kernel(ScoresBwdArgs a) {
   const float inv = 1.0f / sqrtf((float)a.D);
   const T* qb = reinterpret_cast<const T*>(a.q) + (int64_t)b * a.q_bs;
   float* out = a.dk + ((int64_t)b * a.nC + j) * a.D;
-  for (int d = threadIdx.x; d < a.D; d += blockDim.x) {
-    float acc = 0.f;
-    for (int c = e0; c < e1; ++c) {
-      const int e = ent[c];
-      const int i = e / a.topk;
-      const float ds = a.ds[(int64_t)b * a.nQ * a.topk + e];
-      acc = fmaf(ds, Elem<T>::ld(qb + (int64_t)i * a.q_rs + d), acc);
+  constexpr int kMaxD = 4;  // D <= 1024 in registers; larger D loops below
+  float acc[kMaxD] = {0.f, 0.f, 0.f, 0.f};
+  // The chunk's consumers (query row, score gradient) go to shared memory 256 at a time,
+  // in CSR order, so the sum below has a fixed order and independent loads.
+  for (int c0 = e0; c0 < e1; c0 += 256) {
+    const int nc = min(256, e1 - c0);
+    __syncthreads();
+    if (threadIdx.x < nc) {
+      const int e = ent[c0 + threadIdx.x];
+      row_s[threadIdx.x] = e / a.topk;
+      ds_s[threadIdx.x] = a.ds[(int64_t)b * a.nQ * a.topk + e];
     }
-    out[d] = acc * inv;
+    __syncthreads();
+    if (a.D <= kMaxD * 256) {
+#pragma unroll
+      for (int u = 0; u < kMaxD; ++u) {
+        const int d = threadIdx.x + 256 * u;
+        if (d < a.D)
+          for (int c = 0; c < nc; ++c)
+            acc[u] = fmaf(ds_s[c], Elem<T>::ld(qb + (int64_t)row_s[c] * a.q_rs + d), acc[u]);
+      }
+    } else {
+      for (int d = threadIdx.x; d < a.D; d += 256) {
+        float x = c0 == e0 ? 0.f : out[d];
+        for (int c = 0; c < nc; ++c) x = fmaf(ds_s[c], Elem<T>::ld(qb + (int64_t)row_s[c] * a.q_rs + d), x);
+        out[d] = x;
+      }
+    }
+  }
+  if (a.D <= kMaxD * 256) {
+#pragma unroll
+    for (int u = 0; u < kMaxD; ++u) {
+      const int d = threadIdx.x + 256 * u;
+      if (d < a.D) out[d] = acc[u] * inv;
+    }
+  } else {
+    __syncthreads();
+    for (int d = threadIdx.x; d < a.D; d += 256) out[d] = e1 > e0 ? out[d] * inv : 0.f;
   }
 }
 
