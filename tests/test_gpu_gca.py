@@ -187,3 +187,38 @@ def test_scores_backward_and_strided_accumulate():
     want = base.copy()
     want[:, 63::64] += dq_ref.reshape(B, nC, H, dh)
     assert_close(host(t), want, TOL["bf16"], "accumulated dO")
+
+
+@pytest.mark.parametrize("nC", [9000, 17000])
+def test_long_sequence_consumer_lists(nC):
+    """576k and 1.09M tokens, one head: 36k and 68k (row, slot) entries take the CSR of
+    consumers past its shared-memory fill (counters in shared memory for nC <= 16384,
+    in global memory beyond).  dK, dV of sampled key chunks (chunk 0 has the longest
+    consumer list) and dQ, dscores of sampled query chunks against the oracle."""
+    g = _g()
+    B, H, dh, K = 1, 1, 64, 4
+    rng = np.random.default_rng(nC)
+    idx = np.full((B, nC, K), -1, dtype=np.int32)
+    for r in range(1, nC):
+        n = min(K, r)
+        idx[0, r, :n] = rng.choice(r, n, replace=False) if r > K else np.arange(r)[:n]
+    sc = np.where(idx >= 0, rng.standard_normal(idx.shape), -np.inf).astype(np.float32).astype(np.float64)
+    x = synth.gca_inputs(60, B, nC, nC, H, dh, 1.0, "bf16")
+    q, k, v, do = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    it = torch.from_numpy(idx).cuda()
+    st = torch.from_numpy(sc.astype(np.float32)).cuda()
+    o, lse = g.gca_forward(q, k, v, it, st, shift=1)
+    dq, dk, dv, ds = g.gca_backward(q, k, v, it, st, do, lse, shift=1)
+    torch.cuda.synchronize()
+    for j in (0, 1, 7, int(rng.integers(8, nC - 2)), nC - 3):
+        rk, rv = orc.gca_backward_chunks(x["q"], x["k"], x["v"], idx, sc, x["do"], 0, [j])
+        sl = slice(64 * j, 64 * (j + 1))
+        assert_close(host(dk[0, sl]), rk[j], TOL["bf16"], f"dK chunk {j}")
+        assert_close(host(dv[0, sl]), rv[j], TOL["bf16"], f"dV chunk {j}")
+    assert np.all(host(dk[0, 64 * (nC - 1):]) == 0) and np.all(host(dv[0, 64 * (nC - 1):]) == 0)  # never retrieved
+    for c in (1, 2, int(rng.integers(3, nC)), nC - 1):
+        sl = slice(64 * c, 64 * (c + 1))
+        rq, _, _, rds = orc.gca_chunk_backward(x["q"][0, sl], x["k"][0], x["v"][0], idx[0, c - 1], sc[0, c - 1],
+                                               x["do"][0, sl])
+        assert_close(host(dq[0, sl]), rq, TOL["bf16"], f"dQ chunk {c}")
+        assert_close(host(ds[0, c - 1]), rds, TOL["bf16"], f"dscores row {c - 1}")
