@@ -337,6 +337,53 @@ def cca_forward(q, kv_k, kv_v, idx, shift=1, chunk=CHUNK, chunks=None):
     return o, lse
 
 
+def cca_chunk_backward(qc, kv_k, kv_v, idx_row, doc, chunk=CHUNK):
+    """Backward of cca_chunk_forward for one query chunk (the chain rule of the joint
+    softmax, computed directly).  With K, V the valid retrieved chunks concatenated in
+    slot order and P the joint row softmax of the dh^-1/2-scaled logits:
+        dP = dO V^T,  dS = P * (dP - rowsum(P * dP)),
+        dQ = dS K / sqrt(dh),  dK = dS^T Q / sqrt(dh),  dV = P^T dO.
+    Returns dq [S, H, dh] and a list of (chunk j, dK_j, dV_j) per valid slot; the
+    retrieval scores take no part, so there is no score gradient."""
+    S_, H, dh = qc.shape
+    js = [int(j) for j in idx_row if j >= 0]
+    if not js:
+        return np.zeros((S_, H, dh)), []
+    Kc = np.concatenate([kv_k[j * chunk:(j + 1) * chunk] for j in js]).transpose(1, 0, 2)
+    Vc = np.concatenate([kv_v[j * chunk:(j + 1) * chunk] for j in js]).transpose(1, 0, 2)
+    Qh, dOh = qc.transpose(1, 0, 2), doc.transpose(1, 0, 2)
+    S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S, n*S]
+    P, _ = _softmax_rows(S)
+    dP = dOh @ Vc.transpose(0, 2, 1)
+    dS = P * (dP - np.sum(P * dP, axis=2, keepdims=True))
+    dq = (dS @ Kc / math.sqrt(dh)).transpose(1, 0, 2)
+    dK = (dS.transpose(0, 2, 1) @ Qh / math.sqrt(dh)).transpose(1, 0, 2)  # [n*S, H, dh]
+    dV = (P.transpose(0, 2, 1) @ dOh).transpose(1, 0, 2)
+    return dq, [(j, dK[m * chunk:(m + 1) * chunk], dV[m * chunk:(m + 1) * chunk]) for m, j in enumerate(js)]
+
+
+def cca_backward(q, kv_k, kv_v, idx, do, shift=1, chunk=CHUNK):
+    """Gradients of cca_forward: dq like q, dk and dv like kv_k (a retrieved chunk
+    gathers the contributions of every query chunk whose row retrieved it)."""
+    B, L, H, dh = q.shape
+    nQ = L // chunk
+    dq = np.zeros((B, L, H, dh))
+    dk = np.zeros(kv_k.shape)
+    dv = np.zeros(kv_v.shape)
+    for b in range(B):
+        for c in range(nQ):
+            r = c - shift
+            if r < 0:
+                continue
+            sl = slice(c * chunk, (c + 1) * chunk)
+            dqc, parts = cca_chunk_backward(q[b, sl], kv_k[b], kv_v[b], idx[b, r], do[b, sl], chunk)
+            dq[b, sl] = dqc
+            for j, dkj, dvj in parts:
+                dk[b, j * chunk:(j + 1) * chunk] += dkj
+                dv[b, j * chunk:(j + 1) * chunk] += dvj
+    return dq, dk, dv
+
+
 # ---------------------------------------------------------------------------
 # GCA backward (chain rule of the forward, computed directly)
 # ---------------------------------------------------------------------------

@@ -558,6 +558,51 @@ def pin_cca_no_slot_and_shift(orc):
     assert np.all(np.abs(o[0, 4:8]) > 0)
 
 
+def pin_cca_backward_single_slot_equals_gca(orc):
+    """One valid slot: CCA's gradients are GCA's with weight 1 (the score gradient of
+    GCA is zero then, and CCA has none)."""
+    rng = np.random.default_rng(44)
+    q, k, v = _rand_gca(rng, nQ=3, nC=4, chunk=8)
+    do = rng.standard_normal(q.shape)
+    idx = np.array([[[2, -1], [0, -1], [3, -1]]], dtype=np.int32)
+    sc = np.array([[[0.3, -np.inf], [1.0, -np.inf], [-2.0, -np.inf]]])
+    gq, gk, gv, _ = orc.gca_backward(q, k, v, idx, sc, do, shift=0, chunk=8)
+    cq, ck, cv = orc.cca_backward(q, k, v, idx, do, shift=0, chunk=8)
+    for a, b in ((gq, cq), (gk, ck), (gv, cv)):
+        assert np.max(np.abs(a - b)) < 1e-12
+
+
+def pin_cca_backward_finite_differences(orc):
+    """Two and three retrieved chunks (one retrieved twice, by different rows), shift 1:
+    central differences of <dO, O> in float64."""
+    rng = np.random.default_rng(45)
+    S = 4
+    q = rng.standard_normal((1, 4 * S, 2, 3))
+    k = rng.standard_normal((1, 5 * S, 2, 3))
+    v = rng.standard_normal((1, 5 * S, 2, 3))
+    do = rng.standard_normal(q.shape)
+    idx = np.array([[[4, 1, -1], [0, 2, 4], [-1, -1, -1], [3, 3, -1]]], dtype=np.int32)
+    idx[0, 3] = [3, 1, -1]
+    dq, dk, dv = orc.cca_backward(q, k, v, idx, do, shift=1, chunk=S)
+
+    def loss(qq, kk, vv):
+        return float(np.sum(orc.cca_forward(qq, kk, vv, idx, shift=1, chunk=S)[0] * do))
+    args = {"q": q, "k": k, "v": v}
+    for name, g in (("q", dq), ("k", dk), ("v", dv)):
+        x = args[name]
+        for ix in [(0, 5, 0, 1), (0, 9, 1, 2), (0, 17, 0, 0), (0, 1, 1, 1), (0, 13, 0, 2)]:
+            if ix[1] >= x.shape[1]:
+                continue
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += 1e-6
+            xm[ix] -= 1e-6
+            fp = loss(*[xp if n == name else args[n] for n in ("q", "k", "v")])
+            fm = loss(*[xm if n == name else args[n] for n in ("q", "k", "v")])
+            fd = (fp - fm) / 2e-6
+            assert abs(fd - g[ix]) <= 1e-6 * max(1.0, abs(fd)), (name, ix, fd, g[ix])
+    assert np.all(dq[0, :S] == 0) and np.all(dq[0, 3 * S:4 * S] == 0)  # no row; a row with no slot
+
+
 # ------------------------------------------------------------------------ chunk encoder
 
 def _enc_params(rng, d):

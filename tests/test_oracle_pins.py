@@ -46,12 +46,17 @@ MUTATIONS = {
     "window_one_short": ("s0 = max(0, t - window + 1)", "s0 = max(0, t - window + 2)"),
     "window_not_causal": ("Kh = k[b, s0:t + 1].transpose(1, 0, 2)  # [H, n, dh]",
                           "Kh = k[b, s0:t + 2].transpose(1, 0, 2)  # [H, n, dh]"),
-    "cca_softmax_per_chunk": ("S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S, n*S]",
-                              "S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh) / len(js)  # [H, S, n*S]"),
-    "cca_drops_slot": ("js = [int(j) for j in idx_row if j >= 0]", "js = [int(j) for j in idx_row if j > 0]"),
+    "cca_softmax_per_chunk": ("S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh)  # [H, S, n*S]\n    P, l = _softmax_rows(S)",
+                              "S = Qh @ Kc.transpose(0, 2, 1) / math.sqrt(dh) / len(js)  # [H, S, n*S]\n    P, l = _softmax_rows(S)"),
+    "cca_drops_slot": ("js = [int(j) for j in idx_row if j >= 0]\n    if not js:\n        return np.zeros((S_, H, dh)), np.full(",
+                       "js = [int(j) for j in idx_row if j > 0]\n    if not js:\n        return np.zeros((S_, H, dh)), np.full("),
     "swa_bwd_window_mask": ("allowed = (t[None, :] <= t[:, None]) & (t[None, :] > t[:, None] - window)  # [query, key]",
                             "allowed = (t[None, :] <= t[:, None]) & (t[None, :] >= t[:, None] - window)  # [query, key]"),
     "swa_bwd_dk_scale": ("dk[b, :, h] = dS.T @ Q / math.sqrt(dh)", "dk[b, :, h] = dS.T @ Q"),
+    "cca_bwd_rowsum": ("dS = P * (dP - np.sum(P * dP, axis=2, keepdims=True))\n    dq = (dS @ Kc",
+                       "dS = P * (dP - np.sum(dP, axis=2, keepdims=True))\n    dq = (dS @ Kc"),
+    "cca_bwd_dk_not_accumulated": ("                dk[b, j * chunk:(j + 1) * chunk] += dkj",
+                                   "                dk[b, j * chunk:(j + 1) * chunk] = dkj"),
     "encoder_causal": ("P, _ = _softmax_rows(S)\n    a = (P @ heads[2])",
                        "P, _ = _softmax_rows(np.where(np.tri(ENC_CHUNK, dtype=bool), S, -np.inf))\n    a = (P @ heads[2])"),
     "encoder_lmk_not_a_key": ("P, _ = _softmax_rows(S)\n    a = (P @ heads[2])",
