@@ -468,8 +468,8 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
 
 def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):
     """Forward and backward of the sliding-window self-attention (W = 512) beside GCA (the
-    forward accumulated onto GCA's output as in the attention block), and the forward of
-    CCA (one joint softmax over the same retrieved chunks), at the training shape.
+    forward accumulated onto GCA's output as in the attention block), and of CCA (one
+    joint softmax over the same retrieved chunks), at the training shape.
     Algorithmic flops count the unmasked (query, key) pairs: 4 dh flops each forward (QK^T,
     PV) and 2.5 times that backward (S recompute, dO V^T, dQ, dK, dV)."""
     W = 512
@@ -491,14 +491,21 @@ def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):
     def cca(i):
         gca.cca_forward(q, k, v, out["idx"], shift=1, out=o_c, lse=lse_c)
 
+    dqc, dkc, dvc = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def cca_bwd(i):
+        gca.cca_backward(q, k, v, o_c, do, lse_c, out["idx"], shift=1, dq=dqc, dk=dkc, dv=dvc)
+
     gca.window_forward(q, k, v, window=W, out=o_w, lse=lse_w)  # the window attention's own output
     for i in range(args.warmup):
         win_bwd(i)
         win(i)
         cca(i)
+        cca_bwd(i)
     ms_wb = timed(win_bwd, args.steps) / args.steps
     ms_w = timed(win, args.steps) / args.steps
     ms_c = timed(cca, args.steps) / args.steps
+    ms_cb = timed(cca_bwd, args.steps) / args.steps
     t = torch.arange(L, dtype=torch.float64)
     pairs_w = float(torch.clamp(t + 1, max=W).sum()) * B * H
     valid = int((out["idx"][:, : NC - 1] >= 0).sum()) * H  # rows 0..nC-2 feed chunks 1..nC-1
@@ -514,7 +521,11 @@ def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):
                        "backward_frac_of_bf16_peak": round(tf(2.5 * fl_w, ms_wb) / peak, 3),
                        "fwd_bwd_tokens_per_s": round(tok / ((ms_w + ms_wb) / 1e3), 1)},
             "cca": {"ms": round(ms_c, 4), "tokens_per_s": round(tok / (ms_c / 1e3), 1),
-                    "tflops_algorithmic": round(tf(fl_c, ms_c), 1), "frac_of_bf16_peak": round(tf(fl_c, ms_c) / peak, 3)}}
+                    "tflops_algorithmic": round(tf(fl_c, ms_c), 1), "frac_of_bf16_peak": round(tf(fl_c, ms_c) / peak, 3),
+                    "backward_ms": round(ms_cb, 4),
+                    "backward_tflops_algorithmic": round(tf(2.5 * fl_c, ms_cb), 1),
+                    "backward_frac_of_bf16_peak": round(tf(2.5 * fl_c, ms_cb) / peak, 3),
+                    "fwd_bwd_tokens_per_s": round(tok / ((ms_c + ms_cb) / 1e3), 1)}}
 
 
 ENC_D, ENC_H = 768, 12  # the 128M model's width: the encoder's rows have d = H * 64 = 768

@@ -218,6 +218,31 @@ GCA_API gca_status gca_cca_forward(const void* q, const void* k, const void* v, 
                            size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * gca_cca_backward - gradients of gca_cca_forward.
+ *
+ * With P the joint row softmax of a query chunk over its valid retrieved chunks (from the
+ * saved LSE) and D = rowsum(dO * O):  dS = P * (dO V^T - D),  dQ = dS K / sqrt(dh),
+ * dK_j += dS^T Q / sqrt(dh),  dV_j += P^T dO  for every retrieved chunk j.  The scores take
+ * no part in CCA, so there is no score gradient.  Deterministic (no atomics): a query-side
+ * pass, and a key-side pass over each chunk's consumers in entry order.
+ *
+ *   q, k, v, idx, topk, shift, lse: as passed to / produced by gca_cca_forward (K/V
+ *           contiguous per sequence: no shared store).
+ *   o       [B][nQ*64][H][dh] CCA's own output (before any accumulation).
+ *   dout    [B][nQ*64][H][dh] gradient of o.
+ *   dq [B][nQ*64][H][dh], dk, dv [B][nC*64][H][dh] out (accumulate != 0: added to).  Query
+ *           chunks without a valid slot get dq = 0, chunks never retrieved dk = dv = 0.
+ *   ws      >= gca_cca_backward_workspace_size(B, nQ, nC, H, topk) bytes (error word,
+ *           D rows, consumer lists); idx outside [-1, nC) is flagged there and skipped.
+ * ------------------------------------------------------------------------------- */
+GCA_API size_t gca_cca_backward_workspace_size(int B, int nQ, int nC, int H, int topk);
+GCA_API gca_status gca_cca_backward(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, gca_dtype dtype, int B, int nQ,
+                            int nC, int H, int dh, const int32_t* idx, int topk, int shift,
+                            void* dq, void* dk, void* dv, int accumulate, void* ws,
+                            size_t ws_bytes, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * gca_chunk_encoder_forward - the chunk / landmark encoder and the shared K/V transform.
  *
  * Paper-Notes page, 整体框架 (framework): the lower layers' output, with an LMK token

@@ -62,6 +62,8 @@ def _load():
         "gca_cca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, I, I, P, P, I, P, SZ, P]),
         "gca_window_backward_workspace_size": (SZ, [I, I, I]),
         "gca_window_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, I, P, SZ, P]),
+        "gca_cca_backward_workspace_size": (SZ, [I, I, I, I, I]),
+        "gca_cca_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, P, I, I, P, P, P, I, P, SZ, P]),
         "gca_chunk_encoder_workspace_size": (SZ, [I, I, I]),
         "gca_chunk_encoder_forward": (I, [P, I, I, I, I, I, ctypes.POINTER(EncoderWeights), P, P, P, P, P, SZ, P]),
         "gca_gather_workspace_size": (SZ, []),
@@ -92,6 +94,7 @@ EXPORTS = (
     "gca_window_backward_workspace_size", "gca_window_backward",
     "gca_gather_workspace_size", "gca_gather_chunks",
     "gca_chunk_encoder_workspace_size", "gca_chunk_encoder_forward",
+    "gca_cca_backward_workspace_size", "gca_cca_backward",
     "gca_backward_workspace_size", "gca_backward",
     "gca_scores_backward_workspace_size", "gca_scores_backward", "gca_check_error", "gca_launch_count",
     "gca_profile_begin", "gca_profile_end", "gca_profile_row",
@@ -275,6 +278,34 @@ def window_backward(q, k, v, o, dout, lse, window: int = 512, ws: Workspace = No
     _check(LIB.gca_window_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _dtype(q), B, L, H, dh,
                                    window, _ptr(dq), _ptr(dk), _ptr(dv), 1 if accumulate else 0, _ptr(buf), buf.numel(),
                                    _stream()))
+    return dq, dk, dv
+
+
+def cca_backward(q, k, v, o, dout, lse, idx, shift: int = 1, ws: Workspace = None, dq=None, dk=None, dv=None,
+                 accumulate: bool = False):
+    """Gradients of cca_forward (gca_cca_backward).  o is CCA's own output and lse the
+    LSE it returned; returns dq like q and dk, dv like k (added to the given buffers when
+    accumulate)."""
+    _cuda(q, k, v, o, dout, lse, idx)
+    B, L, H, dh = q.shape
+    nQ, nC, topk = L // CHUNK, k.shape[1] // CHUNK, idx.shape[2]
+    _need(L % CHUNK == 0 and k.shape[1] % CHUNK == 0, "sequence lengths must be multiples of 64")
+    _need(k.dim() == 4 and k.shape[0] == B and k.shape[2:] == q.shape[2:] and v.shape == k.shape, "k/v shape mismatch")
+    for t in (o, dout):
+        _need(t.shape == q.shape and t.dtype == q.dtype and t.is_contiguous(), "o/dout must be like q")
+    _need(q.is_contiguous() and k.is_contiguous() and v.is_contiguous(), "q, k, v must be contiguous")
+    _need(lse.shape == (B, nQ, H, CHUNK) and lse.dtype == torch.float32, "lse must be [B, nQ, H, 64] float32")
+    _need(idx.dtype == torch.int32 and idx.shape[:2] == (B, nQ) and idx.is_contiguous(), "idx must be [B, nQ, k] int32")
+    if accumulate:
+        _need(dq is not None and dk is not None and dv is not None, "accumulate needs dq, dk and dv buffers")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = ws or default_workspace(q.device)
+    buf = ws.get(LIB.gca_cca_backward_workspace_size(B, nQ, nC, H, topk))
+    _check(LIB.gca_cca_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _dtype(q), B, nQ, nC, H, dh,
+                                _ptr(idx), topk, shift, _ptr(dq), _ptr(dk), _ptr(dv), 1 if accumulate else 0, _ptr(buf),
+                                buf.numel(), _stream()))
     return dq, dk, dv
 
 

@@ -295,6 +295,7 @@ extern "C" gca_status gca_window_backward(const void* q, const void* k, const vo
   a.Dbuf = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kErrBytes);
   a.dq = dq; a.dk = dk; a.dv = dv;
   a.bf16 = dtype == GCA_BF16; a.B = B; a.nQ = L / 64; a.H = H; a.dh = dh; a.window = window;
+  a.mode = 0; a.nC = a.nQ;
   a.accumulate = accumulate ? 1 : 0;
   a.err = reinterpret_cast<ErrWord*>(ws);
   cudaError_t e = launch_window_backward(a, reinterpret_cast<cudaStream_t>(stream));
@@ -322,6 +323,43 @@ extern "C" gca_status gca_cca_forward(const void* q, const void* k, const void* 
   a.err = reinterpret_cast<ErrWord*>(ws);
   cudaError_t e = launch_block_attn(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gca_cca_forward launch");
+  return GCA_OK;
+}
+
+// ==================================================================== CCA backward
+extern "C" size_t gca_cca_backward_workspace_size(int B, int nQ, int nC, int H, int topk) {
+  if (B < 1 || nQ < 1 || nC < 1 || H < 1 || topk < 1) return kErrBytes;
+  return kErrBytes + align256((size_t)B * nQ * H * 64 * 4) + align256((size_t)B * (nC + 1) * 4) +
+         align256((size_t)B * nQ * topk * 4) + align256((size_t)B * nC * 4);
+}
+
+extern "C" gca_status gca_cca_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                       const float* lse, gca_dtype dtype, int B, int nQ, int nC, int H, int dh,
+                                       const int32_t* idx, int topk, int shift, void* dq, void* dk, void* dv,
+                                       int accumulate, void* ws, size_t ws_bytes, gca_stream_t stream) {
+  gca_status st = check_gca(q, k, v, dtype, B, nQ, nC, H, dh, idx, nullptr, topk, shift, false);
+  if (st != GCA_OK) return st;
+  if (!o || !dout || !lse || !dq || !dk || !dv) return fail(GCA_ERR_INVALID_ARG, "a pointer is NULL");
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(GCA_ERR_INVALID_ARG, "all tensors must be 16-byte aligned");
+  if ((st = check_ws(ws, ws_bytes, gca_cca_backward_workspace_size(B, nQ, nC, H, topk))) != GCA_OK) return st;
+  unsigned char* base = static_cast<unsigned char*>(ws) + kErrBytes;
+  WindowBwdArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse = lse;
+  a.Dbuf = reinterpret_cast<float*>(base);
+  base += align256((size_t)B * nQ * H * 64 * 4);
+  a.csr_off = reinterpret_cast<int32_t*>(base);
+  base += align256((size_t)B * (nC + 1) * 4);
+  a.csr_ent = reinterpret_cast<int32_t*>(base);
+  base += align256((size_t)B * nQ * topk * 4);
+  a.csr_cur = reinterpret_cast<int32_t*>(base);
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.bf16 = dtype == GCA_BF16; a.B = B; a.nQ = nQ; a.H = H; a.dh = dh; a.window = 64;
+  a.mode = 1; a.nC = nC; a.idx = idx; a.topk = topk; a.shift = shift;
+  a.accumulate = accumulate ? 1 : 0;
+  a.err = reinterpret_cast<ErrWord*>(ws);
+  cudaError_t e = launch_window_backward(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gca_cca_backward launch");
   return GCA_OK;
 }
 

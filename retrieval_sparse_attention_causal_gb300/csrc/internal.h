@@ -88,6 +88,12 @@ struct WindowBwdArgs {
   void* dq; void* dk; void* dv;
   int bf16, B, nQ, H, dh, window, accumulate;
   ErrWord* err;
+  // mode 0: sliding window (K/V as long as Q, nC = nQ).  mode 1: CCA, query chunk c over
+  // the valid retrieved chunks of row c - shift (K/V [B][nC*64][H][dh]), key chunk j over
+  // the query chunks whose row retrieved it (csr_off [B][nC+1], csr_ent [B][nQ*topk]).
+  int mode, nC;
+  const int32_t* idx; int topk, shift;
+  const int32_t* csr_off; const int32_t* csr_ent; int32_t* csr_cur;
 };
 cudaError_t launch_window_backward(const WindowBwdArgs& a, cudaStream_t s);
 

@@ -8,7 +8,13 @@
 //     dQ = dS K / sqrt(dh),  dK = dS^T Q / sqrt(dh),  dV = P^T dO.
 // Three kernels: D per row; a query-side pass (per query chunk over its window blocks,
 // dQ); a key-side pass (per key chunk over the query chunks whose window covers it, dK and
-// dV).  Neither needs atomics, so the result is deterministic.  Both tensor-core passes
+// dV).  Neither needs atomics, so the result is deterministic.
+//
+// The same passes give the backward of CCA (block_attn.cu, CCA mode; Paper-Notes page,
+// 关键设计 / Grouped Cross-Attention: one joint softmax over the concatenated retrieved
+// chunks): the query side walks the valid retrieved chunks of row c - shift instead of
+// the window blocks, the key side walks the query chunks whose row retrieved the chunk
+// (the consumer lists of the GCA backward, in entry order), and no block is masked.  Both tensor-core passes
 // follow the GCA backward's layout: a control warp issues TMA loads and tcgen05.mma, eight
 // element warps (TMEM lane quarter w % 4, column half w / 4) do the arithmetic and store
 // the bf16 A operand of the next product into TMEM over the columns they read.
@@ -56,6 +62,21 @@ __global__ void __launch_bounds__(256) window_d_kernel(WindowBwdArgs a) {
   }
 }
 
+// CCA: the valid retrieved chunks of the row that query chunk c reads (slot order);
+// indices outside [-1, nC) are flagged and skipped.  Returns their count.
+__device__ __forceinline__ int cca_blocks(const WindowBwdArgs& a, int b, int c, int (&blk)[kMaxTopk]) {
+  const int r = c - a.shift;
+  int n = 0;
+  if (r < 0) return 0;
+  const int32_t* row = a.idx + ((int64_t)b * a.nQ + r) * a.topk;
+  for (int m = 0; m < a.topk; ++m) {
+    const int j = row[m];
+    if (j >= 0 && j < a.nC) blk[n++] = j;
+    else if (j != -1 && threadIdx.x == 0) flag_bad_index(a.err, j);
+  }
+  return n;
+}
+
 // Mask of key column kc against query row qr inside a block pair: kind 1 (tail block of
 // the window) keeps kc > qr, kind 2 (diagonal block) keeps kc <= qr.
 __device__ __forceinline__ bool dropped(int kind, int kc, int qr) {
@@ -86,9 +107,20 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
   bf16* dqg = reinterpret_cast<bf16*>(a.dq) + tok0;
   const int64_t rowbase = (((int64_t)b * a.nQ + c) * a.H + h) * 64;
   const int wb = a.window / 64;
-  const int j0 = c - wb < 0 ? 0 : c - wb;  // key blocks j0 .. c
-  const int nb = c - j0 + 1;
-  auto kind_of = [&](int n) { const int j = j0 + n; return j == c ? 2 : (j == c - wb ? 1 : 0); };
+  const int j0 = c - wb < 0 ? 0 : c - wb;  // window: key blocks j0 .. c
+  int blk[kMaxTopk];                        // CCA: the row's valid retrieved chunks
+  const int nb = a.mode == 0 ? c - j0 + 1 : cca_blocks(a, b, c, blk);
+  auto block_of = [&](int n) { return a.mode == 0 ? j0 + n : blk[n]; };
+  auto kind_of = [&](int n) {
+    const int j = j0 + n;
+    return a.mode != 0 ? 0 : (j == c ? 2 : (j == c - wb ? 1 : 0));
+  };
+  if (nb == 0) {  // CCA: no valid slot, dQ = 0
+    if (!a.accumulate)
+      for (int u = tid; u < 64 * UPR; u += kThreads)
+        *reinterpret_cast<uint4*>(dqg + (u / UPR) * ts + (u % UPR) * 8) = make_uint4(0, 0, 0, 0);
+    return;
+  }
 
   if (tid == 0) {
     tc::mbar_init(&bar_q, 1);
@@ -110,8 +142,8 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
       const int st = x % NST;
       unsigned char* Ks = ring + 2 * st * TILE;
       tc::mbar_expect_tx(&bar_kv[st], 2 * TILE);
-      tc::tma_load_4d(Ks, &tmK, 0, h, (j0 + x) * 64, b, &bar_kv[st]);
-      tc::tma_load_4d(Ks + TILE, &tmV, 0, h, (j0 + x) * 64, b, &bar_kv[st]);
+      tc::tma_load_4d(Ks, &tmK, 0, h, block_of(x) * 64, b, &bar_kv[st]);
+      tc::tma_load_4d(Ks + TILE, &tmV, 0, h, block_of(x) * 64, b, &bar_kv[st]);
     };
     const uint64_t dQd = tc::desc_km(tc::su32(Qs)), dOd = tc::desc_km(tc::su32(dOs));
     const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
@@ -254,15 +286,27 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ts = (int64_t)a.H * DH;
-  const int64_t ktok0 = ((int64_t)b * a.nQ * 64 + (int64_t)j * 64) * ts + h * DH;
+  const int64_t ktok0 = ((int64_t)b * a.nC * 64 + (int64_t)j * 64) * ts + h * DH;
   bf16* dkg = reinterpret_cast<bf16*>(a.dk) + ktok0;
   bf16* dvg = reinterpret_cast<bf16*>(a.dv) + ktok0;
   const int wb = a.window / 64;
-  const int c1 = j + wb < a.nQ - 1 ? j + wb : a.nQ - 1;  // query chunks j .. c1 see key chunk j
-  const int ncons = c1 - j + 1;
-  // Consumer x is query chunk j + x: x = 0 the diagonal block (keep key <= query), x = wb the
-  // block where the window starts (keep key > query).
-  auto kind_of = [&](int x) { return x == 0 ? 2 : (x == wb ? 1 : 0); };
+  const int c1 = j + wb < a.nQ - 1 ? j + wb : a.nQ - 1;  // window: query chunks j .. c1 see key chunk j
+  const int e0 = a.mode == 0 ? 0 : a.csr_off[(int64_t)b * (a.nC + 1) + j];
+  const int ncons = a.mode == 0 ? c1 - j + 1 : a.csr_off[(int64_t)b * (a.nC + 1) + j + 1] - e0;
+  const int32_t* ent = a.mode == 0 ? nullptr : a.csr_ent + (int64_t)b * a.nQ * a.topk + e0;
+  // Window: consumer x is query chunk j + x, x = 0 the diagonal block (keep key <= query),
+  // x = wb the block where the window starts (keep key > query).  CCA: the query chunk of
+  // the x-th entry of the chunk's consumer list, unmasked.
+  auto cons_of = [&](int x) { return a.mode == 0 ? j + x : ent[x] / a.topk + a.shift; };
+  auto kind_of = [&](int x) { return a.mode != 0 ? 0 : (x == 0 ? 2 : (x == wb ? 1 : 0)); };
+  if (ncons == 0) {  // CCA: never retrieved, dK = dV = 0
+    if (!a.accumulate)
+      for (int u = tid; u < 64 * UPR; u += kThreads) {
+        *reinterpret_cast<uint4*>(dkg + (u / UPR) * ts + (u % UPR) * 8) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(dvg + (u / UPR) * ts + (u % UPR) * 8) = make_uint4(0, 0, 0, 0);
+      }
+    return;
+  }
 
   if (warp == kCtl && lane == 0) {
     tc::mbar_init(&bar_k, 1);
@@ -283,9 +327,9 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
   if (warp == kCtl) {
     // ------------------------------------------------------------ control warp
     bool ok = true;
-    auto load_cons = [&](int x) {  // lane 0: query chunk j + x's Q, dO tiles, LSE and D rows
+    auto load_cons = [&](int x) {  // lane 0: consumer x's Q, dO tiles, LSE and D rows
       const int st = x % NST;
-      const int c = j + x;
+      const int c = cons_of(x);
       unsigned char* base = ring + st * kKVStageBytes;
       const int64_t rb = (((int64_t)b * a.nQ + c) * a.H + h) * 64;
       tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
@@ -448,16 +492,19 @@ __global__ void __launch_bounds__(64) window_bwd_q_simt_kernel(WindowBwdArgs a) 
     dq[d] = 0.f;
   }
   const int wb = a.window / 64, j0 = c - wb < 0 ? 0 : c - wb;
-  for (int jb = j0; jb <= c; ++jb) {
+  int blk[kMaxTopk];
+  const int nb = a.mode == 0 ? c - j0 + 1 : cca_blocks(a, b, c, blk);
+  for (int n = 0; n < nb; ++n) {
+    const int jb = a.mode == 0 ? j0 + n : blk[n];
     __syncthreads();
-    const int64_t kb = ((int64_t)b * a.nQ * 64 + (int64_t)jb * 64) * ts + h * DHT;
+    const int64_t kb = ((int64_t)b * a.nC * 64 + (int64_t)jb * 64) * ts + h * DHT;
     for (int x = t; x < 64 * DHT; x += 64) {
       const int row = x / DHT, d = x % DHT;
       Ks[row][d] = Elem<T>::ld(reinterpret_cast<const T*>(a.k) + kb + row * ts + d);
       Vs[row][d] = Elem<T>::ld(reinterpret_cast<const T*>(a.v) + kb + row * ts + d);
     }
     __syncthreads();
-    const int kind = jb == c ? 2 : (jb == c - wb ? 1 : 0);
+    const int kind = a.mode != 0 ? 0 : (jb == c ? 2 : (jb == c - wb ? 1 : 0));
     for (int key = 0; key < 64; ++key) {
       if (dropped(kind, key, t)) continue;
       float s = 0.f, dp = 0.f;
@@ -480,7 +527,7 @@ __global__ void __launch_bounds__(64) window_bwd_kv_simt_kernel(WindowBwdArgs a)
   __shared__ float Qs[64][DHT + 1], dOs[64][DHT + 1], ls[64], Ds[64];
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z, t = threadIdx.x;
   const int64_t ts = (int64_t)a.H * DHT;
-  const int64_t tok = ((int64_t)b * a.nQ * 64 + (int64_t)j * 64 + t) * ts + h * DHT;
+  const int64_t tok = ((int64_t)b * a.nC * 64 + (int64_t)j * 64 + t) * ts + h * DHT;
   const float scale = 1.0f / sqrtf((float)DHT);
   float kv[DHT], vv[DHT], dk[DHT], dv[DHT];
   for (int d = 0; d < DHT; ++d) {
@@ -490,7 +537,11 @@ __global__ void __launch_bounds__(64) window_bwd_kv_simt_kernel(WindowBwdArgs a)
   }
   const int wb = a.window / 64;
   const int c1 = j + wb < a.nQ - 1 ? j + wb : a.nQ - 1;
-  for (int c = j; c <= c1; ++c) {
+  const int e0 = a.mode == 0 ? 0 : a.csr_off[(int64_t)b * (a.nC + 1) + j];
+  const int ncons = a.mode == 0 ? c1 - j + 1 : a.csr_off[(int64_t)b * (a.nC + 1) + j + 1] - e0;
+  const int32_t* ent = a.mode == 0 ? nullptr : a.csr_ent + (int64_t)b * a.nQ * a.topk + e0;
+  for (int x = 0; x < ncons; ++x) {
+    const int c = a.mode == 0 ? j + x : ent[x] / a.topk + a.shift;
     __syncthreads();
     const int64_t qb = ((int64_t)b * a.nQ * 64 + (int64_t)c * 64) * ts + h * DHT;
     for (int x = t; x < 64 * DHT; x += 64) {
@@ -502,7 +553,7 @@ __global__ void __launch_bounds__(64) window_bwd_kv_simt_kernel(WindowBwdArgs a)
     ls[t] = a.lse[rb + t];
     Ds[t] = a.Dbuf[rb + t];
     __syncthreads();
-    const int kind = c == j ? 2 : (c == j + wb ? 1 : 0);
+    const int kind = a.mode != 0 ? 0 : (c == j ? 2 : (c == j + wb ? 1 : 0));
     for (int qr = 0; qr < 64; ++qr) {
       if (dropped(kind, t, qr)) continue;  // this thread's key t against query row qr
       float s = 0.f, dp = 0.f;
@@ -542,34 +593,43 @@ cudaError_t launch_window_backward(const WindowBwdArgs& a, cudaStream_t s) {
   }
   cudaError_t e = launch_end("window_d", s);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.nQ, a.H, a.B);
+  const char* nq = a.mode == 0 ? "window_bwd_q" : "cca_bwd_q";
+  const char* nkv = a.mode == 0 ? "window_bwd_kv" : "cca_bwd_kv";
+  if (a.mode != 0) {  // the consumers of every key chunk, in entry order
+    const int nrows = a.nQ - a.shift;
+    e = launch_csr(a.idx, a.B, a.nQ, nrows > 0 ? nrows : 0, a.topk, a.nC, const_cast<int32_t*>(a.csr_off),
+                   const_cast<int32_t*>(a.csr_ent), a.csr_cur, a.err, s);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(a.nQ, a.H, a.B), gridk(a.nC, a.H, a.B);
   if (a.bf16 && a.dh == 64) {
     CUtensorMap tq, tdo, tk, tv;
     const int64_t bs = (int64_t)a.nQ * 64 * a.H * 64, rows = (int64_t)a.nQ * 64;
+    const int64_t kbs = (int64_t)a.nC * 64 * a.H * 64, krows = (int64_t)a.nC * 64;
     e = make_head_tmap(&tq, a.q, 64, a.H, rows, a.B, bs);
     if (e == cudaSuccess) e = make_head_tmap(&tdo, a.dout, 64, a.H, rows, a.B, bs);
-    if (e == cudaSuccess) e = make_head_tmap(&tk, a.k, 64, a.H, rows, a.B, bs);
-    if (e == cudaSuccess) e = make_head_tmap(&tv, a.v, 64, a.H, rows, a.B, bs);
+    if (e == cudaSuccess) e = make_head_tmap(&tk, a.k, 64, a.H, krows, a.B, kbs);
+    if (e == cudaSuccess) e = make_head_tmap(&tv, a.v, 64, a.H, krows, a.B, kbs);
     if (e == cudaSuccess) e = allow_smem((const void*)window_bwd_q_tc_kernel, kQSmem);
     if (e == cudaSuccess) e = allow_smem((const void*)window_bwd_kv_tc_kernel, kKVSmem);
     if (e != cudaSuccess) return e;
-    launch_begin("window_bwd_q", s);
+    launch_begin(nq, s);
     window_bwd_q_tc_kernel<<<grid, kThreads, kQSmem, s>>>(a, tq, tdo, tk, tv);
-    if ((e = launch_end("window_bwd_q", s)) != cudaSuccess) return e;
-    launch_begin("window_bwd_kv", s);
-    window_bwd_kv_tc_kernel<<<grid, kThreads, kKVSmem, s>>>(a, tq, tdo, tk, tv);
-    return launch_end("window_bwd_kv", s);
+    if ((e = launch_end(nq, s)) != cudaSuccess) return e;
+    launch_begin(nkv, s);
+    window_bwd_kv_tc_kernel<<<gridk, kThreads, kKVSmem, s>>>(a, tq, tdo, tk, tv);
+    return launch_end(nkv, s);
   }
-  launch_begin("window_bwd_q", s);
+  launch_begin(nq, s);
   if (a.bf16) window_bwd_q_simt_kernel<bf16, 32><<<grid, 64, 0, s>>>(a);
   else if (a.dh == 64) window_bwd_q_simt_kernel<float, 64><<<grid, 64, 0, s>>>(a);
   else window_bwd_q_simt_kernel<float, 32><<<grid, 64, 0, s>>>(a);
-  if ((e = launch_end("window_bwd_q", s)) != cudaSuccess) return e;
-  launch_begin("window_bwd_kv", s);
-  if (a.bf16) window_bwd_kv_simt_kernel<bf16, 32><<<grid, 64, 0, s>>>(a);
-  else if (a.dh == 64) window_bwd_kv_simt_kernel<float, 64><<<grid, 64, 0, s>>>(a);
-  else window_bwd_kv_simt_kernel<float, 32><<<grid, 64, 0, s>>>(a);
-  return launch_end("window_bwd_kv", s);
+  if ((e = launch_end(nq, s)) != cudaSuccess) return e;
+  launch_begin(nkv, s);
+  if (a.bf16) window_bwd_kv_simt_kernel<bf16, 32><<<gridk, 64, 0, s>>>(a);
+  else if (a.dh == 64) window_bwd_kv_simt_kernel<float, 64><<<gridk, 64, 0, s>>>(a);
+  else window_bwd_kv_simt_kernel<float, 32><<<gridk, 64, 0, s>>>(a);
+  return launch_end(nkv, s);
 }
 
 }  // namespace gca

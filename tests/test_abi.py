@@ -167,6 +167,26 @@ def test_backward_and_scores_backward_reject_bad_arguments(gca):
     assert r == gca.GCA_ERR_INVALID_ARG  # shared k_lmk not allowed here
 
 
+def test_cca_backward_rejects_bad_arguments(gca):
+    L = gca.LIB
+    need = L.gca_cca_backward_workspace_size(4, 256, 256, 12, 8)
+    assert need >= 256 + 4 * 256 * 12 * 64 * 4 + 4 * 257 * 4 + 4 * 256 * 8 * 4
+
+    def cb(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dt=gca.GCA_BF16, B=4, nQ=256, nC=256, H=12, dh=64,
+                 idx=FAKE, topk=8, shift=1, dq=FAKE, dk=FAKE, dv=FAKE, acc=0, ws=FAKE, wsb=need)
+        a.update(kw)
+        return L.gca_cca_backward(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dt"], a["B"], a["nQ"], a["nC"],
+                                  a["H"], a["dh"], a["idx"], a["topk"], a["shift"], a["dq"], a["dk"], a["dv"], a["acc"],
+                                  a["ws"], a["wsb"], None)
+    assert cb(topk=17) == gca.GCA_ERR_UNSUPPORTED
+    assert cb(shift=2) == gca.GCA_ERR_INVALID_ARG
+    assert cb(dh=48) == gca.GCA_ERR_UNSUPPORTED
+    assert cb(o=0) == gca.GCA_ERR_INVALID_ARG
+    assert cb(dk=FAKE + 4) == gca.GCA_ERR_INVALID_ARG
+    assert cb(wsb=need - 1) == gca.GCA_ERR_WORKSPACE
+
+
 def test_chunk_encoder_rejects_bad_arguments(gca):
     L = gca.LIB
     w = gca.EncoderWeights(*([FAKE] * len(gca.ENCODER_WEIGHTS)))

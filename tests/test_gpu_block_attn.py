@@ -139,3 +139,79 @@ def test_cca_flags_bad_index():
     ok[0, 1, 0] = -1  # the bad entry is skipped
     oo, _ = orc.cca_forward(x["q"], x["k"], x["v"], ok, 0)
     assert_close(host(o), oo, TOL["bf16"], "O")
+
+
+@pytest.mark.parametrize("dtype,dh,shift", [("bf16", 64, 1), ("bf16", 64, 0), ("f32", 32, 1), ("bf16", 32, 1),
+                                            ("f32", 64, 0)])
+def test_cca_backward_against_oracle(dtype, dh, shift):
+    g = _g()
+    B, nC, H, K = 2, 24, 3, 8
+    x, idx = _cca_case(38, B, nC, H, dh, K, dtype)
+    qd, kd, vd, dod = (dev(x[n], dtype) for n in ("q", "k", "v", "do"))
+    it = torch.from_numpy(idx).cuda()
+    o, lse = g.cca_forward(qd, kd, vd, it, shift=shift)
+    dq, dk, dv = g.cca_backward(qd, kd, vd, o, dod, lse, it, shift=shift)
+    torch.cuda.synchronize()
+    rq, rk, rv = orc.cca_backward(x["q"], x["k"], x["v"], idx, x["do"], shift)
+    assert_close(host(dq), rq, TOL[dtype], "dQ")
+    assert_close(host(dk), rk, TOL[dtype], "dK")
+    assert_close(host(dv), rv, TOL[dtype], "dV")
+
+
+def test_cca_backward_more_keys_than_queries_and_accumulate():
+    """nQ = 10 query chunks over a store of 40 chunks, rows with 0..6 valid slots (padded
+    with -1), accumulated onto existing gradients."""
+    g = _g()
+    B, nQ, nC, H, dh, K = 2, 10, 40, 2, 64, 6
+    x = synth.gca_inputs(39, B, nQ, nC, H, dh, 1.0, "bf16")
+    rng = np.random.default_rng(39)
+    idx = np.full((B, nQ, K), -1, dtype=np.int32)
+    for b in range(B):
+        for r in range(nQ):
+            n = (r + b) % (K + 1)
+            idx[b, r, :n] = rng.choice(nC, n, replace=False)
+    qd, kd, vd, dod = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    it = torch.from_numpy(idx).cuda()
+    o, lse = g.cca_forward(qd, kd, vd, it, shift=1)
+    base = [torch.full_like(qd, 0.25), torch.full_like(kd, 0.25), torch.full_like(vd, 0.25)]
+    dq, dk, dv = g.cca_backward(qd, kd, vd, o, dod, lse, it, shift=1, dq=base[0], dk=base[1], dv=base[2],
+                                accumulate=True)
+    torch.cuda.synchronize()
+    rq, rk, rv = orc.cca_backward(x["q"], x["k"], x["v"], idx, x["do"], 1)
+    for got, ref, n in ((dq, rq, "dQ"), (dk, rk, "dK"), (dv, rv, "dV")):
+        assert_close(host(got), ref + 0.25, 3e-2, n)
+
+
+def test_cca_backward_flags_bad_index():
+    g = _g()
+    B, nC, H, dh, K = 1, 4, 2, 64, 2
+    x, _ = _cca_case(40, B, nC, H, dh, K, "bf16")
+    idx = np.array([[[0, -1], [9, 1], [2, 0], [-1, -1]]], dtype=np.int32)
+    ok = idx.copy()
+    ok[0, 1, 0] = -1
+    qd, kd, vd, dod = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    o, lse = g.cca_forward(qd, kd, vd, torch.from_numpy(ok).cuda(), shift=0)
+    ws = g.Workspace()
+    dq, dk, dv = g.cca_backward(qd, kd, vd, o, dod, lse, torch.from_numpy(idx).cuda(), shift=0, ws=ws)
+    with pytest.raises(g.GCAError, match="DEVICE_INDEX"):
+        ws.check()
+    rq, rk, rv = orc.cca_backward(x["q"], x["k"], x["v"], ok, x["do"], 0)  # the bad entry is skipped
+    for got, ref, n in ((dq, rq, "dQ"), (dk, rk, "dK"), (dv, rv, "dV")):
+        assert_close(host(got), ref, TOL["bf16"], n)
+
+
+def test_cca_backward_training_shape():
+    """One sequence of the 128M shape (256 chunks, 12 heads, 8 retrieved chunks per row
+    from the oracle's retrieval with Gumbel noise), against the oracle."""
+    g = _g()
+    B, nC, H, dh, K = 1, 256, 12, 64, 8
+    x, idx = _cca_case(41, B, nC, H, dh, K, "bf16")
+    qd, kd, vd, dod = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    it = torch.from_numpy(idx).cuda()
+    o, lse = g.cca_forward(qd, kd, vd, it, shift=1)
+    dq, dk, dv = g.cca_backward(qd, kd, vd, o, dod, lse, it, shift=1)
+    torch.cuda.synchronize()
+    rq, rk, rv = orc.cca_backward(x["q"], x["k"], x["v"], idx, x["do"], 1)
+    assert_close(host(dq), rq, TOL["bf16"], "dQ")
+    assert_close(host(dk), rk, TOL["bf16"], "dK")
+    assert_close(host(dv), rv, TOL["bf16"], "dV")
