@@ -293,6 +293,7 @@ def gpu_arm(args):
         if blk is not None:
             blk["window"]["cpu_baseline"] = side["window"]
             blk["cca"]["cpu_baseline"] = side["cca"]
+            blk["cca"]["backward_cpu_baseline"] = side["cca_backward"]
         if enc is not None:
             enc["cpu_baseline"] = side["encoder"]
 
@@ -738,6 +739,12 @@ def next_rows_cpu(seed):
     nq = 16
     t = _cpu_timed(lambda: orc.cca_forward(x["q"], x["k"], x["v"], idx, 1, chunks=[(0, r) for r in range(1, nq + 1)]))
     out["cca"] = entry(nq * 64 / t[0], "tokens/s", t, f"{nq} query chunks of one sequence, {K} retrieved chunks each")
+    sl = [slice(c * 64, (c + 1) * 64) for c in range(1, nq + 1)]
+    dxo = synth.normal(seed, synth.S_DO, (1, NC * 64, H, DH), 1 / 8, "bf16")
+    t = _cpu_timed(lambda: [orc.cca_chunk_backward(x["q"][0, s_], x["k"][0], x["v"][0], idx[0, c], dxo[0, s_])
+                            for c, s_ in enumerate(sl)])
+    out["cca_backward"] = entry(nq * 64 / t[0], "tokens/s", t,
+                                f"{nq} query chunks of one sequence, {K} retrieved chunks each: backward")
     # Chunk encoder: 8 chunks (520 rows) of one sequence at d = 768.
     ne = 8
     xe = synth.encoder_inputs(seed, 1, ne, ENC_D, "bf16")
