@@ -316,10 +316,12 @@ def gpu_arm(args):
 
 def e2e_leg(args, torch, gca, step_outputs_template, inputs, seed, world, timed_barrier, tokens):
     """The training step end to end through the public API: every step copies its inputs
-    from pinned host memory to the device and its results (gradients, indices, scores)
-    back.  Copies run on their own streams and overlap the previous/next step's compute
-    (inputs and outputs are double-buffered); the timed region covers all of it."""
-    res = ["dq", "dk", "dv", "dql", "dkl", "idx", "sc", "ds"]
+    from pinned host memory to the device and reads its result back: the retrieval
+    decision (indices, scores) and the score gradients.  dQ, dK, dV and the landmark
+    gradients stay on the device, where an optimizer would consume them.  Copies run on
+    their own streams and overlap the previous/next step's compute (inputs and outputs
+    are double-buffered); the timed region covers all of it."""
+    res = ["idx", "sc", "ds"]
     hin = {n: t.cpu().pin_memory() for n, t in inputs.items()}
     din = [{n: torch.empty_like(t) for n, t in inputs.items()} for _ in range(2)]
     dout = [{n: torch.empty_like(t) for n, t in step_outputs_template.items()} for _ in range(2)]
@@ -388,7 +390,8 @@ def e2e_leg(args, torch, gca, step_outputs_template, inputs, seed, world, timed_
             "host_wall_ms_per_step": ms_wall / args.steps,
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
             "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout[0].values()),
-            "overlap": "inputs of step i+1 and results of step i-1 move while step i computes"}
+            "overlap": "inputs of step i+1 and results of step i-1 move while step i computes",
+            "d2h": "retrieval indices, scores and score gradients; dQ/dK/dV and landmark gradients stay on the device"}
 
 
 def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
