@@ -218,6 +218,19 @@ GCA_API gca_status gca_cca_forward(const void* q, const void* k, const void* v, 
                            size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * gca_selftest_timeout - exercise the device error path of a wait that runs out.
+ *
+ * Launches one CTA that waits, with the library's bounded mbarrier wait limited to
+ * `spins` probes, on a barrier that nothing ever arrives at.  The wait runs out, the CTA
+ * records GCA_ERR_TIMEOUT (wait site 30) in the error word of `ws` and exits; no fault,
+ * trap or hang.  gca_check_error(ws) then returns GCA_ERR_TIMEOUT and clears the word, and
+ * the context stays usable.  For tests of the failure path.
+ *
+ *   ws      >= 256 bytes (the error word).   spins in 1..2^20.
+ * ------------------------------------------------------------------------------- */
+GCA_API gca_status gca_selftest_timeout(void* ws, size_t ws_bytes, uint32_t spins, gca_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * gca_cca_backward - gradients of gca_cca_forward.
  *
  * With P the joint row softmax of a query chunk over its valid retrieved chunks (from the

@@ -62,6 +62,7 @@ def _load():
         "gca_cca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, I, I, P, P, I, P, SZ, P]),
         "gca_window_backward_workspace_size": (SZ, [I, I, I]),
         "gca_window_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, I, P, SZ, P]),
+        "gca_selftest_timeout": (I, [P, SZ, ctypes.c_uint32, P]),
         "gca_cca_backward_workspace_size": (SZ, [I, I, I, I, I]),
         "gca_cca_backward": (I, [P, P, P, P, P, P, I, I, I, I, I, I, P, I, I, P, P, P, I, P, SZ, P]),
         "gca_chunk_encoder_workspace_size": (SZ, [I, I, I]),
@@ -94,7 +95,7 @@ EXPORTS = (
     "gca_window_backward_workspace_size", "gca_window_backward",
     "gca_gather_workspace_size", "gca_gather_chunks",
     "gca_chunk_encoder_workspace_size", "gca_chunk_encoder_forward",
-    "gca_cca_backward_workspace_size", "gca_cca_backward",
+    "gca_cca_backward_workspace_size", "gca_cca_backward", "gca_selftest_timeout",
     "gca_backward_workspace_size", "gca_backward",
     "gca_scores_backward_workspace_size", "gca_scores_backward", "gca_check_error", "gca_launch_count",
     "gca_profile_begin", "gca_profile_end", "gca_profile_row",
@@ -279,6 +280,13 @@ def window_backward(q, k, v, o, dout, lse, window: int = 512, ws: Workspace = No
                                    window, _ptr(dq), _ptr(dk), _ptr(dv), 1 if accumulate else 0, _ptr(buf), buf.numel(),
                                    _stream()))
     return dq, dk, dv
+
+
+def selftest_timeout(ws: Workspace, spins: int = 4096):
+    """Launch the wait self-test (gca_selftest_timeout): a bounded wait on a barrier that
+    nothing arrives at runs out and records GCA_ERR_TIMEOUT in ws's error word."""
+    buf = ws.get(256)
+    _check(LIB.gca_selftest_timeout(_ptr(buf), buf.numel(), spins, _stream()))
 
 
 def cca_backward(q, k, v, o, dout, lse, idx, shift: int = 1, ws: Workspace = None, dq=None, dk=None, dv=None,

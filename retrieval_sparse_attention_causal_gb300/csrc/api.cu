@@ -12,6 +12,7 @@
 #include "../../include/gca.h"
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace gca {
 namespace {
@@ -563,6 +564,38 @@ extern "C" gca_status gca_check_error(void* ws, gca_stream_t stream, int* bad_va
                 (unsigned)h.wait_sites, h.first[0] - 1, h.first[1], h.first[2], h.first[3]);
   if (bad_value) *bad_value = h.bad_value;
   return fail(GCA_ERR_DEVICE_INDEX, "a kernel met retrieved index %d outside [-1, nC)", h.bad_value);
+}
+
+// ==================================================================== wait self-test
+namespace gca {
+namespace {
+constexpr int kSelftestSite = 30;
+
+// One CTA waits on an mbarrier that nothing arrives at, with the same bounded wait the
+// kernels use for tensor-core and copy completion: the wait runs out, every thread records
+// the timeout in the error word, and the CTA exits normally.
+__global__ void __launch_bounds__(32) selftest_timeout_kernel(ErrWord* err, uint32_t spins) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncwarp();
+  if (!tc::mbar_wait(&bar, 0, spins)) flag_timeout(err, kSelftestSite, blockIdx.x, -1, threadIdx.x);
+}
+}  // namespace
+}  // namespace gca
+
+extern "C" gca_status gca_selftest_timeout(void* ws, size_t ws_bytes, uint32_t spins, gca_stream_t stream) {
+  gca_status st;
+  if ((st = check_ws(ws, ws_bytes, kErrBytes)) != GCA_OK) return st;
+  if (spins < 1 || spins > (1u << 20)) return fail(GCA_ERR_INVALID_ARG, "spins must be in 1..2^20");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  launch_begin("selftest_timeout", s);
+  gca::selftest_timeout_kernel<<<1, 32, 0, s>>>(reinterpret_cast<ErrWord*>(ws), spins);
+  cudaError_t e = launch_end("selftest_timeout", s);
+  if (e != cudaSuccess) return cuda_fail(e, "gca_selftest_timeout launch");
+  return GCA_OK;
 }
 
 extern "C" uint64_t gca_launch_count(void) { return g_launches.load(); }

@@ -167,6 +167,14 @@ def test_backward_and_scores_backward_reject_bad_arguments(gca):
     assert r == gca.GCA_ERR_INVALID_ARG  # shared k_lmk not allowed here
 
 
+def test_selftest_timeout_rejects_bad_arguments(gca):
+    L = gca.LIB
+    assert L.gca_selftest_timeout(None, 256, 10, None) == gca.GCA_ERR_WORKSPACE
+    assert L.gca_selftest_timeout(FAKE, 16, 10, None) == gca.GCA_ERR_WORKSPACE
+    assert L.gca_selftest_timeout(FAKE, 256, 0, None) == gca.GCA_ERR_INVALID_ARG
+    assert L.gca_selftest_timeout(FAKE, 256, (1 << 20) + 1, None) == gca.GCA_ERR_INVALID_ARG
+
+
 def test_cca_backward_rejects_bad_arguments(gca):
     L = gca.LIB
     need = L.gca_cca_backward_workspace_size(4, 256, 256, 12, 8)
