@@ -31,11 +31,28 @@ import time
 import numpy as np
 
 METRIC = "GCA fwd+bwd tokens/s at L=16K; landmark top-k GB/s at 16M ctx (1 GB300)"
-B, NC, H, DH, D, K = 4, 256, 12, 64, 768, 8
-L = NC * 64
+
+def _workloads():
+    """The workload presets, loaded by path: importing the package would load the CUDA
+    library, which the reference arm does not need."""
+    import importlib.util
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "retrieval_sparse_attention_causal_gb300",
+                        "workloads.py")
+    spec = importlib.util.spec_from_file_location("gca_workloads", path)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[spec.name] = mod  # dataclasses resolve the module by name
+    spec.loader.exec_module(mod)
+    return mod
+
+
+_W = _workloads()
+TRAIN_128M, DECODE_16M = _W.TRAIN_128M, _W.DECODE_16M
+
+B, NC, H, DH, D, K = TRAIN_128M.B, TRAIN_128M.n_chunks, TRAIN_128M.H, TRAIN_128M.dh, TRAIN_128M.D, TRAIN_128M.topk
+L = TRAIN_128M.L
 WORKLOAD = (f"GCA training step, 128M-model shape: B={B}, L={L} ({NC} chunks of 64), H={H} x dh={DH}, "
             f"landmark dim {D}, top-k {K}, Gumbel noise; retrieval + fwd + bwd + landmark grads")
-DEC_B, DEC_NC = 16, 262144
+DEC_B, DEC_NC = DECODE_16M.B, DECODE_16M.n_chunks
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -219,3 +219,15 @@ def test_chunk_encoder_rejects_bad_arguments(gca):
     need = L.gca_chunk_encoder_workspace_size(4, 256, 768)
     assert need >= 256 + 4 * 256 * 65 * 768 * 2 * 6
     assert enc(wsb=need - 1) == gca.GCA_ERR_WORKSPACE
+
+
+def test_workload_presets():
+    """The named workloads carry the shapes the benchmark and the parity tests use."""
+    from retrieval_sparse_attention_causal_gb300 import workloads as w
+    t = w.TRAIN_128M
+    assert (t.B, t.L, t.H, t.dh, t.D, t.topk, t.dtype, t.gumbel, t.qkv_std) == (4, 16384, 12, 64, 768, 8, "bf16", True,
+                                                                                0.125)
+    assert w.TRAIN_350M_G2.groups == 2 and w.TRAIN_350M_G2.H * w.TRAIN_350M_G2.dh == w.TRAIN_350M_G2.D
+    assert w.PREFILL_1M.L == 1 << 20 and w.DECODE_16M.L == 1 << 24 and w.DECODE_16M.nQ == 1
+    assert w.TINY_F32.dtype == "f32" and not w.TINY_F32.gumbel
+    assert len({x.name for x in w.ALL}) == len(w.ALL)
