@@ -473,10 +473,36 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
     nbytes = nb * DEC_NC * D * 2
     rows_ms = prof["retrieve_stream"][1] / prof["retrieve_stream"][0]
     ach = nbytes / (rows_ms / 1e3) / 1e9
+    # Batch 1: a decode step is a few short launches, so the host's launch cost matters.
+    # The eager step against the same step captured once as a CUDA graph and replayed.
+    from retrieval_sparse_attention_causal_gb300 import pipeline
+    q1, ql1, kl1 = qn[:1], ql[:1], kl[:1]
+    ws1 = gca.Workspace()
+
+    def eager1(i):
+        return pipeline.decode(q1, kst, vst, ql1, kl1, topk=K, kv_shared=True, ws=ws1)
+
+    graph = pipeline.DecodeGraph(q1, kst, vst, ql1, kl1, topk=K, kv_shared=True)
+
+    def graph1(i):
+        graph.replay()
+
+    for i in range(args.warmup):
+        eager1(i)
+        graph1(i)
+    ms_e1 = time_loop(eager1, args.steps)
+    ms_g1 = time_loop(graph1, args.steps)
+    ref1 = eager1(0)
+    graph1(0)
+    torch.cuda.synchronize()
+    batch1 = {"eager_ms_per_decode_chunk": round(ms_e1, 4), "graph_ms_per_decode_chunk": round(ms_g1, 4),
+              "graph_equals_eager": bool(torch.equal(ref1["o"], graph.out["o"]) and
+                                         torch.equal(ref1["idx"], graph.out["idx"]))}
+    ws1.check()
     offload = None
     if not args.no_offload:
         offload = offload_leg(args, torch, gca, kst, vst, qn, ql, kl, ws, o, lse, idx, sc, time_loop)
-    del kst, vst
+    del kst, vst, graph
     return {"metric": "landmark top-k GB/s at 16M ctx", "value": round(nbytes * world / (ms_r / 1e3) / 1e9, 1),
             "unit": "GB/s", "batch": nb, "past_chunks": DEC_NC, "landmark_dim": D, "ms_per_retrieval": round(ms_r, 4),
             "ms_per_decode_chunk": round(ms_f, 4), "planted_chunk_found": ok,
@@ -484,7 +510,7 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                          "traffic": stream_traffic(nb), "peak_source": f"{src} copy bandwidth",
                          "bytes_per_launch": nbytes},
-            "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "offload": offload}
+            "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "batch1": batch1, "offload": offload}
 
 
 def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):

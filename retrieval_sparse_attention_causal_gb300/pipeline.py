@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (CHUNK, default_workspace, gather_chunks, gca_backward, gca_forward, retrieve_topk,
+from . import (CHUNK, Workspace, default_workspace, gather_chunks, gca_backward, gca_forward, retrieve_topk,
                scores_backward)
 
 
@@ -94,3 +94,31 @@ def decode_offload(q_new, k_host, v_host, q_lmk_new, k_lmk_store, topk=8, kv_sha
     kd, vd, il = gather_chunks(k_host, v_host, idx, kv_shared=kv_shared, ws=ws, k_dst=kd, v_dst=vd, idx_local=il)
     o, lse = gca_forward(q_new, kd, vd, il, scores, shift=0, ws=ws)
     return dict(idx=idx, scores=scores, o=o, lse=lse, idx_local=il)
+
+
+class DecodeGraph:
+    """A decode step captured once as a CUDA graph and replayed.
+
+    One decode step is a few short launches (retrieval, merge, forward; plus the gather
+    with offload=True).  At small batch the host's launch cost is a large part of the
+    step, so the step is captured after a warm-up call (which sizes the workspace and
+    sets the kernels' attributes) and each replay() launches the whole graph at once.
+    Replays read the current contents of the tensors given here: update them in place
+    (copy_) between steps.  replay() returns the same output dict every time, whose
+    tensors the replay overwrites."""
+
+    def __init__(self, q_new, k_store, v_store, q_lmk_new, k_lmk_store, topk=8, kv_shared=False, offload=False,
+                 ws=None):
+        self.ws = ws or Workspace(q_new.device)
+        fn = decode_offload if offload else decode
+        args = (q_new, k_store, v_store, q_lmk_new, k_lmk_store)
+        fn(*args, topk=topk, kv_shared=kv_shared, ws=self.ws)  # warm-up, outside the capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.out = fn(*args, topk=topk, kv_shared=kv_shared, ws=self.ws)
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
+

@@ -203,3 +203,25 @@ def test_decode_16m_context(B):
         oc, lc, _ = orc.gca_chunk_forward(qn[b], kh, vh, loc, sc_o[b, 0])
         assert_close(host(r["o"][b]), oc, TOL["bf16"], f"O[{b}]")
         assert_close(host(r["lse"][b, 0]), lc, TOL["bf16"], f"LSE[{b}]")
+
+
+def test_decode_graph_replays_the_eager_step():
+    """A decode step captured as a CUDA graph gives the eager step's results bit for bit,
+    and follows in-place updates of its inputs between replays."""
+    from retrieval_sparse_attention_causal_gb300 import pipeline
+    B, nC, H, dh, D, K = 2, 3000, 4, 64, 256, 8
+    lm = synth.planted_landmarks(62, B, nC, D, "bf16")
+    qn = dev(synth.normal(62, synth.S_Q, (B, 64, H, dh), 1 / 8, "bf16"), "bf16")
+    kst = dev(synth.normal(62, synth.S_K, (nC * 64, H, dh), 1 / 8, "bf16"), "bf16")
+    vst = dev(synth.normal(62, synth.S_V, (nC * 64, H, dh), 1 / 8, "bf16"), "bf16")
+    ql, kl = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
+    g = pipeline.DecodeGraph(qn, kst, vst, ql, kl, topk=K, kv_shared=True)
+    for step in range(2):
+        out = g.replay()
+        ref = pipeline.decode(qn, kst, vst, ql, kl, topk=K, kv_shared=True)
+        torch.cuda.synchronize()
+        for n in ("idx", "scores", "o", "lse"):
+            assert torch.equal(out[n], ref[n]), (step, n)
+        assert int(out["idx"][0, 0, 0]) == (lm["jstar"][0] if step == 0 else 17)
+        ql[0].copy_(kl[0, 17])  # the next step's query landmark plants chunk 17 for sequence 0
+    g.ws.check()
