@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgca.so")
 SOURCES = ["api.cu", "retrieve.cu", "gca_fwd.cu", "gca_bwd.cu", "scores_bwd.cu", "noalloc.cu", "tmap.cu", "gca_bwd_tc.cu",
-           "gather.cu", "block_attn.cu", "window_bwd.cu", "encoder.cu"]
+           "gather.cu", "block_attn.cu", "window_bwd.cu", "encoder.cu", "retrieve_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

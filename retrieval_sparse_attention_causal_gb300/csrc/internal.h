@@ -33,6 +33,10 @@ cudaError_t make_rows_tmap(CUtensorMap* out, const void* base, int64_t cols, int
 // Token rows of a [chunks][65][cols] bf16 tensor (64 tokens and an LMK row per chunk) as
 // 128-row boxes of two chunks' tokens, 64 columns wide, 128-byte swizzled (tmap.cu).
 cudaError_t make_chunk_token_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t chunks);
+// Landmark rows [batches][rows][D] bf16 with free row and batch strides (in elements;
+// batch stride 0 = one table for every sequence) as boxes of 64 dims x box_rows rows.
+cudaError_t make_lmk_tmap(CUtensorMap* out, const void* base, int64_t D, int64_t rows, int64_t batches,
+                          int64_t row_stride, int64_t batch_stride, int box_rows);
 // The same matrix as a TMA store target: 32 x 32 boxes, 64-byte swizzle (tmap.cu).
 cudaError_t make_store_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows);
 
@@ -52,10 +56,17 @@ struct RetrievePlan {
   int rowwise;   // 1: one CTA per (row, split) streaming kernel; 0: 64-row tile kernel
   int nsplit;    // splits of the candidate range
   int seg;       // candidates per split
-  size_t part_bytes;
+  int tc_ns;     // tcgen05 scoring (bf16, TMA-compatible layouts): candidate segments per
+  int tc_sl;     //   128-row block and 256-candidate tiles per segment; two partial lists
+                 //   (column halves) per segment and row
+  size_t part_bytes;  // enough for whichever row-block kernel the launch picks
 };
 RetrievePlan retrieve_plan(int B, int nQ, int nC, int topk, int off);
 cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaStream_t s);
+// tcgen05 scoring of 128 query rows x 256-candidate tiles with the top-k in the epilogue
+// (retrieve_tc.cu): whether a call can take it, and the stage-1 launch (2 tc_ns lists).
+bool retrieve_tc_eligible(const RetrieveArgs& a);
+cudaError_t launch_retrieve_tc(const RetrieveArgs& a, const RetrievePlan& p, cudaStream_t s);
 
 // ---- GCA forward (gca_fwd.cu)
 struct FwdArgs {

@@ -17,9 +17,14 @@
 //                         shared memory while 64-candidate tiles stream through a
 //                         double-buffered cp.async pipeline; the 64x64 score tile is a
 //                         bf16 tensor-core product (fp32 SIMT for f32 inputs).
+//   retrieve_tc_kernel    (retrieve_tc.cu) the same for bf16 landmarks in TMA-compatible
+//                         layouts: 128-row x 256-candidate score tiles on tcgen05 with
+//                         the selection in the epilogue; the row-block path then takes it
+//                         instead of retrieve_tile_kernel.
 //   retrieve_merge_kernel merges the per-split candidate lists of a row.
 // Every stage keeps candidates under one total order (key descending, then index
 // ascending), so the result does not depend on how the candidates were split.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -455,8 +460,19 @@ RetrievePlan retrieve_plan(int B, int nQ, int nC, int topk, int off) {
     if (ns < 1) ns = 1;
     p.nsplit = (int)ns;
     p.seg = (int)seg;
+    // tcgen05 path: 128-row blocks, 256-candidate tiles; the last block has the most tiles.
+    // Segments of tc_sl tiles per block, about four CTAs per SM over the whole grid.
+    const long long nmb = (nQ + 127) / 128;
+    const long long nt_max = ncand_max > 0 ? (ncand_max + 255) / 256 : 1;
+    long long tns = (4 * 152 + B * nmb - 1) / (B * nmb);
+    if (tns > nt_max) tns = nt_max;
+    if (tns < 1) tns = 1;
+    const long long tsl = (nt_max + tns - 1) / tns;
+    p.tc_sl = (int)tsl;
+    p.tc_ns = (int)((nt_max + tsl - 1) / tsl);
   }
   p.part_bytes = p.nsplit > 1 ? (size_t)B * nQ * p.nsplit * topk * sizeof(Cand) : 0;
+  if (!p.rowwise) p.part_bytes = std::max(p.part_bytes, (size_t)B * nQ * 2 * p.tc_ns * topk * sizeof(Cand));
   return p;
 }
 
@@ -498,6 +514,9 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
       if (nv == 3) return go(std::integral_constant<int, 3>{});
       return go(std::integral_constant<int, 4>{});
     });
+  } else if (retrieve_tc_eligible(a)) {
+    e = launch_retrieve_tc(a, p, s);
+    nsplit = 2 * p.tc_ns;
   } else {
     dim3 grid(p.nsplit, (a.nQ + 63) / 64, a.B);
     const int smem = (int)TileSmem::bytes(a.D, a.bf16 != 0);

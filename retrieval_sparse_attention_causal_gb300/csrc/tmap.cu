@@ -75,6 +75,24 @@ cudaError_t make_chunk_token_tmap(CUtensorMap* out, const void* base, int64_t co
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_lmk_tmap(CUtensorMap* out, const void* base, int64_t D, int64_t rows, int64_t batches,
+                          int64_t row_stride, int64_t batch_stride, int box_rows) {
+  std::call_once(g_once, load_encode);
+  if (g_encode_err != cudaSuccess) return g_encode_err;
+  // dims innermost first: landmark dim, row, sequence; the box is 64 dims (128 bytes) by
+  // box_rows rows of one sequence.  A batch stride of 0 (one table shared by every
+  // sequence) becomes a single-sequence map.
+  const bool shared = batch_stride == 0;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)(shared ? 1 : batches)};
+  cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)(shared ? rows * row_stride : batch_stride) * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_store_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows) {
   std::call_once(g_once, load_encode);
   if (g_encode_err != cudaSuccess) return g_encode_err;

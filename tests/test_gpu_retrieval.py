@@ -130,3 +130,32 @@ def test_deterministic():
     a = g.retrieve_topk(q, k, 8, 0, True, 9)
     b = g.retrieve_topk(q, k, 8, 0, True, 9)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("gumbel,off,K", [(False, 0, 8), (True, 0, 8), (False, 300, 16), (True, 5, 3)])
+def test_large_row_blocks_tcgen05_path(gumbel, off, K):
+    """B = 4, 4096 query rows over 4096 + off candidates, D = 128: enough 128 x 256 score
+    tiles to take the tcgen05 scoring path (selection in its epilogue, partial lists per
+    candidate segment and column half, then the merge).  Every row against the oracle."""
+    B, nQ, D = 4, 4096, 128
+    nC = nQ + off
+    _, _, _, nd, nt = run_case(B, nQ, nC, D, K, "bf16", off=off, gumbel=gumbel, seed=7)
+    assert nd > 0.5 * B * nQ  # most rows decidable: the test is not vacuous
+
+
+def test_large_row_blocks_strided_queries_and_shared_keys():
+    """The tcgen05 path with query rows read at a stride out of a wider tensor (as group 2
+    reads its landmarks out of group 1's output) and one key table shared by the batch."""
+    g = _gca()
+    B, nQ, D, K = 4, 4096, 128, 8
+    wide = synth.normal(8, synth.S_QL, (B, nQ, 3 * D), 1.0, "bf16")
+    k = synth.normal(8, synth.S_KL, (nQ, D), 1.0, "bf16")
+    qv = wide[:, :, D:2 * D]
+    qd = dev(wide, "bf16")[:, :, D:2 * D]
+    idx_g, sc_g = g.retrieve_topk(qd, dev(k, "bf16"), K, 0, True, 8, 0, k_shared=True)
+    torch.cuda.synchronize()
+    kb = np.broadcast_to(k, (B,) + k.shape)
+    idx_o, sc_o, m = orc.retrieve_topk(qv, kb, K, 0, True, 8, 0)
+    nd, _ = compare_retrieval(idx_g.cpu().numpy(), host(sc_g), idx_o, sc_o, m, SCORE_TOL["bf16"], orc=orc, q=qv, k=kb,
+                              gumbel=True, seed=8)
+    assert nd > 0.5 * B * nQ  # most rows decidable: the test is not vacuous
