@@ -46,7 +46,7 @@ def _workloads():
 
 
 _W = _workloads()
-TRAIN_128M, DECODE_16M = _W.TRAIN_128M, _W.DECODE_16M
+TRAIN_128M, DECODE_16M, PREFILL_1M = _W.TRAIN_128M, _W.DECODE_16M, _W.PREFILL_1M
 
 B, NC, H, DH, D, K = TRAIN_128M.B, TRAIN_128M.n_chunks, TRAIN_128M.H, TRAIN_128M.dh, TRAIN_128M.D, TRAIN_128M.topk
 L = TRAIN_128M.L
@@ -174,7 +174,7 @@ KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); 
     "gca_bwd_kv": (603.0e6, "5c4fccd2ea985839"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (808.35e6 / 2, "74df39448ea668d2")
+STREAM_TRAFFIC_PER_SEQ = (808378368 / 2, "6842be433ae6a28f")
 
 
 def source_fingerprint(kernel: str) -> str:
@@ -292,6 +292,8 @@ def gpu_arm(args):
     blk = None if args.no_block else block_attn_leg(args, torch, gca, q, k, v, out, timed, pk)
     # The chunk / landmark encoder that produces K, V and the key landmarks.
     enc = None if args.no_encoder else encoder_leg(args, torch, gca, synth, timed, pk)
+    # Retrieval for a 1M-token prefill (the scoring as a dense tensor-core product).
+    pre = None if args.no_prefill else prefill_leg(args, torch, gca, synth, pk)
 
     # End to end through the public API from pinned host buffers.
     e2e = None
@@ -313,6 +315,8 @@ def gpu_arm(args):
             blk["cca"]["backward_cpu_baseline"] = side["cca_backward"]
         if enc is not None:
             enc["cpu_baseline"] = side["encoder"]
+        if pre is not None:
+            pre["cpu_baseline"] = side["prefill"]
 
     if rank == 0:
         line = {
@@ -324,7 +328,8 @@ def gpu_arm(args):
             "step_tflops_algorithmic": round(step_tflops, 2),
             "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary(),
             "kernels": {n: round(x["avg_ms"], 5) for n, x in kern.items()},
-            "e2e": e2e, "decode": dec, "block_attention": blk, "encoder": enc, "cpu_baseline": cpu,
+            "e2e": e2e, "decode": dec, "block_attention": blk, "encoder": enc, "prefill_retrieval": pre,
+            "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -578,6 +583,55 @@ def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):
 ENC_D, ENC_H = 768, 12  # the 128M model's width: the encoder's rows have d = H * 64 = 768
 
 
+def prefill_flops(nc, d):
+    """2 D flops per (query row, candidate) pair; row i has the i chunks before it."""
+    return 2 * d * nc * (nc - 1) // 2
+
+
+def prefill_leg(args, torch, gca, synth, pk):
+    """Landmark retrieval for a 1M-token prefill: one sequence of 16384 chunks, D = 768,
+    k = 8, no noise; every chunk's query landmark against all earlier chunks' landmarks.
+    The two landmark tensors (25 MB each) fit in L2, so a 256 MB buffer is written before
+    every call; the call's kernels are timed alone with CUDA events.  Reports the call's
+    time, tokens/s (the prefill's tokens per call time) and the scoring kernel's
+    algorithmic TFLOP/s against the measured bf16 peak."""
+    wl = PREFILL_1M
+    nc, d, k = wl.n_chunks, wl.D, wl.topk
+    ql = synth.device_normal(args.seed, synth.S_QL, (1, nc, d), 1.0, torch.bfloat16)
+    kl = synth.device_normal(args.seed, synth.S_KL, (1, nc, d), 1.0, torch.bfloat16)
+    ws = gca.Workspace()
+    idx = torch.empty((1, nc, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((1, nc, k), dtype=torch.float32, device="cuda")
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+
+    def call():
+        gca.retrieve_topk(ql, kl, k, 0, False, ws=ws, idx=idx, scores=sc)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    ws.check()
+    n = 20
+    torch.cuda.synchronize()
+    gca.profile_begin()
+    for _ in range(n):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    prof = gca.profile_end()
+    ms = sum(t for _, t in prof.values()) / n
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    dom_ms = prof[dom][1] / prof[dom][0]
+    fl = prefill_flops(nc, d)
+    ach = fl / (dom_ms / 1e3) / 1e12
+    return {"workload": f"{wl.name}: B=1, {nc} chunks, landmark dim {d}, top-k {k}, no noise",
+            "ms": round(ms, 4), "tokens_per_s": round(wl.L / (ms / 1e3), 1),
+            "kernels": {nm: round(t / c, 5) for nm, (c, t) in prof.items()},
+            "l2": "256 MB buffer written before every call",
+            "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
+                         "flops_per_launch": fl}}
+
+
 def encoder_flops(nb, nc, d, h):
     """Algorithmic flops of one encoder pass, per kernel: 2 m n k for each GEMM over the
     rows it needs (every row of the layer; token rows only for the K/V transform) and
@@ -797,6 +851,15 @@ def next_rows_cpu(seed):
     pe = synth.encoder_params(seed, ENC_D, "bf16")
     t = _cpu_timed(lambda: orc.chunk_encoder_forward(xe, pe, ENC_H))
     out["encoder"] = entry(ne * 64 / t[0], "tokens/s", t, f"{ne} chunks of one sequence (their {ne * 65} rows), d = {ENC_D}")
+    # Prefill retrieval: 16 query rows spread evenly over the 16384-chunk sequence (so that
+    # their mean candidate count is the full prefill's), each against all its past chunks.
+    pn, ns = PREFILL_1M.n_chunks, 16
+    qp = synth.normal(seed, synth.S_QL, (1, pn, D), 1.0, "bf16")
+    kp = synth.normal(seed, synth.S_KL, (1, pn, D), 1.0, "bf16")
+    rows = [(0, (2 * r + 1) * pn // (2 * ns)) for r in range(ns)]
+    t = _cpu_timed(lambda: orc.retrieve_topk(qp, kp, PREFILL_1M.topk, 0, False, 0, rows=rows))
+    out["prefill"] = entry(ns * 64 / t[0], "tokens/s", t,
+                           f"{ns} query rows spread evenly over one {pn}-chunk sequence, each against all its past chunks")
     return out
 
 
@@ -848,6 +911,7 @@ def main():
     ap.add_argument("--no-offload", action="store_true", help="skip the host-memory K/V store decode")
     ap.add_argument("--no-block", action="store_true", help="skip the window-attention and CCA leg")
     ap.add_argument("--no-encoder", action="store_true", help="skip the chunk / landmark encoder leg")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the 1M-token prefill retrieval leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

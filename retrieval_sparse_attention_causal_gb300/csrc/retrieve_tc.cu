@@ -30,8 +30,9 @@ namespace {
 
 constexpr int kBM = 128, kBN = 256, kStages = 3, kThreads = 320;
 constexpr uint32_t kABytes = kBM * 128, kStage = (kBM + kBN) * 128;
-constexpr int kRowF = 33;  // floats per selection thread's staging row (32 scores + 1: no bank conflicts)
-constexpr int kSmem = kStages * kStage + 8 * 32 * kRowF * 4 + 1024;
+constexpr int kRowF = 33;  // floats per selection thread's staging row (32 values + 1: no bank conflicts)
+constexpr int kKeyRow = 8 * 32 * kRowF;  // the keys' rows follow the 256 threads' score rows
+constexpr int kSmem = kStages * kStage + 2 * kKeyRow * 4 + 1024;
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ int n_cand(int i, int off, int nC) {
@@ -168,8 +169,8 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
     // ------------------------------------------------------------ selection warps
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const int lim = row < a.nQ ? n_cand(row, a.off, a.nC) : 0;
-    // The thread's 32 scores of a chunk go through its own shared-memory row, so that the
-    // selection loop indexes them without spilling the register array.
+    // The thread's 32 scores and keys of a chunk go through its own shared-memory rows, so
+    // that the selection loop indexes them without spilling the register array.
     float* mine = reinterpret_cast<float*>(sm + NST * kStage) + ((warp - 2) * 32 + lane) * kRowF;
     const float inv = 1.0f / sqrtf((float)a.D);
     Cand L[KC];
@@ -187,18 +188,32 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
       for (int c = 0; c < 4; ++c) {
         if (c + 1 < 4) tc::ld32x32b_x32(tcol + 32 * (c + 1), v[(c + 1) & 1]);
         const float(&cur)[32] = v[c & 1];
-        if (j0 + 32 * c < lim) {
+        const int jc = j0 + 32 * c;
+        if (jc < lim) {
+          // The row's scores and keys of this chunk, and the largest key.  A key enters
+          // the list only if it beats the last entry, so a chunk whose largest key is below
+          // that entry's is skipped whole; equal keys go through the insertion, which
+          // orders them by index.
+          float km = -CUDART_INF_F;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mine[e] = cur[e];
-          const int n = min(32, lim - (j0 + 32 * c));
-#pragma unroll 2
-          for (int e = 0; e < n; ++e) {
-            const int j = j0 + 32 * c + e;
-            Cand cd;
-            cd.score = mine[e] * inv;
-            cd.key = a.gumbel ? cd.score + gumbel_noise(a.seed, a.group, b, row, j) : cd.score;
-            cd.j = j;
-            list_insert(L, cd);
+          for (int e = 0; e < 32; ++e) {
+            const float sc = cur[e] * inv;
+            const float key = a.gumbel ? sc + gumbel_noise(a.seed, a.group, b, row, jc + e) : sc;
+            mine[e] = sc;
+            mine[kKeyRow + e] = key;
+            if (jc + e < lim) km = fmaxf(km, key);
+          }
+          if (km >= L[KC - 1].key) {
+            const int n = min(32, lim - jc);
+            for (int e = 0; e < n; ++e) {
+              Cand cd;
+              cd.key = mine[kKeyRow + e];
+              cd.j = jc + e;
+              if (better(cd, L[KC - 1])) {
+                cd.score = mine[e];
+                list_insert(L, cd);
+              }
+            }
           }
         }
         if (c + 1 < 4) tc::ld_wait_row(v[(c + 1) & 1]);
