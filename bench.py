@@ -174,7 +174,7 @@ KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); 
     "gca_bwd_kv": (603.0e6, "5c4fccd2ea985839"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (808378368 / 2, "6842be433ae6a28f")
+STREAM_TRAFFIC_PER_SEQ = (808441600 / 2, "8cf0263a298f2697")
 
 
 def source_fingerprint(kernel: str) -> str:
@@ -749,6 +749,25 @@ def decode_retrieval_only(args):
     print(json.dumps({"decode_retrieval_only": True, "batch": nb, "launches": args.warmup + args.steps}))
 
 
+def prefill_retrieval_only(args):
+    """Only the prefill retrieval (one sequence of --prefill-chunks chunks, D = 768, k = 8,
+    no noise), for ncu captures of the tensor-core scoring kernel."""
+    import torch
+    import retrieval_sparse_attention_causal_gb300 as gca
+    from retrieval_sparse_attention_causal_gb300 import synth
+    nc, d, k = args.prefill_chunks, PREFILL_1M.D, PREFILL_1M.topk
+    ql = synth.device_normal(args.seed, synth.S_QL, (1, nc, d), 1.0, torch.bfloat16)
+    kl = synth.device_normal(args.seed, synth.S_KL, (1, nc, d), 1.0, torch.bfloat16)
+    ws = gca.Workspace()
+    idx = torch.empty((1, nc, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((1, nc, k), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        gca.retrieve_topk(ql, kl, k, 0, False, ws=ws, idx=idx, scores=sc)
+    torch.cuda.synchronize()
+    ws.check()
+    print(json.dumps({"prefill_retrieval_only": True, "chunks": nc, "launches": args.warmup + args.steps}))
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def cpu_sample(seed, rows, budget_s=None):
     """The oracle on one sequence of the benchmarked workload, for query chunks
@@ -917,6 +936,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--decode-retrieval-only", action="store_true",
                     help="run only the 16M-context landmark retrieval (for profiling captures)")
+    ap.add_argument("--prefill-retrieval-only", action="store_true",
+                    help="run only the prefill landmark retrieval (for profiling captures)")
+    ap.add_argument("--prefill-chunks", type=int, default=PREFILL_1M.n_chunks)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gb300":
         args.warmup = 3
@@ -924,6 +946,8 @@ def main():
         reference_arm(args)
     elif args.decode_retrieval_only:
         decode_retrieval_only(args)
+    elif args.prefill_retrieval_only:
+        prefill_retrieval_only(args)
     else:
         gpu_arm(args)
 

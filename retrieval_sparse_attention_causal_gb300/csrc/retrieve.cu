@@ -21,7 +21,9 @@
 //                         layouts: 128-row x 256-candidate score tiles on tcgen05 with
 //                         the selection in the epilogue; the row-block path then takes it
 //                         instead of retrieve_tile_kernel.
-//   retrieve_merge_kernel merges the per-split candidate lists of a row.
+//   retrieve_merge_kernel / retrieve_merge_warp_kernel merge the per-split candidate
+//                         lists of a row (a block per row for few rows, a warp per row
+//                         for many).
 // Every stage keeps candidates under one total order (key descending, then index
 // ascending), so the result does not depend on how the candidates were split.
 #include <algorithm>
@@ -36,6 +38,7 @@ namespace gca {
 namespace {
 
 constexpr int kTileThreads = 256;
+constexpr long long kWarpMergeRows = 256;  // from this many rows on, the merge takes a warp per row
 
 __device__ __forceinline__ int n_cand_row(int i, int off, int nC) {
   long long n = (long long)i + off;
@@ -205,6 +208,40 @@ __global__ void __launch_bounds__(128) retrieve_merge_kernel(RetrieveArgs a, int
   }
   block_select(L, a.topk, sel, red);
   if (threadIdx.x == 0) write_row(a, b, i, sel);
+}
+
+// One warp per row, for problems with many rows (training, prefill): the lanes take the
+// row's candidates in turn into register lists, then k rounds of a butterfly maximum under
+// the total order pick the winners, the owning lane dropping each from its list.
+template <int KC>
+__global__ void __launch_bounds__(256) retrieve_merge_warp_kernel(RetrieveArgs a, int nsplit, int rows) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);  // row b * nQ + i
+  if (r >= rows) return;
+  const Cand* p = reinterpret_cast<const Cand*>(a.part) + (int64_t)r * nsplit * a.topk;
+  Cand L[KC];
+  list_init(L);
+  const int n = nsplit * a.topk;
+  for (int c = lane; c < n; c += 32) {
+    const Cand x = p[c];
+    if (x.j != 0x7fffffff) list_insert(L, x);
+  }
+  Cand mine = empty_cand();  // lane q keeps the q-th winner
+  for (int q = 0; q < a.topk; ++q) {
+    Cand best = L[0];
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      const Cand o = shfl_xor_cand(best, m);
+      if (better(o, best)) best = o;
+    }
+    if (lane == q) mine = best;
+    if (best.j != 0x7fffffff && L[0].j == best.j && L[0].key == best.key) list_pop(L);
+  }
+  if (lane < a.topk) {
+    const bool ok = mine.j != 0x7fffffff;
+    a.idx[(int64_t)r * a.topk + lane] = ok ? mine.j : -1;
+    a.scores[(int64_t)r * a.topk + lane] = ok ? mine.score : -CUDART_INF_F;
+  }
 }
 
 // ------------------------------------------------------------------ tile kernel
@@ -533,11 +570,14 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
     });
   }
   if (e != cudaSuccess || nsplit == 1) return e;
-  dim3 mg(a.nQ, a.B);
+  const long long rows = (long long)a.B * a.nQ;
   return with_kc(a.topk, [&](auto kc) -> cudaError_t {
     constexpr int KC = decltype(kc)::value;
     launch_begin("retrieve_merge", s);
-    retrieve_merge_kernel<KC><<<mg, 128, 0, s>>>(a, nsplit);
+    if (rows >= kWarpMergeRows)  // a warp per row
+      retrieve_merge_warp_kernel<KC><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, nsplit, (int)rows);
+    else  // a block per row: few rows, long lists (decode)
+      retrieve_merge_kernel<KC><<<dim3(a.nQ, a.B), 128, 0, s>>>(a, nsplit);
     return launch_end("retrieve_merge", s);
   });
 }

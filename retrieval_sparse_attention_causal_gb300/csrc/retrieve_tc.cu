@@ -190,30 +190,28 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
         const float(&cur)[32] = v[c & 1];
         const int jc = j0 + 32 * c;
         if (jc < lim) {
-          // The row's scores and keys of this chunk, and the largest key.  A key enters
-          // the list only if it beats the last entry, so a chunk whose largest key is below
-          // that entry's is skipped whole; equal keys go through the insertion, which
-          // orders them by index.
-          float km = -CUDART_INF_F;
+          // Bit e of `pass` marks the chunk's candidates whose key is at least that of the
+          // list's last entry as it stands before the chunk.  That entry only improves, so
+          // an unmarked candidate cannot enter; the marked ones go through the insertion in
+          // index order, which checks each against the list as it is then (ties included).
+          const float last = L[KC - 1].key;
+          uint32_t pass = 0;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float sc = cur[e] * inv;
             const float key = a.gumbel ? sc + gumbel_noise(a.seed, a.group, b, row, jc + e) : sc;
             mine[e] = sc;
-            mine[kKeyRow + e] = key;
-            if (jc + e < lim) km = fmaxf(km, key);
+            if (a.gumbel) mine[kKeyRow + e] = key;
+            if (key >= last && jc + e < lim) pass |= 1u << e;
           }
-          if (km >= L[KC - 1].key) {
-            const int n = min(32, lim - jc);
-            for (int e = 0; e < n; ++e) {
-              Cand cd;
-              cd.key = mine[kKeyRow + e];
-              cd.j = jc + e;
-              if (better(cd, L[KC - 1])) {
-                cd.score = mine[e];
-                list_insert(L, cd);
-              }
-            }
+          while (pass) {
+            const int e = __ffs(pass) - 1;
+            pass &= pass - 1;
+            Cand cd;
+            cd.score = mine[e];
+            cd.key = a.gumbel ? mine[kKeyRow + e] : cd.score;
+            cd.j = jc + e;
+            list_insert(L, cd);
           }
         }
         if (c + 1 < 4) tc::ld_wait_row(v[(c + 1) & 1]);
