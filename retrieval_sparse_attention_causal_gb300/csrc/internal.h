@@ -56,15 +56,15 @@ struct RetrievePlan {
   int rowwise;   // 1: one CTA per (row, split) streaming kernel; 0: 64-row tile kernel
   int nsplit;    // splits of the candidate range
   int seg;       // candidates per split
-  int tc_ns;     // tcgen05 scoring (bf16, TMA-compatible layouts): candidate segments per
-  int tc_sl;     //   128-row block and 256-candidate tiles per segment; two partial lists
-                 //   (column halves) per segment and row
+  int tc_ns[2];  // tcgen05 scoring (bf16, TMA-compatible layouts): candidate segments per
+  int tc_sl[2];  //   128-row block and 256-candidate tiles per segment, without [0] and
+                 //   with [1] noise; two partial lists (column halves) per segment and row
   size_t part_bytes;  // enough for whichever row-block kernel the launch picks
 };
 RetrievePlan retrieve_plan(int B, int nQ, int nC, int topk, int off);
 cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaStream_t s);
 // tcgen05 scoring of 128 query rows x 256-candidate tiles with the top-k in the epilogue
-// (retrieve_tc.cu): whether a call can take it, and the stage-1 launch (2 tc_ns lists).
+// (retrieve_tc.cu): whether a call can take it, and the stage-1 launch (2 tc_ns[noise] lists).
 bool retrieve_tc_eligible(const RetrieveArgs& a);
 cudaError_t launch_retrieve_tc(const RetrieveArgs& a, const RetrievePlan& p, cudaStream_t s);
 

@@ -498,18 +498,24 @@ RetrievePlan retrieve_plan(int B, int nQ, int nC, int topk, int off) {
     p.nsplit = (int)ns;
     p.seg = (int)seg;
     // tcgen05 path: 128-row blocks, 256-candidate tiles; the last block has the most tiles.
-    // Segments of tc_sl tiles per block, about four CTAs per SM over the whole grid.
+    // Segments of tc_sl tiles per block.  Every segment's lists start empty and fill at a
+    // cost, so without noise (cheap candidates) about two CTAs per SM over the grid; with
+    // noise each candidate costs more and the balance counts for more: about four.
     const long long nmb = (nQ + 127) / 128;
     const long long nt_max = ncand_max > 0 ? (ncand_max + 255) / 256 : 1;
-    long long tns = (4 * 152 + B * nmb - 1) / (B * nmb);
-    if (tns > nt_max) tns = nt_max;
-    if (tns < 1) tns = 1;
-    const long long tsl = (nt_max + tns - 1) / tns;
-    p.tc_sl = (int)tsl;
-    p.tc_ns = (int)((nt_max + tsl - 1) / tsl);
+    for (int g = 0; g < 2; ++g) {
+      const long long target = (g ? 4 : 2) * 152;
+      long long tns = (target + B * nmb - 1) / (B * nmb);
+      if (tns > nt_max) tns = nt_max;
+      if (tns < 1) tns = 1;
+      const long long tsl = (nt_max + tns - 1) / tns;
+      p.tc_sl[g] = (int)tsl;
+      p.tc_ns[g] = (int)((nt_max + tsl - 1) / tsl);
+    }
   }
   p.part_bytes = p.nsplit > 1 ? (size_t)B * nQ * p.nsplit * topk * sizeof(Cand) : 0;
-  if (!p.rowwise) p.part_bytes = std::max(p.part_bytes, (size_t)B * nQ * 2 * p.tc_ns * topk * sizeof(Cand));
+  if (!p.rowwise)
+    p.part_bytes = std::max(p.part_bytes, (size_t)B * nQ * 2 * std::max(p.tc_ns[0], p.tc_ns[1]) * topk * sizeof(Cand));
   return p;
 }
 
@@ -553,7 +559,7 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
     });
   } else if (retrieve_tc_eligible(a)) {
     e = launch_retrieve_tc(a, p, s);
-    nsplit = 2 * p.tc_ns;
+    nsplit = 2 * p.tc_ns[a.gumbel ? 1 : 0];
   } else {
     dim3 grid(p.nsplit, (a.nQ + 63) / 64, a.B);
     const int smem = (int)TileSmem::bytes(a.D, a.bf16 != 0);

@@ -90,6 +90,8 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
   __shared__ __align__(8) uint64_t full[NST], empty[NST], acc_full[2], acc_empty[2], drain;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_s;
+  // Last key of each (half, row) list, published after every chunk (see the selection).
+  __shared__ float thr_s[2][kBM];
   const int kt = a.D / 64;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -107,6 +109,7 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
   }
   if (warp == 1) tc::tmem_alloc(&tmem_slot, 2 * kBN);
+  for (int t = threadIdx.x; t < 2 * kBM; t += blockDim.x) (&thr_s[0][0])[t] = -CUDART_INF_F;
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -173,6 +176,11 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
     // that the selection loop indexes them without spilling the register array.
     float* mine = reinterpret_cast<float*>(sm + NST * kStage) + ((warp - 2) * 32 + lane) * kRowF;
     const float inv = 1.0f / sqrtf((float)a.D);
+    // The row's other half-list publishes its last key: a candidate below it has KC >= k
+    // better candidates of the same row there, so it cannot be among the row's best k and
+    // is not inserted (a stale value is an older, lower last key: still a valid bound).
+    volatile float* thr_own = &thr_s[half][32 * (warp & 3) + lane];
+    const volatile float* thr_other = &thr_s[half ^ 1][32 * (warp & 3) + lane];
     Cand L[KC];
     list_init(L);
     for (int i = 0; i < nt; ++i) {
@@ -191,10 +199,11 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
         const int jc = j0 + 32 * c;
         if (jc < lim) {
           // Bit e of `pass` marks the chunk's candidates whose key is at least that of the
-          // list's last entry as it stands before the chunk.  That entry only improves, so
-          // an unmarked candidate cannot enter; the marked ones go through the insertion in
-          // index order, which checks each against the list as it is then (ties included).
-          const float last = L[KC - 1].key;
+          // list's last entry as it stands before the chunk (and at least the other half's).
+          // That entry only improves, so an unmarked candidate cannot enter; the marked ones
+          // go through the insertion in index order, which checks each against the list as
+          // it is then (ties included).
+          const float last = fmaxf(L[KC - 1].key, *thr_other);
           uint32_t pass = 0;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -213,6 +222,7 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
             cd.j = jc + e;
             list_insert(L, cd);
           }
+          *thr_own = L[KC - 1].key;
         }
         if (c + 1 < 4) tc::ld_wait_row(v[(c + 1) & 1]);
       }
@@ -247,12 +257,13 @@ cudaError_t launch_retrieve_tc(const RetrieveArgs& a, const RetrievePlan& p, cud
   cudaError_t e = make_lmk_tmap(&tq, a.q, a.D, a.nQ, a.B, a.q_rs, a.q_bs, kBM);
   if (e == cudaSuccess) e = make_lmk_tmap(&tk, a.k, a.D, a.nC, a.B, a.D, a.k_bs, kBN);
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.tc_ns, (a.nQ + kBM - 1) / kBM, a.B);
+  const int g = a.gumbel ? 1 : 0;
+  const dim3 grid(p.tc_ns[g], (a.nQ + kBM - 1) / kBM, a.B);
   auto go = [&](auto kernel) -> cudaError_t {
     cudaError_t e2 = allow_smem((const void*)kernel, kSmem);
     if (e2 != cudaSuccess) return e2;
     launch_begin("retrieve_tc", s);
-    kernel<<<grid, kThreads, kSmem, s>>>(a, p.tc_ns, p.tc_sl, tq, tk);
+    kernel<<<grid, kThreads, kSmem, s>>>(a, p.tc_ns[g], p.tc_sl[g], tq, tk);
     return launch_end("retrieve_tc", s);
   };
   if (a.topk <= 4) return go(retrieve_tc_kernel<4>);
