@@ -167,6 +167,7 @@ KERNEL_SOURCES = {
     "gca_bwd_q": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh"),
     "gca_bwd_kv": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh"),
     "retrieve_stream": ("retrieve.cu", "common.cuh"),
+    "retrieve_tc": ("retrieve_tc.cu", "tc.cuh", "tc_rows.cuh", "common.cuh"),
 }
 KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
     "gca_fwd": (382.37e6, "7e6df2385ac4ce02"),
@@ -175,6 +176,11 @@ KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); 
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
 STREAM_TRAFFIC_PER_SEQ = (808441600 / 2, "8cf0263a298f2697")
+
+
+# profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
+# nothing written back past L2; traffic grows with the number of chunks)
+PREFILL_TRAFFIC_PER_CHUNK = (25269504 / 8192, "fd98c5f9b9e865f7")
 
 
 def source_fingerprint(kernel: str) -> str:
@@ -192,6 +198,11 @@ def stream_traffic(nb: int):
         return None
     per_seq, fp = STREAM_TRAFFIC_PER_SEQ
     return round(per_seq * nb) if fp == source_fingerprint("retrieve_stream") else None
+
+
+def prefill_traffic(nc: int):
+    per_chunk, fp = PREFILL_TRAFFIC_PER_CHUNK
+    return round(per_chunk * nc) if fp == source_fingerprint("retrieve_tc") else None
 
 
 def measured_traffic(kernel: str, table=None):
@@ -293,7 +304,7 @@ def gpu_arm(args):
     # The chunk / landmark encoder that produces K, V and the key landmarks.
     enc = None if args.no_encoder else encoder_leg(args, torch, gca, synth, timed, pk)
     # Retrieval for a 1M-token prefill (the scoring as a dense tensor-core product).
-    pre = None if args.no_prefill else prefill_leg(args, torch, gca, synth, pk)
+    pre = None if args.no_prefill else prefill_leg(args, torch, gca, synth, pk, src)
 
     # End to end through the public API from pinned host buffers.
     e2e = None
@@ -588,7 +599,7 @@ def prefill_flops(nc, d):
     return 2 * d * nc * (nc - 1) // 2
 
 
-def prefill_leg(args, torch, gca, synth, pk):
+def prefill_leg(args, torch, gca, synth, pk, src):
     """Landmark retrieval for a 1M-token prefill: one sequence of 16384 chunks, D = 768,
     k = 8, no noise; every chunk's query landmark against all earlier chunks' landmarks.
     The two landmark tensors (25 MB each) fit in L2, so a 256 MB buffer is written before
@@ -628,8 +639,9 @@ def prefill_leg(args, torch, gca, synth, pk):
             "kernels": {nm: round(t / c, 5) for nm, (c, t) in prof.items()},
             "l2": "256 MB buffer written before every call",
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": None,
-                         "flops_per_launch": fl}}
+                         "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
+                         "traffic": prefill_traffic(nc) if dom == "retrieve_tc" else None,
+                         "peak_source": f"{src} bf16 dense (burst)", "flops_per_launch": fl}}
 
 
 def encoder_flops(nb, nc, d, h):
