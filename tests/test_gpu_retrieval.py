@@ -132,11 +132,14 @@ def test_deterministic():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-@pytest.mark.parametrize("gumbel,off,K", [(False, 0, 8), (True, 0, 8), (False, 300, 16), (True, 5, 3)])
+@pytest.mark.parametrize("gumbel,off,K", [(False, 0, 8), (True, 0, 8), (False, 300, 16), (True, 5, 3), (False, 0, 5),
+                                          (True, 4096, 8)])
 def test_large_row_blocks_tcgen05_path(gumbel, off, K):
     """B = 4, 4096 query rows over 4096 + off candidates, D = 128: enough 128 x 256 score
     tiles to take the tcgen05 scoring path (selection in its epilogue, partial lists per
-    candidate segment and column half, then the merge).  Every row against the oracle."""
+    candidate segment and column half, then the merge).  Every row against the oracle.
+    k = 3 and 5 keep lists longer than k (4 and 8 entries), whose last entries bound what
+    the other half-list of the row inserts; off = 4096 gives every row all 8192 chunks."""
     B, nQ, D = 4, 4096, 128
     nC = nQ + off
     _, _, _, nd, nt = run_case(B, nQ, nC, D, K, "bf16", off=off, gumbel=gumbel, seed=7)
@@ -159,3 +162,11 @@ def test_large_row_blocks_strided_queries_and_shared_keys():
     nd, _ = compare_retrieval(idx_g.cpu().numpy(), host(sc_g), idx_o, sc_o, m, SCORE_TOL["bf16"], orc=orc, q=qv, k=kb,
                               gumbel=True, seed=8)
     assert nd > 0.5 * B * nQ  # most rows decidable: the test is not vacuous
+
+
+@pytest.mark.parametrize("nQ", [255, 256])
+def test_merge_block_and_warp_paths(nQ):
+    """Below 256 rows the partial lists of a row are merged by a block, from 256 rows on by
+    a warp: both against the oracle at the boundary (several candidate splits per row)."""
+    _, _, _, nd, _ = run_case(1, nQ, nQ, 256, 8, "bf16", off=0, gumbel=True, seed=9)
+    assert nd > 0.5 * nQ
