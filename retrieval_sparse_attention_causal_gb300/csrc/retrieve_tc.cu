@@ -51,16 +51,54 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
   return false;
 }
 
-template <int KC>
+// Selection-list entries: with noise a candidate carries its key and its clean score;
+// without, the key is the score and the entry is one float lighter to move.
+struct KeyJ {
+  float key;
+  int j;
+};
+template <bool kNoise>
+struct EntryOf {
+  using T = Cand;
+};
+template <>
+struct EntryOf<false> {
+  using T = KeyJ;
+};
+__device__ __forceinline__ Cand as_cand(const Cand& c) { return c; }
+__device__ __forceinline__ Cand as_cand(const KeyJ& c) { return Cand{c.key, c.key, c.j}; }
+__device__ __forceinline__ void set_empty(Cand& c) { c = empty_cand(); }
+__device__ __forceinline__ void set_empty(KeyJ& c) { c = KeyJ{-CUDART_INF_F, 0x7fffffff}; }
+
+// The same sorted insertion and total order as the other retrieval kernels' lists.
+template <class T>
+__device__ __forceinline__ bool ahead(const T& x, const T& y) {
+  return x.key > y.key || (x.key == y.key && x.j < y.j);
+}
+template <class T, int KC>
+__device__ __forceinline__ void insert_sorted(T (&L)[KC], const T& c) {
+  if (!ahead(c, L[KC - 1])) return;
+  bool placed = false;
+#pragma unroll
+  for (int t = KC - 1; t > 0; --t) {
+    const bool mv = ahead(c, L[t - 1]);
+    T nt = placed ? L[t] : (mv ? L[t - 1] : c);
+    placed = placed || !mv;
+    L[t] = nt;
+  }
+  if (!placed) L[0] = c;
+}
+
+template <class T, int KC>
 __device__ __forceinline__ void put_list(const RetrieveArgs& a, int nsplit, int b, int i, int split,
-                                         const Cand (&L)[KC]) {
+                                         const T (&L)[KC]) {
   Cand* p = reinterpret_cast<Cand*>(a.part) + (((int64_t)b * a.nQ + i) * nsplit + split) * a.topk;
 #pragma unroll
   for (int r = 0; r < KC; ++r)
-    if (r < a.topk) p[r] = L[r];
+    if (r < a.topk) p[r] = as_cand(L[r]);
 }
 
-template <int KC>
+template <int KC, bool kNoise>
 __global__ void __launch_bounds__(kThreads, 1)
 retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK) {
@@ -181,8 +219,10 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
     // is not inserted (a stale value is an older, lower last key: still a valid bound).
     volatile float* thr_own = &thr_s[half][32 * (warp & 3) + lane];
     const volatile float* thr_other = &thr_s[half ^ 1][32 * (warp & 3) + lane];
-    Cand L[KC];
-    list_init(L);
+    using T = typename EntryOf<kNoise>::T;
+    T L[KC];
+#pragma unroll
+    for (int r = 0; r < KC; ++r) set_empty(L[r]);
     for (int i = 0; i < nt; ++i) {
       const int buf = i & 1;
       if (!wait_or_abort(&acc_full[buf], (uint32_t)(i >> 1) & 1, &abort_s, a.err, 24, t0 + i)) break;
@@ -208,19 +248,23 @@ retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUten
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float sc = cur[e] * inv;
-            const float key = a.gumbel ? sc + gumbel_noise(a.seed, a.group, b, row, jc + e) : sc;
+            const float key = kNoise ? sc + gumbel_noise(a.seed, a.group, b, row, jc + e) : sc;
             mine[e] = sc;
-            if (a.gumbel) mine[kKeyRow + e] = key;
+            if (kNoise) mine[kKeyRow + e] = key;
             if (key >= last && jc + e < lim) pass |= 1u << e;
           }
           while (pass) {
             const int e = __ffs(pass) - 1;
             pass &= pass - 1;
-            Cand cd;
-            cd.score = mine[e];
-            cd.key = a.gumbel ? mine[kKeyRow + e] : cd.score;
+            T cd;
+            if constexpr (kNoise) {
+              cd.score = mine[e];
+              cd.key = mine[kKeyRow + e];
+            } else {
+              cd.key = mine[e];
+            }
             cd.j = jc + e;
-            list_insert(L, cd);
+            insert_sorted(L, cd);
           }
           *thr_own = L[KC - 1].key;
         }
@@ -266,9 +310,14 @@ cudaError_t launch_retrieve_tc(const RetrieveArgs& a, const RetrievePlan& p, cud
     kernel<<<grid, kThreads, kSmem, s>>>(a, p.tc_ns[g], p.tc_sl[g], tq, tk);
     return launch_end("retrieve_tc", s);
   };
-  if (a.topk <= 4) return go(retrieve_tc_kernel<4>);
-  if (a.topk <= 8) return go(retrieve_tc_kernel<8>);
-  return go(retrieve_tc_kernel<16>);
+  if (a.gumbel) {
+    if (a.topk <= 4) return go(retrieve_tc_kernel<4, true>);
+    if (a.topk <= 8) return go(retrieve_tc_kernel<8, true>);
+    return go(retrieve_tc_kernel<16, true>);
+  }
+  if (a.topk <= 4) return go(retrieve_tc_kernel<4, false>);
+  if (a.topk <= 8) return go(retrieve_tc_kernel<8, false>);
+  return go(retrieve_tc_kernel<16, false>);
 }
 
 }  // namespace gca
