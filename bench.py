@@ -605,7 +605,8 @@ def prefill_leg(args, torch, gca, synth, pk, src):
     The two landmark tensors (25 MB each) fit in L2, so a 256 MB buffer is written before
     every call; the call's kernels are timed alone with CUDA events.  Reports the call's
     time, tokens/s (the prefill's tokens per call time) and the scoring kernel's
-    algorithmic TFLOP/s against the measured bf16 peak."""
+    algorithmic TFLOP/s against the measured bf16 peak; then the whole prefill (retrieval
+    and GCA forward, `with_forward`)."""
     wl = PREFILL_1M
     nc, d, k = wl.n_chunks, wl.D, wl.topk
     ql = synth.device_normal(args.seed, synth.S_QL, (1, nc, d), 1.0, torch.bfloat16)
@@ -634,10 +635,56 @@ def prefill_leg(args, torch, gca, synth, pk, src):
     dom_ms = prof[dom][1] / prof[dom][0]
     fl = prefill_flops(nc, d)
     ach = fl / (dom_ms / 1e3) / 1e12
+
+    # The whole prefill: the retrieval, then GCA's forward for every chunk over the chunks
+    # its predecessor's landmark retrieved (Q/K/V of 1M tokens, 1.6 GB each, past L2).
+    shape = (1, wl.L, wl.H, wl.dh)
+    q, kk, vv = (synth.device_normal(args.seed, st, shape, wl.qkv_std, torch.bfloat16)
+                 for st in (synth.S_Q, synth.S_K, synth.S_V))
+    o = torch.empty_like(q)
+    lse = torch.empty((1, nc, wl.H, k, 64), dtype=torch.float32, device="cuda")
+
+    def full():
+        call()
+        gca.gca_forward(q, kk, vv, idx, sc, shift=1, ws=ws, out=o, lse=lse)
+
+    for _ in range(3):
+        full()
+    ws.check()
+    nf = 10
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(nf):
+        full()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_full = e0.elapsed_time(e1) / nf
+    gca.profile_begin()
+    for _ in range(nf):
+        full()
+    torch.cuda.synchronize()
+    fwd_ms = gca.profile_end()["gca_fwd"]
+    fwd_ms = fwd_ms[1] / fwd_ms[0]
+    af = algorithmic_flops(1, nc, wl.H, wl.dh, k)
+    fl_fwd = af["gca_fwd"]
+    # Bytes the forward must move at this size: the retrieved K and V chunk of every
+    # (slot, head) unit (the 16384 chunks' consumers are spread over the whole sequence,
+    # so L2 gives no reuse), plus Q and O of every chunk and head, plus the LSE rows.
+    by_fwd = af["units"] * 2 * 64 * wl.dh * 2 + nc * wl.H * 2 * 64 * wl.dh * 2 + nc * wl.H * k * 64 * 4
+    del q, kk, vv, o, lse
     return {"workload": f"{wl.name}: B=1, {nc} chunks, landmark dim {d}, top-k {k}, no noise",
             "ms": round(ms, 4), "tokens_per_s": round(wl.L / (ms / 1e3), 1),
             "kernels": {nm: round(t / c, 5) for nm, (c, t) in prof.items()},
             "l2": "256 MB buffer written before every call",
+            "with_forward": {"ms": round(ms_full, 4), "tokens_per_s": round(wl.L / (ms_full / 1e3), 1),
+                             "gca_fwd_ms": round(fwd_ms, 4),
+                             "gca_fwd_tflops_algorithmic": round(fl_fwd / (fwd_ms / 1e3) / 1e12, 1),
+                             "gca_fwd_frac_of_bf16_peak": round(fl_fwd / (fwd_ms / 1e3) / 1e12 / pk["bf16_tflops"], 3),
+                             "gca_fwd_bytes_algorithmic": by_fwd,
+                             "gca_fwd_gbs": round(by_fwd / (fwd_ms / 1e3) / 1e9, 1),
+                             "gca_fwd_frac_of_hbm": round(by_fwd / (fwd_ms / 1e3) / 1e9 / pk["hbm_gbs"], 3),
+                             "what": "retrieval + GCA forward of every chunk (H 12 x dh 64), next-chunk shift"},
             "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4),
                          "traffic": prefill_traffic(nc) if dom == "retrieve_tc" else None,
