@@ -52,3 +52,27 @@ def test_single_rank_is_local_time():
     import bench
     assert bench.max_over_ranks(12.5, 1) == 12.5
     assert bench.job_throughput(1000, 1, 2.0) == pytest.approx(500000.0)
+
+
+def test_algorithmic_counts():
+    """The work the roofline figures divide by, against brute-force counts: prefill
+    scoring pairs (row i has the i chunks before it), and the training step's valid
+    (slot, head) units (4 x 12 x 2004 at 256 chunks, k = 8)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    nc, d = 1000, 64
+    assert bench.prefill_flops(nc, d) == 2 * d * sum(len(range(i)) for i in range(nc))
+    assert bench.prefill_flops(16384, 768) == 206145847296
+    assert bench.algorithmic_flops(4, 256, 12, 64, 8)["units"] == 4 * 12 * 2004
+    assert bench.algorithmic_flops(1, 3, 1, 64, 8)["units"] == 1  # rows 0, 1 feed chunks 1, 2
+
+
+def test_traffic_figures_follow_the_sources():
+    """A stored DRAM traffic figure is reported only while the kernel's sources still hash
+    to the fingerprint taken at capture time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    fp = bench.source_fingerprint("gca_fwd")
+    assert bench.measured_traffic("gca_fwd", {"gca_fwd": (123.0, fp)}) == 123.0
+    assert bench.measured_traffic("gca_fwd", {"gca_fwd": (123.0, "0" * 16)}) is None
+    assert bench.measured_traffic("gca_fwd", {}) is None
