@@ -6,7 +6,7 @@
 // the best k; in training the selection key carries Gumbel noise, the returned score does
 // not.
 //
-// For many query rows (training, prefill) the scores are a dense product: S = Q K^T with
+// For many query rows (prefill-sized problems) the scores are a dense product: S = Q K^T with
 // Q [128 rows][D] and K [256 candidates][D] per tile, D in steps of 64 through a 3-stage
 // TMA ring, tcgen05.mma M = 128, N = 256 into one of two TMEM accumulators (so that a
 // tile's selection overlaps the next tile's products).  A CTA takes one 128-row block and
@@ -15,9 +15,10 @@
 // columns, scale by D^-1/2, drop candidates j >= i + offset, add the noise of
 // (seed, group, b, i, j) for the key, and keep the row's best k in registers under the
 // total order of the other retrieval kernels (key descending, then index ascending)
-// across the segment's tiles.  Each (row, segment, half) list goes to the partial buffer,
-// which retrieve_merge_kernel reduces to the row's result, so the outcome does not depend
-// on the split.
+// across the segment's tiles.  Per 32 candidates a bitmask marks those at or above the
+// list's last key (and the row's other half-list's), and only those go through the
+// sorted insertion.  Each (row, segment, half) list goes to the partial buffer, which the
+// merge kernels reduce to the row's result, so the outcome does not depend on the split.
 #include <algorithm>
 
 #include "common.cuh"
