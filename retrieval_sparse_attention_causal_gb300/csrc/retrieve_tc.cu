@@ -76,18 +76,18 @@ template <class T>
 __device__ __forceinline__ bool ahead(const T& x, const T& y) {
   return x.key > y.key || (x.key == y.key && x.j < y.j);
 }
+// The entries ahead of c form a prefix of the sorted list, so all KC comparisons are
+// independent: entry t keeps its value inside the prefix, takes c just past it and its
+// predecessor's value beyond.
 template <class T, int KC>
 __device__ __forceinline__ void insert_sorted(T (&L)[KC], const T& c) {
   if (!ahead(c, L[KC - 1])) return;
-  bool placed = false;
+  bool in[KC];
 #pragma unroll
-  for (int t = KC - 1; t > 0; --t) {
-    const bool mv = ahead(c, L[t - 1]);
-    T nt = placed ? L[t] : (mv ? L[t - 1] : c);
-    placed = placed || !mv;
-    L[t] = nt;
-  }
-  if (!placed) L[0] = c;
+  for (int t = 0; t < KC; ++t) in[t] = ahead(L[t], c);
+#pragma unroll
+  for (int t = KC - 1; t > 0; --t) L[t] = in[t] ? L[t] : (in[t - 1] ? c : L[t - 1]);
+  if (!in[0]) L[0] = c;
 }
 
 template <class T, int KC>
