@@ -180,7 +180,7 @@ STREAM_TRAFFIC_PER_SEQ = (808355840 / 2, "5a1efa117742d5ce")
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
 # nothing written back past L2; traffic grows with the number of chunks)
-PREFILL_TRAFFIC_PER_CHUNK = (25220352 / 8192, "403747d331511952")
+PREFILL_TRAFFIC_PER_CHUNK = (25215744 / 8192, "ec85a0f70d57e879")
 
 
 def source_fingerprint(kernel: str) -> str:
