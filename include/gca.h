@@ -82,6 +82,9 @@ GCA_API const char* gca_last_error_detail(void);
  *     ctr    = group << 56 | b << 48 | i << 24 | j.
  * The min(topk, n_i) candidates with the largest keys are written in descending key
  * order (equal keys: lower j first).  Unused slots get idx = -1 and score = -inf.
+ * The call picks its kernels from the shape (a streaming scan for up to 8 query rows;
+ * tensor-core score tiles with the selection in their epilogue for large bf16 problems;
+ * 64-row tiles otherwise); the selected indices do not depend on that choice.
  *
  *   q_lmk   [B][nQ][D] at q_row_stride / q_batch_stride elements (row stride >= D,
  *           a multiple of 8 elements for bf16 and 4 for f32; strides allow reading the
