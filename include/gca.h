@@ -84,7 +84,10 @@ GCA_API const char* gca_last_error_detail(void);
  * order (equal keys: lower j first).  Unused slots get idx = -1 and score = -inf.
  * The call picks its kernels from the shape (a streaming scan for up to 8 query rows;
  * tensor-core score tiles with the selection in their epilogue for large bf16 problems;
- * 64-row tiles otherwise); the selected indices do not depend on that choice.
+ * 64-row tiles otherwise).  All apply the same order and tie rule; their float32 sums
+ * may round differently, so only keys within that rounding of each other can be
+ * ordered differently by different kernels.  A given shape always takes the same
+ * kernels, and its result does not depend on how the candidates are split.
  *
  *   q_lmk   [B][nQ][D] at q_row_stride / q_batch_stride elements (row stride >= D,
  *           a multiple of 8 elements for bf16 and 4 for f32; strides allow reading the
