@@ -175,7 +175,7 @@ KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); 
     "gca_bwd_kv": (603.0e6, "5c4fccd2ea985839"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (808355840 / 2, "5a1efa117742d5ce")
+STREAM_TRAFFIC_PER_SEQ = (808436224 / 2, "12cf7c72783b197e")
 
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,

@@ -21,9 +21,10 @@
 //                         layouts: 128-row x 256-candidate score tiles on tcgen05 with
 //                         the selection in the epilogue; the row-block path then takes it
 //                         instead of retrieve_tile_kernel.
-//   retrieve_merge_kernel / retrieve_merge_warp_kernel merge the per-split candidate
-//                         lists of a row (a block per row for few rows, a warp per row
-//                         for many).
+//   retrieve_merge_kernel / retrieve_merge_warp_kernel / retrieve_merge_heads_kernel
+//                         merge the per-split candidate lists of a row (a block per row
+//                         for few rows; a warp per row for many, walking the sorted lists'
+//                         heads when they are few and short).
 // Every stage keeps candidates under one total order (key descending, then index
 // ascending), so the result does not depend on how the candidates were split.
 #include <algorithm>
@@ -241,6 +242,55 @@ __global__ void __launch_bounds__(256) retrieve_merge_warp_kernel(RetrieveArgs a
     const bool ok = mine.j != 0x7fffffff;
     a.idx[(int64_t)r * a.topk + lane] = ok ? mine.j : -1;
     a.scores[(int64_t)r * a.topk + lane] = ok ? mine.score : -CUDART_INF_F;
+  }
+}
+
+// One warp per row when the row's lists are few and short (up to 32 lists, kHeadsMax
+// candidates): the lists are sorted already, so they are staged in shared memory, lane l
+// holds the head of list l, and each of k rounds takes the best head (a butterfly over
+// the lists' lanes on (key, index)) and moves the winning lane to its list's next entry.
+constexpr int kHeadsMax = 128;
+__global__ void __launch_bounds__(256) retrieve_merge_heads_kernel(RetrieveArgs a, int nsplit, int rows) {
+  __shared__ Cand st[8][kHeadsMax];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int r = blockIdx.x * 8 + w;  // row b * nQ + i
+  if (r >= rows) return;
+  const int n = nsplit * a.topk;
+  const Cand* p = reinterpret_cast<const Cand*>(a.part) + (int64_t)r * n;
+  for (int c = lane; c < n; c += 32) st[w][c] = p[c];
+  __syncwarp();
+  int width = 1;
+  while (width < nsplit) width <<= 1;
+  int pos = 0;
+  Cand head = lane < nsplit ? st[w][lane * a.topk] : empty_cand();
+  int32_t* idx = a.idx + (int64_t)r * a.topk;
+  float* sc = a.scores + (int64_t)r * a.topk;
+  for (int q = 0; q < a.topk; ++q) {
+    float bk = head.key;
+    int bj = head.j;
+    for (int m = width >> 1; m >= 1; m >>= 1) {
+      const float ok = __shfl_xor_sync(0xffffffffu, bk, m);
+      const int oj = __shfl_xor_sync(0xffffffffu, bj, m);
+      if (ok > bk || (ok == bk && oj < bj)) {
+        bk = ok;
+        bj = oj;
+      }
+    }
+    bj = __shfl_sync(0xffffffffu, bj, 0);  // lanes 0 .. width-1 hold the lists' best
+    if (bj == 0x7fffffff) {                // every list is spent: pad the rest
+      if (lane == 0)
+        for (int t = q; t < a.topk; ++t) {
+          idx[t] = -1;
+          sc[t] = -CUDART_INF_F;
+        }
+      break;
+    }
+    if (lane < nsplit && head.j == bj) {  // indices are unique across the lists
+      idx[q] = bj;
+      sc[q] = head.score;
+      ++pos;
+      head = pos < a.topk ? st[w][lane * a.topk + pos] : empty_cand();
+    }
   }
 }
 
@@ -580,7 +630,9 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
   return with_kc(a.topk, [&](auto kc) -> cudaError_t {
     constexpr int KC = decltype(kc)::value;
     launch_begin("retrieve_merge", s);
-    if (rows >= kWarpMergeRows)  // a warp per row
+    if (rows >= kWarpMergeRows && nsplit <= 32 && (long long)nsplit * a.topk <= kHeadsMax)
+      retrieve_merge_heads_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, nsplit, (int)rows);
+    else if (rows >= kWarpMergeRows)  // a warp per row, lists into registers
       retrieve_merge_warp_kernel<KC><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, nsplit, (int)rows);
     else  // a block per row: few rows, long lists (decode)
       retrieve_merge_kernel<KC><<<dim3(a.nQ, a.B), 128, 0, s>>>(a, nsplit);
