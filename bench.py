@@ -6,7 +6,9 @@ landmark retrieval, GCA forward, GCA backward (dQ, dK, dV, dscores) and the
 landmark-score backward, all in this library's kernels, timed with CUDA events.
 Secondary (same JSON line, key "decode"): decode-time retrieval at 16M context,
 B=16 sequences x 262144 past chunk landmarks of dim 768, plus the GCA forward over the
-8 retrieved chunks.
+8 retrieved chunks.  Further keys: "prefill_retrieval" (a 1M-token prefill: retrieval on
+tensor cores, then with GCA's forward), "block_attention" (window attention and CCA,
+forward and backward) and "encoder" (the chunk / landmark encoder).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
