@@ -34,17 +34,28 @@ import numpy as np
 
 METRIC = "GCA fwd+bwd tokens/s at L=16K; landmark top-k GB/s at 16M ctx (1 GB300)"
 
-def _workloads():
-    """The workload presets, loaded by path: importing the package would load the CUDA
-    library, which the reference arm does not need."""
+def _by_path(fname, modname):
+    """A module of the package loaded from its file: importing the package would load the
+    CUDA library, which the oracle legs (and the reference arm) must not map."""
     import importlib.util
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "retrieval_sparse_attention_causal_gb300",
-                        "workloads.py")
-    spec = importlib.util.spec_from_file_location("gca_workloads", path)
+    if modname in sys.modules:
+        return sys.modules[modname]
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "retrieval_sparse_attention_causal_gb300", fname)
+    spec = importlib.util.spec_from_file_location(modname, path)
     mod = importlib.util.module_from_spec(spec)
     sys.modules[spec.name] = mod  # dataclasses resolve the module by name
     spec.loader.exec_module(mod)
     return mod
+
+
+def _workloads():
+    """The workload presets (sizes only)."""
+    return _by_path("workloads.py", "gca_workloads")
+
+
+def _synth():
+    """The seeded input generators (no method arithmetic, no CUDA library)."""
+    return _by_path("synth.py", "gca_synth")
 
 
 _W = _workloads()
@@ -276,9 +287,9 @@ def gpu_arm(args):
     ws.check()
     n0 = gca.launch_count()
     with ClockSampler(torch) as clk:
-        ms = timed(step, args.steps)
-    launches = gca.launch_count() - n0
-    ms_step = ms / args.steps
+        reps = timed_repeats(timed, step, args.steps, args.min_seconds)
+    launches = (gca.launch_count() - n0) // len(reps)
+    ms_step = statistics.median(reps) / args.steps
     tokens = B * L
     value = job_throughput(tokens, world, ms_step)
 
@@ -313,6 +324,12 @@ def gpu_arm(args):
     if not args.no_e2e:
         e2e = e2e_leg(args, torch, gca, step_outputs_template=out, inputs=dict(q=q, k=k, v=v, do=do, ql=ql, kl=kl),
                       seed=seed, world=world, timed_barrier=barrier, tokens=tokens)
+        # The same, reading back every result of the step (O, dQ, dK, dV, the landmark
+        # gradients and the retrieval decision): inputs in, all results out.
+        e2e["full_readback"] = e2e_leg(
+            args, torch, gca, step_outputs_template=out, inputs=dict(q=q, k=k, v=v, do=do, ql=ql, kl=kl), seed=seed,
+            world=world, timed_barrier=barrier, tokens=tokens,
+            res=("idx", "sc", "ds", "o", "dq", "dk", "dv", "dql", "dkl"))
 
     dec = None if args.no_decode else decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world)
 
@@ -336,27 +353,58 @@ def gpu_arm(args):
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)/8 Q/K/V/dO, N(0,1) landmarks)",
-            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": L, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (Q, K, V, dO: 4 x 100.7 MB per step)"},
+            "config": bench_config(world),
             "step_tflops_algorithmic": round(step_tflops, 2),
+            "timed_repeats": {"n": len(reps), "ms_per_step_min": round(min(reps) / args.steps, 4),
+                              "ms_per_step_max": round(max(reps) / args.steps, 4),
+                              "ms_x_sm_mhz": (round(ms_step * clk.summary()["sm_mhz"], 1)
+                                              if clk.summary().get("sm_mhz") else None)},
             "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary(),
             "kernels": {n: round(x["avg_ms"], 5) for n, x in kern.items()},
             "e2e": e2e, "decode": dec, "block_attention": blk, "encoder": enc, "prefill_retrieval": pre,
             "cpu_baseline": cpu,
         }
+        # Compact copies of the secondary headlines, last on the line so that a reader of
+        # the line's tail sees them.
+        if dec is not None:
+            line["decode_headline"] = {
+                "metric": "landmark top-k GB/s at 16M ctx", "B": dec["batch"], "GBps": dec["value"],
+                "ms_per_retrieval": dec["ms_per_retrieval"], "stream_kernel_GBps": dec["roofline"]["achieved"],
+                "frac_of_hbm": dec["roofline"]["frac"], "peak_GBps": dec["roofline"]["peak"],
+                "sweep_GBps": {b: x["GBps"] for b, x in dec["batch_sweep"].items()},
+                "sweep_frac_of_hbm": {b: x["stream_kernel_frac_of_hbm"] for b, x in dec["batch_sweep"].items()}}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def e2e_leg(args, torch, gca, step_outputs_template, inputs, seed, world, timed_barrier, tokens):
+def timed_repeats(timed, fn, steps, min_seconds, max_repeats=500):
+    """The K-step timed region (barrier + synchronize on both sides, CUDA events on the
+    launching stream), repeated until at least `min_seconds` of timed work have run, so
+    that a short step still gives a stable figure.  Returns the milliseconds of every
+    repeat; the step time is their median over K."""
+    reps = []
+    while True:
+        reps.append(timed(fn, steps))
+        if sum(reps) >= min_seconds * 1e3 or len(reps) >= max_repeats:
+            return reps
+
+
+def bench_config(world):
+    """The `config` object of the JSON line: the same for the GPU arm and the oracle arm."""
+    return {"workload": WORKLOAD, "global_batch": B * world, "seq_len": L, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (Q, K, V, dO: 4 x 100.7 MB per step)"}
+
+
+def e2e_leg(args, torch, gca, step_outputs_template, inputs, seed, world, timed_barrier, tokens,
+            res=("idx", "sc", "ds")):
     """The training step end to end through the public API: every step copies its inputs
     from pinned host memory to the device and reads its result back: the retrieval
     decision (indices, scores) and the score gradients.  dQ, dK, dV and the landmark
     gradients stay on the device, where an optimizer would consume them.  Copies run on
     their own streams and overlap the previous/next step's compute (inputs and outputs
     are double-buffered); the timed region covers all of it."""
-    res = ["idx", "sc", "ds"]
+    res = list(res)
     hin = {n: t.cpu().pin_memory() for n, t in inputs.items()}
     din = [{n: torch.empty_like(t) for n, t in inputs.items()} for _ in range(2)]
     dout = [{n: torch.empty_like(t) for n, t in step_outputs_template.items()} for _ in range(2)]
@@ -426,7 +474,13 @@ def e2e_leg(args, torch, gca, step_outputs_template, inputs, seed, world, timed_
             "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
             "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout[0].values()),
             "overlap": "inputs of step i+1 and results of step i-1 move while step i computes",
-            "d2h": "retrieval indices, scores and score gradients; dQ/dK/dV and landmark gradients stay on the device"}
+            "d2h": ", ".join(RESULT_NAMES[n] for n in res) +
+                   ("" if "dq" in res else "; dQ/dK/dV and landmark gradients stay on the device")}
+
+
+RESULT_NAMES = {"idx": "retrieval indices", "sc": "retrieval scores", "ds": "score gradients", "o": "O",
+                "dq": "dQ", "dk": "dK", "dv": "dV", "dql": "query-landmark gradients",
+                "dkl": "key-landmark gradients"}
 
 
 def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
@@ -491,6 +545,29 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
     nbytes = nb * DEC_NC * D * 2
     rows_ms = prof["retrieve_stream"][1] / prof["retrieve_stream"][0]
     ach = nbytes / (rows_ms / 1e3) / 1e9
+    # Batch sweep: the same retrieval over the first b sequences (every sequence's 402.7 MB
+    # of landmarks is larger than L2, so each call streams from HBM).
+    sweep = {}
+    for nbs in (1, 2, 4, 8, 16):
+        if nbs > nb:
+            break
+        qs, ks, ids, scs = ql[:nbs], kl[:nbs], idx[:nbs], sc[:nbs]
+
+        def rs(i, qs=qs, ks=ks, ids=ids, scs=scs):
+            gca.retrieve_topk(qs, ks, K, DEC_NC, False, ws=ws, idx=ids, scores=scs)
+
+        for i in range(3):
+            rs(i)
+        ms_b = time_loop(rs, args.steps)
+        gca.profile_begin()
+        time_loop(rs, args.steps)
+        pr = gca.profile_end()
+        st_ms = pr["retrieve_stream"][1] / pr["retrieve_stream"][0]
+        by = nbs * DEC_NC * D * 2
+        sweep[str(nbs)] = {"ms_per_retrieval": round(ms_b, 4), "GBps": round(by / (ms_b / 1e3) / 1e9, 1),
+                           "stream_kernel_ms": round(st_ms, 4),
+                           "stream_kernel_GBps": round(by / (st_ms / 1e3) / 1e9, 1),
+                           "stream_kernel_frac_of_hbm": round(by / (st_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
     # Batch 1: a decode step is a few short launches, so the host's launch cost matters.
     # The eager step against the same step captured once as a CUDA graph and replayed.
     from retrieval_sparse_attention_causal_gb300 import pipeline
@@ -528,7 +605,8 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
                          "traffic": stream_traffic(nb), "peak_source": f"{src} copy bandwidth",
                          "bytes_per_launch": nbytes},
-            "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "batch1": batch1, "offload": offload}
+            "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "batch_sweep": sweep, "batch1": batch1,
+            "offload": offload}
 
 
 def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):
@@ -836,7 +914,7 @@ def cpu_sample(seed, rows, budget_s=None):
     Returns (tokens processed, seconds, cpu seconds)."""
     sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
     import oracle.gca_oracle as orc
-    from retrieval_sparse_attention_causal_gb300 import synth
+    synth = _synth()
 
     x = synth.gca_inputs(seed, 1, NC, NC, H, DH, 1 / 8, "bf16")
     lm = synth.landmark_inputs(seed, 1, NC, NC, D, "bf16")
@@ -880,7 +958,7 @@ def next_rows_cpu(seed):
     that leg's workload (a few seconds each), in the leg's own unit."""
     sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
     import oracle.gca_oracle as orc
-    from retrieval_sparse_attention_causal_gb300 import synth
+    synth = _synth()
 
     cores = len(os.sched_getaffinity(0))
     out = {}
@@ -971,7 +1049,7 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": B, "seq_len": L},
+            "config": bench_config(world),
             "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "kind": "oracle",
                              "cores": len(os.sched_getaffinity(0)), "threads_busy": round(tot_cpu / tot_t, 2),
                              "sample": f"per step: one sequence, query chunks 1..{rows} ({rows * 64} tokens)"},
@@ -995,6 +1073,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat the K-step timed region until this much timed work has run (median reported)")
     ap.add_argument("--decode-retrieval-only", action="store_true",
                     help="run only the 16M-context landmark retrieval (for profiling captures)")
     ap.add_argument("--prefill-retrieval-only", action="store_true",

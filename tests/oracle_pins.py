@@ -343,6 +343,45 @@ def pin_backward_finite_differences(orc):
     assert np.all(ds[0, 3] == 0)
 
 
+def pin_backward_chunks_equals_full_backward(orc):
+    """gca_backward_chunks (the per-key-chunk dK, dV used for sampled checks at full size)
+    equals the full backward's dK, dV, itself pinned by finite differences, on two
+    sequences with different inputs and a retrieval table where one row retrieves a chunk
+    twice, several rows retrieve the same chunk, and some chunks are never retrieved; for
+    both next-chunk shifts.  Finite differences of the loss <dO, O> in one element of a
+    twice-retrieved chunk pin the duplicate's double contribution directly."""
+    rng = np.random.default_rng(43)
+    S, nC, k = 4, 6, 3
+    q, kk, vv = _rand_gca(rng, B=2, nQ=nC, nC=nC, chunk=S, H=2, dh=3)
+    do = rng.standard_normal(q.shape)
+    idx = np.array([[[-1, -1, -1], [0, 0, -1], [0, 1, -1], [2, 0, 1], [1, 1, 3], [0, 3, -1]],
+                    [[-1, -1, -1], [0, -1, -1], [1, 0, -1], [1, 2, 2], [3, 0, -1], [2, 2, 0]]], dtype=np.int32)
+    sc = np.where(idx >= 0, rng.standard_normal(idx.shape), -np.inf)
+    for shift in (0, 1):
+        _, dk, dv, _ = orc.gca_backward(q, kk, vv, idx, sc, do, shift=shift, chunk=S)
+        for b in range(2):
+            ok, ov = orc.gca_backward_chunks(q, kk, vv, idx, sc, do, b, range(nC), shift=shift, chunk=S)
+            for j in range(nC):
+                _close(ok[j], dk[b, j * S:(j + 1) * S], 1e-12)
+                _close(ov[j], dv[b, j * S:(j + 1) * S], 1e-12)
+        # chunks 4 and 5 are never retrieved
+        assert np.all(dk[:, 4 * S:] == 0) and np.all(dv[:, 4 * S:] == 0)
+    # The duplicate: sequence 1, row 3 holds chunk 2 twice (shift 0: query chunk 3).
+    ok, ov = orc.gca_backward_chunks(q, kk, vv, idx, sc, do, 1, [2], shift=0, chunk=S)
+    for name, t, g in (("k", kk, ok[2]), ("v", vv, ov[2])):
+        e = (1, 2 * S + 1, 1, 2)  # an element of chunk 2 of sequence 1
+
+        def loss(x, name=name, t=t, e=e):
+            t2 = t.copy()
+            t2[e] = x
+            a = (t2, vv) if name == "k" else (kk, t2)
+            o, _ = orc.gca_forward(q, a[0], a[1], idx, sc, shift=0, chunk=S)
+            return float(np.sum(do * o))
+        h = 1e-6
+        fd = (loss(t[e] + h) - loss(t[e] - h)) / (2 * h)
+        assert abs(g[e[1] - 2 * S, e[2], e[3]] - fd) < 1e-6 * max(1.0, abs(fd)), (name, g[e[1] - 2 * S, e[2], e[3]], fd)
+
+
 def pin_dscores_sum_to_zero(orc):
     """The weights are a softmax, so the score gradient sums to zero over a row."""
     rng = np.random.default_rng(41)

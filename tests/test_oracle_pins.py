@@ -71,6 +71,11 @@ MUTATIONS = {
                                 "tok = yc[:, :, 1:].reshape(B, nC * CHUNK, d)"),
     "encoder_heads_interleaved": ("for i in range(3)]  # q, k, v [B, nC, H, 65, dh]",
                                   "for i in range(3)]  # q, k, v [B, nC, H, 65, dh]\n    heads = [h.reshape(B, nC, dh, ENC_CHUNK, H).transpose(0, 1, 4, 3, 2) for h in heads]"),
+    "chunks_drop_duplicate": ("hit = [m for m in range(idx.shape[2]) if int(idx[b, r, m]) in want]",
+                              "hit = sorted({int(idx[b, r, m]): m for m in range(idx.shape[2]) if int(idx[b, r, m]) in want}.values())"),
+    "chunks_wrong_sequence": ("_, dkc, dvc, _ = gca_chunk_backward(q[b, sl]", "_, dkc, dvc, _ = gca_chunk_backward(q[0, sl]"),
+    "chunks_shift_off_by_one": ("r = c - shift\n        if r < 0:\n            continue\n        hit =",
+                                "r = c - shift - 1\n        if r < 0:\n            continue\n        hit ="),
     "swa_bwd_rowsum": ("dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True))", "dS = P * (dP - np.sum(dP, axis=1, keepdims=True))"),
 }
 
