@@ -138,6 +138,19 @@ GCA_API gca_status gca_retrieve_topk_noalloc(const void* q_lmk, int64_t q_row_st
                                      int nC, int D, int topk, int causal_offset,
                                      int use_gumbel, uint64_t seed, int group, int32_t* idx,
                                      float* scores, gca_stream_t stream);
+/* gca_retrieve_noalloc_check_error - gca_check_error() for the static array of
+ * gca_retrieve_topk_noalloc on the current device: synchronises `stream`, reads and clears
+ * the array's device error word.  Returns GCA_OK, GCA_ERR_TIMEOUT (a bounded wait ran out:
+ * the idx/scores of that call are not valid), GCA_ERR_DEVICE_INDEX or GCA_ERR_CUDA.  Each
+ * gca_retrieve_topk_noalloc call clears the word when it starts, so check after a call and
+ * before the next one.  Argument errors of a rejected call are returned by that call and
+ * leave the word untouched. */
+GCA_API gca_status gca_retrieve_noalloc_check_error(gca_stream_t stream, int* bad_value);
+/* Test hook: gca_selftest_timeout() run against the same array's error word (a wait on a
+ * barrier that nothing arrives at runs out after `spins` probes and records
+ * GCA_ERR_TIMEOUT; no fault or hang), so that a test can see the error reach
+ * gca_retrieve_noalloc_check_error(). */
+GCA_API gca_status gca_retrieve_noalloc_selftest_timeout(uint32_t spins, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * gca_forward - grouped cross-attention over the retrieved chunks.

@@ -56,6 +56,8 @@ def _load():
         "gca_retrieve_topk": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P, SZ, P]),
         "gca_retrieve_noalloc_max_scratch": (SZ, []),
         "gca_retrieve_topk_noalloc": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P]),
+        "gca_retrieve_noalloc_check_error": (I, [P, ctypes.POINTER(I)]),
+        "gca_retrieve_noalloc_selftest_timeout": (I, [ctypes.c_uint32, P]),
         "gca_forward_workspace_size": (SZ, []),
         "gca_forward": (I, [P, P, P, I64, I, I, I, I, I, I, P, P, I, I, P, P, P, SZ, P]),
         "gca_window_forward": (I, [P, P, P, I, I, I, I, I, I, P, P, I, P, SZ, P]),
@@ -90,7 +92,8 @@ def _load():
 LIB = _load()
 EXPORTS = (
     "gca_status_string", "gca_last_error_detail", "gca_retrieve_workspace_size", "gca_retrieve_topk",
-    "gca_retrieve_noalloc_max_scratch", "gca_retrieve_topk_noalloc",
+    "gca_retrieve_noalloc_max_scratch", "gca_retrieve_topk_noalloc", "gca_retrieve_noalloc_check_error",
+    "gca_retrieve_noalloc_selftest_timeout",
     "gca_forward_workspace_size", "gca_forward", "gca_window_forward", "gca_cca_forward",
     "gca_window_backward_workspace_size", "gca_window_backward",
     "gca_gather_workspace_size", "gca_gather_chunks",

@@ -175,11 +175,10 @@ extern "C" size_t gca_retrieve_workspace_size(int B, int nQ, int nC, int topk, i
   return kErrBytes + align256(p.part_bytes);
 }
 
-extern "C" gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
-                                        const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype, int B,
-                                        int nQ, int nC, int D, int topk, int causal_offset, int use_gumbel,
-                                        uint64_t seed, int group, int32_t* idx, float* scores, void* ws,
-                                        size_t ws_bytes, gca_stream_t stream) {
+gca_status gca::check_retrieve_args(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
+                                    const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype, int B, int nQ,
+                                    int nC, int D, int topk, int causal_offset, int use_gumbel, int group,
+                                    const int32_t* idx, const float* scores) {
   gca_status st = check_landmarks(q_lmk, q_row_stride, q_batch_stride, k_lmk, k_batch_stride, dtype, B, nQ,
                                   nC, D, topk);
   if (st != GCA_OK) return st;
@@ -187,6 +186,17 @@ extern "C" gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride,
   if (causal_offset < 0) return fail(GCA_ERR_INVALID_ARG, "causal_offset must be >= 0");
   if (use_gumbel && (B > 256 || nQ > (1 << 24) || nC > (1 << 24) || group < 0 || group > 255))
     return fail(GCA_ERR_INVALID_ARG, "Gumbel noise needs B <= 256, nQ, nC <= 2^24, 0 <= group < 256");
+  return GCA_OK;
+}
+
+extern "C" gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
+                                        const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype, int B,
+                                        int nQ, int nC, int D, int topk, int causal_offset, int use_gumbel,
+                                        uint64_t seed, int group, int32_t* idx, float* scores, void* ws,
+                                        size_t ws_bytes, gca_stream_t stream) {
+  gca_status st = check_retrieve_args(q_lmk, q_row_stride, q_batch_stride, k_lmk, k_batch_stride, dtype, B, nQ,
+                                      nC, D, topk, causal_offset, use_gumbel, group, idx, scores);
+  if (st != GCA_OK) return st;
   if ((st = check_ws(ws, ws_bytes, gca_retrieve_workspace_size(B, nQ, nC, topk, causal_offset))) != GCA_OK)
     return st;
   RetrievePlan p = retrieve_plan(B, nQ, nC, topk, causal_offset);

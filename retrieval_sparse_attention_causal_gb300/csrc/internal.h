@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/gca.h"
+
 namespace gca {
 
 struct ErrWord;
@@ -39,6 +41,13 @@ cudaError_t make_lmk_tmap(CUtensorMap* out, const void* base, int64_t D, int64_t
                           int64_t row_stride, int64_t batch_stride, int box_rows);
 // The same matrix as a TMA store target: 32 x 32 boxes, 64-byte swizzle (tmap.cu).
 cudaError_t make_store_tmap(CUtensorMap* out, const void* base, int64_t cols, int64_t rows);
+
+// Argument checks of gca_retrieve_topk other than the workspace (api.cu); records the
+// error detail and returns the status of the first problem, or GCA_OK.
+gca_status check_retrieve_args(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride, const void* k_lmk,
+                               int64_t k_batch_stride, gca_dtype dtype, int B, int nQ, int nC, int D, int topk,
+                               int causal_offset, int use_gumbel, int group, const int32_t* idx,
+                               const float* scores);
 
 // ---- retrieval (retrieve.cu)
 struct RetrieveArgs {

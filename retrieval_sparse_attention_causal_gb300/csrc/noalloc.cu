@@ -60,19 +60,21 @@ extern "C" gca_status gca_retrieve_topk_noalloc(const void* q_lmk, int64_t q_row
                                                 int nC, int D, int topk, int causal_offset, int use_gumbel,
                                                 uint64_t seed, int group, int32_t* idx, float* scores,
                                                 gca_stream_t stream) {
+  // Every argument is checked before anything is queued on the stream, so a rejected call
+  // leaves the array (and an error word that a previous call set) as it was.
+  gca_status st = check_retrieve_args(q_lmk, q_row_stride, q_batch_stride, k_lmk, k_batch_stride, dtype, B, nQ,
+                                      nC, D, topk, causal_offset, use_gumbel, group, idx, scores);
+  if (st != GCA_OK) return st;
   // Size the scratch that the workspace-taking entry point would need and refuse a
-  // problem that does not fit the fixed array (other argument errors are reported by
-  // gca_retrieve_topk below).
-  if (B >= 1 && nQ >= 1 && nC >= 1 && topk >= 1 && topk <= GCA_MAX_TOPK && causal_offset >= 0) {
-    const size_t need = gca_retrieve_workspace_size(B, nQ, nC, topk, causal_offset);
-    if (need > kNoAllocBytes) {
-      char msg[256];
-      snprintf(msg, sizeof msg,
-               "gca_retrieve_topk_noalloc: this problem needs %zu bytes of candidate scratch, more than the "
-               "fixed %zu; use gca_retrieve_topk with a workspace",
-               need - kErrBytes, kNoAllocPartBytes);
-      return set_error(GCA_ERR_UNSUPPORTED, msg);
-    }
+  // problem that does not fit the fixed array.
+  const size_t need = gca_retrieve_workspace_size(B, nQ, nC, topk, causal_offset);
+  if (need > kNoAllocBytes) {
+    char msg[256];
+    snprintf(msg, sizeof msg,
+             "gca_retrieve_topk_noalloc: this problem needs %zu bytes of candidate scratch, more than the "
+             "fixed %zu; use gca_retrieve_topk with a workspace",
+             need - kErrBytes, kNoAllocPartBytes);
+    return set_error(GCA_ERR_UNSUPPORTED, msg);
   }
   void* ws = nullptr;
   cudaError_t e = scratch_ptr(&ws);
@@ -83,4 +85,18 @@ extern "C" gca_status gca_retrieve_topk_noalloc(const void* q_lmk, int64_t q_row
   if (e != cudaSuccess) return set_error(GCA_ERR_CUDA, cudaGetErrorString(e));
   return gca_retrieve_topk(q_lmk, q_row_stride, q_batch_stride, k_lmk, k_batch_stride, dtype, B, nQ, nC, D,
                            topk, causal_offset, use_gumbel, seed, group, idx, scores, ws, kNoAllocBytes, stream);
+}
+
+extern "C" gca_status gca_retrieve_noalloc_check_error(gca_stream_t stream, int* bad_value) {
+  void* ws = nullptr;
+  cudaError_t e = scratch_ptr(&ws);
+  if (e != cudaSuccess) return set_error(GCA_ERR_CUDA, cudaGetErrorString(e));
+  return gca_check_error(ws, stream, bad_value);
+}
+
+extern "C" gca_status gca_retrieve_noalloc_selftest_timeout(uint32_t spins, gca_stream_t stream) {
+  void* ws = nullptr;
+  cudaError_t e = scratch_ptr(&ws);
+  if (e != cudaSuccess) return set_error(GCA_ERR_CUDA, cudaGetErrorString(e));
+  return gca_selftest_timeout(ws, kErrBytes, spins, stream);
 }

@@ -58,6 +58,11 @@ __device__ __forceinline__ void write_row(const RetrieveArgs& a, int b, int i, c
   }
 }
 
+// Partial lists: every producer (write_part here, put_list in retrieve_tc.cu) writes
+// each (row, split) list in the order of better(): best first, ties by the lower index,
+// empty entries (j = 0x7fffffff) only at the tail.  retrieve_merge_heads_kernel relies on
+// it: it only ever looks at the head of each list.  The other merges re-insert every
+// entry and do not need it.
 __device__ __forceinline__ void write_part(const RetrieveArgs& a, int nsplit, int b, int i,
                                            int split, const Cand* sel) {
   Cand* p = reinterpret_cast<Cand*>(a.part) +
@@ -629,14 +634,23 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
   const long long rows = (long long)a.B * a.nQ;
   return with_kc(a.topk, [&](auto kc) -> cudaError_t {
     constexpr int KC = decltype(kc)::value;
-    launch_begin("retrieve_merge", s);
-    if (rows >= kWarpMergeRows && nsplit <= 32 && (long long)nsplit * a.topk <= kHeadsMax)
+    // Each variant has its own launch name, so that the profile table and the tests can
+    // tell which one ran.
+    const char* name;
+    if (rows >= kWarpMergeRows && nsplit <= 32 && (long long)nsplit * a.topk <= kHeadsMax) {
+      name = "retrieve_merge_heads";
+      launch_begin(name, s);
       retrieve_merge_heads_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, nsplit, (int)rows);
-    else if (rows >= kWarpMergeRows)  // a warp per row, lists into registers
+    } else if (rows >= kWarpMergeRows) {  // a warp per row, lists into registers
+      name = "retrieve_merge_warp";
+      launch_begin(name, s);
       retrieve_merge_warp_kernel<KC><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a, nsplit, (int)rows);
-    else  // a block per row: few rows, long lists (decode)
+    } else {  // a block per row: few rows, long lists (decode)
+      name = "retrieve_merge_block";
+      launch_begin(name, s);
       retrieve_merge_kernel<KC><<<dim3(a.nQ, a.B), 128, 0, s>>>(a, nsplit);
-    return launch_end("retrieve_merge", s);
+    }
+    return launch_end(name, s);
   });
 }
 

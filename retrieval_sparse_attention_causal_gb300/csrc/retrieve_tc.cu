@@ -90,6 +90,9 @@ __device__ __forceinline__ void insert_sorted(T (&L)[KC], const T& c) {
   if (!in[0]) L[0] = c;
 }
 
+// Writes one (row, segment, half) list to the partial buffer.  The register list is kept
+// sorted by better() with its empty entries at the tail, and the merge of the heads of the
+// lists (retrieve.cu) relies on that order.
 template <class T, int KC>
 __device__ __forceinline__ void put_list(const RetrieveArgs& a, int nsplit, int b, int i, int split,
                                          const T (&L)[KC]) {

@@ -231,3 +231,16 @@ def test_workload_presets():
     assert w.PREFILL_1M.L == 1 << 20 and w.DECODE_16M.L == 1 << 24 and w.DECODE_16M.nQ == 1
     assert w.TINY_F32.dtype == "f32" and not w.TINY_F32.gumbel
     assert len({x.name for x in w.ALL}) == len(w.ALL)
+
+
+def test_noalloc_rejects_bad_arguments_on_the_host(gca):
+    """The noalloc entry point checks its arguments before any CUDA call (so also here,
+    without a GPU)."""
+    def call(q=FAKE, topk=8, D=768, off=0, group=0):
+        return gca.LIB.gca_retrieve_topk_noalloc(q, 768, 256 * 768, FAKE, 256 * 768, gca.GCA_BF16, 4, 256, 256, D,
+                                                 topk, off, 1, ctypes.c_uint64(0), group, FAKE, FAKE, None)
+    assert call(q=0) == gca.GCA_ERR_INVALID_ARG
+    assert call(topk=17) == gca.GCA_ERR_UNSUPPORTED
+    assert call(D=700) == gca.GCA_ERR_UNSUPPORTED
+    assert call(off=-1) == gca.GCA_ERR_INVALID_ARG
+    assert call(group=300) == gca.GCA_ERR_INVALID_ARG

@@ -164,9 +164,19 @@ def test_large_row_blocks_strided_queries_and_shared_keys():
     assert nd > 0.5 * B * nQ  # most rows decidable: the test is not vacuous
 
 
-@pytest.mark.parametrize("nQ", [255, 256])
-def test_merge_block_and_warp_paths(nQ):
+@pytest.mark.parametrize("nQ,off,K,merge", [(255, 0, 8, "retrieve_merge_block"), (256, 0, 8, "retrieve_merge_heads"),
+                                             (256, 4096, 16, "retrieve_merge_warp"),
+                                             (256, 4096, 8, "retrieve_merge_warp")])
+def test_merge_block_and_warp_paths(nQ, off, K, merge):
     """Below 256 rows the partial lists of a row are merged by a block, from 256 rows on by
-    a warp: both against the oracle at the boundary (several candidate splits per row)."""
-    _, _, _, nd, _ = run_case(1, nQ, nQ, 256, 8, "bf16", off=0, gumbel=True, seed=9)
+    a warp: by walking the heads of the row's sorted lists when there are at most 32 lists
+    of at most 128 entries in all, otherwise by re-inserting every entry (here 68 lists per
+    row: 4352 candidates in 64-candidate splits).  Each variant, identified by its launch
+    name, against the oracle."""
+    g = _gca()
+    g.profile_begin()
+    _, _, _, nd, _ = run_case(1, nQ, nQ + off, 256, K, "bf16", off=off, gumbel=True, seed=9)
+    prof = g.profile_end()
     assert nd > 0.5 * nQ
+    assert merge in prof, sorted(prof)
+    assert not any(n.startswith("retrieve_merge") and n != merge for n in prof), sorted(prof)

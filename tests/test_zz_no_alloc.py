@@ -76,3 +76,37 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
         8, 0, 0, ctypes.c_uint64(0), 0, ctypes.c_void_p(idx.data_ptr()), ctypes.c_void_p(sc.data_ptr()), None)
     assert st == g.GCA_ERR_UNSUPPORTED
     assert b"scratch" in g.LIB.gca_last_error_detail()
+
+
+def test_noalloc_device_errors_reach_the_caller():
+    """A device-side error of a noalloc call lands in the static array's error word, and
+    gca_retrieve_noalloc_check_error reads it back and clears it.  The error is made
+    without a fault: a bounded wait on a barrier that nothing arrives at runs out against
+    the same error word (the library's test hook).  A call rejected for its arguments
+    queues nothing, so it leaves a pending error in place."""
+    g = _g()
+    from retrieval_sparse_attention_causal_gb300 import synth
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    bad = ctypes.c_int(0)
+    lm = synth.landmark_inputs(7, 2, 1, 5000, 256, "bf16")
+    q, k = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
+    idx, sc = _noalloc(g, q, k, 8, 5000, False, 0)
+    assert g.LIB.gca_retrieve_noalloc_check_error(stream, ctypes.byref(bad)) == g.GCA_OK
+    ref_idx, _ = g.retrieve_topk(q, k, 8, 5000, False, 0)
+    assert torch.equal(idx, ref_idx)
+
+    assert g.LIB.gca_retrieve_noalloc_selftest_timeout(4096, stream) == g.GCA_OK
+    # a call with bad arguments is rejected on the host and must not clear the word
+    st = g.LIB.gca_retrieve_topk_noalloc(
+        ctypes.c_void_p(q.data_ptr()), q.stride(1), q.stride(0), ctypes.c_void_p(k.data_ptr()), k.stride(0),
+        g.GCA_BF16, 2, 1, 5000, 256, 99, 5000, 0, ctypes.c_uint64(0), 0, ctypes.c_void_p(idx.data_ptr()),
+        ctypes.c_void_p(sc.data_ptr()), stream)
+    assert st == g.GCA_ERR_UNSUPPORTED
+    assert g.LIB.gca_retrieve_noalloc_check_error(stream, ctypes.byref(bad)) == g.GCA_ERR_TIMEOUT
+    assert b"site 30" in g.LIB.gca_last_error_detail()
+    # read once, then clear
+    assert g.LIB.gca_retrieve_noalloc_check_error(stream, ctypes.byref(bad)) == g.GCA_OK
+    # and the array still serves correct calls
+    idx2, _ = _noalloc(g, q, k, 8, 5000, False, 0)
+    assert g.LIB.gca_retrieve_noalloc_check_error(stream, ctypes.byref(bad)) == g.GCA_OK
+    assert torch.equal(idx2, ref_idx)
