@@ -59,7 +59,7 @@ def _synth():
 
 
 _W = _workloads()
-TRAIN_128M, DECODE_16M, PREFILL_1M = _W.TRAIN_128M, _W.DECODE_16M, _W.PREFILL_1M
+TRAIN_128M, DECODE_16M, PREFILL_1M, TRAIN_350M = _W.TRAIN_128M, _W.DECODE_16M, _W.PREFILL_1M, _W.TRAIN_350M_G2
 
 B, NC, H, DH, D, K = TRAIN_128M.B, TRAIN_128M.n_chunks, TRAIN_128M.H, TRAIN_128M.dh, TRAIN_128M.D, TRAIN_128M.topk
 L = TRAIN_128M.L
@@ -311,6 +311,10 @@ def gpu_arm(args):
                 "peak_source": f"{src} bf16 dense (burst)", "flops_per_launch": dom_flops}
     step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
 
+    # The 350M-model step: two retrieval groups, the second group's query landmarks read
+    # out of the first group's output.
+    t350 = None if args.no_350m else train_350m_leg(args, torch, gca, synth, seed, timed, pk, src, clk_cls=ClockSampler)
+
     # The rest of the attention block at the same shape: sliding-window self-attention
     # (W = 512) and, as the ablation, chunked cross-attention over the same retrieval.
     blk = None if args.no_block else block_attn_leg(args, torch, gca, q, k, v, out, timed, pk)
@@ -347,6 +351,8 @@ def gpu_arm(args):
             enc["cpu_baseline"] = side["encoder"]
         if pre is not None:
             pre["cpu_baseline"] = side["prefill"]
+        if t350 is not None:
+            t350["cpu_baseline"] = cpu_baseline_350m(args.seed)
 
     if rank == 0:
         line = {
@@ -361,11 +367,17 @@ def gpu_arm(args):
                                               if clk.summary().get("sm_mhz") else None)},
             "roofline": roof, "gpu_launches": int(launches), "clocks": clk.summary(),
             "kernels": {n: round(x["avg_ms"], 5) for n, x in kern.items()},
-            "e2e": e2e, "decode": dec, "block_attention": blk, "encoder": enc, "prefill_retrieval": pre,
-            "cpu_baseline": cpu,
+            "e2e": e2e, "decode": dec, "train_350m": t350, "block_attention": blk, "encoder": enc,
+            "prefill_retrieval": pre, "cpu_baseline": cpu,
         }
         # Compact copies of the secondary headlines, last on the line so that a reader of
         # the line's tail sees them.
+        if t350 is not None:
+            line["train_350m_headline"] = {
+                "metric": "GCA fwd+bwd tokens/s, 350M shape, two groups", "tokens_per_s": t350["tokens_per_s"],
+                "ms_per_step": t350["ms_per_step"], "gca_tflops_algorithmic": t350["tflops_algorithmic"],
+                "gca_frac_of_bf16_peak": t350["frac_of_bf16_peak"],
+                "cpu_baseline_tokens_per_s": (t350.get("cpu_baseline") or {}).get("value")}
         if dec is not None:
             line["decode_headline"] = {
                 "metric": "landmark top-k GB/s at 16M ctx", "B": dec["batch"], "GBps": dec["value"],
@@ -607,6 +619,86 @@ def decode_leg(args, torch, gca, synth, seed, pk, src, barrier, world):
                          "bytes_per_launch": nbytes},
             "kernels": {n: round(t / c, 5) for n, (c, t) in prof.items()}, "batch_sweep": sweep, "batch1": batch1,
             "offload": offload}
+
+
+def train_350m_leg(args, torch, gca, synth, seed, timed, pk, src, clk_cls):
+    """The 350M-model training step: B = 8, L = 16384 (256 chunks), H = 16 x 64, D = 1024,
+    k = 8 per group, Gumbel noise, two retrieval groups sharing K/V.  Per step: group 1's
+    retrieval and forward; group 2's retrieval over landmarks read straight out of group 1's
+    output at every chunk's last token (a strided view, no copy) and its forward; group 2's
+    backward (dQ2, dK, dV, dscores); its landmark gradient added into group 1's output
+    gradient at those tokens; group 1's backward accumulating into dK, dV; both groups'
+    landmark gradients.  Group 1's output gradient buffer holds the upper layers' dO1; its
+    chunk-last rows are restored from a saved copy before each step (4 MB), so that every
+    step adds group 2's landmark gradient to the same dO1."""
+    wl = TRAIN_350M
+    b_, nc, h, dh, d, k = wl.B, wl.n_chunks, wl.H, wl.dh, wl.D, wl.topk
+    bf = torch.bfloat16
+    shape = (b_, wl.L, h, dh)
+    q1, q2, kk, vv, do1, do2 = (synth.device_normal(seed, st, shape, wl.qkv_std, bf)
+                                for st in (synth.S_Q, synth.S_Q2, synth.S_K, synth.S_V, synth.S_DO, synth.S_DO2))
+    q1l, k1l, k2l = (synth.device_normal(seed, st, (b_, nc, d), 1.0, bf) for st in (synth.S_QL, synth.S_KL,
+                                                                                     synth.S_KL2))
+    from retrieval_sparse_attention_causal_gb300.pipeline import landmark_view
+    last = landmark_view(do1)
+    last_saved = last.clone()
+    ws = gca.Workspace()
+    f32, i32 = torch.float32, torch.int32
+    o = {n: torch.empty((b_, nc, k), dtype=i32 if n.startswith("idx") else f32, device="cuda")
+         for n in ("idx1", "s1", "idx2", "s2", "ds1", "ds2")}
+    o.update({n: torch.empty_like(q1) for n in ("o1", "o2", "dq1", "dq2", "dk", "dv")})
+    o.update({n: torch.empty((b_, nc, h, k, 64), dtype=f32, device="cuda") for n in ("lse1", "lse2")})
+    o.update({n: torch.empty((b_, nc, d), dtype=f32, device="cuda") for n in ("dq1l", "dk1l", "dk2l")})
+    q2l = landmark_view(o["o1"])
+
+    def step(i):
+        last.copy_(last_saved)
+        gca.retrieve_topk(q1l, k1l, k, 0, True, seed + i, 0, ws=ws, idx=o["idx1"], scores=o["s1"])
+        gca.gca_forward(q1, kk, vv, o["idx1"], o["s1"], shift=1, ws=ws, out=o["o1"], lse=o["lse1"])
+        gca.retrieve_topk(q2l, k2l, k, 0, True, seed + i, 1, ws=ws, idx=o["idx2"], scores=o["s2"])
+        gca.gca_forward(q2, kk, vv, o["idx2"], o["s2"], shift=1, ws=ws, out=o["o2"], lse=o["lse2"])
+        gca.gca_backward(q2, kk, vv, o["idx2"], o["s2"], do2, o["lse2"], shift=1, ws=ws, dq=o["dq2"], dk=o["dk"],
+                         dv=o["dv"], dscores=o["ds2"])
+        gca.scores_backward(q2l, k2l, o["idx2"], o["ds2"], ws=ws, dq_out=last, accumulate=True, dk_lmk=o["dk2l"])
+        gca.gca_backward(q1, kk, vv, o["idx1"], o["s1"], do1, o["lse1"], shift=1, ws=ws, dq=o["dq1"], dk=o["dk"],
+                         dv=o["dv"], dscores=o["ds1"], accumulate_dkv=True)
+        gca.scores_backward(q1l, k1l, o["idx1"], o["ds1"], ws=ws, dq_out=o["dq1l"], dk_lmk=o["dk1l"])
+
+    for i in range(args.warmup):
+        step(i)
+    ws.check()
+    n0 = gca.launch_count()
+    with clk_cls(torch) as clk:
+        reps = timed_repeats(timed, step, args.steps, args.min_seconds)
+    launches = (gca.launch_count() - n0) // len(reps)
+    ms = statistics.median(reps) / args.steps
+    gca.profile_begin()
+    timed(step, args.steps)
+    prof = gca.profile_end()
+    fl = algorithmic_flops(b_, nc, h, dh, k)  # one group
+    per_group = {"gca_fwd": fl["gca_fwd"], "gca_bwd_q": fl["gca_bwd_q"], "gca_bwd_kv": fl["gca_bwd_kv"]}
+    kern = {}
+    for n, (c, t) in prof.items():
+        row = {"launches_per_step": c // args.steps, "avg_ms": round(t / c, 5)}
+        if n in per_group:
+            tf = per_group[n] / (t / c / 1e3) / 1e12
+            row["tflops_algorithmic"] = round(tf, 1)
+            row["frac_of_bf16_peak"] = round(tf / pk["bf16_tflops"], 4)
+        kern[n] = row
+    step_fl = 2 * fl["step"]
+    tf_step = step_fl / (ms / 1e3) / 1e12
+    tokens = b_ * wl.L
+    out = {"workload": f"{wl.name}: B={b_}, L={wl.L} ({nc} chunks), H={h} x dh={dh}, landmark dim {d}, top-k {k} "
+                       f"per group, Gumbel noise",
+           "tokens_per_s": round(tokens / (ms / 1e3), 1), "ms_per_step": round(ms, 4), "steps": args.steps,
+           "timed_repeats": len(reps), "gpu_launches": int(launches), "clocks": clk.summary(),
+           "flops_algorithmic_per_step": step_fl, "tflops_algorithmic": round(tf_step, 1),
+           "frac_of_bf16_peak": round(tf_step / pk["bf16_tflops"], 4),
+           "peak_source": f"{src} bf16 dense (burst)", "kernels": kern,
+           "l2": "inputs larger than L2 (Q1, Q2, K, V, dO1, dO2: 6 x 268 MB per step)",
+           "not_ours": "one 4 MB torch copy per step restores dO1's chunk-last rows"}
+    del q1, q2, kk, vv, do1, do2, o
+    return out
 
 
 def block_attn_leg(args, torch, gca, q, k, v, out, timed, pk):
@@ -1021,6 +1113,50 @@ def next_rows_cpu(seed):
     return out
 
 
+def cpu_baseline_350m(seed, budget_s=10.0):
+    """The oracle on one sequence of the 350M-model two-group step, for query chunks
+    1..n of both groups (group 2's landmark rows from the oracle's own group-1 output at
+    those chunks), until the budget runs out.  Returns a cpu_baseline object in tokens/s
+    (a token counted once for both groups, as on the GPU)."""
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    import oracle.gca_oracle as orc
+    synth = _synth()
+    wl = TRAIN_350M
+    nc, h, dh, d, k = wl.n_chunks, wl.H, wl.dh, wl.D, wl.topk
+    x = synth.gca_inputs(seed, 1, nc, nc, h, dh, wl.qkv_std, "bf16")
+    q2 = synth.normal(seed, synth.S_Q2, x["q"].shape, wl.qkv_std, "bf16")
+    do2 = synth.normal(seed, synth.S_DO2, x["q"].shape, wl.qkv_std, "bf16")
+    lm = synth.landmark_inputs(seed, 1, nc, nc, d, "bf16")
+    k2l = synth.normal(seed, synth.S_KL2, (1, nc, d), 1.0, "bf16")
+    r0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    done = 0
+    q2l = np.zeros((1, nc, d))
+    for c in range(1, nc):
+        sl = slice(c * 64, (c + 1) * 64)
+        i1, s1, _ = orc.retrieve_topk(lm["q_lmk"], lm["k_lmk"], k, 0, True, seed, 0, rows=[(0, c - 1)])
+        o1, _, _ = orc.gca_chunk_forward(x["q"][0, sl], x["k"][0], x["v"][0], i1[0, c - 1], s1[0, c - 1])
+        q2l[0, c] = synth.quantize(o1[63].reshape(d), "bf16")
+        i2, s2, _ = orc.retrieve_topk(q2l, k2l, k, 0, True, seed, 1, rows=[(0, c - 1)])
+        orc.gca_chunk_forward(q2[0, sl], x["k"][0], x["v"][0], i2[0, c - 1], s2[0, c - 1])
+        _, _, _, ds2 = orc.gca_chunk_backward(q2[0, sl], x["k"][0], x["v"][0], i2[0, c - 1], s2[0, c - 1],
+                                              do2[0, sl])
+        _, _, _, ds1 = orc.gca_chunk_backward(x["q"][0, sl], x["k"][0], x["v"][0], i1[0, c - 1], s1[0, c - 1],
+                                              x["do"][0, sl])
+        orc.scores_backward(q2l[:, c - 1:c], k2l, i2[:, c - 1:c], ds2[None, None])
+        orc.scores_backward(lm["q_lmk"][:, c - 1:c], lm["k_lmk"], i1[:, c - 1:c], ds1[None, None])
+        done = c
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    r1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu_s = (r1.ru_utime + r1.ru_stime) - (r0.ru_utime + r0.ru_stime)
+    return {"value": round(done * 64 / dt, 2), "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "threads_busy": round(cpu_s / dt, 2), "kind": "oracle",
+            "sample": f"one sequence of the 350M two-group step, query chunks 1..{done} ({done * 64} tokens) of both "
+                      f"groups: retrieval rows, forward, backward, landmark gradients, float64 numpy; {dt:.1f} s wall"}
+
+
 def cpu_baseline(seed, budget_s=20.0):
     tok, dt, cpu_s = cpu_sample(seed, NC - 1, budget_s)
     return {"value": round(tok / dt, 2), "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
@@ -1071,6 +1207,7 @@ def main():
     ap.add_argument("--no-encoder", action="store_true", help="skip the chunk / landmark encoder leg")
     ap.add_argument("--no-prefill", action="store_true", help="skip the 1M-token prefill retrieval leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-350m", action="store_true", help="skip the 350M-model two-group training step")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--min-seconds", type=float, default=1.0,
