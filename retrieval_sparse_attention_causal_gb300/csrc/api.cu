@@ -450,7 +450,7 @@ extern "C" gca_status gca_gather_chunks(const void* k_src, const void* v_src, in
 // ==================================================================== GCA backward
 namespace {
 struct BwdLayout {
-  size_t D, dwp, off, ent, cur, wrow, total;
+  size_t D, dwp, off, ent, cur, wrow, ctr, total;
 };
 BwdLayout bwd_layout(int B, int nQ, int nC, int H, int topk) {
   BwdLayout L{};
@@ -461,6 +461,7 @@ BwdLayout bwd_layout(int B, int nQ, int nC, int H, int topk) {
   L.ent = p; p += align256((size_t)B * nQ * topk * 4);
   L.cur = p; p += align256((size_t)B * nC * 4);
   L.wrow = p; p += align256((size_t)B * nQ * topk * 4);
+  L.ctr = p; p += 256;
   L.total = p;
   return L;
 }
@@ -497,6 +498,7 @@ extern "C" gca_status gca_backward(const void* q, const void* k, const void* v, 
   a.csr_ent = reinterpret_cast<int32_t*>(w + L.ent);
   a.csr_cur = reinterpret_cast<int32_t*>(w + L.cur);
   a.wrow = reinterpret_cast<float*>(w + L.wrow);
+  a.kv_ctr = reinterpret_cast<int32_t*>(w + L.ctr);
   cudaError_t e = launch_backward(a, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gca_backward launch");
   return GCA_OK;

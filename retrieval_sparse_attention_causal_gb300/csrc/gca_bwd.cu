@@ -584,6 +584,9 @@ __global__ void __launch_bounds__(256) gca_dscores_kernel(BwdArgs a) {
   const int r = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = r + a.shift;
   float* out = a.dscores + ((int64_t)b * a.nQ + r) * a.topk;
+  // The persistent key-side kernel that runs after this one claims its tiles from this
+  // counter.
+  if (r == 0 && b == 0 && tid == 0 && a.kv_ctr) *a.kv_ctr = 0;
   if (c >= a.nQ) {
     if (tid < a.topk) out[tid] = 0.f;
     return;

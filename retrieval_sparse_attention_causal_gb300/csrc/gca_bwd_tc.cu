@@ -96,6 +96,61 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, in
   return false;
 }
 
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// One probe of phase `parity` of `bar` that lets the hardware park the thread until the
+// phase completes, for at most `hint_ns` (so that a waiting warp takes no issue slots
+// from the warps that work).
+__device__ __forceinline__ bool mbar_try_park(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(tc::su32(bar)), "r"(parity), "r"(hint_ns));
+  return done != 0;
+}
+
+// Bounded wait with parking, for kernels with many waiting warps: gives up once the CTA's
+// abort flag is raised, or after kParkLimitNs of global time, recording `site` (with CTA,
+// tile, slot) and raising the flag.
+constexpr uint64_t kParkLimitNs = 2000000000ull;
+__device__ __forceinline__ bool park_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag, ErrWord* err,
+                                              int site, int tile, int slot) {
+  if (tc::mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    if (mbar_try_park(bar, parity, 20000)) return true;
+    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+    if (global_ns() - t0 > kParkLimitNs) break;
+  }
+  flag_timeout(err, site, blockIdx.x, tile, slot);
+  atomicExch(abort_flag, 1);
+  return false;
+}
+
+// The same bounded wait without parking (for the warp whose wake-up latency is on the
+// critical path).
+__device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag, ErrWord* err,
+                                              int site, int tile, int slot) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (tc::mbar_try(bar, parity)) return true;
+    if ((it & 15) == 15) {
+      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+      if (global_ns() - t0 > kParkLimitNs) break;
+    }
+  }
+  flag_timeout(err, site, blockIdx.x, tile, slot);
+  atomicExch(abort_flag, 1);
+  return false;
+}
+
 __global__ void __launch_bounds__(kQThreads, 2)
 gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -454,238 +509,515 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
 }
 
 // ================================================================== key side
+// Persistent, two CTAs per SM.  The tiles (key chunk j, head h, sequence b) are claimed
+// from a counter in the workspace (zeroed by the dscores kernel that runs before), in
+// blocks of a few heads of one sequence whose Q, dO, K and V fit in L2 together (8 MB per
+// head at L = 16K; a.kv_hb heads per block), chunk-major inside a block: the CTAs in
+// flight share those operands in L2, and inside a block the chunks with the most
+// consumers (the early ones) start first, so the last tiles of the kernel are light.  A
+// tile's consumers are taken in CSR (entry) order, so every dK, dV sum runs in a fixed
+// order: the result does not depend on which CTA claimed the tile.
+//
+// The pipe takes an M = 64 product only about as fast as it runs it, and one issuing warp
+// with its own waits keeps it busy only part of the time; two CTAs per SM give it two
+// issuers whose waits overlap each other's products.
+//
+// Roles (11 warps):
+//   * warp 10 (metadata): claims tiles two at a time, writes the zero gradients of the
+//     chunks nobody retrieved, and for the others loads the consumer table (query chunk,
+//     slot and fusion weight of each consumer, all lanes at once) into a ring of metadata
+//     records a few tiles ahead of the producer;
+//   * warp 9 (producer, lane 0): streams the tiles: K and V of each tile into one of two
+//     buffers, and per consumer Q, dO, its LSE row and its D row into a ring of stages,
+//     with a record (fusion weight, tile, first / last flags, buffer indices);
+//   * warp 8 (MMA): per consumer x, S^T = K Q^T and dPo^T = V dO^T into TMEM (each with
+//     its own commit); dV += (w P^T) dO as soon as the element warps have stored w P^T,
+//     dK += dS^T Q once dS^T is in, then the next consumer's S^T, dPo^T over the same
+//     columns (the tensor pipe runs this warp's products in issue order).  The barriers of the next batch
+//     are tested (test_wait, which does not block) and the records read before the
+//     current batch is issued, and looked at after it;
+//   * warps 0-7 (element): P^T = exp(S^T - LSE), dS^T = w P^T (dPo^T - D) / sqrt(dh);
+//     each warp stores its bf16 operands over the TMEM columns it has itself read (no
+//     cross-warp barrier).  After the consumer that follows a tile's last one they read
+//     the tile's dK and dV (each warp its 16 rows and 32 columns), release the
+//     accumulators and write the rows out as bf16 (adding to dK, dV when accumulating),
+//     straight from registers.
+// TMEM (256 columns): S^T 0-63, dPo^T 64-127, dV 128-191, dK 192-255.
+//
+// Every wait is bounded: one that runs out records (site, CTA, tile, consumer) and raises
+// a CTA-wide abort flag; the roles stop, the MMA warp drains its products and the producer
+// its copies, and the CTA exits.
 constexpr int kKVStages = 4;
-constexpr int kKVStageBytes = 2 * TILE + 1024;  // Q, dO tiles + LSE and D rows (1 KB keeps tiles aligned)
-constexpr int kKVSmem = TILE * 2 + kKVStages * kKVStageBytes + 1024;  // K, V, ring
-constexpr int kConsTab = 256;
+constexpr int kKVStageBytes = 2 * TILE + 1024;  // Q, dO; LSE row, D row, consumer record
+constexpr int kKVMma = kEW;                      // 8
+constexpr int kKVProd = kKVMma + 1;              // 9
+constexpr int kKVMetaW = kKVProd + 1;            // 10
+constexpr int kKVThreads = 32 * (kKVMetaW + 1);  // 352
+constexpr int kKVMetaRecs = 4, kKVMetaCons = 64, kKVBatch = 2;
+constexpr int kKVSmem = 2 * 2 * TILE + kKVStages * kKVStageBytes + 1024;  // K/V x 2, ring
 
-__global__ void __launch_bounds__(kThreads, 2)
+enum { kRecFirst = 1, kRecLast = 2, kRecEnd = 4 };
+struct KVConsRec {
+  float w;
+  int flags;
+  int kb;  // K/V buffer of the consumer's tile
+  int tc;  // ordinal of the tile among this CTA's tiles with consumers
+  int j, h, b;
+};
+// A tile's consumer table: query chunk c and slot m packed as (c << 4) | m, and the fusion
+// weight, for its first kKVMetaCons consumers (the producer reads any further ones from
+// the CSR itself).
+struct KVMeta {
+  int j, h, b, ncons, e0, end;
+  int cm[kKVMetaCons];
+  float w[kKVMetaCons];
+};
+
+// Tile t of the key side: blocks of a.kv_hb heads of one sequence (the last block of a
+// sequence may have fewer), chunk-major inside a block.
+__device__ __forceinline__ void kv_tile(const BwdArgs& a, int t, int& j, int& h, int& b) {
+  const int per_seq = a.H * a.nC;
+  b = t / per_seq;
+  const int rem = t - b * per_seq;
+  const int hb0 = rem / (a.kv_hb * a.nC) * a.kv_hb;
+  const int hbn = min(a.kv_hb, a.H - hb0);
+  const int r2 = rem - hb0 * a.nC;
+  j = r2 / hbn;
+  h = hb0 + r2 % hbn;
+}
+
+__global__ void __launch_bounds__(kKVThreads, 2)
 gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
-  constexpr int NST = kKVStages, NT = kThreads;
+  constexpr int NST = kKVStages, MR = kKVMetaRecs, MC = kKVMetaCons, NB = kKVBatch;
   constexpr uint32_t kIdKm = tc::idesc_bf16(64, 64, false);
   constexpr uint32_t kIdMn = tc::idesc_bf16(64, 64, true);
   extern __shared__ __align__(1024) unsigned char dsm[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
-  unsigned char* Ks = sm;
-  unsigned char* Vs = sm + TILE;
-  unsigned char* ring = sm + 2 * TILE;  // stage st at ring + st * kKVStageBytes: Q, dO, lse[64], D[64]
-  __shared__ float w_st[NST];
-  __shared__ float wtab[kConsTab];  // weight of each consumer (first kConsTab consumers)
-  __shared__ int etab[kConsTab];    // its (row, slot) entry
+  unsigned char* kvbuf = sm;            // buffer kb: K at kvbuf + 2 kb TILE, V after it
+  unsigned char* ring = sm + 4 * TILE;  // stage st: Q, dO, lse[64], D[64], record
+  __shared__ KVMeta meta[MR];
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t bar_k, bar_c[NST], bar_s, bar_o;
-  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  __shared__ int abort_s;
+  __shared__ __align__(8) uint64_t bar_c[NST], ring_empty[NST], bar_kv[2], kv_empty[2], bar_s1, bar_s2, op_v, op_k,
+      acc_full, acc_empty, meta_full[MR], meta_empty[MR], drain;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ts = (int64_t)a.H * DH;
-  const int64_t ktok0 = ((int64_t)b * a.nC * 64 + (int64_t)j * 64) * ts + h * DH;
-  const int e0 = a.csr_off[(int64_t)b * (a.nC + 1) + j];
-  const int e1 = a.csr_off[(int64_t)b * (a.nC + 1) + j + 1];
-  const int32_t* ent = a.csr_ent + (int64_t)b * a.nQ * a.topk;
-  const float* wrow = a.wrow + (int64_t)b * a.nQ * a.topk;
-  bf16* dkg = reinterpret_cast<bf16*>(a.dk) + ktok0;
-  bf16* dvg = reinterpret_cast<bf16*>(a.dv) + ktok0;
-  const int ncons = e1 - e0;
-  if (ncons == 0) {
-    if (!a.acc_dkv) {
-      for (int u = tid; u < 64 * UPR; u += NT) {
-        const int row = u / UPR, w = u % UPR;
-        *reinterpret_cast<uint4*>(dkg + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(dvg + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
-      }
+  const int ntiles = a.nC * a.H * a.B;
+  auto crec = [&](int x) -> KVConsRec* {
+    return reinterpret_cast<KVConsRec*>(ring + (x % NST) * kKVStageBytes + 2 * TILE + 512);
+  };
+
+  if (warp == kKVProd && lane == 0) {
+    for (int st = 0; st < NST; ++st) {
+      tc::mbar_init(&bar_c[st], 1);
+      tc::mbar_init(&ring_empty[st], 1);
     }
-    return;
-  }
-  if (warp == kCtl && lane == 0) {
-    tc::mbar_init(&bar_k, 1);
-    for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_c[st], 1);
-    tc::mbar_init(&bar_s, 1);
-    tc::mbar_init(&bar_o, 1);
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(&bar_kv[x], 1);
+      tc::mbar_init(&kv_empty[x], 1);
+    }
+    tc::mbar_init(&bar_s1, 1);
+    tc::mbar_init(&bar_s2, 1);
+    tc::mbar_init(&op_v, kEW);
+    tc::mbar_init(&op_k, kEW);
+    tc::mbar_init(&acc_full, 1);
+    tc::mbar_init(&acc_empty, kEW);
+    for (int x = 0; x < MR; ++x) {
+      tc::mbar_init(&meta_full[x], 1);
+      tc::mbar_init(&meta_empty[x], 1);
+    }
+    tc::mbar_init(&drain, 1);
     tc::fence_mbar_init();
+    abort_s = 0;
     prefetch_tmap(&tmQ);
     prefetch_tmap(&tmdO);
-    // K and V of this chunk first: they do not depend on the consumer table.
-    tc::mbar_expect_tx(&bar_k, 2 * TILE);
-    tc::tma_load_4d(Ks, &tmK, 0, h, j * 64, b, &bar_k);
-    tc::tma_load_4d(Vs, &tmV, 0, h, j * 64, b, &bar_k);
-  }
-  if (warp == kCtl) {  // consumer table: entries and fusion weights (from the query side)
-    for (int x = lane; x < ncons && x < kConsTab; x += 32) {
-      const int e = ent[e0 + x];
-      etab[x] = e;
-      wtab[x] = wrow[e];
-    }
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tdV = tmem_slot + 128, tdK = tmem_slot + 192;
+  const uint32_t tm = tmem_slot;
+  // Waits of the roles off the critical path park the warp (no issue slots taken); the
+  // MMA warp and the element warps spin (a parked warp wakes up later).
+  auto W = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
+    return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
+  };
+  auto S = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
+    return spin_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
+  };
 
-  if (warp == kCtl) {
-    // ------------------------------------------------------------ control warp
-    bool ok = true;
-    auto load_cons = [&](int x) {  // lane 0: consumer x's Q, dO tiles, LSE and D rows
-      const int st = x % NST;
-      const int e = x < kConsTab ? etab[x] : ent[e0 + x];
-      const int r = e / a.topk, m = e % a.topk;
-      const int c = r + a.shift;
-      w_st[st] = x < kConsTab ? wtab[x] : wrow[e];
-      unsigned char* base = ring + st * kKVStageBytes;
-      const int64_t rb = ((((int64_t)b * a.nQ + c) * a.H + h) * a.topk + m) * 64;
-      tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
-      tc::tma_load_4d(base, &tmQ, 0, h, c * 64, b, &bar_c[st]);
-      tc::tma_load_4d(base + TILE, &tmdO, 0, h, c * 64, b, &bar_c[st]);
-      tc::bulk_load(base + 2 * TILE, a.lse + rb, 256, &bar_c[st]);
-      tc::bulk_load(base + 2 * TILE + 256, a.Dbuf + rb, 256, &bar_c[st]);
-    };
-    // Operand descriptors, built once (ring stages: base + stage offset).
-    const uint64_t dKd = tc::desc_km(tc::su32(Ks)), dVd = tc::desc_km(tc::su32(Vs));
-    const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
-    constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
-    auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x (whole warp)
-      const uint64_t dq = dRingKm + (x % NST) * kStage, ddo = dq + kTileStep;
+  if (warp == kKVMetaW) {
+    // ------------------------------------------------------------ metadata warp
+    int k = 0;  // metadata records written
+    bool alive = true;
+    while (alive) {
+      int t0 = 0;
+      if (lane == 0) t0 = atomicAdd(a.kv_ctr, NB);
+      t0 = __shfl_sync(0xffffffffu, t0, 0);
+      if (t0 >= ntiles) break;
+      // CSR bounds of the batch's tiles: lane l < NB reads the start of tile t0 + l, lane
+      // NB + l its end.
+      int v = 0;
+      if (lane < 2 * NB && t0 + lane % NB < ntiles) {
+        int jj, hh, bb;
+        kv_tile(a, t0 + lane % NB, jj, hh, bb);
+        v = a.csr_off[(int64_t)bb * (a.nC + 1) + jj + (lane >= NB ? 1 : 0)];
+      }
+      int e0s[NB], ns[NB], rk[NB];
 #pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma_warp(tS, dKd + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
-        tc::mma_warp(tP, dVd + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+      for (int l = 0; l < NB; ++l) {
+        e0s[l] = __shfl_sync(0xffffffffu, v, l);
+        const int e1 = __shfl_sync(0xffffffffu, v, NB + l);
+        ns[l] = t0 + l < ntiles ? e1 - e0s[l] : 0;
       }
-      tc::commit_warp(&bar_s);
-    };
-    if (lane == 0)
-      for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
-    __syncwarp();
-    ok = tc::mbar_wait(&bar_k, 0) && ok;
-    ok = tc::mbar_wait(&bar_c[0], 0) && ok;
-    issue_s(0);
-    for (int ci = 0; ci < ncons; ++ci) {
-      tc::named_sync(kBarOpReady, NT);  // w P^T and dS^T are in TMEM columns 0-31, 64-95
-      tc::fence_after();
-      const uint64_t bq = dRingMn + (ci % NST) * kStage, bdo = bq + kTileStep;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
-        tc::mma_ts_warp(tdV, tS + 8 * kk, bdo + kk * tc::kKStepMn, kIdMn, acc);
-        tc::mma_ts_warp(tdK, tP + 8 * kk, bq + kk * tc::kKStepMn, kIdMn, acc);
+      for (int l = 0; l < NB; ++l) {
+        rk[l] = -1;
+        const int tt = t0 + l;
+        if (tt >= ntiles) continue;
+        int j, h, b;
+        kv_tile(a, tt, j, h, b);
+        if (ns[l] == 0) {  // nobody retrieved the chunk: zero gradients
+          if (!a.acc_dkv) {
+            const int64_t ktok0 = ((int64_t)b * a.nC * 64 + (int64_t)j * 64) * ts + h * DH;
+            bf16* dkg = reinterpret_cast<bf16*>(a.dk) + ktok0;
+            bf16* dvg = reinterpret_cast<bf16*>(a.dv) + ktok0;
+            for (int u = lane; u < 64 * UPR; u += 32) {
+              const int row = u / UPR, w = u % UPR;
+              *reinterpret_cast<uint4*>(dkg + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(dvg + row * ts + w * 8) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          continue;
+        }
+        rk[l] = k++;
+        if (rk[l] >= MR && lane == 0 && !W(&meta_empty[rk[l] % MR], ((rk[l] / MR) - 1) & 1, 18, rk[l], -1))
+          alive = false;
+        alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+        if (!alive) break;
+        if (lane == 0) {
+          KVMeta& M = meta[rk[l] % MR];
+          M.j = j; M.h = h; M.b = b; M.ncons = ns[l]; M.e0 = e0s[l]; M.end = 0;
+        }
       }
-      tc::commit_warp(&bar_o);
-      if (ci + 1 < ncons) {
-        ok = tc::mbar_wait(&bar_c[(ci + 1) % NST], ((ci + 1) / NST) & 1) && ok;
-        issue_s(ci + 1);
+      if (!alive) break;
+      // The consumer tables of the batch, every lane at once: entry x of tile l is taken
+      // by lane x % 32 in step 2 l + x / 32 (entries, then their fusion weights).
+      int ev[2 * NB];
+#pragma unroll
+      for (int i = 0; i < 2 * NB; ++i) {
+        const int l = i >> 1, x = lane + 32 * (i & 1);
+        ev[i] = -1;
+        if (rk[l] >= 0 && x < ns[l]) {
+          const int b = (t0 + l) / (a.nC * a.H);  // the sequence of tile t0 + l
+          ev[i] = a.csr_ent[(int64_t)b * a.nQ * a.topk + e0s[l] + x];
+        }
       }
-      ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // ring stage ci % NST is free
-      if (lane == 0) {
-        if (ci + NST < ncons) load_cons(ci + NST);
-        if (!ok) flag_timeout(a.err);
+#pragma unroll
+      for (int i = 0; i < 2 * NB; ++i) {
+        const int l = i >> 1, x = lane + 32 * (i & 1);
+        if (ev[i] >= 0) {
+          const int b = (t0 + l) / (a.nC * a.H);
+          KVMeta& M = meta[rk[l] % MR];
+          M.w[x] = a.wrow[(int64_t)b * a.nQ * a.topk + ev[i]];
+          M.cm[x] = ((ev[i] / a.topk + a.shift) << 4) | (ev[i] % a.topk);
+        }
       }
       __syncwarp();
+      if (lane == 0)
+#pragma unroll
+        for (int l = 0; l < NB; ++l)
+          if (rk[l] >= 0) tc::mbar_arrive(&meta_full[rk[l] % MR]);
+      __syncwarp();
+    }
+    if (lane == 0 && alive && (k < MR || W(&meta_empty[k % MR], ((k / MR) - 1) & 1, 18, k, -1))) {
+      meta[k % MR].end = 1;
+      tc::mbar_arrive(&meta_full[k % MR]);
+    }
+    __syncwarp();
+  } else if (warp == kKVProd) {
+    // ------------------------------------------------------------ producer warp (lane 0)
+    if (lane == 0) {
+      int gx = 0, tcn = 0, nkv[2] = {0, 0}, nc[NST];
+      for (int st = 0; st < NST; ++st) nc[st] = 0;
+      bool alive = true;
+      // Stage for consumer record gx (waits until the stage's last consumer is finished).
+      auto take_stage = [&](int site) -> bool {
+        return gx < NST || W(&ring_empty[gx % NST], ((gx / NST) - 1) & 1, site, tcn, gx);
+      };
+      for (int k = 0; alive; ++k) {
+        if (!W(&meta_full[k % MR], (k / MR) & 1, 19, k, -1)) {
+          alive = false;
+          break;
+        }
+        const KVMeta& M = meta[k % MR];
+        if (M.end) break;
+        const int j = M.j, h = M.h, b = M.b, ncons = M.ncons, e0 = M.e0;
+        const int kb = tcn & 1;
+        if (tcn >= 2 && !W(&kv_empty[kb], ((tcn >> 1) - 1) & 1, 21, tcn, -1)) {
+          alive = false;
+          break;
+        }
+        tc::mbar_expect_tx(&bar_kv[kb], 2 * TILE);
+        tc::tma_load_4d(kvbuf + 2 * kb * TILE, &tmK, 0, h, j * 64, b, &bar_kv[kb]);
+        tc::tma_load_4d(kvbuf + (2 * kb + 1) * TILE, &tmV, 0, h, j * 64, b, &bar_kv[kb]);
+        ++nkv[kb];
+        for (int x = 0; x < ncons; ++x, ++gx) {
+          if (!take_stage(22)) {
+            alive = false;
+            break;
+          }
+          int c, m;
+          float w;
+          if (x < MC) {
+            c = M.cm[x] >> 4;
+            m = M.cm[x] & 15;
+            w = M.w[x];
+          } else {  // beyond the table: straight from the CSR
+            const int e = a.csr_ent[(int64_t)b * a.nQ * a.topk + e0 + x];
+            c = e / a.topk + a.shift;
+            m = e % a.topk;
+            w = a.wrow[(int64_t)b * a.nQ * a.topk + e];
+          }
+          const int st = gx % NST;
+          KVConsRec* rec = crec(gx);
+          rec->w = w;
+          rec->flags = (x == 0 ? kRecFirst : 0) | (x == ncons - 1 ? kRecLast : 0);
+          rec->kb = kb;
+          rec->tc = tcn;
+          rec->j = j;
+          rec->h = h;
+          rec->b = b;
+          unsigned char* base = ring + st * kKVStageBytes;
+          const int64_t rb = ((((int64_t)b * a.nQ + c) * a.H + h) * a.topk + m) * 64;
+          tc::mbar_expect_tx(&bar_c[st], 2 * TILE + 512);
+          tc::tma_load_4d(base, &tmQ, 0, h, c * 64, b, &bar_c[st]);
+          tc::tma_load_4d(base + TILE, &tmdO, 0, h, c * 64, b, &bar_c[st]);
+          tc::bulk_load(base + 2 * TILE, a.lse + rb, 256, &bar_c[st]);
+          tc::bulk_load(base + 2 * TILE + 256, a.Dbuf + rb, 256, &bar_c[st]);
+          ++nc[st];
+        }
+        tc::mbar_arrive(&meta_empty[k % MR]);  // the record has been read
+        ++tcn;
+      }
+      // End marker: a consumer record with the end flag.
+      if (alive && take_stage(23)) {
+        crec(gx)->flags = kRecEnd;
+        tc::mbar_arrive(&bar_c[gx % NST]);
+      }
+      // After an abort, let the copies already issued land before the CTA exits.
+      if (*reinterpret_cast<volatile int*>(&abort_s)) {
+        for (int x = 0; x < 2; ++x)
+          if (nkv[x] > 0) tc::mbar_wait(&bar_kv[x], (nkv[x] - 1) & 1);
+        for (int st = 0; st < NST; ++st)
+          if (nc[st] > 0) tc::mbar_wait(&bar_c[st], (nc[st] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kKVMma) {
+    // ------------------------------------------------------------ MMA warp
+    const uint32_t tS = tm, tP = tm + 64, tdV = tm + 128, tdK = tm + 192;
+    const uint64_t dKV = tc::desc_km(tc::su32(kvbuf));
+    const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
+    constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
+    bool issued = false;
+    // S^T, then dPo^T of consumer y, each with its own commit, so that the element warps
+    // start on P while dPo^T is still in the pipe (its operands are loaded; r is its
+    // record).
+    auto issue_sdp = [&](int y, const KVConsRec& r) -> bool {
+      if ((r.flags & kRecFirst) && !S(&bar_kv[r.kb], (r.tc >> 1) & 1, 25, r.tc, y)) return false;
+      const uint64_t dk = dKV + (2 * r.kb) * kTileStep, dv = dk + kTileStep;
+      const uint64_t dq = dRingKm + (y % NST) * kStage, ddo = dq + kTileStep;
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks)
+        tc::mma_warp(tS, dk + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+      tc::commit_warp(&bar_s1);
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks)
+        tc::mma_warp(tP, dv + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+      tc::commit_warp(&bar_s2);
+      if (r.flags & kRecLast) tc::commit_warp(&kv_empty[r.kb]);
+      issued = true;
+      return true;
+    };
+    int nend = 0x7fffffff, x = 0;
+    KVConsRec rx;  // record of consumer x
+    bool ok = S(&bar_c[0], 0, 24, -1, 0);
+    if (ok) {
+      rx = *crec(0);
+      if (rx.flags & kRecEnd) nend = 0;
+      else ok = issue_sdp(0, rx);
+    }
+    for (x = 0; ok && x < nend; ++x) {
+      // dV += (w P^T) dO as soon as w P^T is in, while the element warps form dS^T.
+      if (!S(&op_v, x & 1, 26, rx.tc, x)) break;
+      tc::fence_after();
+      if ((rx.flags & kRecFirst) && rx.tc >= 1 && !S(&acc_empty, (rx.tc - 1) & 1, 27, rx.tc, x)) break;
+      const uint64_t bq = dRingMn + (x % NST) * kStage, bdo = bq + kTileStep;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t acc = ((rx.flags & kRecFirst) && kk == 0) ? 0u : 1u;
+        const uint32_t aoff = kk < 2 ? 8 * kk : 16 + 8 * kk;  // columns of this K step's query pairs
+        tc::mma_ts_warp(tdV, tS + aoff, bdo + kk * tc::kKStepMn, kIdMn, acc);
+      }
+      // Probe what S^T(x + 1) needs while dK(x) is issued.
+      const uint32_t c_seen = tc::mbar_test(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1);
+      if (!S(&op_k, x & 1, 32, rx.tc, x)) break;
+      tc::fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t acc = ((rx.flags & kRecFirst) && kk == 0) ? 0u : 1u;
+        const uint32_t aoff = kk < 2 ? 8 * kk : 16 + 8 * kk;
+        tc::mma_ts_warp(tdK, tP + aoff, bq + kk * tc::kKStepMn, kIdMn, acc);
+      }
+      tc::commit_warp(&ring_empty[x % NST]);
+      if (rx.flags & kRecLast) tc::commit_warp(&acc_full);
+      if (!c_seen && !S(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1, 24, rx.tc, x + 1)) break;
+      rx = *crec(x + 1);
+      if (rx.flags & kRecEnd) {
+        nend = x + 1;
+        break;
+      }
+      if (!issue_sdp(x + 1, rx)) break;
+    }
+    // No product may still be running when TMEM is released (after an abort in particular).
+    if (issued) {
+      tc::commit_warp(&drain);
+      if (!tc::mbar_wait(&drain, 0) && lane == 0) flag_timeout(a.err, 28, blockIdx.x, -1, x);
     }
   } else {
     // ------------------------------------------------------------ element-wise warps
-    const int cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
+    const int cq = lane & 3, g = lane >> 2, quarter = warp & 3, hc = warp >> 2;
     const uint32_t lane_q = (uint32_t)(32 * quarter) << 16;
-    const uint32_t lane_base = lane_q + 32 * hc;
+    const uint32_t tb = tm + lane_q + 32 * hc;  // this warp's 32 columns of S^T
     const float scale = 1.0f / sqrtf((float)DH);
     const float sl2 = scale * kLog2e;
-    for (int ci = 0; ci < ncons; ++ci) {
-      if (!tc::mbar_wait(&bar_s, ci & 1)) flag_timeout(a.err);  // acquire S^T(ci), dPo^T(ci)
-      const int st = ci % NST;
-      // The rows came in by bulk copy: observe their mbarrier phase (already complete).
-      tc::mbar_wait(&bar_c[st], (ci / NST) & 1);
-      const float* lrow = reinterpret_cast<const float*>(ring + st * kKVStageBytes + 2 * TILE) + 32 * hc;
+    // A finished tile's dK and dV from TMEM, straight to global memory.
+    auto write_out = [&](const KVConsRec& r) -> bool {
+      if (!S(&acc_full, r.tc & 1, 31, r.tc, -1)) return false;
+      tc::fence_after();
+      float ov[4][4], ok[4][4];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tm + 128 + lane_q + 32 * hc + cb * 8, ov[cb]);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tm + 192 + lane_q + 32 * hc + cb * 8, ok[cb]);
+      tc::ld_wait(ov);
+      tc::ld_wait(ok);
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acc_empty);
+      const int64_t ktok0 = ((int64_t)r.b * a.nC * 64 + (int64_t)r.j * 64) * ts + r.h * DH;
+      bf16* dkg = reinterpret_cast<bf16*>(a.dk) + ktok0;
+      bf16* dvg = reinterpret_cast<bf16*>(a.dv) + ktok0;
+      const int r0 = 16 * quarter + g;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {  // key rows r0, r0 + 8; columns 32hc + 8n + 2cq (+1)
+        const int col = 32 * hc + 8 * n + 2 * cq;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int64_t off = (int64_t)(r0 + 8 * half) * ts + col;
+          float k0 = ok[n][2 * half], k1 = ok[n][2 * half + 1], v0 = ov[n][2 * half], v1 = ov[n][2 * half + 1];
+          if (a.acc_dkv) {
+            const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162*>(dkg + off);
+            const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162*>(dvg + off);
+            k0 += __low2float(kk);
+            k1 += __high2float(kk);
+            v0 += __low2float(vv);
+            v1 += __high2float(vv);
+          }
+          *reinterpret_cast<uint32_t*>(dkg + off) = pack_bf16(k0, k1);
+          *reinterpret_cast<uint32_t*>(dvg + off) = pack_bf16(v0, v1);
+        }
+      }
+      return true;
+    };
+    // A tile is written out after the next consumer's operands are in (its products run
+    // meanwhile), so that the wait for the tile's last products leaves the pipe busy.
+    KVConsRec pend;
+    bool have_pend = false, alive = true;
+    for (int x = 0;; ++x) {
+      if (!W(&bar_c[x % NST], (x / NST) & 1, 29, -1, x)) {
+        alive = false;
+        break;
+      }  // record and rows are in
+      const KVConsRec r = *crec(x);
+      if (r.flags & kRecEnd) break;
+      const unsigned char* sb = ring + (x % NST) * kKVStageBytes;
+      const float* lrow = reinterpret_cast<const float*>(sb + 2 * TILE) + 32 * hc;
       const float* drow = lrow + 64;
-      const float w = w_st[st];
-      float s[4][4], dp[4][4];
+      const float w = r.w, cs = w * scale;
+      // P^T from S^T, and w P^T into TMEM over the columns just read.
+      if (!S(&bar_s1, x & 1, 30, r.tc, x)) {
+        alive = false;
+        break;
+      }
+      float p[4][4];
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
-      tc::ld_wait(s);
-      tc::ld_wait(dp);
-      const float cs = w * scale;
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tb + cb * 8, p[cb]);
+      tc::ld_wait(p);
+      uint32_t pv[8];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {  // columns are queries 32hc + 8n + 2cq (+1)
         const float2 l2 = *reinterpret_cast<const float2*>(lrow + 8 * n + 2 * cq);
-        const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
         const float la = l2.x * kLog2e, lb = l2.y * kLog2e;
-        const float p0 = tc::ex2(fmaf(s[n][0], sl2, -la)), p1 = tc::ex2(fmaf(s[n][1], sl2, -lb));
-        const float p2 = tc::ex2(fmaf(s[n][2], sl2, -la)), p3 = tc::ex2(fmaf(s[n][3], sl2, -lb));
-        dp[n][0] = p0 * (dp[n][0] - d2.x) * cs;
-        dp[n][1] = p1 * (dp[n][1] - d2.y) * cs;
-        dp[n][2] = p2 * (dp[n][2] - d2.x) * cs;
-        dp[n][3] = p3 * (dp[n][3] - d2.y) * cs;
-        s[n][0] = p0 * w;
-        s[n][1] = p1 * w;
-        s[n][2] = p2 * w;
-        s[n][3] = p3 * w;
+        p[n][0] = tc::ex2(fmaf(p[n][0], sl2, -la));
+        p[n][1] = tc::ex2(fmaf(p[n][1], sl2, -lb));
+        p[n][2] = tc::ex2(fmaf(p[n][2], sl2, -la));
+        p[n][3] = tc::ex2(fmaf(p[n][3], sl2, -lb));
+        pv[2 * n] = pack_bf16(p[n][0] * w, p[n][1] * w);
+        pv[2 * n + 1] = pack_bf16(p[n][2] * w, p[n][3] * w);
       }
-      // w P^T and dS^T as TMEM A operands (keys are rows): queries (32hc + 8n + 2cq, +1)
-      // of key rows g and g + 8 go to column 16hc + 4n + cq of S^T's and dPo^T's columns.
-      // Both column halves must have read S^T and dPo^T before either half stores.
-      uint32_t pv[8], dv[8];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        pv[2 * n] = pack_bf16(s[n][0], s[n][1]);
-        pv[2 * n + 1] = pack_bf16(s[n][2], s[n][3]);
-        dv[2 * n] = pack_bf16(dp[n][0], dp[n][1]);
-        dv[2 * n + 1] = pack_bf16(dp[n][2], dp[n][3]);
-      }
-      tc::named_sync(kBarEW, 32 * kEW);
-      tc::st16x128_x4(tS + lane_q + 16 * hc, pv);
-      tc::st16x128_x4(tP + lane_q + 16 * hc, dv);
+      // w P^T and dS^T as TMEM A operands (keys are rows): the pair of queries
+      // (32hc + 8n + 2cq, +1) of key rows g and g + 8 goes to column 32hc + 4n + cq, inside
+      // the 32 columns this warp has read.
+      tc::st16x128_x4(tb, pv);
       tc::st_wait();
       tc::fence_before();
-      tc::named_arrive(kBarOpReady, NT);
-    }
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  // Epilogue: dK from TMEM columns 192-255 into the K tile, dV (128-191) into the V tile
-  // (fp32 values staged as bf16 in the same swizzled layout), then 16-byte rows.
-  if (warp < kEW) {
-    const int g = lane >> 2, cq = lane & 3, quarter = warp & 3, hc = warp >> 2;
-    const uint32_t lane_base = ((uint32_t)(32 * quarter) << 16) + 32 * hc;
-    float o[4][4];
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&op_v);
+      // dS^T from dPo^T.
+      if (!S(&bar_s2, x & 1, 33, r.tc, x)) {
+        alive = false;
+        break;
+      }
+      float dp[4][4];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      unsigned char* dst = half ? Vs : Ks;
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256((half ? tdV : tdK) + lane_base + cb * 8, o[cb]);
-      tc::ld_wait(o);
+      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tb + 64 + cb * 8, dp[cb]);
+      tc::ld_wait(dp);
+      uint32_t dv[8];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
-        const int r0 = 16 * quarter + g;
-        *reinterpret_cast<uint32_t*>(dst + swz<ROWB>(r0, 4 * hc + n) + cq * 4) = pack_bf16(o[n][0], o[n][1]);
-        *reinterpret_cast<uint32_t*>(dst + swz<ROWB>(r0 + 8, 4 * hc + n) + cq * 4) = pack_bf16(o[n][2], o[n][3]);
+        const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
+        dv[2 * n] = pack_bf16(p[n][0] * (dp[n][0] - d2.x) * cs, p[n][1] * (dp[n][1] - d2.y) * cs);
+        dv[2 * n + 1] = pack_bf16(p[n][2] * (dp[n][2] - d2.x) * cs, p[n][3] * (dp[n][3] - d2.y) * cs);
+      }
+      tc::st16x128_x4(tb + 64, dv);
+      tc::st_wait();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&op_k);
+      if (have_pend) {
+        have_pend = false;
+        if (!write_out(pend)) {
+          alive = false;
+          break;
+        }
+      }
+      if (r.flags & kRecLast) {
+        pend = r;
+        have_pend = true;
       }
     }
+    if (alive && have_pend) write_out(pend);
   }
   tc::fence_before();
   __syncthreads();
   if (warp == 0) {
     tc::fence_after();
-    tc::tmem_dealloc(tmem_slot, 256);
-  }
-  for (int u = tid; u < 64 * UPR; u += NT) {
-    const int row = u / UPR, w = u % UPR;
-    uint4 vk = *reinterpret_cast<const uint4*>(Ks + swz<ROWB>(row, w));
-    uint4 vv = *reinterpret_cast<const uint4*>(Vs + swz<ROWB>(row, w));
-    if (a.acc_dkv) {
-      const uint4 ok = *reinterpret_cast<const uint4*>(dkg + row * ts + w * 8);
-      const uint4 ov = *reinterpret_cast<const uint4*>(dvg + row * ts + w * 8);
-      float fk[8], fv[8], nk[8], nv[8];
-      unpack16(ok, fk, (const bf16*)nullptr);
-      unpack16(ov, fv, (const bf16*)nullptr);
-      unpack16(vk, nk, (const bf16*)nullptr);
-      unpack16(vv, nv, (const bf16*)nullptr);
-      vk.x = pack_bf16(nk[0] + fk[0], nk[1] + fk[1]); vk.y = pack_bf16(nk[2] + fk[2], nk[3] + fk[3]);
-      vk.z = pack_bf16(nk[4] + fk[4], nk[5] + fk[5]); vk.w = pack_bf16(nk[6] + fk[6], nk[7] + fk[7]);
-      vv.x = pack_bf16(nv[0] + fv[0], nv[1] + fv[1]); vv.y = pack_bf16(nv[2] + fv[2], nv[3] + fv[3]);
-      vv.z = pack_bf16(nv[4] + fv[4], nv[5] + fv[5]); vv.w = pack_bf16(nv[6] + fv[6], nv[7] + fv[7]);
-    }
-    *reinterpret_cast<uint4*>(dkg + row * ts + w * 8) = vk;
-    *reinterpret_cast<uint4*>(dvg + row * ts + w * 8) = vv;
+    tc::tmem_dealloc(tm, 256);
   }
 }
 
@@ -719,9 +1051,18 @@ cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t s) {
   if (e == cudaSuccess) e = make_head_tmap(&tk, a.k, 64, a.H, (int64_t)a.nC * 64, a.B, kb);
   if (e == cudaSuccess) e = make_head_tmap(&tv, a.v, 64, a.H, (int64_t)a.nC * 64, a.B, kb);
   if (e == cudaSuccess) e = allow_smem((const void*)gca_bwd_kv_tc_kernel, kKVSmem);
+  int dev = 0, sms = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  const long long ntiles = (long long)a.nC * a.H * a.B;
+  const int grid = (int)std::min<long long>(ntiles, 2LL * sms);  // two CTAs per SM (TMEM: 256 columns each)
+  // Heads per tile block: as many as keep their Q, dO, K and V within about 48 MB of L2.
+  BwdArgs b2 = a;
+  const long long per_head = 4LL * 64 * 64 * 2 * std::max(a.nQ, a.nC);
+  b2.kv_hb = (int)std::max<long long>(1, std::min<long long>(a.H, (48LL << 20) / per_head));
   launch_begin("gca_bwd_kv", s);
-  gca_bwd_kv_tc_kernel<<<dim3(a.nC, a.H, a.B), kThreads, kKVSmem, s>>>(a, tq, tdo, tk, tv);
+  gca_bwd_kv_tc_kernel<<<grid, kKVThreads, kKVSmem, s>>>(b2, tq, tdo, tk, tv);
   return launch_end("gca_bwd_kv", s);
 }
 

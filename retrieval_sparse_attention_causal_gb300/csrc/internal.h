@@ -142,6 +142,8 @@ struct BwdArgs {
   int32_t* csr_ent; // [B][nQ*topk]
   int32_t* csr_cur; // [B][nC]
   float* wrow;      // [B][nQ][topk] fusion weight of every slot (written by the tensor-core query side)
+  int32_t* kv_ctr;  // tile counter of the persistent key side (zeroed by the dscores kernel)
+  int kv_hb;        // heads per tile block of the key side (set at its launch)
 };
 cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s);
 // Tensor-core (tcgen05) query-side and key-side passes, bf16 with dh = 64 (gca_bwd_tc.cu).

@@ -132,6 +132,17 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of phase `parity` of `bar` (1 if it has completed).
+__device__ __forceinline__ uint32_t mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(su32(bar)), "r"(parity));
+  return done;
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;"); }
 // Make generic-proxy shared-memory writes (st.shared, cp.async) visible to tcgen05.mma.
