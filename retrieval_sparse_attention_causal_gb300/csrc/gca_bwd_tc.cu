@@ -60,11 +60,11 @@ enum { kBarOpReady = 2, kBarEW = 3 };
 // site and raises a CTA-wide abort flag; every role then stops issuing work (the MMA
 // warp drains its products, the producer its copies) and the CTA exits, so a protocol
 // fault can neither hang the kernel nor let a role run on stale metadata.
-constexpr int kQStages = 3;
+constexpr int kQStages = 4;
 constexpr int kQThreads = kThreads + 32;  // + producer warp
 constexpr int kProd = kEW + 1;
 constexpr int kQBuf = 2 * TILE + kMaxTopk * 64 * 4;  // Q, dO, LSE rows of every slot
-constexpr int kQSmem = 2 * kQBuf + TILE * (2 * kQStages + 1) + 1024;  // 2 x (Q, dO, LSE), ring of (K, V), dQ staging
+constexpr int kQSmem = 2 * kQBuf + TILE * 2 * kQStages + 1024;  // 2 x (Q, dO, LSE), ring of (K, V)
 static_assert(kQBuf % 1024 == 0, "Q / dO tiles must stay 1024-byte aligned");
 constexpr uint32_t kWaitLimit = 1u << 21;
 // Metadata records in flight: the producer fills tile k+1's record while tile k's loads
@@ -161,7 +161,6 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
   unsigned char* qbuf = sm;                 // buffer x at qbuf + x kQBuf: Q, dO, LSE
   unsigned char* ring = sm + 2 * kQBuf;     // stage st: K at ring + 2 st TILE, V after it
-  unsigned char* dqst = ring + 2 * NST * TILE;
   __shared__ QTileMeta meta[kMetaBufs];
   __shared__ float Dx[2][2][64];  // [slot parity][column half][row]: partial row sums of D
   __shared__ uint32_t tmem_slot;
@@ -336,16 +335,11 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       // S(g), dPo(g) are in the element warps' registers: the next pair may overwrite them.
       if (!W(&sfree[g & 1], (g >> 1) & 1, 10, k, g)) break;
       int nk = k, nt = t, nns = ns, nsi = si + 1;
-      if (nsi == ns) {
-        // Look one tile ahead only: the tile after an empty one cannot be prepared before
-        // this tile's metadata is released, which waits for this tile's dQ.
-        nk = k + 1;
-        nt = t + gridDim.x;
-        nsi = 0;
-        nns = take_tile(nk, nt);
-      }
-      if (nns > 0 && !issue_s(g + 1, nk & 1, nk)) break;
-      if (nns == -2) break;
+      const bool last = nsi == ns;
+      // Inside a tile the next slot's S, dPo go first, to overlap this slot's dS.  After a
+      // tile's last slot its dQ goes first: the next tile's first K / V tiles may still be
+      // on their way, and the tile's write-out should not wait for them.
+      if (!last && !issue_s(g + 1, k & 1, k)) break;
       if (!W(&opready[g & 1], (g >> 1) & 1, 11, k, g)) break;  // dS(g) is in buffer g & 1
       tc::fence_after();
       const uint64_t dk = dRingMn + (g % NST) * kStage;
@@ -354,12 +348,17 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
         tc::mma_ts_warp(tQ, ta + 8 * kk, dk + kk * tc::kKStepMn, kIdMn, (si > 0 || kk > 0) ? 1u : 0u);
       tc::commit_warp(&ring_empty[g % NST]);
-      if (si == ns - 1) {
+      if (last) {
         tc::commit_warp(&qfree[k & 1]);
         tc::commit_warp(&dq_full);
-      }
-      if (nns == 0) {  // the next tile was empty: with this tile finished, skip ahead
+        // The next tile with slots (the one after is prepared only once this tile's
+        // metadata is released, which the take releases).
+        nk = k + 1;
+        nt = t + gridDim.x;
+        nsi = 0;
+        nns = take_tile(nk, nt);
         while (nns == 0) nns = take_tile(++nk, nt += gridDim.x);
+        if (nns == -2) break;
         if (nns > 0 && !issue_s(g + 1, nk & 1, nk)) break;
       }
       k = nk;
@@ -475,26 +474,20 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         }
       }
       if (!alive) break;
-      // Tile epilogue: dQ from TMEM through the staging tile to global memory, and dw.
+      // Tile epilogue: dQ from TMEM straight to global memory (each warp its 16 rows and
+      // 32 columns; no staging, so the K / V ring can hold one more stage).
       if (!W(&dq_full, kq & 1, 9, k, gs)) break;
       ++kq;
       float o[4][4];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tQ + lane_base + cb * 8, o[cb]);
       tc::ld_wait(o);
+      tc::fence_before();
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
-        *reinterpret_cast<uint32_t*>(dqst + swz<ROWB>(row0, 4 * hc + n) + cq * 4) = pack_bf16(o[n][0], o[n][1]);
-        *reinterpret_cast<uint32_t*>(dqst + swz<ROWB>(row0 + 8, 4 * hc + n) + cq * 4) = pack_bf16(o[n][2], o[n][3]);
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&ewb);
-      if (!W(&ewb, ewc & 1, 12, k, gs)) break;
-      ++ewc;
-      for (int u = etid; u < 64 * UPR; u += 32 * kEW) {
-        const int row = u / UPR, w = u % UPR;
-        *reinterpret_cast<uint4*>(dqg + row * ts + w * 8) = *reinterpret_cast<const uint4*>(dqst + swz<ROWB>(row, w));
+        const int col = 32 * hc + 8 * n + 2 * cq;
+        *reinterpret_cast<uint32_t*>(dqg + (int64_t)row0 * ts + col) = pack_bf16(o[n][0], o[n][1]);
+        *reinterpret_cast<uint32_t*>(dqg + (int64_t)(row0 + 8) * ts + col) = pack_bf16(o[n][2], o[n][3]);
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&meta_empty[mb]);
