@@ -25,6 +25,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
+#include "waits.cuh"
 
 namespace gca {
 namespace {
@@ -66,7 +67,6 @@ constexpr int kProd = kEW + 1;
 constexpr int kQBuf = 2 * TILE + kMaxTopk * 64 * 4;  // Q, dO, LSE rows of every slot
 constexpr int kQSmem = 2 * kQBuf + TILE * 2 * kQStages + 1024;  // 2 x (Q, dO, LSE), ring of (K, V)
 static_assert(kQBuf % 1024 == 0, "Q / dO tiles must stay 1024-byte aligned");
-constexpr uint32_t kWaitLimit = 1u << 21;
 // Metadata records in flight: the producer fills tile k+1's record while tile k's loads
 // are issued, and that must not wait for a record still in use (tile k-1's is released
 // only when its dQ is out, which needs tile k's first loads).
@@ -78,78 +78,6 @@ struct QTileMeta {
   int j[kMaxTopk];
   float w[kMaxTopk];
 };
-
-__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
-}
-
-// Bounded wait for phase `parity` of `bar` that gives up early once the CTA's abort flag
-// is raised; on running out it records `site` (with CTA, tile, slot) and raises the flag.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag, ErrWord* err,
-                                              int site, int tile, int slot) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (tc::mbar_try(bar, parity)) return true;
-    if ((it & 15) == 15 && *reinterpret_cast<volatile int*>(abort_flag)) return false;
-  }
-  flag_timeout(err, site, blockIdx.x, tile, slot);
-  atomicExch(abort_flag, 1);
-  return false;
-}
-
-// Nanoseconds of the GPU's global timer.
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// One probe of phase `parity` of `bar` that lets the hardware park the thread until the
-// phase completes, for at most `hint_ns` (so that a waiting warp takes no issue slots
-// from the warps that work).
-__device__ __forceinline__ bool mbar_try_park(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(tc::su32(bar)), "r"(parity), "r"(hint_ns));
-  return done != 0;
-}
-
-// Bounded wait with parking, for kernels with many waiting warps: gives up once the CTA's
-// abort flag is raised, or after kParkLimitNs of global time, recording `site` (with CTA,
-// tile, slot) and raising the flag.
-constexpr uint64_t kParkLimitNs = 2000000000ull;
-__device__ __forceinline__ bool park_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag, ErrWord* err,
-                                              int site, int tile, int slot) {
-  if (tc::mbar_try(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    if (mbar_try_park(bar, parity, 20000)) return true;
-    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-    if (global_ns() - t0 > kParkLimitNs) break;
-  }
-  flag_timeout(err, site, blockIdx.x, tile, slot);
-  atomicExch(abort_flag, 1);
-  return false;
-}
-
-// The same bounded wait without parking (for the warp whose wake-up latency is on the
-// critical path).
-__device__ __forceinline__ bool spin_or_abort(uint64_t* bar, uint32_t parity, int* abort_flag, ErrWord* err,
-                                              int site, int tile, int slot) {
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (tc::mbar_try(bar, parity)) return true;
-    if ((it & 15) == 15) {
-      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-      if (global_ns() - t0 > kParkLimitNs) break;
-    }
-  }
-  flag_timeout(err, site, blockIdx.x, tile, slot);
-  atomicExch(abort_flag, 1);
-  return false;
-}
 
 __global__ void __launch_bounds__(kQThreads, 2)
 gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
@@ -817,32 +745,41 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
     constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
     bool issued = false;
-    // S^T, then dPo^T of consumer y, each with its own commit, so that the element warps
-    // start on P while dPo^T is still in the pipe (its operands are loaded; r is its
-    // record).
-    auto issue_sdp = [&](int y, const KVConsRec& r) -> bool {
+    // The products of consumer x are issued in the order dV(x), S^T(x + 1), dK(x),
+    // dPo^T(x + 1): S^T(x + 1) overwrites w P^T(x), which only dV(x) reads, and dPo^T(x + 1)
+    // overwrites dS^T(x), which only dK(x) reads; so S^T(x + 1) runs while the element warps
+    // still form dS^T(x), and they find it done when they move on.
+    auto issue_st = [&](int y, const KVConsRec& r) -> bool {  // S^T(y) = K Q^T
       if ((r.flags & kRecFirst) && !S(&bar_kv[r.kb], (r.tc >> 1) & 1, 25, r.tc, y)) return false;
-      const uint64_t dk = dKV + (2 * r.kb) * kTileStep, dv = dk + kTileStep;
-      const uint64_t dq = dRingKm + (y % NST) * kStage, ddo = dq + kTileStep;
+      const uint64_t dk = dKV + (2 * r.kb) * kTileStep;
+      const uint64_t dq = dRingKm + (y % NST) * kStage;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks)
         tc::mma_warp(tS, dk + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
       tc::commit_warp(&bar_s1);
+      issued = true;
+      return true;
+    };
+    auto issue_dpt = [&](int y, const KVConsRec& r) {  // dPo^T(y) = V dO^T
+      const uint64_t dv = dKV + (2 * r.kb + 1) * kTileStep;
+      const uint64_t ddo = dRingKm + (y % NST) * kStage + kTileStep;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks)
         tc::mma_warp(tP, dv + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
       tc::commit_warp(&bar_s2);
-      if (r.flags & kRecLast) tc::commit_warp(&kv_empty[r.kb]);
-      issued = true;
-      return true;
+      if (r.flags & kRecLast) tc::commit_warp(&kv_empty[r.kb]);  // the tile's K, V are read
     };
     int nend = 0x7fffffff, x = 0;
     KVConsRec rx;  // record of consumer x
     bool ok = S(&bar_c[0], 0, 24, -1, 0);
     if (ok) {
       rx = *crec(0);
-      if (rx.flags & kRecEnd) nend = 0;
-      else ok = issue_sdp(0, rx);
+      if (rx.flags & kRecEnd) {
+        nend = 0;
+      } else {
+        ok = issue_st(0, rx);
+        if (ok) issue_dpt(0, rx);
+      }
     }
     for (x = 0; ok && x < nend; ++x) {
       // dV += (w P^T) dO as soon as w P^T is in, while the element warps form dS^T.
@@ -856,8 +793,12 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         const uint32_t aoff = kk < 2 ? 8 * kk : 16 + 8 * kk;  // columns of this K step's query pairs
         tc::mma_ts_warp(tdV, tS + aoff, bdo + kk * tc::kKStepMn, kIdMn, acc);
       }
-      // Probe what S^T(x + 1) needs while dK(x) is issued.
-      const uint32_t c_seen = tc::mbar_test(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1);
+      // S^T(x + 1), if there is a next consumer.
+      if (!S(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1, 24, rx.tc, x + 1)) break;
+      const KVConsRec rn = *crec(x + 1);
+      const bool more = !(rn.flags & kRecEnd);
+      if (more && !issue_st(x + 1, rn)) break;
+      // dK += dS^T Q once dS^T is in.
       if (!S(&op_k, x & 1, 32, rx.tc, x)) break;
       tc::fence_after();
 #pragma unroll
@@ -868,13 +809,12 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       }
       tc::commit_warp(&ring_empty[x % NST]);
       if (rx.flags & kRecLast) tc::commit_warp(&acc_full);
-      if (!c_seen && !S(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1, 24, rx.tc, x + 1)) break;
-      rx = *crec(x + 1);
-      if (rx.flags & kRecEnd) {
+      if (!more) {
         nend = x + 1;
         break;
       }
-      if (!issue_sdp(x + 1, rx)) break;
+      issue_dpt(x + 1, rn);
+      rx = rn;
     }
     // No product may still be running when TMEM is released (after an abort in particular).
     if (issued) {
