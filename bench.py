@@ -176,24 +176,24 @@ def job_throughput(units_per_rank: float, world: int, ms_per_step: float) -> flo
 # fingerprint of the sources the kernel is built from at capture time; once the sources
 # change, the figure no longer describes the kernel and the bench reports null.
 KERNEL_SOURCES = {
-    "gca_fwd": ("gca_fwd.cu", "tc.cuh", "common.cuh"),
-    "gca_bwd_q": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh"),
-    "gca_bwd_kv": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh"),
+    "gca_fwd": ("gca_fwd.cu", "tc.cuh", "common.cuh", "waits.cuh"),
+    "gca_bwd_q": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh", "waits.cuh"),
+    "gca_bwd_kv": ("gca_bwd_tc.cu", "tc.cuh", "common.cuh", "waits.cuh"),
     "retrieve_stream": ("retrieve.cu", "common.cuh"),
     "retrieve_tc": ("retrieve_tc.cu", "tc.cuh", "tc_rows.cuh", "common.cuh"),
 }
 KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
-    "gca_fwd": (382.37e6, "7e6df2385ac4ce02"),
-    "gca_bwd_q": (510.45e6, "5c4fccd2ea985839"),
-    "gca_bwd_kv": (603.0e6, "5c4fccd2ea985839"),
+    "gca_fwd": (3.8263e+08, "bd233dfe6ec2acf0"),
+    "gca_bwd_q": (5.0982e+08, "6ab8d7c85f80cf33"),
+    "gca_bwd_kv": (7.0303e+08, "6ab8d7c85f80cf33"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (808436224 / 2, "12cf7c72783b197e")
+STREAM_TRAFFIC_PER_SEQ = (805839360 / 2, "0f3bb0342dd59ee5")
 
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
 # nothing written back past L2; traffic grows with the number of chunks)
-PREFILL_TRAFFIC_PER_CHUNK = (25215744 / 8192, "ec85a0f70d57e879")
+PREFILL_TRAFFIC_PER_CHUNK = (25217280 / 8192, "59beecd0297b3b03")
 
 
 def source_fingerprint(kernel: str) -> str:
