@@ -15,7 +15,7 @@ constexpr int kMaxTopk = 16;  // largest supported top-k
 struct ErrWord {
   int flags;      // bit 0: an index outside [-1, nC) was met; bit 1: a bounded wait ran out
   int bad_value;  // last offending index
-  int wait_sites; // bit s: the wait at site s ran out (sites are numbered per kernel)
+  int wait_sites; // bit s % 32: the wait at site s ran out (sites are numbered per kernel)
   int first[4];   // the first wait that ran out: site + 1, CTA, tile, slot (0 until then)
 };
 constexpr int kErrIndex = 1;
@@ -33,7 +33,7 @@ __device__ __forceinline__ void flag_bad_index(ErrWord* e, int v) {
 __device__ __forceinline__ void flag_timeout(ErrWord* e, int site = 0, int cta = -1, int tile = -1, int slot = -1) {
   if (e) {
     atomicOr(&e->flags, kErrTimeout);
-    atomicOr(&e->wait_sites, 1 << site);
+    atomicOr(&e->wait_sites, 1 << (site & 31));
     if (atomicCAS(&e->first[0], 0, site + 1) == 0) {
       e->first[1] = cta;
       e->first[2] = tile;

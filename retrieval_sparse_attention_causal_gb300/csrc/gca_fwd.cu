@@ -481,14 +481,13 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
           break;
         }
         float s[8][4];
-#pragma unroll
-        for (int cb = 0; cb < 8; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
+        tc::ld16x256_x8(tS + lane_base, s);
         tc::ld_wait(s);
         float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-          mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
-          mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
+          mx0 = tc::max3(mx0, s[n][0], s[n][1]);
+          mx1 = tc::max3(mx1, s[n][2], s[n][3]);
         }
 #pragma unroll
         for (int m = 1; m <= 2; m <<= 1) {
@@ -541,8 +540,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       if (!W(&o_full, tq & 1, 52, k, gs)) break;
       tc::fence_after();
       float o[8][4];
-#pragma unroll
-      for (int cb = 0; cb < 8; ++cb) tc::ld16x256(tO + lane_base + cb * 8, o[cb]);
+      tc::ld16x256_x8(tO + lane_base, o);
       tc::ld_wait(o);
       tc::fence_before();
       __syncwarp();

@@ -283,3 +283,78 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }  // namespace tc
 }  // namespace gca
 
+
+namespace gca {
+namespace tc {
+
+// Packed pairs of f32 in one 64-bit register (x in the low half) and the paired
+// arithmetic of sm_100-class GPUs: one instruction for both halves, each rounded as its
+// scalar counterpart.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void uf2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Four 8 x 8 matrices of 16-bit pairs to shared memory: register i of thread t holds
+// row t/4, columns 2(t%4), 2(t%4)+1 of matrix i (the mma.sync accumulator fragment, and
+// the tcgen05.ld.16x256b one); thread t gives the address of row t%8 of matrix t/8.
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+}  // namespace tc
+}  // namespace gca
+
+namespace gca {
+namespace tc {
+
+// ld16x256 repeated along the columns: repetition r reads columns 8r..8r+7 into v[r].
+__device__ __forceinline__ void ld16x256_x4(uint32_t taddr, float (&v)[4][4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=f"(v[0][0]), "=f"(v[0][1]), "=f"(v[0][2]), "=f"(v[0][3]), "=f"(v[1][0]), "=f"(v[1][1]), "=f"(v[1][2]),
+        "=f"(v[1][3]), "=f"(v[2][0]), "=f"(v[2][1]), "=f"(v[2][2]), "=f"(v[2][3]), "=f"(v[3][0]), "=f"(v[3][1]),
+        "=f"(v[3][2]), "=f"(v[3][3])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void ld16x256_x8(uint32_t taddr, float (&v)[8][4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=f"(v[0][0]), "=f"(v[0][1]), "=f"(v[0][2]), "=f"(v[0][3]), "=f"(v[1][0]), "=f"(v[1][1]), "=f"(v[1][2]),
+        "=f"(v[1][3]), "=f"(v[2][0]), "=f"(v[2][1]), "=f"(v[2][2]), "=f"(v[2][3]), "=f"(v[3][0]), "=f"(v[3][1]),
+        "=f"(v[3][2]), "=f"(v[3][3]), "=f"(v[4][0]), "=f"(v[4][1]), "=f"(v[4][2]), "=f"(v[4][3]), "=f"(v[5][0]),
+        "=f"(v[5][1]), "=f"(v[5][2]), "=f"(v[5][3]), "=f"(v[6][0]), "=f"(v[6][1]), "=f"(v[6][2]), "=f"(v[6][3]),
+        "=f"(v[7][0]), "=f"(v[7][1]), "=f"(v[7][2]), "=f"(v[7][3])
+      : "r"(taddr));
+}
+
+}  // namespace tc
+}  // namespace gca
