@@ -152,6 +152,16 @@ def algorithmic_flops(B_, nC, H_, dh, k):
             "step": 14 * u * units, "units": units}
 
 
+def algorithmic_bytes(B_, nC, H_, dh, k, esize=2):
+    """Per kernel launch, each tensor moved once (query and key chunks alike, nQ = nC):
+    forward reads Q, K, V and writes O and the LSE rows; the query side reads Q, dO, K, V
+    and the LSE rows and writes dQ and the D rows; the key side reads Q, dO, K, V, the LSE
+    and D rows and writes dK, dV."""
+    t = B_ * nC * 64 * H_ * dh * esize        # one [B][L][H][dh] tensor
+    rows = B_ * nC * H_ * k * 64 * 4          # one f32 [B][nQ][H][k][64] row set
+    return {"gca_fwd": 4 * t + rows, "gca_bwd_q": 5 * t + 2 * rows, "gca_bwd_kv": 6 * t + 2 * rows}
+
+
 # ----------------------------------------------------------------------------- replicas
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """Slowest rank's time (the job's time).  Works with any initialised backend: NCCL
@@ -183,17 +193,17 @@ KERNEL_SOURCES = {
     "retrieve_tc": ("retrieve_tc.cu", "tc.cuh", "tc_rows.cuh", "common.cuh"),
 }
 KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
-    "gca_fwd": (3.8263e+08, "bd233dfe6ec2acf0"),
-    "gca_bwd_q": (5.0982e+08, "6ab8d7c85f80cf33"),
-    "gca_bwd_kv": (7.0303e+08, "6ab8d7c85f80cf33"),
+    "gca_fwd": (3.8264e+08, "9db82854879ee7b2"),
+    "gca_bwd_q": (5.0959e+08, "a93699f6857b04e8"),
+    "gca_bwd_kv": (7.0233e+08, "a93699f6857b04e8"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (805839360 / 2, "0f3bb0342dd59ee5")
+STREAM_TRAFFIC_PER_SEQ = (805479936 / 2, "4123911e1562b21a")
 
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
 # nothing written back past L2; traffic grows with the number of chunks)
-PREFILL_TRAFFIC_PER_CHUNK = (25217280 / 8192, "59beecd0297b3b03")
+PREFILL_TRAFFIC_PER_CHUNK = (25216768 / 8192, "e88e251646775069")
 
 
 def source_fingerprint(kernel: str) -> str:
@@ -309,6 +319,16 @@ def gpu_arm(args):
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops"], 4), "traffic": measured_traffic(dom),
                 "peak_source": f"{src} bf16 dense (burst)", "flops_per_launch": dom_flops}
+        # The same launch against HBM: its algorithmic bytes over the measured copy rate.
+        # (Both figures are algorithmic; at this shape the bytes take longer at peak than
+        # the flops, i.e. the kernel's arithmetic intensity is below the ridge point.)
+        by = algorithmic_bytes(B, NC, H, DH, K).get(dom)
+        if by:
+            gbs = by / avg_s / 1e9
+            roof["hbm_view"] = {"bytes_per_launch": by, "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                                "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                                "flop_per_byte": round(dom_flops / by, 1),
+                                "ridge_flop_per_byte": round(pk["bf16_tflops"] * 1e3 / pk["hbm_gbs"], 1)}
     step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
 
     # The 350M-model step: two retrieval groups, the second group's query landmarks read
