@@ -51,9 +51,10 @@ enum { kBarOpReady = 2, kBarEW = 3 };
 //     current tile;
 //   * warp 8 (MMA): issues S = Q K^T and dPo = dO V^T one slot ahead of the element warps
 //     (also across tile boundaries) and dQ += dS K once dS is in TMEM;
-//   * warps 0-7 (element): P = exp(S - LSE), D = rowsum(P * dPo) (stored; the retrieval
-//     score gradient sums it later), dS = w P (dPo - D) / sqrt(dh) into TMEM, and at the
-//     end of a tile dQ from TMEM to global memory.
+//   * warps 0-7 (element): w P = exp(S - LSE + log w) (the weight in the exponent),
+//     D = rowsum(w P * dPo) / w (stored; the retrieval score gradient sums it later),
+//     w P (dPo - D) into TMEM, and at the end of a tile dQ from TMEM to global memory,
+//     where it takes the 1/sqrt(dh) of the logits once.
 // TMEM (256 columns): S 0-63, dPo 64-127, dQ 128-191, two dS buffers (bf16 pairs, the A
 // operand of dQ += dS K) 192-223 and 224-255.
 //
@@ -337,17 +338,19 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       const float* lse_s = reinterpret_cast<const float*>(qbuf + buf * kQBuf + 2 * TILE);
       for (int si = 0; si < ns; ++si, ++gs) {
         const int m = M.slot[si];
-        const float lse0 = lse_s[m * 64 + row0] * kLog2e, lse1 = lse_s[m * 64 + row0 + 8] * kLog2e;
+        // w P = exp2(S sl2 - LSE log2 e + log2 w): the fusion weight rides in the exponent,
+        // so D comes out as w D and dS as dS / sqrt(dh) (the 1/sqrt(dh) goes onto dQ once
+        // per tile).
+        const float wm = M.w[m], lw = __log2f(wm);
+        const float lse0 = fmaf(-lse_s[m * 64 + row0], kLog2e, lw), lse1 = fmaf(-lse_s[m * 64 + row0 + 8], kLog2e, lw);
         // S(gs) complete; it was issued after dQ(gs - 2), so dS buffer gs & 1 is free too.
         if (!W(&bar_s, gs & 1, 8, k, gs)) {
           alive = false;
           break;
         }
         float s[4][4], dp[4][4];
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
+        tc::ld16x256_x4(tS + lane_base, s);
+        tc::ld16x256_x4(tP + lane_base, dp);
         tc::ld_wait(s);
         tc::ld_wait(dp);
         tc::fence_before();
@@ -356,10 +359,10 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         float D0 = 0.f, D1 = 0.f;
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          s[n][0] = tc::ex2(fmaf(s[n][0], sl2, -lse0));
-          s[n][1] = tc::ex2(fmaf(s[n][1], sl2, -lse0));
-          s[n][2] = tc::ex2(fmaf(s[n][2], sl2, -lse1));
-          s[n][3] = tc::ex2(fmaf(s[n][3], sl2, -lse1));
+          s[n][0] = tc::ex2(fmaf(s[n][0], sl2, lse0));
+          s[n][1] = tc::ex2(fmaf(s[n][1], sl2, lse0));
+          s[n][2] = tc::ex2(fmaf(s[n][2], sl2, lse1));
+          s[n][3] = tc::ex2(fmaf(s[n][3], sl2, lse1));
           D0 = fmaf(s[n][0], dp[n][0], fmaf(s[n][1], dp[n][1], D0));
           D1 = fmaf(s[n][2], dp[n][2], fmaf(s[n][3], dp[n][3], D1));
         }
@@ -380,16 +383,18 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
           break;
         }
         ++ewc;
-        D0 = Dx[gs & 1][0][row0] + Dx[gs & 1][1][row0];
-        D1 = Dx[gs & 1][0][row0 + 8] + Dx[gs & 1][1][row0 + 8];
-        const float cs = M.w[m] * scale;
+        // D = (w D) / w; a slot whose weight underflowed to 0 has w P = 0 and dS = 0, and
+        // its D rows are weighted by 0 wherever they are used.
+        const float rw = wm > 0.f ? 1.0f / wm : 0.f;
+        D0 = (Dx[gs & 1][0][row0] + Dx[gs & 1][1][row0]) * rw;
+        D1 = (Dx[gs & 1][0][row0 + 8] + Dx[gs & 1][1][row0 + 8]) * rw;
         // dS as the TMEM A operand of dQ += dS K: keys (32hc + 8n + 2cq, +1) of rows g and
         // g + 8 go to column 16hc + 4n + cq of buffer gs & 1.
         uint32_t dv[8];
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          dv[2 * n] = pack_bf16(s[n][0] * (dp[n][0] - D0) * cs, s[n][1] * (dp[n][1] - D0) * cs);
-          dv[2 * n + 1] = pack_bf16(s[n][2] * (dp[n][2] - D1) * cs, s[n][3] * (dp[n][3] - D1) * cs);
+          dv[2 * n] = pack_bf16(s[n][0] * (dp[n][0] - D0), s[n][1] * (dp[n][1] - D0));
+          dv[2 * n + 1] = pack_bf16(s[n][2] * (dp[n][2] - D1), s[n][3] * (dp[n][3] - D1));
         }
         tc::st16x128_x4(tdS + 32 * (gs & 1) + lane_q + 16 * hc, dv);
         tc::st_wait();
@@ -407,15 +412,15 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       if (!W(&dq_full, kq & 1, 9, k, gs)) break;
       ++kq;
       float o[4][4];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tQ + lane_base + cb * 8, o[cb]);
+      tc::ld16x256_x4(tQ + lane_base, o);
       tc::ld_wait(o);
       tc::fence_before();
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
         const int col = 32 * hc + 8 * n + 2 * cq;
-        *reinterpret_cast<uint32_t*>(dqg + (int64_t)row0 * ts + col) = pack_bf16(o[n][0], o[n][1]);
-        *reinterpret_cast<uint32_t*>(dqg + (int64_t)(row0 + 8) * ts + col) = pack_bf16(o[n][2], o[n][3]);
+        *reinterpret_cast<uint32_t*>(dqg + (int64_t)row0 * ts + col) = pack_bf16(o[n][0] * scale, o[n][1] * scale);
+        *reinterpret_cast<uint32_t*>(dqg + (int64_t)(row0 + 8) * ts + col) =
+            pack_bf16(o[n][2] * scale, o[n][3] * scale);
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&meta_empty[mb]);
@@ -457,7 +462,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
 //     columns (the tensor pipe runs this warp's products in issue order).  The barriers of the next batch
 //     are tested (test_wait, which does not block) and the records read before the
 //     current batch is issued, and looked at after it;
-//   * warps 0-7 (element): P^T = exp(S^T - LSE), dS^T = w P^T (dPo^T - D) / sqrt(dh);
+//   * warps 0-7 (element): w P^T = exp(S^T - LSE + log w) (the weight in the exponent),
+//     dS^T = w P^T (dPo^T - D) (the 1/sqrt(dh) goes onto dK once per tile);
 //     each warp stores its bf16 operands over the TMEM columns it has itself read (no
 //     cross-warp barrier).  After the consumer that follows a tile's last one they read
 //     the tile's dK and dV (each warp its 16 rows and 32 columns), release the
@@ -833,10 +839,8 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       if (!S(&acc_full, r.tc & 1, 31, r.tc, -1)) return false;
       tc::fence_after();
       float ov[4][4], ok[4][4];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tm + 128 + lane_q + 32 * hc + cb * 8, ov[cb]);
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tm + 192 + lane_q + 32 * hc + cb * 8, ok[cb]);
+      tc::ld16x256_x4(tm + 128 + lane_q + 32 * hc, ov);
+      tc::ld16x256_x4(tm + 192 + lane_q + 32 * hc, ok);
       tc::ld_wait(ov);
       tc::ld_wait(ok);
       tc::fence_before();
@@ -852,7 +856,8 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int64_t off = (int64_t)(r0 + 8 * half) * ts + col;
-          float k0 = ok[n][2 * half], k1 = ok[n][2 * half + 1], v0 = ov[n][2 * half], v1 = ov[n][2 * half + 1];
+          float k0 = ok[n][2 * half] * scale, k1 = ok[n][2 * half + 1] * scale;
+          float v0 = ov[n][2 * half], v1 = ov[n][2 * half + 1];
           if (a.acc_dkv) {
             const __nv_bfloat162 kk = *reinterpret_cast<const __nv_bfloat162*>(dkg + off);
             const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162*>(dvg + off);
@@ -881,27 +886,28 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       const unsigned char* sb = ring + (x % NST) * kKVStageBytes;
       const float* lrow = reinterpret_cast<const float*>(sb + 2 * TILE) + 32 * hc;
       const float* drow = lrow + 64;
-      const float w = r.w, cs = w * scale;
+      // w P^T = exp2(S^T sl2 - LSE log2 e + log2 w): the fusion weight rides in the exponent,
+      // and the 1/sqrt(dh) of dS^T goes onto dK once per tile.
+      const float lw = __log2f(r.w);
       // P^T from S^T, and w P^T into TMEM over the columns just read.
       if (!S(&bar_s1, x & 1, 30, r.tc, x)) {
         alive = false;
         break;
       }
       float p[4][4];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tb + cb * 8, p[cb]);
+      tc::ld16x256_x4(tb, p);
       tc::ld_wait(p);
       uint32_t pv[8];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {  // columns are queries 32hc + 8n + 2cq (+1)
         const float2 l2 = *reinterpret_cast<const float2*>(lrow + 8 * n + 2 * cq);
-        const float la = l2.x * kLog2e, lb = l2.y * kLog2e;
-        p[n][0] = tc::ex2(fmaf(p[n][0], sl2, -la));
-        p[n][1] = tc::ex2(fmaf(p[n][1], sl2, -lb));
-        p[n][2] = tc::ex2(fmaf(p[n][2], sl2, -la));
-        p[n][3] = tc::ex2(fmaf(p[n][3], sl2, -lb));
-        pv[2 * n] = pack_bf16(p[n][0] * w, p[n][1] * w);
-        pv[2 * n + 1] = pack_bf16(p[n][2] * w, p[n][3] * w);
+        const float oa = fmaf(-l2.x, kLog2e, lw), ob = fmaf(-l2.y, kLog2e, lw);
+        p[n][0] = tc::ex2(fmaf(p[n][0], sl2, oa));
+        p[n][1] = tc::ex2(fmaf(p[n][1], sl2, ob));
+        p[n][2] = tc::ex2(fmaf(p[n][2], sl2, oa));
+        p[n][3] = tc::ex2(fmaf(p[n][3], sl2, ob));
+        pv[2 * n] = pack_bf16(p[n][0], p[n][1]);
+        pv[2 * n + 1] = pack_bf16(p[n][2], p[n][3]);
       }
       // w P^T and dS^T as TMEM A operands (keys are rows): the pair of queries
       // (32hc + 8n + 2cq, +1) of key rows g and g + 8 goes to column 32hc + 4n + cq, inside
@@ -917,15 +923,14 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         break;
       }
       float dp[4][4];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tb + 64 + cb * 8, dp[cb]);
+      tc::ld16x256_x4(tb + 64, dp);
       tc::ld_wait(dp);
       uint32_t dv[8];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
         const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
-        dv[2 * n] = pack_bf16(p[n][0] * (dp[n][0] - d2.x) * cs, p[n][1] * (dp[n][1] - d2.y) * cs);
-        dv[2 * n + 1] = pack_bf16(p[n][2] * (dp[n][2] - d2.x) * cs, p[n][3] * (dp[n][3] - d2.y) * cs);
+        dv[2 * n] = pack_bf16(p[n][0] * (dp[n][0] - d2.x), p[n][1] * (dp[n][1] - d2.y));
+        dv[2 * n + 1] = pack_bf16(p[n][2] * (dp[n][2] - d2.x), p[n][3] * (dp[n][3] - d2.y));
       }
       tc::st16x128_x4(tb + 64, dv);
       tc::st_wait();
