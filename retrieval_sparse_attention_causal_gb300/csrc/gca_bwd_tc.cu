@@ -356,15 +356,27 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         tc::fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sfree[gs & 1]);
-        float D0 = 0.f, D1 = 0.f;
+        const uint64_t sl2x2 = tc::f2(sl2, sl2), o0 = tc::f2(lse0, lse0), o1 = tc::f2(lse1, lse1);
+        uint64_t D0x2 = tc::f2(0.f, 0.f), D1x2 = D0x2;
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          s[n][0] = tc::ex2(fmaf(s[n][0], sl2, lse0));
-          s[n][1] = tc::ex2(fmaf(s[n][1], sl2, lse0));
-          s[n][2] = tc::ex2(fmaf(s[n][2], sl2, lse1));
-          s[n][3] = tc::ex2(fmaf(s[n][3], sl2, lse1));
-          D0 = fmaf(s[n][0], dp[n][0], fmaf(s[n][1], dp[n][1], D0));
-          D1 = fmaf(s[n][2], dp[n][2], fmaf(s[n][3], dp[n][3], D1));
+          float x0, x1, x2, x3;
+          tc::uf2(tc::fma2(tc::f2(s[n][0], s[n][1]), sl2x2, o0), x0, x1);
+          tc::uf2(tc::fma2(tc::f2(s[n][2], s[n][3]), sl2x2, o1), x2, x3);
+          s[n][0] = tc::ex2(x0);
+          s[n][1] = tc::ex2(x1);
+          s[n][2] = tc::ex2(x2);
+          s[n][3] = tc::ex2(x3);
+          D0x2 = tc::fma2(tc::f2(s[n][0], s[n][1]), tc::f2(dp[n][0], dp[n][1]), D0x2);
+          D1x2 = tc::fma2(tc::f2(s[n][2], s[n][3]), tc::f2(dp[n][2], dp[n][3]), D1x2);
+        }
+        float D0, D1;
+        {
+          float u0, u1;
+          tc::uf2(D0x2, u0, u1);
+          D0 = u0 + u1;
+          tc::uf2(D1x2, u0, u1);
+          D1 = u0 + u1;
         }
 #pragma unroll
         for (int kx = 1; kx <= 2; kx <<= 1) {
@@ -391,10 +403,14 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         // dS as the TMEM A operand of dQ += dS K: keys (32hc + 8n + 2cq, +1) of rows g and
         // g + 8 go to column 16hc + 4n + cq of buffer gs & 1.
         uint32_t dv[8];
+        const uint64_t nD0 = tc::f2(-D0, -D0), nD1 = tc::f2(-D1, -D1);
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          dv[2 * n] = pack_bf16(s[n][0] * (dp[n][0] - D0), s[n][1] * (dp[n][1] - D0));
-          dv[2 * n + 1] = pack_bf16(s[n][2] * (dp[n][2] - D1), s[n][3] * (dp[n][3] - D1));
+          float a0, a1, b0, b1;
+          tc::uf2(tc::mul2(tc::f2(s[n][0], s[n][1]), tc::add2(tc::f2(dp[n][0], dp[n][1]), nD0)), a0, a1);
+          tc::uf2(tc::mul2(tc::f2(s[n][2], s[n][3]), tc::add2(tc::f2(dp[n][2], dp[n][3]), nD1)), b0, b1);
+          dv[2 * n] = pack_bf16(a0, a1);
+          dv[2 * n + 1] = pack_bf16(b0, b1);
         }
         tc::st16x128_x4(tdS + 32 * (gs & 1) + lane_q + 16 * hc, dv);
         tc::st_wait();
@@ -898,14 +914,18 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       tc::ld16x256_x4(tb, p);
       tc::ld_wait(p);
       uint32_t pv[8];
+      const uint64_t sl2x2 = tc::f2(sl2, sl2), nl2e = tc::f2(-kLog2e, -kLog2e), lwx2 = tc::f2(lw, lw);
 #pragma unroll
       for (int n = 0; n < 4; ++n) {  // columns are queries 32hc + 8n + 2cq (+1)
-        const float2 l2 = *reinterpret_cast<const float2*>(lrow + 8 * n + 2 * cq);
-        const float oa = fmaf(-l2.x, kLog2e, lw), ob = fmaf(-l2.y, kLog2e, lw);
-        p[n][0] = tc::ex2(fmaf(p[n][0], sl2, oa));
-        p[n][1] = tc::ex2(fmaf(p[n][1], sl2, ob));
-        p[n][2] = tc::ex2(fmaf(p[n][2], sl2, oa));
-        p[n][3] = tc::ex2(fmaf(p[n][3], sl2, ob));
+        const uint64_t l2 = *reinterpret_cast<const uint64_t*>(lrow + 8 * n + 2 * cq);
+        const uint64_t off = tc::fma2(l2, nl2e, lwx2);  // log2 w - LSE log2 e of both columns
+        float x0, x1, x2, x3;
+        tc::uf2(tc::fma2(tc::f2(p[n][0], p[n][1]), sl2x2, off), x0, x1);
+        tc::uf2(tc::fma2(tc::f2(p[n][2], p[n][3]), sl2x2, off), x2, x3);
+        p[n][0] = tc::ex2(x0);
+        p[n][1] = tc::ex2(x1);
+        p[n][2] = tc::ex2(x2);
+        p[n][3] = tc::ex2(x3);
         pv[2 * n] = pack_bf16(p[n][0], p[n][1]);
         pv[2 * n + 1] = pack_bf16(p[n][2], p[n][3]);
       }
@@ -926,11 +946,15 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       tc::ld16x256_x4(tb + 64, dp);
       tc::ld_wait(dp);
       uint32_t dv[8];
+      const uint64_t neg1 = tc::f2(-1.f, -1.f);
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
-        const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
-        dv[2 * n] = pack_bf16(p[n][0] * (dp[n][0] - d2.x), p[n][1] * (dp[n][1] - d2.y));
-        dv[2 * n + 1] = pack_bf16(p[n][2] * (dp[n][2] - d2.x), p[n][3] * (dp[n][3] - d2.y));
+        const uint64_t d2 = *reinterpret_cast<const uint64_t*>(drow + 8 * n + 2 * cq);
+        float a0, a1, b0, b1;
+        tc::uf2(tc::mul2(tc::f2(p[n][0], p[n][1]), tc::fma2(d2, neg1, tc::f2(dp[n][0], dp[n][1]))), a0, a1);
+        tc::uf2(tc::mul2(tc::f2(p[n][2], p[n][3]), tc::fma2(d2, neg1, tc::f2(dp[n][2], dp[n][3]))), b0, b1);
+        dv[2 * n] = pack_bf16(a0, a1);
+        dv[2 * n + 1] = pack_bf16(b0, b1);
       }
       tc::st16x128_x4(tb + 64, dv);
       tc::st_wait();
