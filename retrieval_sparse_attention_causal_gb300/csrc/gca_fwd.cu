@@ -213,9 +213,10 @@ __global__ void __launch_bounds__(128) gca_fwd_mma_kernel(FwdArgs a) {
 //     have stored P~, O += P~ V into columns 64-127 (M = 64, N = 64, K steps of 16); the
 //     next slot's S goes into the same columns after the PV product (the tensor pipe runs
 //     this warp's products in issue order), across tile boundaries too;
-//   * warps 0-3 (softmax): read S with tcgen05.ld, do the row softmax in registers, write
-//     the slot's LSE row and store P~ = (w_m / l) P as bf16 pairs into TMEM columns 0-31,
-//     the A operand of O += P~ V (V MN-major from shared memory).  After a tile's last slot
+//   * warps 0-3 (softmax): read S with tcgen05.ld, do the row softmax in registers (packed
+//     f32x2 arithmetic on pairs of columns), write the slot's LSE row and store
+//     P~ = (w_m / l) P as bf16 pairs into TMEM columns 0-31, the A operand of O += P~ V
+//     (V MN-major from shared memory).  After a tile's last slot
 //     they read O, release the accumulator and write O out as bf16 from registers.
 // A tile's only start-up cost is then reading O out: the next tile's metadata, Q and first
 // K/V tiles are loaded while the current tile runs.
@@ -494,16 +495,28 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
         }
-        const float o0 = -mx0 * sl2, o1 = -mx1 * sl2;
-        float l0 = 0.f, l1 = 0.f;
+        const uint64_t sl2x2 = tc::f2(sl2, sl2);
+        const uint64_t o0 = tc::f2(-mx0 * sl2, -mx0 * sl2), o1 = tc::f2(-mx1 * sl2, -mx1 * sl2);
+        uint64_t l0x2 = tc::f2(0.f, 0.f), l1x2 = l0x2;
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
-          s[n][0] = tc::ex2(fmaf(s[n][0], sl2, o0));
-          s[n][1] = tc::ex2(fmaf(s[n][1], sl2, o0));
-          s[n][2] = tc::ex2(fmaf(s[n][2], sl2, o1));
-          s[n][3] = tc::ex2(fmaf(s[n][3], sl2, o1));
-          l0 += s[n][0] + s[n][1];
-          l1 += s[n][2] + s[n][3];
+          float x0, x1, x2, x3;
+          tc::uf2(tc::fma2(tc::f2(s[n][0], s[n][1]), sl2x2, o0), x0, x1);
+          tc::uf2(tc::fma2(tc::f2(s[n][2], s[n][3]), sl2x2, o1), x2, x3);
+          s[n][0] = tc::ex2(x0);
+          s[n][1] = tc::ex2(x1);
+          s[n][2] = tc::ex2(x2);
+          s[n][3] = tc::ex2(x3);
+          l0x2 = tc::add2(l0x2, tc::f2(s[n][0], s[n][1]));
+          l1x2 = tc::add2(l1x2, tc::f2(s[n][2], s[n][3]));
+        }
+        float l0, l1;
+        {
+          float u0, u1;
+          tc::uf2(l0x2, u0, u1);
+          l0 = u0 + u1;
+          tc::uf2(l1x2, u0, u1);
+          l1 = u0 + u1;
         }
 #pragma unroll
         for (int m = 1; m <= 2; m <<= 1) {
@@ -517,6 +530,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
           lse[mslot * 64 + row0 + 8] = mx1 * scale + __logf(l1);
         }
         const float c0 = __fdividef(wm, l0), c1 = __fdividef(wm, l1);
+        const uint64_t c0x2 = tc::f2(c0, c0), c1x2 = tc::f2(c1, c1);
         // P~ as the TMEM A operand: the pair of keys (8n + 2cq, +1) of rows g and g + 8
         // goes to column 4n + cq (two 16-column stores).
 #pragma unroll
@@ -524,8 +538,11 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
           uint32_t pv[8];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            pv[2 * i] = pack_bf16(s[4 * half + i][0] * c0, s[4 * half + i][1] * c0);
-            pv[2 * i + 1] = pack_bf16(s[4 * half + i][2] * c1, s[4 * half + i][3] * c1);
+            float a0, a1, b0, b1;
+            tc::uf2(tc::mul2(tc::f2(s[4 * half + i][0], s[4 * half + i][1]), c0x2), a0, a1);
+            tc::uf2(tc::mul2(tc::f2(s[4 * half + i][2], s[4 * half + i][3]), c1x2), b0, b1);
+            pv[2 * i] = pack_bf16(a0, a1);
+            pv[2 * i + 1] = pack_bf16(b0, b1);
           }
           tc::st16x128_x4(tS + lane_base + 16 * half, pv);
         }
