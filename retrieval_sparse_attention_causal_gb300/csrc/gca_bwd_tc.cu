@@ -134,6 +134,11 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   __syncthreads();
   tc::fence_after();
   const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tQ = tmem_slot + 128, tdS = tmem_slot + 192;
+  // The producer and the element warps park while they wait (no issue slots taken from
+  // the warps that work); the MMA warp spins.
+  auto P = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
+    return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
+  };
   auto W = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
     return wait_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
   };
@@ -146,7 +151,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     // Metadata of tile k (whole warp): slots and fusion weights of its retrieval row.
     auto prepare_meta = [&](int k, int t) -> bool {
       const int mb = k % kMetaBufs;
-      if (k >= kMetaBufs && !W(&meta_empty[mb], ((k / kMetaBufs) - 1) & 1, 1, k, -1)) return false;
+      if (k >= kMetaBufs && !P(&meta_empty[mb], ((k / kMetaBufs) - 1) & 1, 1, k, -1)) return false;
       const int c = t % a.nQ, b = t / (a.nQ * a.H);
       const int r = c - a.shift;
       QTileMeta& M = meta[mb];
@@ -175,7 +180,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       const int buf = k & 1;
       const int c = t % a.nQ, h = (t / a.nQ) % a.H, b = t / (a.nQ * a.H);
       if (lane == 0) {  // Q, dO and the LSE rows of tile k
-        if (k >= 2 && !W(&qfree[buf], ((k - 2) >> 1) & 1, 2, k, -1)) {
+        if (k >= 2 && !P(&qfree[buf], ((k - 2) >> 1) & 1, 2, k, -1)) {
           alive = false;
         } else {
           unsigned char* Qs = qbuf + buf * kQBuf;
@@ -197,7 +202,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         const int n = M.ns;
         for (int x = 0; x < n; ++x, ++gs) {
           const int st = gs % NST;
-          if (gs >= NST && !W(&ring_empty[st], ((gs / NST) - 1) & 1, 3, k, gs)) {
+          if (gs >= NST && !P(&ring_empty[st], ((gs / NST) - 1) & 1, 3, k, gs)) {
             alive = false;
             break;
           }
@@ -320,7 +325,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       const int64_t rowbase = ((int64_t)b * a.nQ + c) * a.H + h;
       float* Dg = a.Dbuf + rowbase * a.topk * 64;
       const int mb = k % kMetaBufs;
-      if (!W(&meta_full[mb], (k / kMetaBufs) & 1, 7, k, -1)) break;
+      if (!P(&meta_full[mb], (k / kMetaBufs) & 1, 7, k, -1)) break;
       const QTileMeta& M = meta[mb];
       const int ns = M.ns;
       if (ns == 0) {  // nothing retrieved: dQ is zero
@@ -334,7 +339,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       }
       // The tile's LSE rows came with its Q and dO (observe that phase; the MMA warp has
       // waited for it before issuing the tile's first product).
-      if (!W(&bar_q[buf], (k >> 1) & 1, 14, k, -1)) break;
+      if (!P(&bar_q[buf], (k >> 1) & 1, 14, k, -1)) break;
       const float* lse_s = reinterpret_cast<const float*>(qbuf + buf * kQBuf + 2 * TILE);
       for (int si = 0; si < ns; ++si, ++gs) {
         const int m = M.slot[si];
@@ -344,7 +349,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         const float wm = M.w[m], lw = __log2f(wm);
         const float lse0 = fmaf(-lse_s[m * 64 + row0], kLog2e, lw), lse1 = fmaf(-lse_s[m * 64 + row0 + 8], kLog2e, lw);
         // S(gs) complete; it was issued after dQ(gs - 2), so dS buffer gs & 1 is free too.
-        if (!W(&bar_s, gs & 1, 8, k, gs)) {
+        if (!P(&bar_s, gs & 1, 8, k, gs)) {
           alive = false;
           break;
         }
@@ -390,7 +395,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&ewb);
-        if (!W(&ewb, ewc & 1, 12, k, gs)) {
+        if (!P(&ewb, ewc & 1, 12, k, gs)) {
           alive = false;
           break;
         }
@@ -425,7 +430,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       if (!alive) break;
       // Tile epilogue: dQ from TMEM straight to global memory (each warp its 16 rows and
       // 32 columns; no staging, so the K / V ring can hold one more stage).
-      if (!W(&dq_full, kq & 1, 9, k, gs)) break;
+      if (!P(&dq_full, kq & 1, 9, k, gs)) break;
       ++kq;
       float o[4][4];
       tc::ld16x256_x4(tQ + lane_base, o);
@@ -583,8 +588,8 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
   __syncthreads();
   tc::fence_after();
   const uint32_t tm = tmem_slot;
-  // Waits of the roles off the critical path park the warp (no issue slots taken); the
-  // MMA warp and the element warps spin (a parked warp wakes up later).
+  // Waits park the warp (no issue slots taken from the warps that work), except the MMA
+  // warp's, which spin: it has the shortest hand-overs and a parked warp wakes up later.
   auto W = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
     return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
   };
@@ -852,7 +857,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     const float sl2 = scale * kLog2e;
     // A finished tile's dK and dV from TMEM, straight to global memory.
     auto write_out = [&](const KVConsRec& r) -> bool {
-      if (!S(&acc_full, r.tc & 1, 31, r.tc, -1)) return false;
+      if (!W(&acc_full, r.tc & 1, 31, r.tc, -1)) return false;
       tc::fence_after();
       float ov[4][4], ok[4][4];
       tc::ld16x256_x4(tm + 128 + lane_q + 32 * hc, ov);
@@ -906,7 +911,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       // and the 1/sqrt(dh) of dS^T goes onto dK once per tile.
       const float lw = __log2f(r.w);
       // P^T from S^T, and w P^T into TMEM over the columns just read.
-      if (!S(&bar_s1, x & 1, 30, r.tc, x)) {
+      if (!W(&bar_s1, x & 1, 30, r.tc, x)) {
         alive = false;
         break;
       }
@@ -938,7 +943,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&op_v);
       // dS^T from dPo^T.
-      if (!S(&bar_s2, x & 1, 33, r.tc, x)) {
+      if (!W(&bar_s2, x & 1, 33, r.tc, x)) {
         alive = false;
         break;
       }
