@@ -134,8 +134,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   __syncthreads();
   tc::fence_after();
   const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tQ = tmem_slot + 128, tdS = tmem_slot + 192;
-  // The producer and the element warps park while they wait (no issue slots taken from
-  // the warps that work); the MMA warp spins.
+  // Every role but the metadata one parks while it waits (try_wait with a suspend hint),
+  // so that a waiting warp takes no issue slots from the warps that work.
   auto P = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
     return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
   };
@@ -237,9 +237,9 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     auto take_tile = [&](int k, int t) -> int {
       if (t >= ntiles) return -1;
       const int buf = k & 1, mb = k % kMetaBufs;
-      if (!W(&meta_full[mb], (k / kMetaBufs) & 1, 4, k, -1)) return -2;
+      if (!P(&meta_full[mb], (k / kMetaBufs) & 1, 4, k, -1)) return -2;
       const int ns = meta[mb].ns;
-      if (!W(&bar_q[buf], (k >> 1) & 1, 5, k, -1)) return -2;
+      if (!P(&bar_q[buf], (k >> 1) & 1, 5, k, -1)) return -2;
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(&meta_empty[mb]);
@@ -250,7 +250,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     auto issue_s = [&](int g, int buf, int k) -> bool {  // S, dPo of global slot g (whole warp)
       const uint64_t dq = dQ0 + buf * (kQBuf >> 4), ddo = dq + kTileStep;
       const uint64_t dk = dRingKm + (g % NST) * kStage, dv = dk + kTileStep;
-      if (!W(&bar_kv[g % NST], (g / NST) & 1, 6, k, g)) return false;
+      if (!P(&bar_kv[g % NST], (g / NST) & 1, 6, k, g)) return false;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks) {
         tc::mma_warp(tS, dq + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
@@ -267,14 +267,14 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     if (ns > 0 && !issue_s(0, k & 1, k)) ns = -2;
     while (ns > 0) {
       // S(g), dPo(g) are in the element warps' registers: the next pair may overwrite them.
-      if (!W(&sfree[g & 1], (g >> 1) & 1, 10, k, g)) break;
+      if (!P(&sfree[g & 1], (g >> 1) & 1, 10, k, g)) break;
       int nk = k, nt = t, nns = ns, nsi = si + 1;
       const bool last = nsi == ns;
       // Inside a tile the next slot's S, dPo go first, to overlap this slot's dS.  After a
       // tile's last slot its dQ goes first: the next tile's first K / V tiles may still be
       // on their way, and the tile's write-out should not wait for them.
       if (!last && !issue_s(g + 1, k & 1, k)) break;
-      if (!W(&opready[g & 1], (g >> 1) & 1, 11, k, g)) break;  // dS(g) is in buffer g & 1
+      if (!P(&opready[g & 1], (g >> 1) & 1, 11, k, g)) break;  // dS(g) is in buffer g & 1
       tc::fence_after();
       const uint64_t dk = dRingMn + (g % NST) * kStage;
       const uint32_t ta = tdS + 32 * (g & 1);
@@ -402,7 +402,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
         ++ewc;
         // D = (w D) / w; a slot whose weight underflowed to 0 has w P = 0 and dS = 0, and
         // its D rows are weighted by 0 wherever they are used.
-        const float rw = wm > 0.f ? 1.0f / wm : 0.f;
+        const float rw = wm > 0.f ? __frcp_rn(wm) : 0.f;
         D0 = (Dx[gs & 1][0][row0] + Dx[gs & 1][1][row0]) * rw;
         D1 = (Dx[gs & 1][0][row0 + 8] + Dx[gs & 1][1][row0 + 8]) * rw;
         // dS as the TMEM A operand of dQ += dS K: keys (32hc + 8n + 2cq, +1) of rows g and
@@ -588,13 +588,10 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
   __syncthreads();
   tc::fence_after();
   const uint32_t tm = tmem_slot;
-  // Waits park the warp (no issue slots taken from the warps that work), except the MMA
-  // warp's, which spin: it has the shortest hand-overs and a parked warp wakes up later.
+  // Every role parks while it waits (try_wait with a suspend hint), so that a waiting warp
+  // takes no issue slots from the warps that work.
   auto W = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
     return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
-  };
-  auto S = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
-    return spin_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
   };
 
   if (warp == kKVMetaW) {
@@ -777,7 +774,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     // overwrites dS^T(x), which only dK(x) reads; so S^T(x + 1) runs while the element warps
     // still form dS^T(x), and they find it done when they move on.
     auto issue_st = [&](int y, const KVConsRec& r) -> bool {  // S^T(y) = K Q^T
-      if ((r.flags & kRecFirst) && !S(&bar_kv[r.kb], (r.tc >> 1) & 1, 25, r.tc, y)) return false;
+      if ((r.flags & kRecFirst) && !W(&bar_kv[r.kb], (r.tc >> 1) & 1, 25, r.tc, y)) return false;
       const uint64_t dk = dKV + (2 * r.kb) * kTileStep;
       const uint64_t dq = dRingKm + (y % NST) * kStage;
 #pragma unroll
@@ -798,7 +795,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     };
     int nend = 0x7fffffff, x = 0;
     KVConsRec rx;  // record of consumer x
-    bool ok = S(&bar_c[0], 0, 24, -1, 0);
+    bool ok = W(&bar_c[0], 0, 24, -1, 0);
     if (ok) {
       rx = *crec(0);
       if (rx.flags & kRecEnd) {
@@ -810,9 +807,9 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     }
     for (x = 0; ok && x < nend; ++x) {
       // dV += (w P^T) dO as soon as w P^T is in, while the element warps form dS^T.
-      if (!S(&op_v, x & 1, 26, rx.tc, x)) break;
+      if (!W(&op_v, x & 1, 26, rx.tc, x)) break;
       tc::fence_after();
-      if ((rx.flags & kRecFirst) && rx.tc >= 1 && !S(&acc_empty, (rx.tc - 1) & 1, 27, rx.tc, x)) break;
+      if ((rx.flags & kRecFirst) && rx.tc >= 1 && !W(&acc_empty, (rx.tc - 1) & 1, 27, rx.tc, x)) break;
       const uint64_t bq = dRingMn + (x % NST) * kStage, bdo = bq + kTileStep;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -821,12 +818,12 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
         tc::mma_ts_warp(tdV, tS + aoff, bdo + kk * tc::kKStepMn, kIdMn, acc);
       }
       // S^T(x + 1), if there is a next consumer.
-      if (!S(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1, 24, rx.tc, x + 1)) break;
+      if (!W(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1, 24, rx.tc, x + 1)) break;
       const KVConsRec rn = *crec(x + 1);
       const bool more = !(rn.flags & kRecEnd);
       if (more && !issue_st(x + 1, rn)) break;
       // dK += dS^T Q once dS^T is in.
-      if (!S(&op_k, x & 1, 32, rx.tc, x)) break;
+      if (!W(&op_k, x & 1, 32, rx.tc, x)) break;
       tc::fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {

@@ -283,6 +283,12 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
   auto W = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
     return wait_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
   };
+  // The MMA and softmax warps park while they wait (try_wait with a suspend hint), so that
+  // a waiting warp leaves its SM sub-partition's issue slots to the warps that work.
+  auto P = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
+    return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
+  };
+
 
   if (warp == kFwdMeta) {
     // ------------------------------------------------------------ metadata warp
@@ -376,7 +382,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
     int gs = 0, tq = 0;
     // S of global slot g (tile with Q buffer qb).
     auto issue_s = [&](int g, int qb) -> bool {
-      if (!W(&bar_kv[g % NST], (g / NST) & 1, 44, -1, g)) return false;
+      if (!P(&bar_kv[g % NST], (g / NST) & 1, 44, -1, g)) return false;
       const uint64_t dq = dQ0 + qb * kTileStep, dk = dRingKm + (g % NST) * kStage;
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks)
@@ -389,7 +395,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
     bool pending_s = false;  // S of the current tile's first slot was issued at the end of the last tile
     for (int k = 0; alive; ++k) {
       const int mb = k % MR;
-      if (!W(&meta_full[mb], (k / MR) & 1, 45, k, -1)) break;
+      if (!P(&meta_full[mb], (k / MR) & 1, 45, k, -1)) break;
       const int ns = meta[mb].ns, end = meta[mb].end;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&meta_empty[mb]);
@@ -397,17 +403,17 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       if (ns == 0) continue;
       const int qb = tq & 1;
       if (!pending_s) {
-        if (!W(&bar_q[qb], (tq >> 1) & 1, 46, k, -1)) break;
+        if (!P(&bar_q[qb], (tq >> 1) & 1, 46, k, -1)) break;
         if (!issue_s(gs, qb)) break;
       }
       pending_s = false;
       for (int si = 0; si < ns; ++si, ++gs) {
-        if (!W(&pready, gs & 1, 47, k, gs)) {  // P~(gs) is in TMEM columns 0-31
+        if (!P(&pready, gs & 1, 47, k, gs)) {  // P~(gs) is in TMEM columns 0-31
           alive = false;
           break;
         }
         tc::fence_after();
-        if (si == 0 && tq >= 1 && !W(&o_free, (tq - 1) & 1, 48, k, gs)) {  // the last tile's O is read
+        if (si == 0 && tq >= 1 && !P(&o_free, (tq - 1) & 1, 48, k, gs)) {  // the last tile's O is read
           alive = false;
           break;
         }
@@ -428,7 +434,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
           const int nb = (k + 1) % MR;
           if (tc::mbar_test(&meta_full[nb], ((k + 1) / MR) & 1)) {
             const FwdMeta& N = meta[nb];
-            if (!N.end && N.ns > 0 && W(&bar_q[(tq + 1) & 1], ((tq + 1) >> 1) & 1, 46, k + 1, -1)) {
+            if (!N.end && N.ns > 0 && P(&bar_q[(tq + 1) & 1], ((tq + 1) >> 1) & 1, 46, k + 1, -1)) {
               if (!issue_s(gs + 1, (tq + 1) & 1)) {
                 alive = false;
                 break;
@@ -455,7 +461,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
     int gs = 0, tq = 0;
     for (int k = 0;; ++k) {
       const int mb = k % MR;
-      if (!W(&meta_full[mb], (k / MR) & 1, 50, k, -1)) break;
+      if (!P(&meta_full[mb], (k / MR) & 1, 50, k, -1)) break;
       const FwdMeta& M = meta[mb];
       if (M.end) break;
       const int ns = M.ns, c = M.c, h = M.h, b = M.b;
@@ -477,7 +483,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       for (int si = 0; si < ns; ++si, ++gs) {
         // S(gs) from the MMA-completion barrier (the next S is issued only after every
         // softmax warp has handed over P~(gs), so the phase cannot run ahead).
-        if (!W(&bar_s, gs & 1, 51, k, gs)) {
+        if (!P(&bar_s, gs & 1, 51, k, gs)) {
           alive = false;
           break;
         }
@@ -554,7 +560,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       if (!alive) break;
       // The tile's O: from TMEM (once the last O += P~ V is done), then straight to global
       // memory from registers.
-      if (!W(&o_full, tq & 1, 52, k, gs)) break;
+      if (!P(&o_full, tq & 1, 52, k, gs)) break;
       tc::fence_after();
       float o[8][4];
       tc::ld16x256_x8(tO + lane_base, o);
