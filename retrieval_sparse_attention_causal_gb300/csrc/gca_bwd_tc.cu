@@ -96,9 +96,10 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   __shared__ int abort_s;
   // Phases: meta_* and bar_q / qfree per use of a buffer; bar_kv / ring_empty per use of
   // a stage; bar_s per slot; sfree / opready alternate by slot parity (each waited once per
-  // two slots, so no waiter can be lapped); ewb per element-warp exchange; dq_full per tile.
+  // two slots, so no waiter can be lapped); ewb[q] per exchange between the two element
+  // warps of row quarter q; dq_full per tile.
   __shared__ __align__(8) uint64_t meta_full[kMetaBufs], meta_empty[kMetaBufs], bar_q[2], qfree[2], bar_kv[NST],
-      ring_empty[NST], bar_s, sfree[2], opready[2], ewb, dq_full, drain;
+      ring_empty[NST], bar_s, sfree[2], opready[2], ewb[4], dq_full, drain;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ts = (int64_t)a.H * DH;
   const int ntiles = a.nQ * a.H * a.B;
@@ -119,7 +120,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       tc::mbar_init(&ring_empty[st], 1);
     }
     tc::mbar_init(&bar_s, 1);
-    tc::mbar_init(&ewb, kEW);
+    for (int x = 0; x < 4; ++x) tc::mbar_init(&ewb[x], 2);
     tc::mbar_init(&dq_full, 1);
     tc::mbar_init(&drain, 1);
     tc::fence_mbar_init();
@@ -394,8 +395,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
           Dx[gs & 1][hc][row0 + 8] = D1;
         }
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&ewb);
-        if (!P(&ewb, ewc & 1, 12, k, gs)) {
+        if (lane == 0) tc::mbar_arrive(&ewb[quarter]);
+        if (!W(&ewb[quarter], ewc & 1, 12, k, gs)) {
           alive = false;
           break;
         }

@@ -236,7 +236,7 @@ struct FwdMeta {
 __global__ void __launch_bounds__(kFwdThreads, 4)
 gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV) {
-  constexpr int DH = 64, ROWB = 128, TILE = 8192, NST = kFwdStages, MR = kFwdMetaRecs;
+  constexpr int DH = 64, TILE = 8192, NST = kFwdStages, MR = kFwdMetaRecs;
   constexpr uint32_t kIdS = tc::idesc_bf16(64, 64, false);
   constexpr uint32_t kIdPV = tc::idesc_bf16(64, DH, true);
   extern __shared__ __align__(1024) unsigned char dsm[];
@@ -280,11 +280,8 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
   __syncthreads();
   tc::fence_after();
   const uint32_t tS = tmem_slot, tO = tmem_slot + 64;
-  auto W = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
-    return wait_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
-  };
-  // The MMA and softmax warps park while they wait (try_wait with a suspend hint), so that
-  // a waiting warp leaves its SM sub-partition's issue slots to the warps that work.
+  // Every role parks while it waits (try_wait with a suspend hint), so that a waiting warp
+  // leaves its SM sub-partition's issue slots to the warps that work.
   auto P = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
     return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
   };
@@ -295,7 +292,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
     int k = 0;
     for (int t = blockIdx.x;; t += gridDim.x, ++k) {
       const int mb = k % MR;
-      if (k >= MR && !W(&meta_empty[mb], ((k / MR) - 1) & 1, 40, k, -1)) break;
+      if (k >= MR && !P(&meta_empty[mb], ((k / MR) - 1) & 1, 40, k, -1)) break;
       FwdMeta& M = meta[mb];
       if (t >= ntiles) {
         if (lane == 0) {
@@ -334,7 +331,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
       for (int st = 0; st < NST; ++st) nkv[st] = 0;
       for (int k = 0;; ++k) {
         const int mb = k % MR;
-        if (!W(&meta_full[mb], (k / MR) & 1, 41, k, -1)) break;
+        if (!P(&meta_full[mb], (k / MR) & 1, 41, k, -1)) break;
         const FwdMeta& M = meta[mb];
         if (M.end) break;
         const int ns = M.ns, c = M.c, h = M.h, b = M.b;
@@ -342,13 +339,13 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
         bool ok = true;
         if (ns > 0) {
           const int qb = tq & 1;
-          if (tq >= 2 && !W(&qfree[qb], ((tq >> 1) - 1) & 1, 42, k, -1)) break;
+          if (tq >= 2 && !P(&qfree[qb], ((tq >> 1) - 1) & 1, 42, k, -1)) break;
           tc::mbar_expect_tx(&bar_q[qb], TILE);
           tc::tma_load_4d(qbuf + qb * TILE, &tmQ, 0, h, c * 64, b, &bar_q[qb]);
           ++nq[qb];
           for (int x = 0; x < ns; ++x, ++gs) {
             const int st = gs % NST;
-            if (gs >= NST && !W(&ring_empty[st], ((gs / NST) - 1) & 1, 43, k, gs)) {
+            if (gs >= NST && !P(&ring_empty[st], ((gs / NST) - 1) & 1, 43, k, gs)) {
               ok = false;
               break;
             }
