@@ -300,11 +300,13 @@ __global__ void __launch_bounds__(256) retrieve_merge_heads_kernel(RetrieveArgs 
 }
 
 // ------------------------------------------------------------------ tile kernel
-// Shared memory: Q block (64 rows x D), two candidate chunk buffers, score tile.
+// Shared memory: Q block (64 rows x D), a ring of candidate chunk buffers (bf16; two for
+// f32), score tile.
+constexpr int kTileStages = 6;  // 64-candidate x 64-dim chunks in flight (bf16)
 struct TileSmem {
   static constexpr int kSt = 65;  // padded score-tile row (floats)
   static size_t bytes(int D, bool bf16) {
-    if (bf16) return (size_t)64 * D * 2 + 2 * 64 * 128 + 64 * kSt * 4 + 1024;
+    if (bf16) return (size_t)64 * D * 2 + kTileStages * 64 * 128 + 64 * kSt * 4 + 1024;
     return (size_t)64 * (D + 1) * 4 + 64 * 33 * 4 + 64 * kSt * 4 + 1024;
   }
 };
@@ -383,8 +385,8 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
       // ---------------- bf16: tensor-core score tiles
       const int nkc = a.D / 64;
       unsigned char* Qs = smem;                        // [nkc][64][128B] swizzled
-      unsigned char* Ks = smem + (size_t)64 * a.D * 2;  // [2][64][128B]
-      float* St = reinterpret_cast<float*>(Ks + 2 * 64 * 128);
+      unsigned char* Ks = smem + (size_t)64 * a.D * 2;  // [kTileStages][64][128B]
+      float* St = reinterpret_cast<float*>(Ks + kTileStages * 64 * 128);
       // Q block, all chunks.
       for (int u = tid; u < 64 * a.D / 8; u += kTileThreads) {
         const int r = u / (a.D / 8), cu = u % (a.D / 8);
@@ -405,9 +407,14 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
           else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
         }
       };
+      // A ring of kTileStages chunks: kTileStages - 1 loads stay in flight ahead of the
+      // products (one commit group per step, empty ones past the end, so that the group
+      // count stays uniform; the Q block rides in the first group).
       const int nsteps = ntiles * nkc;
-      load_chunk(0, 0);
-      cp_async_commit();
+      for (int st = 0; st < kTileStages - 1; ++st) {
+        if (st < nsteps) load_chunk(st, st);
+        cp_async_commit();
+      }
       const int rw = 16 * (warp & 3), cw = 32 * (warp >> 2);
       float acc[4][4];
 #pragma unroll
@@ -415,11 +422,11 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
       for (int step = 0; step < nsteps; ++step) {
-        const int stage = step & 1;
-        if (step + 1 < nsteps) load_chunk(step + 1, stage ^ 1);
+        const int stage = step % kTileStages;
+        cp_async_wait<kTileStages - 2>();
+        __syncthreads();  // chunk `step` is in; the stage of step - 1 is free
+        if (step + kTileStages - 1 < nsteps) load_chunk(step + kTileStages - 1, (step + kTileStages - 1) % kTileStages);
         cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
         const int kc = step % nkc;
         const uint32_t qbase = smem_u32(Qs + (size_t)kc * 8192);
         const uint32_t kbase = smem_u32(Ks + stage * 8192);
