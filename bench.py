@@ -193,17 +193,17 @@ KERNEL_SOURCES = {
     "retrieve_tc": ("retrieve_tc.cu", "tc.cuh", "tc_rows.cuh", "common.cuh"),
 }
 KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
-    "gca_fwd": (3.8264e+08, "9db82854879ee7b2"),
-    "gca_bwd_q": (5.0959e+08, "a93699f6857b04e8"),
-    "gca_bwd_kv": (7.0233e+08, "a93699f6857b04e8"),
+    "gca_fwd": (3.8215e+08, "32cbda635a9277de"),
+    "gca_bwd_q": (5.1005e+08, "9c16b486d058caa1"),
+    "gca_bwd_kv": (6.9441e+08, "9c16b486d058caa1"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (805479936 / 2, "4123911e1562b21a")
+STREAM_TRAFFIC_PER_SEQ = (805415424 / 2, "5d39e2bed0dad9dc")
 
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
 # nothing written back past L2; traffic grows with the number of chunks)
-PREFILL_TRAFFIC_PER_CHUNK = (25216768 / 8192, "e88e251646775069")
+PREFILL_TRAFFIC_PER_CHUNK = (25217280 / 8192, "e88e251646775069")
 
 
 def source_fingerprint(kernel: str) -> str:
