@@ -401,9 +401,10 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
           break;
         }
         ++ewc;
-        // D = (w D) / w; a slot whose weight underflowed to 0 has w P = 0 and dS = 0, and
-        // its D rows are weighted by 0 wherever they are used.
-        const float rw = wm > 0.f ? __frcp_rn(wm) : 0.f;
+        // D = (w D) / w.  A slot whose weight is 0 or subnormal (its 1/w would overflow) has
+        // w P = 0 and dS = 0, and its D rows are weighted by that w wherever they are used,
+        // so they are set to 0.
+        const float rw = wm >= 1.17549435e-38f ? __frcp_rn(wm) : 0.f;
         D0 = (Dx[gs & 1][0][row0] + Dx[gs & 1][1][row0]) * rw;
         D1 = (Dx[gs & 1][0][row0 + 8] + Dx[gs & 1][1][row0 + 8]) * rw;
         // dS as the TMEM A operand of dQ += dS K: keys (32hc + 8n + 2cq, +1) of rows g and

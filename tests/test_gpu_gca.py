@@ -97,6 +97,24 @@ def test_irregular_slots_and_shift0():
         check_against_oracle(x, idx, sc, res, "bf16", shift=shift)
 
 
+def test_fusion_weights_that_underflow():
+    """Retrieval scores far apart, so that some fusion weights are tiny normal floats, some
+    subnormal and some exactly 0 in float32 (the oracle keeps them in float64).  The
+    backward kernels carry w in the exponent of w P and recover D = rowsum(w P dPo) / w;
+    every output must still match, without NaN."""
+    B, nC, H, dh, K = 2, 12, 2, 64, 8
+    x = synth.gca_inputs(5, B, nC, nC, H, dh, 1.0, "bf16")
+    rng = np.random.default_rng(5)
+    idx = rng.integers(0, nC, size=(B, nC, K)).astype(np.int32)
+    offs = np.array([0.0, -1.0, -80.0, -200.0, -300.0, 2.0, -95.0, 1.5])
+    sc = offs[None, None, :] + 0.01 * rng.standard_normal((B, nC, K))
+    w = np.exp(sc - sc.max(-1, keepdims=True)).astype(np.float32)
+    assert (w == 0).any() and ((w > 0) & (w < 1e-30)).any()  # the case is what it claims
+    for shift in (0, 1):
+        res = run_fwd_bwd(x, idx, sc, "bf16", shift=shift)
+        check_against_oracle(x, idx, sc, res, "bf16", shift=shift)
+
+
 def test_kv_shared_across_sequences_forward():
     """Batch stride 0 for K/V: every sequence reads one store (decode with aliasing)."""
     g = _g()
