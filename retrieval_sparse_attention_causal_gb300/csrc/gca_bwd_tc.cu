@@ -252,11 +252,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       const uint64_t dq = dQ0 + buf * (kQBuf >> 4), ddo = dq + kTileStep;
       const uint64_t dk = dRingKm + (g % NST) * kStage, dv = dk + kTileStep;
       if (!P(&bar_kv[g % NST], (g / NST) & 1, 6, k, g)) return false;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma_warp(tS, dq + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
-        tc::mma_warp(tP, ddo + ks * tc::kKStepKm, dv + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
-      }
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dq, dk, kIdKm, 0u);
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tP, ddo, dv, kIdKm, 0u);
       tc::commit_warp(&bar_s);
       issued = true;
       return true;
@@ -279,9 +276,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       tc::fence_after();
       const uint64_t dk = dRingMn + (g % NST) * kStage;
       const uint32_t ta = tdS + 32 * (g & 1);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
-        tc::mma_ts_warp(tQ, ta + 8 * kk, dk + kk * tc::kKStepMn, kIdMn, (si > 0 || kk > 0) ? 1u : 0u);
+      // dQ += dS K  (K as the MN-major B operand)
+      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tQ, ta, dk, kIdMn, si > 0 ? 1u : 0u);
       tc::commit_warp(&ring_empty[g % NST]);
       if (last) {
         tc::commit_warp(&qfree[k & 1]);
@@ -779,9 +775,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       if ((r.flags & kRecFirst) && !W(&bar_kv[r.kb], (r.tc >> 1) & 1, 25, r.tc, y)) return false;
       const uint64_t dk = dKV + (2 * r.kb) * kTileStep;
       const uint64_t dq = dRingKm + (y % NST) * kStage;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks)
-        tc::mma_warp(tS, dk + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dk, dq, kIdKm, 0u);
       tc::commit_warp(&bar_s1);
       issued = true;
       return true;
@@ -789,9 +783,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
     auto issue_dpt = [&](int y, const KVConsRec& r) {  // dPo^T(y) = V dO^T
       const uint64_t dv = dKV + (2 * r.kb + 1) * kTileStep;
       const uint64_t ddo = dRingKm + (y % NST) * kStage + kTileStep;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks)
-        tc::mma_warp(tP, dv + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tP, dv, ddo, kIdKm, 0u);
       tc::commit_warp(&bar_s2);
       if (r.flags & kRecLast) tc::commit_warp(&kv_empty[r.kb]);  // the tile's K, V are read
     };
@@ -813,12 +805,8 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       tc::fence_after();
       if ((rx.flags & kRecFirst) && rx.tc >= 1 && !W(&acc_empty, (rx.tc - 1) & 1, 27, rx.tc, x)) break;
       const uint64_t bq = dRingMn + (x % NST) * kStage, bdo = bq + kTileStep;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t acc = ((rx.flags & kRecFirst) && kk == 0) ? 0u : 1u;
-        const uint32_t aoff = kk < 2 ? 8 * kk : 16 + 8 * kk;  // columns of this K step's query pairs
-        tc::mma_ts_warp(tdV, tS + aoff, bdo + kk * tc::kKStepMn, kIdMn, acc);
-      }
+      // The A columns of the four K steps' query pairs: 0, 8, 32, 40.
+      tc::mma4_ts<8, 32, 40, tc::kKStepMn>(tdV, tS, bdo, kIdMn, (rx.flags & kRecFirst) ? 0u : 1u);
       // S^T(x + 1), if there is a next consumer.
       if (!W(&bar_c[(x + 1) % NST], ((x + 1) / NST) & 1, 24, rx.tc, x + 1)) break;
       const KVConsRec rn = *crec(x + 1);
@@ -827,12 +815,7 @@ gca_bwd_kv_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const _
       // dK += dS^T Q once dS^T is in.
       if (!W(&op_k, x & 1, 32, rx.tc, x)) break;
       tc::fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t acc = ((rx.flags & kRecFirst) && kk == 0) ? 0u : 1u;
-        const uint32_t aoff = kk < 2 ? 8 * kk : 16 + 8 * kk;
-        tc::mma_ts_warp(tdK, tP + aoff, bq + kk * tc::kKStepMn, kIdMn, acc);
-      }
+      tc::mma4_ts<8, 32, 40, tc::kKStepMn>(tdK, tP, bq, kIdMn, (rx.flags & kRecFirst) ? 0u : 1u);
       tc::commit_warp(&ring_empty[x % NST]);
       if (rx.flags & kRecLast) tc::commit_warp(&acc_full);
       if (!more) {

@@ -381,9 +381,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
     auto issue_s = [&](int g, int qb) -> bool {
       if (!P(&bar_kv[g % NST], (g / NST) & 1, 44, -1, g)) return false;
       const uint64_t dq = dQ0 + qb * kTileStep, dk = dRingKm + (g % NST) * kStage;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks)
-        tc::mma_warp(tS, dq + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdS, ks > 0 ? 1u : 0u);
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dq, dk, kIdS, 0u);
       tc::commit_warp(&bar_s);
       issued = true;
       return true;
@@ -415,9 +413,7 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
           break;
         }
         const uint64_t dv = dRingMn + (gs % NST) * kStage + kTileStep;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_ts_warp(tO, tS + 8 * kk, dv + kk * tc::kKStepMn, kIdPV, (si > 0 || kk > 0) ? 1u : 0u);
+        tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tO, tS, dv, kIdPV, si > 0 ? 1u : 0u);
         tc::commit_warp(&ring_empty[gs % NST]);
         if (si + 1 < ns) {
           if (!issue_s(gs + 1, qb)) {
