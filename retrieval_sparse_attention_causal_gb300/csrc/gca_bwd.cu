@@ -602,7 +602,19 @@ __global__ void __launch_bounds__(256) gca_dscores_kernel(BwdArgs a) {
   for (int m = warp; m < a.topk; m += 8) {
     float acc = 0.f;
     if (j_s[m] >= 0) {
-      for (int h = 0; h < a.H; ++h) {
+      // Four heads' loads in flight together, the sum in head order.
+      int h = 0;
+      for (; h + 4 <= a.H; h += 4) {
+        float x[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float* p = Dc + ((int64_t)(h + v) * a.topk + m) * 64;
+          x[v] = p[lane] + p[lane + 32];
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc += x[v];
+      }
+      for (; h < a.H; ++h) {
         const float* p = Dc + ((int64_t)h * a.topk + m) * 64;
         acc += p[lane] + p[lane + 32];
       }
