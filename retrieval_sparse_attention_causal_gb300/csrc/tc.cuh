@@ -24,7 +24,9 @@
 //     in column 4n + t%4, the A-operand position of that pair.
 //   * Issue cost: an MMA issued from a one-lane branch costs about 44 cycles of issue,
 //     more than an M = 64, N = 64, K = 16 MMA takes in the pipe (about 35); issued by
-//     an elected lane of a converged warp it costs less than the pipe time.
+//     an elected lane of a converged warp it costs less than the pipe time, unless other
+//     warps keep the MMA warp's SM sub-partition busy (then about 59 cycles one by one,
+//     39 four at a time from one elect: mma4_ss / mma4_ts).
 #pragma once
 
 #include <stdint.h>
