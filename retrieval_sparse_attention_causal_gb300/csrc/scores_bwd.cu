@@ -4,9 +4,11 @@
 // Long-Context Language Modeling", 关键设计 / key design, "Grouped Cross-Attention");
 // the Gumbel noise only chose the slots and has no gradient.
 //
-//   dq_lmk_kernel  one CTA per query row: sum over its k slots of ds * k_lmk[j].
-//   dk_lmk_kernel  one CTA per key chunk: sum over the rows that retrieved it (from the
-//                  stable CSR, so in a fixed order) of ds * q_lmk[i].
+// One launch, lmk_grad_kernel: CTAs 0 .. nQ-1 (per sequence) each take a query row, the
+// sum over its k slots of ds * k_lmk[j]; CTAs nQ .. nQ+nC-1 each take a key chunk, the sum
+// over the rows that retrieved it (from the stable CSR, so in a fixed order) of
+// ds * q_lmk[i].  The two halves are independent; sharing the launch fills the GPU with
+// both at once.
 #include "common.cuh"
 #include "internal.h"
 
@@ -14,10 +16,9 @@ namespace gca {
 namespace {
 
 template <typename T, typename TO>
-__global__ void __launch_bounds__(256) dq_lmk_kernel(ScoresBwdArgs a) {
+__device__ __forceinline__ void dq_lmk_row(const ScoresBwdArgs& a, int i, int b) {
   __shared__ int j_s[kMaxTopk];
   __shared__ float ds_s[kMaxTopk];
-  const int i = blockIdx.x, b = blockIdx.y;
   if (threadIdx.x < a.topk) {
     const int64_t o = ((int64_t)b * a.nQ + i) * a.topk + threadIdx.x;
     int j = a.idx[o];
@@ -45,10 +46,9 @@ __global__ void __launch_bounds__(256) dq_lmk_kernel(ScoresBwdArgs a) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) dk_lmk_kernel(ScoresBwdArgs a) {
+__device__ __forceinline__ void dk_lmk_chunk(const ScoresBwdArgs& a, int j, int b) {
   __shared__ int row_s[256];
   __shared__ float ds_s[256];
-  const int j = blockIdx.x, b = blockIdx.y;
   const int e0 = a.csr_off[(int64_t)b * (a.nC + 1) + j];
   const int e1 = a.csr_off[(int64_t)b * (a.nC + 1) + j + 1];
   const int32_t* ent = a.csr_ent + (int64_t)b * a.nQ * a.topk;
@@ -96,25 +96,28 @@ __global__ void __launch_bounds__(256) dk_lmk_kernel(ScoresBwdArgs a) {
   }
 }
 
+template <typename T, typename TO>
+__global__ void __launch_bounds__(256) lmk_grad_kernel(ScoresBwdArgs a) {
+  const int x = blockIdx.x, b = blockIdx.y;
+  if (x < a.nQ) dq_lmk_row<T, TO>(a, x, b);
+  else dk_lmk_chunk<T>(a, x - a.nQ, b);
+}
+
 }  // namespace
 
 cudaError_t launch_scores_backward(const ScoresBwdArgs& a, cudaStream_t s) {
   cudaError_t e = launch_csr(a.idx, a.B, a.nQ, a.nQ, a.topk, a.nC, a.csr_off, a.csr_ent, a.csr_cur, a.err, s);
   if (e != cudaSuccess) return e;
-  dim3 gq(a.nQ, a.B), gk(a.nC, a.B);
-  launch_begin("lmk_dq", s);
+  dim3 grid(a.nQ + a.nC, a.B);
+  launch_begin("lmk_grads", s);
   if (a.bf16) {
-    if (a.dq_bf16) dq_lmk_kernel<__nv_bfloat16, __nv_bfloat16><<<gq, 256, 0, s>>>(a);
-    else dq_lmk_kernel<__nv_bfloat16, float><<<gq, 256, 0, s>>>(a);
+    if (a.dq_bf16) lmk_grad_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, s>>>(a);
+    else lmk_grad_kernel<__nv_bfloat16, float><<<grid, 256, 0, s>>>(a);
   } else {
-    if (a.dq_bf16) dq_lmk_kernel<float, __nv_bfloat16><<<gq, 256, 0, s>>>(a);
-    else dq_lmk_kernel<float, float><<<gq, 256, 0, s>>>(a);
+    if (a.dq_bf16) lmk_grad_kernel<float, __nv_bfloat16><<<grid, 256, 0, s>>>(a);
+    else lmk_grad_kernel<float, float><<<grid, 256, 0, s>>>(a);
   }
-  if ((e = launch_end("lmk_dq", s)) != cudaSuccess) return e;
-  launch_begin("lmk_dk", s);
-  if (a.bf16) dk_lmk_kernel<__nv_bfloat16><<<gk, 256, 0, s>>>(a);
-  else dk_lmk_kernel<float><<<gk, 256, 0, s>>>(a);
-  return launch_end("lmk_dk", s);
+  return launch_end("lmk_grads", s);
 }
 
 }  // namespace gca
