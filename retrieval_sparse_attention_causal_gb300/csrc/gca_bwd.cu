@@ -654,14 +654,14 @@ constexpr int kCsrParChunks = 8192, kCsrParEntries = 8192;  // the parallel fill
 // a shared atomic (in any order), then one warp per chunk writes each of the segment's
 // entries at its rank, the number of smaller entry indices in the segment, which is the
 // entry-order position.
-__global__ void __launch_bounds__(1024) csr_par_kernel(const int32_t* idx, int ld_rows, int nrows, int topk, int nC,
-                                                       int32_t* off, int32_t* ent, ErrWord* err) {
+__device__ __forceinline__ void csr_par_body(const int32_t* idx, int ld_rows, int nrows, int topk, int nC,
+                                             int32_t* off, int32_t* ent, ErrWord* err, int b) {
   extern __shared__ int32_t sh[];
   int32_t* cnt = sh;         // [nC]: counts, then offsets, then fill cursors
   int32_t* beg = sh + nC;    // [nC + 1]: offsets
   int32_t* tmp = beg + nC + 1;  // [n]: entries, unordered within each segment
   __shared__ int wsum[32];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t* ib = idx + (int64_t)b * ld_rows * topk;
   int32_t* ob = off + (int64_t)b * (nC + 1);
   int32_t* eb = ent + (int64_t)b * ld_rows * topk;
@@ -723,6 +723,81 @@ __global__ void __launch_bounds__(1024) csr_par_kernel(const int32_t* idx, int l
       eb[s0 + rank] = v;
     }
   }
+}
+
+__global__ void __launch_bounds__(1024) csr_par_kernel(const int32_t* idx, int ld_rows, int nrows, int topk, int nC,
+                                                       int32_t* off, int32_t* ent, ErrWord* err) {
+  csr_par_body(idx, ld_rows, nrows, topk, nC, off, ent, err, blockIdx.x);
+}
+
+// The score gradient of four retrieval rows per 1024-thread CTA (eight warps per row; the
+// same sums, in the same order, as gca_dscores_kernel), for the launch shared with the CSR.
+__device__ __forceinline__ void dscores_rows4(const BwdArgs& a, int rb, int b) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, grp = warp >> 3, gw = warp & 7;
+  const int r = 4 * rb + grp, c = r + a.shift;
+  __shared__ float w_s[4][kMaxTopk];
+  __shared__ int j_s[4][kMaxTopk];
+  __shared__ float dw_s[4][kMaxTopk];
+  if (rb == 0 && b == 0 && tid == 0 && a.kv_ctr) *a.kv_ctr = 0;  // the key side's tile counter
+  const bool row_ok = r < a.nQ, act = row_ok && c < a.nQ;
+  float* out = a.dscores + ((int64_t)b * a.nQ + r) * a.topk;
+  if (row_ok && !act && gw == 0 && lane < a.topk) out[lane] = 0.f;
+  if (act && gw == 0)
+    row_weights_warp(a.idx + ((int64_t)b * a.nQ + r) * a.topk, a.scores + ((int64_t)b * a.nQ + r) * a.topk,
+                     a.topk, a.nC, w_s[grp], j_s[grp], nullptr);
+  __syncthreads();
+  if (act) {
+    const float* Dc = a.Dbuf + ((int64_t)b * a.nQ + c) * a.H * a.topk * 64;
+    for (int m = gw; m < a.topk; m += 8) {
+      float acc = 0.f;
+      if (j_s[grp][m] >= 0) {
+        int h = 0;
+        for (; h + 4 <= a.H; h += 4) {
+          float x[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float* p = Dc + ((int64_t)(h + v) * a.topk + m) * 64;
+            x[v] = p[lane] + p[lane + 32];
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc += x[v];
+        }
+        for (; h < a.H; ++h) {
+          const float* p = Dc + ((int64_t)h * a.topk + m) * 64;
+          acc += p[lane] + p[lane + 32];
+        }
+      }
+#pragma unroll
+      for (int k = 16; k >= 1; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
+      if (lane == 0) dw_s[grp][m] = acc;
+    }
+  }
+  __syncthreads();
+  if (act && gw == 0) {
+    float w = 0.f, dw = 0.f;
+    bool valid = false;
+    if (lane < a.topk) {
+      w = w_s[grp][lane];
+      valid = j_s[grp][lane] >= 0;
+      dw = valid ? dw_s[grp][lane] : 0.f;
+    }
+    float sum = w * dw;
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, k);
+    if (lane < a.topk) out[lane] = valid ? w * (dw - sum) : 0.f;
+  }
+}
+
+// One launch for two independent passes of the backward: CTAs 0 .. B-1 build the CSR of
+// consumers of sequence blockIdx.x (the parallel fill), the rest take the score
+// gradient, four retrieval rows each.
+__global__ void __launch_bounds__(1024) dscores_csr_kernel(BwdArgs a, int nrows) {
+  if ((int)blockIdx.x < a.B) {
+    csr_par_body(a.idx, a.nQ, nrows, a.topk, a.nC, a.csr_off, a.csr_ent, a.err, blockIdx.x);
+    return;
+  }
+  const int x = blockIdx.x - a.B, nrb = (a.nQ + 3) / 4;
+  dscores_rows4(a, x % nrb, x / nrb);
 }
 
 template <bool kSmem>
@@ -848,13 +923,22 @@ cudaError_t launch_backward(const BwdArgs& a, cudaStream_t s) {
     else gca_bwd_q_f32_kernel<32><<<gq, 64, 0, s>>>(a);
     if ((e = launch_end("gca_bwd_q_f32", s)) != cudaSuccess) return e;
   }
-  launch_begin("gca_dscores", s);
-  gca_dscores_kernel<<<dim3(a.nQ, a.B), 256, 0, s>>>(a);
-  if ((e = launch_end("gca_dscores", s)) != cudaSuccess) return e;
-  const int nrows = a.nQ - a.shift;
-  if ((e = launch_csr(a.idx, a.B, a.nQ, nrows > 0 ? nrows : 0, a.topk, a.nC, a.csr_off, a.csr_ent,
-                      a.csr_cur, a.err, s)) != cudaSuccess)
-    return e;
+  const int nrows = a.nQ - a.shift > 0 ? a.nQ - a.shift : 0;
+  if (a.nC <= kCsrParChunks && nrows * a.topk <= kCsrParEntries) {
+    // The score gradient and the CSR share one launch.
+    const int sm = (2 * a.nC + 1 + nrows * a.topk) * (int)sizeof(int32_t);
+    if ((e = allow_smem((const void*)dscores_csr_kernel, sm)) != cudaSuccess) return e;
+    launch_begin("gca_dscores_csr", s);
+    dscores_csr_kernel<<<a.B + a.B * ((a.nQ + 3) / 4), 1024, sm, s>>>(a, nrows);
+    if ((e = launch_end("gca_dscores_csr", s)) != cudaSuccess) return e;
+  } else {
+    launch_begin("gca_dscores", s);
+    gca_dscores_kernel<<<dim3(a.nQ, a.B), 256, 0, s>>>(a);
+    if ((e = launch_end("gca_dscores", s)) != cudaSuccess) return e;
+    if ((e = launch_csr(a.idx, a.B, a.nQ, nrows, a.topk, a.nC, a.csr_off, a.csr_ent, a.csr_cur, a.err, s)) !=
+        cudaSuccess)
+      return e;
+  }
   if (tc) return launch_bwd_kv_tc(a, s);
   if (a.bf16) {
     const int sk = (int)bwd_kv_smem(a.dh);
