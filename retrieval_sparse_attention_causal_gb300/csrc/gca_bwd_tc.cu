@@ -135,8 +135,9 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   __syncthreads();
   tc::fence_after();
   const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tQ = tmem_slot + 128, tdS = tmem_slot + 192;
-  // Every role but the metadata one parks while it waits (try_wait with a suspend hint),
-  // so that a waiting warp takes no issue slots from the warps that work.
+  // Waits park (try_wait with a suspend hint), so that a waiting warp takes no issue slots
+  // from the warps that work; only the short exchange between the two element warps of a
+  // row quarter spins (W).
   auto P = [&](uint64_t* bar, uint32_t parity, int site, int tile, int slot) {
     return park_or_abort(bar, parity, &abort_s, a.err, site, tile, slot);
   };
