@@ -65,6 +65,14 @@ def test_algorithmic_counts():
     assert bench.prefill_flops(16384, 768) == 206145847296
     assert bench.algorithmic_flops(4, 256, 12, 64, 8)["units"] == 4 * 12 * 2004
     assert bench.algorithmic_flops(1, 3, 1, 64, 8)["units"] == 1  # rows 0, 1 feed chunks 1, 2
+    # Bytes each GCA kernel must move once, counted tensor by tensor at the 128M shape:
+    # one [B][L][H][dh] bf16 tensor is 4 * 16384 * 12 * 64 * 2 bytes, one LSE or D row set
+    # [B][nQ][H][k][64] f32 is 4 * 256 * 12 * 8 * 64 * 4 bytes.
+    t, rows = 4 * 16384 * 12 * 64 * 2, 4 * 256 * 12 * 8 * 64 * 4
+    by = bench.algorithmic_bytes(4, 256, 12, 64, 8)
+    assert by["gca_fwd"] == 3 * t + t + rows            # reads Q, K, V; writes O, LSE
+    assert by["gca_bwd_q"] == 4 * t + rows + t + rows   # reads Q, dO, K, V, LSE; writes dQ, D
+    assert by["gca_bwd_kv"] == 4 * t + 2 * rows + 2 * t  # reads Q, dO, K, V, LSE, D; writes dK, dV
 
 
 def test_traffic_figures_follow_the_sources():
