@@ -305,24 +305,25 @@ __global__ void __launch_bounds__(256) retrieve_merge_heads_kernel(RetrieveArgs 
 constexpr int kTileStages = 6;  // 64-candidate x 64-dim chunks in flight (bf16)
 struct TileSmem {
   static constexpr int kSt = 65;  // padded score-tile row (floats)
-  static size_t bytes(int D, bool bf16) {
-    if (bf16) return (size_t)64 * D * 2 + kTileStages * 64 * 128 + 64 * kSt * 4 + 1024;
+  static size_t bytes(int D, bool bf16, int rows = 64) {
+    if (bf16) return (size_t)rows * D * 2 + kTileStages * 64 * 128 + rows * kSt * 4 + 1024;
     return (size_t)64 * (D + 1) * 4 + 64 * 33 * 4 + 64 * kSt * 4 + 1024;
   }
 };
 
-// Top-k phase over one 64x64 score tile held in shared memory.  Thread t owns row t/4
-// and the 16 candidates of quarter t%4.
-template <int KC>
+// Top-k phase over one ROWS x 64 score tile held in shared memory.  Thread t owns row
+// t / TPR and the 64 / TPR candidates of part t % TPR (TPR = 256 / ROWS threads a row).
+template <int KC, int ROWS>
 __device__ __forceinline__ void tile_topk(const RetrieveArgs& a, const float* St, int b,
                                           int row0, int tile0, int j1, float inv, Cand (&L)[KC]) {
-  const int rl = threadIdx.x >> 2, quarter = threadIdx.x & 3;
+  constexpr int TPR = kTileThreads / ROWS, CPT = 64 / TPR;
+  const int rl = threadIdx.x / TPR, quarter = threadIdx.x % TPR;
   const int i = row0 + rl;
   if (i >= a.nQ) return;
   const int lim = min(j1, n_cand_row(i, a.off, a.nC));
 #pragma unroll 4
-  for (int cc = 0; cc < 16; ++cc) {
-    const int jl = quarter * 16 + cc;
+  for (int cc = 0; cc < CPT; ++cc) {
+    const int jl = quarter * CPT + cc;
     const int j = tile0 + jl;
     if (j < lim) {
       Cand c;
@@ -334,17 +335,18 @@ __device__ __forceinline__ void tile_topk(const RetrieveArgs& a, const float* St
   }
 }
 
-// Merge the four quarter lists of each row (lanes 4r..4r+3) and write the result.
-template <int KC>
+// Merge the TPR part lists of each row (lanes TPR r .. TPR r + TPR - 1) and write the result.
+template <int KC, int ROWS>
 __device__ __forceinline__ void tile_finish(const RetrieveArgs& a, int nsplit, int b, int row0,
                                             int split, Cand (&L)[KC]) {
-  const int rl = threadIdx.x >> 2, quarter = threadIdx.x & 3;
+  constexpr int TPR = kTileThreads / ROWS;
+  const int rl = threadIdx.x / TPR, quarter = threadIdx.x % TPR;
   const int i = row0 + rl;
   Cand out[kMaxTopk];
   for (int r = 0; r < a.topk; ++r) {
     Cand best = L[0];
 #pragma unroll
-    for (int m = 1; m <= 2; m <<= 1) {
+    for (int m = 1; m < TPR; m <<= 1) {
       Cand o = shfl_xor_cand(best, m);
       if (better(o, best)) best = o;
     }
@@ -357,17 +359,20 @@ __device__ __forceinline__ void tile_finish(const RetrieveArgs& a, int nsplit, i
   }
 }
 
-template <typename T, int KC>
+// ROWS query rows per CTA: 64, or 32 (bf16 only) when the problem has too few 64-row
+// blocks to occupy the GPU.
+template <typename T, int KC, int ROWS>
 __global__ void __launch_bounds__(kTileThreads)
 retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
+  static_assert(ROWS == 64 || (ROWS == 32 && sizeof(T) == 2), "32-row blocks are bf16 only");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int split = blockIdx.x;
   const int rb = gridDim.y - 1 - blockIdx.y;  // largest row blocks first
   const int b = blockIdx.z;
-  const int row0 = rb * 64;
-  const int last_row = min(a.nQ - 1, row0 + 63);
+  const int row0 = rb * ROWS;
+  const int last_row = min(a.nQ - 1, row0 + ROWS - 1);
   const int ncand = n_cand_row(last_row, a.off, a.nC);
   const int j0 = split * seg;
   const int j1 = min(ncand, j0 + seg);
@@ -384,15 +389,15 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
     if constexpr (sizeof(T) == 2) {
       // ---------------- bf16: tensor-core score tiles
       const int nkc = a.D / 64;
-      unsigned char* Qs = smem;                        // [nkc][64][128B] swizzled
-      unsigned char* Ks = smem + (size_t)64 * a.D * 2;  // [kTileStages][64][128B]
+      unsigned char* Qs = smem;                          // [nkc][ROWS][128B] swizzled
+      unsigned char* Ks = smem + (size_t)ROWS * a.D * 2;  // [kTileStages][64][128B]
       float* St = reinterpret_cast<float*>(Ks + kTileStages * 64 * 128);
       // Q block, all chunks.
-      for (int u = tid; u < 64 * a.D / 8; u += kTileThreads) {
+      for (int u = tid; u < ROWS * a.D / 8; u += kTileThreads) {
         const int r = u / (a.D / 8), cu = u % (a.D / 8);
         const int kc = cu >> 3, w = cu & 7;
         const int i = row0 + r;
-        unsigned char* dst = Qs + (size_t)kc * 8192 + swz<128>(r, w);
+        unsigned char* dst = Qs + (size_t)kc * (ROWS * 128) + swz<128>(r, w);
         if (i < a.nQ) cp_async16(dst, qb + (int64_t)i * a.q_rs + cu * 8);
         else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
       }
@@ -415,10 +420,13 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
         if (st < nsteps) load_chunk(st, st);
         cp_async_commit();
       }
-      const int rw = 16 * (warp & 3), cw = 32 * (warp >> 2);
-      float acc[4][4];
+      // Warp tiles of 16 rows x (32 or 16) candidates: NP pairs of 8-candidate MMA tiles.
+      constexpr int NP = ROWS == 64 ? 2 : 1;
+      const int rw = ROWS == 64 ? 16 * (warp & 3) : 16 * (warp & 1);
+      const int cw = ROWS == 64 ? 32 * (warp >> 2) : 16 * (warp >> 1);
+      float acc[2 * NP][4];
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
+      for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
       for (int step = 0; step < nsteps; ++step) {
@@ -428,7 +436,7 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
         if (step + kTileStages - 1 < nsteps) load_chunk(step + kTileStages - 1, (step + kTileStages - 1) % kTileStages);
         cp_async_commit();
         const int kc = step % nkc;
-        const uint32_t qbase = smem_u32(Qs + (size_t)kc * 8192);
+        const uint32_t qbase = smem_u32(Qs + (size_t)kc * (ROWS * 128));
         const uint32_t kbase = smem_u32(Ks + stage * 8192);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -436,7 +444,7 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
           ldsm_x4(af[0], af[1], af[2], af[3],
                   qbase + swz<128>(rw + (lane & 15), 2 * ks + (lane >> 4)));
 #pragma unroll
-          for (int p = 0; p < 2; ++p) {
+          for (int p = 0; p < NP; ++p) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4(b0, b1, b2, b3,
                     kbase + swz<128>(cw + 16 * p + (lane & 7) + ((lane >> 4) << 3),
@@ -448,7 +456,7 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
         if (kc == nkc - 1) {
           const int g = lane >> 2, c = lane & 3;
 #pragma unroll
-          for (int n = 0; n < 4; ++n) {
+          for (int n = 0; n < 2 * NP; ++n) {
             const int col = cw + 8 * n + 2 * c;
             St[(rw + g) * TileSmem::kSt + col] = acc[n][0];
             St[(rw + g) * TileSmem::kSt + col + 1] = acc[n][1];
@@ -458,7 +466,7 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
             for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
           }
           __syncthreads();
-          tile_topk(a, St, b, row0, j0 + (step / nkc) * 64, j1, inv, L);
+          tile_topk<KC, ROWS>(a, St, b, row0, j0 + (step / nkc) * 64, j1, inv, L);
         }
         __syncthreads();
       }
@@ -504,11 +512,11 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
 #pragma unroll
           for (int y = 0; y < 4; ++y) St[(r0 + x) * TileSmem::kSt + c0 + y] = acc[x][y];
         __syncthreads();
-        tile_topk(a, St, b, row0, jt, j1, inv, L);
+        tile_topk<KC, ROWS>(a, St, b, row0, jt, j1, inv, L);
       }
     }
   }
-  tile_finish(a, nsplit, b, row0, split, L);
+  tile_finish<KC, ROWS>(a, nsplit, b, row0, split, L);
 }
 
 template <typename F>
@@ -623,17 +631,29 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
     e = launch_retrieve_tc(a, p, s);
     nsplit = 2 * p.tc_ns[a.gumbel ? 1 : 0];
   } else {
-    dim3 grid(p.nsplit, (a.nQ + 63) / 64, a.B);
-    const int smem = (int)TileSmem::bytes(a.D, a.bf16 != 0);
+    // bf16 problems with fewer 64-row CTAs than two per SM take 32-row blocks (twice the
+    // CTAs, half the selection work per thread).
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const bool r32 = a.bf16 && (long long)p.nsplit * ((a.nQ + 63) / 64) * a.B < 2LL * sms;
+    const int rows = r32 ? 32 : 64;
+    dim3 grid(p.nsplit, (a.nQ + rows - 1) / rows, a.B);
+    const int smem = (int)TileSmem::bytes(a.D, a.bf16 != 0, rows);
     e = with_kc(a.topk, [&](auto kc) -> cudaError_t {
       constexpr int KC = decltype(kc)::value;
-      const void* fn = a.bf16 ? (const void*)retrieve_tile_kernel<__nv_bfloat16, KC>
-                              : (const void*)retrieve_tile_kernel<float, KC>;
+      const void* fn = a.bf16 ? (r32 ? (const void*)retrieve_tile_kernel<__nv_bfloat16, KC, 32>
+                                     : (const void*)retrieve_tile_kernel<__nv_bfloat16, KC, 64>)
+                              : (const void*)retrieve_tile_kernel<float, KC, 64>;
       cudaError_t e2 = allow_smem(fn, smem);
       if (e2 != cudaSuccess) return e2;
       launch_begin("retrieve_tile", s);
-      if (a.bf16) retrieve_tile_kernel<__nv_bfloat16, KC><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
-      else retrieve_tile_kernel<float, KC><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
+      if (a.bf16 && r32)
+        retrieve_tile_kernel<__nv_bfloat16, KC, 32><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
+      else if (a.bf16)
+        retrieve_tile_kernel<__nv_bfloat16, KC, 64><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
+      else
+        retrieve_tile_kernel<float, KC, 64><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
       return launch_end("retrieve_tile", s);
     });
   }
