@@ -1007,10 +1007,12 @@ cudaError_t launch_bwd_kv_tc(const BwdArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const long long ntiles = (long long)a.nC * a.H * a.B;
   const int grid = (int)std::min<long long>(ntiles, 2LL * sms);  // two CTAs per SM (TMEM: 256 columns each)
-  // Heads per tile block: as many as keep their Q, dO, K and V within about 48 MB of L2.
+  // Heads per tile block: as many as keep their Q, dO, K and V within about the size of L2
+  // (128 MB; measured against 24, 48 and 96 MB blocks and blocks of every head: 48 MB and
+  // smaller are slower, the larger ones alike).
   BwdArgs b2 = a;
   const long long per_head = 4LL * 64 * 64 * 2 * std::max(a.nQ, a.nC);
-  b2.kv_hb = (int)std::max<long long>(1, std::min<long long>(a.H, (48LL << 20) / per_head));
+  b2.kv_hb = (int)std::max<long long>(1, std::min<long long>(a.H, (128LL << 20) / per_head));
   launch_begin("gca_bwd_kv", s);
   gca_bwd_kv_tc_kernel<<<grid, kKVThreads, kKVSmem, s>>>(b2, tq, tdo, tk, tv);
   return launch_end("gca_bwd_kv", s);
