@@ -193,17 +193,17 @@ KERNEL_SOURCES = {
     "retrieve_tc": ("retrieve_tc.cu", "tc.cuh", "tc_rows.cuh", "common.cuh"),
 }
 KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
-    "gca_fwd": (3.8194e+08, "241db333501dcbce"),
-    "gca_bwd_q": (5.1014e+08, "471b708a0fe646b5"),
-    "gca_bwd_kv": (6.8183e+08, "471b708a0fe646b5"),
+    "gca_fwd": (3.8188e+08, "241db333501dcbce"),
+    "gca_bwd_q": (5.0978e+08, "56896f4275d0ddf9"),
+    "gca_bwd_kv": (6.9611e+08, "56896f4275d0ddf9"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (805428480 / 2, "5d39e2bed0dad9dc")
+STREAM_TRAFFIC_PER_SEQ = (805513984 / 2, "604458e697ccdb3b")
 
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
 # nothing written back past L2; traffic grows with the number of chunks)
-PREFILL_TRAFFIC_PER_CHUNK = (25216768 / 8192, "11c4cd78c1b2463f")
+PREFILL_TRAFFIC_PER_CHUNK = (25217536 / 8192, "11c4cd78c1b2463f")
 
 
 def source_fingerprint(kernel: str) -> str:
