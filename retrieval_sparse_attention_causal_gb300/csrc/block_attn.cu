@@ -138,9 +138,7 @@ block_attn_tc_kernel(BlockAttnArgs a, const __grid_constant__ CUtensorMap tmQ, c
     }
     auto issue_s = [&](int x) {  // whole warp
       const uint64_t dk = x % NST == 0 ? dK[0] : dK[1];
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks)
-        tc::mma_warp(tS, dQ + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdS, ks > 0 ? 1u : 0u);
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dQ, dk, kIdS, 0u);
       tc::commit_warp(&bar_s);
     };
     if (lane == 0) {
@@ -156,9 +154,7 @@ block_attn_tc_kernel(BlockAttnArgs a, const __grid_constant__ CUtensorMap tmQ, c
       tc::named_sync(kBarPReady, NT);  // P(n) in TMEM columns 0-31 and O rescaled
       tc::fence_after();
       const uint64_t dv = n % NST == 0 ? dV[0] : dV[1];
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc::mma_ts_warp(tO, tS + 8 * kk, dv + kk * tc::kKStepMn, kIdPV, (n > 0 || kk > 0) ? 1u : 0u);
+      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tO, tS, dv, kIdPV, n > 0 ? 1u : 0u);
       tc::commit_warp(&bar_o);
       if (n + 1 < nb) {
         ok = tc::mbar_wait(&bar_kv[(n + 1) % NST], ((n + 1) / NST) & 1) && ok;

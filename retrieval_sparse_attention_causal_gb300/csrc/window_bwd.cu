@@ -150,11 +150,8 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
     constexpr uint64_t kStage = (2 * TILE) >> 4, kTileStep = TILE >> 4;
     auto issue_s = [&](int x) {  // S = Q K^T and dPo = dO V^T of block x (whole warp)
       const uint64_t dk = dRingKm + (x % NST) * kStage, dv = dk + kTileStep;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma_warp(tS, dQd + ks * tc::kKStepKm, dk + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
-        tc::mma_warp(tP, dOd + ks * tc::kKStepKm, dv + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
-      }
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dQd, dk, kIdKm, 0u);
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tP, dOd, dv, kIdKm, 0u);
       tc::commit_warp(&bar_s);
     };
     if (lane == 0) {
@@ -171,9 +168,8 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
       tc::named_sync(kBarOpReady, NT);  // dS(n) is in TMEM columns 0-31
       tc::fence_after();
       const uint64_t dk = dRingMn + (n % NST) * kStage;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // dQ += dS K  (K as the MN-major B operand)
-        tc::mma_ts_warp(tQ, tS + 8 * kk, dk + kk * tc::kKStepMn, kIdMn, (n > 0 || kk > 0) ? 1u : 0u);
+      // dQ += dS K  (K as the MN-major B operand)
+      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tQ, tS, dk, kIdMn, n > 0 ? 1u : 0u);
       tc::commit_warp(&bar_o);
       if (n + 1 < nb) {
         ok = tc::mbar_wait(&bar_kv[(n + 1) % NST], ((n + 1) / NST) & 1) && ok;
@@ -343,11 +339,8 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
     constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
     auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x (whole warp)
       const uint64_t dq = dRingKm + (x % NST) * kStage, ddo = dq + kTileStep;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks) {
-        tc::mma_warp(tS, dKd + ks * tc::kKStepKm, dq + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
-        tc::mma_warp(tP, dVd + ks * tc::kKStepKm, ddo + ks * tc::kKStepKm, kIdKm, ks > 0 ? 1u : 0u);
-      }
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dKd, dq, kIdKm, 0u);
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tP, dVd, ddo, kIdKm, 0u);
       tc::commit_warp(&bar_s);
     };
     if (lane == 0)
@@ -360,12 +353,8 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
       tc::named_sync(kBarOpReady, NT);  // P^T and dS^T are in TMEM columns 0-31, 64-95
       tc::fence_after();
       const uint64_t bq = dRingMn + (ci % NST) * kStage, bdo = bq + kTileStep;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t acc = (ci > 0 || kk > 0) ? 1u : 0u;
-        tc::mma_ts_warp(tdV, tS + 8 * kk, bdo + kk * tc::kKStepMn, kIdMn, acc);
-        tc::mma_ts_warp(tdK, tP + 8 * kk, bq + kk * tc::kKStepMn, kIdMn, acc);
-      }
+      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tdV, tS, bdo, kIdMn, ci > 0 ? 1u : 0u);
+      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tdK, tP, bq, kIdMn, ci > 0 ? 1u : 0u);
       tc::commit_warp(&bar_o);
       if (ci + 1 < ncons) {
         ok = tc::mbar_wait(&bar_c[(ci + 1) % NST], ((ci + 1) / NST) & 1) && ok;
