@@ -99,7 +99,7 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
   unsigned char* dOs = sm + TILE;
   unsigned char* ring = sm + 2 * TILE;
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t bar_q, bar_kv[NST], bar_s, bar_o;
+  __shared__ __align__(8) uint64_t bar_q, bar_kv[NST], bar_s, bar_o, sfree, dq_done[2];
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ts = (int64_t)a.H * DH;
@@ -127,13 +127,18 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
     for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_kv[st], 1);
     tc::mbar_init(&bar_s, 1);
     tc::mbar_init(&bar_o, 1);
+    tc::mbar_init(&sfree, kEW);
+    tc::mbar_init(&dq_done[0], 1);
+    tc::mbar_init(&dq_done[1], 1);
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tQ = tmem_slot + 128;
+  // TMEM: S, dPo, dQ, and two dS buffers (32 columns each): the next block's S, dPo go in
+  // as soon as the element warps hold the current ones in registers.
+  const uint32_t tS = tmem_slot, tP = tmem_slot + 64, tQ = tmem_slot + 128, tdS = tmem_slot + 192;
 
   if (warp == kCtl) {
     // ------------------------------------------------------------ control warp
@@ -165,16 +170,20 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
     ok = tc::mbar_wait(&bar_kv[0], 0) && ok;
     issue_s(0);
     for (int n = 0; n < nb; ++n) {
-      tc::named_sync(kBarOpReady, NT);  // dS(n) is in TMEM columns 0-31
+      // S(n), dPo(n) are in the element warps' registers: the next pair goes in now.
+      ok = tc::mbar_wait(&sfree, n & 1) && ok;
       tc::fence_after();
-      const uint64_t dk = dRingMn + (n % NST) * kStage;
-      // dQ += dS K  (K as the MN-major B operand)
-      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tQ, tS, dk, kIdMn, n > 0 ? 1u : 0u);
-      tc::commit_warp(&bar_o);
       if (n + 1 < nb) {
         ok = tc::mbar_wait(&bar_kv[(n + 1) % NST], ((n + 1) / NST) & 1) && ok;
         issue_s(n + 1);
       }
+      tc::named_sync(kBarOpReady, NT);  // dS(n) is in dS buffer n & 1
+      tc::fence_after();
+      const uint64_t dk = dRingMn + (n % NST) * kStage;
+      // dQ += dS K  (K as the MN-major B operand)
+      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tQ, tdS + 32 * (n & 1), dk, kIdMn, n > 0 ? 1u : 0u);
+      tc::commit_warp(&bar_o);
+      tc::commit_warp(&dq_done[n & 1]);
       ok = tc::mbar_wait(&bar_o, n & 1) && ok;  // ring stage n % NST is free
       if (lane == 0) {
         if (n + NST < nb) load_block(n + NST);
@@ -201,6 +210,9 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
       for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
       tc::ld_wait(s);
       tc::ld_wait(dp);
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sfree);
       const int kind = kind_of(n);
       uint32_t dv[8];
 #pragma unroll
@@ -216,8 +228,9 @@ window_bwd_q_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ,
         dv[2 * cb] = pack_bf16(ds[0], ds[1]);
         dv[2 * cb + 1] = pack_bf16(ds[2], ds[3]);
       }
-      tc::named_sync(kBarEW, 32 * kEW);  // both column halves have read S before stores over it
-      tc::st16x128_x4(tS + lane_q + 16 * hc, dv);
+      // dS buffer n & 1 is free once dQ(n - 2) has read it.
+      if (n >= 2 && !tc::mbar_wait(&dq_done[n & 1], ((n >> 1) - 1) & 1)) flag_timeout(a.err);
+      tc::st16x128_x4(tdS + 32 * (n & 1) + lane_q + 16 * hc, dv);
       tc::st_wait();
       tc::fence_before();
       tc::named_arrive(kBarOpReady, NT);
