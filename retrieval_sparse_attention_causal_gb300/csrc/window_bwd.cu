@@ -29,7 +29,7 @@ using bf16 = __nv_bfloat16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kEW = 8, kThreads = 32 * (kEW + 1), kCtl = kEW;
 constexpr int TILE = 8192, ROWB = 128, UPR = 8, DH = 64;
-enum { kBarOpReady = 2, kBarEW = 3 };
+enum { kBarOpReady = 2 };
 
 // ------------------------------------------------------------------ D = rowsum(dO * O)
 // LPR consecutive lanes per (token, head) row, one 16-byte vector of O and of dO each, so a
@@ -291,7 +291,7 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
   unsigned char* Vs = sm + TILE;
   unsigned char* ring = sm + 2 * TILE;  // stage st: Q, dO, lse[64], D[64]
   __shared__ uint32_t tmem_slot;
-  __shared__ __align__(8) uint64_t bar_k, bar_c[NST], bar_s, bar_o;
+  __shared__ __align__(8) uint64_t bar_k, bar_c[NST], bar_s1, bar_s2, op_v, op_k, bar_o;
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ts = (int64_t)a.H * DH;
@@ -320,7 +320,10 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
   if (warp == kCtl && lane == 0) {
     tc::mbar_init(&bar_k, 1);
     for (int st = 0; st < NST; ++st) tc::mbar_init(&bar_c[st], 1);
-    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_s1, 1);
+    tc::mbar_init(&bar_s2, 1);
+    tc::mbar_init(&op_v, kEW);
+    tc::mbar_init(&op_k, kEW);
     tc::mbar_init(&bar_o, 1);
     tc::fence_mbar_init();
     tc::mbar_expect_tx(&bar_k, 2 * TILE);
@@ -350,29 +353,41 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
     const uint64_t dKd = tc::desc_km(tc::su32(Ks)), dVd = tc::desc_km(tc::su32(Vs));
     const uint64_t dRingKm = tc::desc_km(tc::su32(ring)), dRingMn = tc::desc_mn(tc::su32(ring));
     constexpr uint64_t kStage = kKVStageBytes >> 4, kTileStep = TILE >> 4;
-    auto issue_s = [&](int x) {  // S^T = K Q^T and dPo^T = V dO^T of consumer x (whole warp)
-      const uint64_t dq = dRingKm + (x % NST) * kStage, ddo = dq + kTileStep;
-      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dKd, dq, kIdKm, 0u);
-      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tP, dVd, ddo, kIdKm, 0u);
-      tc::commit_warp(&bar_s);
+    // The products of consumer x go in the order dV(x), S^T(x + 1), dK(x), dPo^T(x + 1):
+    // S^T(x + 1) overwrites P^T(x), which only dV(x) reads, and dPo^T(x + 1) overwrites
+    // dS^T(x), which only dK(x) reads, so each product only follows the one it has to.
+    auto issue_st = [&](int x) {  // S^T = K Q^T of consumer x (whole warp)
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tS, dKd, dRingKm + (x % NST) * kStage, kIdKm, 0u);
+      tc::commit_warp(&bar_s1);
+    };
+    auto issue_dpt = [&](int x) {  // dPo^T = V dO^T of consumer x
+      tc::mma4_ss<tc::kKStepKm, tc::kKStepKm>(tP, dVd, dRingKm + (x % NST) * kStage + kTileStep, kIdKm, 0u);
+      tc::commit_warp(&bar_s2);
     };
     if (lane == 0)
       for (int x = 0; x < NST && x < ncons; ++x) load_cons(x);
     __syncwarp();
     ok = tc::mbar_wait(&bar_k, 0) && ok;
     ok = tc::mbar_wait(&bar_c[0], 0) && ok;
-    issue_s(0);
+    issue_st(0);
+    issue_dpt(0);
     for (int ci = 0; ci < ncons; ++ci) {
-      tc::named_sync(kBarOpReady, NT);  // P^T and dS^T are in TMEM columns 0-31, 64-95
-      tc::fence_after();
       const uint64_t bq = dRingMn + (ci % NST) * kStage, bdo = bq + kTileStep;
-      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tdV, tS, bdo, kIdMn, ci > 0 ? 1u : 0u);
-      tc::mma4_ts<8, 16, 24, tc::kKStepMn>(tdK, tP, bq, kIdMn, ci > 0 ? 1u : 0u);
-      tc::commit_warp(&bar_o);
-      if (ci + 1 < ncons) {
+      // dV += P^T dO once P^T is in (each element warp's query pairs over the first 16 of
+      // its 32 columns: the K steps' A columns are 0, 8, 32, 40).
+      ok = tc::mbar_wait(&op_v, ci & 1) && ok;
+      tc::fence_after();
+      tc::mma4_ts<8, 32, 40, tc::kKStepMn>(tdV, tS, bdo, kIdMn, ci > 0 ? 1u : 0u);
+      const bool more = ci + 1 < ncons;
+      if (more) {
         ok = tc::mbar_wait(&bar_c[(ci + 1) % NST], ((ci + 1) / NST) & 1) && ok;
-        issue_s(ci + 1);
+        issue_st(ci + 1);
       }
+      ok = tc::mbar_wait(&op_k, ci & 1) && ok;
+      tc::fence_after();
+      tc::mma4_ts<8, 32, 40, tc::kKStepMn>(tdK, tP, bq, kIdMn, ci > 0 ? 1u : 0u);
+      tc::commit_warp(&bar_o);
+      if (more) issue_dpt(ci + 1);
       ok = tc::mbar_wait(&bar_o, ci & 1) && ok;  // ring stage ci % NST is free
       if (lane == 0) {
         if (ci + NST < ncons) load_cons(ci + NST);
@@ -389,43 +404,53 @@ window_bwd_kv_tc_kernel(WindowBwdArgs a, const __grid_constant__ CUtensorMap tmQ
     const float scale = 1.0f / sqrtf((float)DH);
     const float sl2 = scale * kLog2e;
     for (int ci = 0; ci < ncons; ++ci) {
-      if (!tc::mbar_wait(&bar_s, ci & 1)) flag_timeout(a.err);  // S^T(ci), dPo^T(ci)
+      if (!tc::mbar_wait(&bar_s1, ci & 1)) flag_timeout(a.err);  // S^T(ci)
       const int st = ci % NST;
       tc::mbar_wait(&bar_c[st], (ci / NST) & 1);  // observe the rows' phase (complete)
       const float* lrow = reinterpret_cast<const float*>(ring + st * kKVStageBytes + 2 * TILE) + 32 * hc;
       const float* drow = lrow + 64;
-      float s[4][4], dp[4][4];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tS + lane_base + cb * 8, s[cb]);
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::ld16x256(tP + lane_base + cb * 8, dp[cb]);
+      float s[4][4];
+      tc::ld16x256_x4(tS + lane_base, s);
       tc::ld_wait(s);
-      tc::ld_wait(dp);
       const int kind = kind_of(ci);
-      uint32_t pv[8], dv[8];
+      // P^T, stored over the columns this warp has read: the pair of queries
+      // (32hc + 8n + 2cq, +1) of key rows g and g + 8 goes to column 32hc + 4n + cq.
+      uint32_t pv[8];
 #pragma unroll
       for (int n = 0; n < 4; ++n) {  // query columns 32hc + 8n + 2cq (+1)
         const float2 l2 = *reinterpret_cast<const float2*>(lrow + 8 * n + 2 * cq);
-        const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
-        float p[4], ds[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int qc = 32 * hc + 8 * n + 2 * cq + (e & 1), kr = key0 + 8 * (e >> 1);
-          const float l = (e & 1) ? l2.y : l2.x, dd = (e & 1) ? d2.y : d2.x;
-          p[e] = dropped(kind, kr, qc) ? 0.f : tc::ex2(fmaf(s[n][e], sl2, -l * kLog2e));
-          ds[e] = p[e] * (dp[n][e] - dd) * scale;
+          const float l = (e & 1) ? l2.y : l2.x;
+          s[n][e] = dropped(kind, kr, qc) ? 0.f : tc::ex2(fmaf(s[n][e], sl2, -l * kLog2e));
         }
-        pv[2 * n] = pack_bf16(p[0], p[1]);
-        pv[2 * n + 1] = pack_bf16(p[2], p[3]);
-        dv[2 * n] = pack_bf16(ds[0], ds[1]);
-        dv[2 * n + 1] = pack_bf16(ds[2], ds[3]);
+        pv[2 * n] = pack_bf16(s[n][0], s[n][1]);
+        pv[2 * n + 1] = pack_bf16(s[n][2], s[n][3]);
       }
-      tc::named_sync(kBarEW, 32 * kEW);  // both column halves have read before stores over it
-      tc::st16x128_x4(tS + lane_q + 16 * hc, pv);
-      tc::st16x128_x4(tP + lane_q + 16 * hc, dv);
+      tc::st16x128_x4(tS + lane_base, pv);
       tc::st_wait();
       tc::fence_before();
-      tc::named_arrive(kBarOpReady, NT);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&op_v);
+      // dS^T from dPo^T, over its own columns too.
+      if (!tc::mbar_wait(&bar_s2, ci & 1)) flag_timeout(a.err);  // dPo^T(ci)
+      tc::fence_after();
+      float dp[4][4];
+      tc::ld16x256_x4(tP + lane_base, dp);
+      tc::ld_wait(dp);
+      uint32_t dv[8];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const float2 d2 = *reinterpret_cast<const float2*>(drow + 8 * n + 2 * cq);
+        dv[2 * n] = pack_bf16(s[n][0] * (dp[n][0] - d2.x) * scale, s[n][1] * (dp[n][1] - d2.y) * scale);
+        dv[2 * n + 1] = pack_bf16(s[n][2] * (dp[n][2] - d2.x) * scale, s[n][3] * (dp[n][3] - d2.y) * scale);
+      }
+      tc::st16x128_x4(tP + lane_base, dv);
+      tc::st_wait();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&op_k);
     }
   }
   tc::fence_before();
