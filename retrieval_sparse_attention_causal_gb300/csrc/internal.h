@@ -181,6 +181,7 @@ struct ScoresBwdArgs {
   void* dq; int dq_bf16; int64_t dq_rs, dq_bs; int dq_acc;
   float* dk; ErrWord* err;
   int32_t* csr_off; int32_t* csr_ent; int32_t* csr_cur;
+  int scan;  // set by the launcher: key chunks scan idx instead of reading the CSR
 };
 cudaError_t launch_scores_backward(const ScoresBwdArgs& a, cudaStream_t s);
 

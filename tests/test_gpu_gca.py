@@ -207,6 +207,67 @@ def test_scores_backward_and_strided_accumulate():
     assert_close(host(t), want, TOL["bf16"], "accumulated dO")
 
 
+@pytest.mark.parametrize("nC,K,dtype,dq_dtype,offset", [
+    (40, 8, "bf16", "f32", 0),     # key chunks scan the index array; 16-byte rows
+    (100, 8, "f32", "f32", 0),     # the same with f32 landmarks (4-wide vectors)
+    (100, 8, "bf16", "bf16", 1),   # dq_lmk rows off the 16-byte grid: element path
+    (128, 16, "bf16", "f32", 0),   # 2048 entries: the largest scanned array
+    (129, 16, "bf16", "f32", 0),   # 2064 entries: the CSR built by a launch before
+    (300, 8, "bf16", "f32", 0),    # CSR; chunk 0's 300 consumers in two passes of 256
+    (300, 8, "f32", "bf16", 1),    # CSR, element path
+])
+def test_scores_backward_paths(nC, K, dtype, dq_dtype, offset):
+    """Landmark gradients on every path of the launch (scan or CSR, vector or element
+    rows), with an index array built to stress them: chunk 0 in slot 0 of every row (the
+    longest consumer list), the same chunk twice in one row, empty slots, and random
+    chunks elsewhere; against the oracle's loops."""
+    g = _g()
+    B, D = 2, 128
+    lm = synth.landmark_inputs(11, B, nC, nC, D, dtype)
+    idx = synth.integers(nC + K, synth.S_PLANT, -1, nC, (B, nC, K)).astype(np.int32)
+    idx[:, :, 0] = 0
+    idx[:, ::3, 1] = idx[:, ::3, 2]  # a repeated chunk within a row
+    ds = synth.normal(nC + K, synth.S_DSC, (B, nC, K), 1.0, "f32")
+    dq_ref, dk_ref = orc.scores_backward(lm["q_lmk"], lm["k_lmk"], idx, ds)
+    ql, kl = dev(lm["q_lmk"], dtype), dev(lm["k_lmk"], dtype)
+    it, dst = torch.from_numpy(idx).cuda(), torch.from_numpy(ds.astype(np.float32)).cuda()
+    tdt = torch.bfloat16 if dq_dtype == "bf16" else torch.float32
+    room = torch.full((B, nC, D + 8), float("nan"), dtype=tdt, device="cuda")
+    dq_out = room[:, :, offset:offset + D]
+    ws = g.Workspace()
+    dq, dk = g.scores_backward(ql, kl, it, dst, ws=ws, dq_out=dq_out)
+    ws.check()
+    tol = TOL["bf16"] if dq_dtype == "bf16" else 1e-5
+    assert_close(host(dq), dq_ref, tol, "dq_lmk")
+    assert_close(host(dk), dk_ref, 1e-5, "dk_lmk")
+    # Deterministic: the same call gives the same bits.
+    dq2, dk2 = g.scores_backward(ql, kl, it, dst, ws=ws)
+    assert torch.equal(dk, dk2)
+
+
+def test_scores_backward_bad_index():
+    """An index outside [-1, nC) is reported through the workspace and left out of both
+    gradients, on the scanned and the CSR path."""
+    g = _g()
+    for nC, K in ((12, 4), (300, 8)):
+        B, D = 1, 64
+        lm = synth.landmark_inputs(12, B, nC, nC, D, "bf16")
+        idx = synth.integers(nC, synth.S_PLANT, -1, nC, (B, nC, K)).astype(np.int32)
+        idx[0, 3, 1], idx[0, 5, 0] = nC, -9
+        ds = synth.normal(nC, synth.S_DSC, (B, nC, K), 1.0, "f32")
+        ws = g.Workspace()
+        it, dst = torch.from_numpy(idx).cuda(), torch.from_numpy(ds.astype(np.float32)).cuda()
+        dq, dk = g.scores_backward(dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16"), it, dst, ws=ws)
+        with pytest.raises(g.GCAError) as e:
+            ws.check()
+        assert e.value.status == g.GCA_ERR_DEVICE_INDEX
+        clean = idx.copy()
+        clean[(clean < -1) | (clean >= nC)] = -1
+        dq_ref, dk_ref = orc.scores_backward(lm["q_lmk"], lm["k_lmk"], clean, ds)
+        assert_close(host(dq), dq_ref, 1e-5, "dq_lmk")
+        assert_close(host(dk), dk_ref, 1e-5, "dk_lmk")
+
+
 @pytest.mark.parametrize("nC", [9000, 17000])
 def test_long_sequence_consumer_lists(nC):
     """576k and 1.09M tokens, one head: 36k and 68k (row, slot) entries take the CSR of
