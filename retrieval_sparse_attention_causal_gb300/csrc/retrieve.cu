@@ -24,7 +24,10 @@
 //   retrieve_merge_kernel / retrieve_merge_warp_kernel / retrieve_merge_heads_kernel
 //                         merge the per-split candidate lists of a row (a block per row
 //                         for few rows; a warp per row for many, walking the sorted lists'
-//                         heads when they are few and short).
+//                         heads when they are few and short).  The bf16 tile kernel with
+//                         2 to 8 splits needs none of them: its split CTAs form a thread-
+//                         block cluster and merge each other's lists through distributed
+//                         shared memory.
 // Every stage keeps candidates under one total order (key descending, then index
 // ascending), so the result does not depend on how the candidates were split.
 #include <algorithm>
@@ -335,10 +338,12 @@ __device__ __forceinline__ void tile_topk(const RetrieveArgs& a, const float* St
   }
 }
 
-// Merge the TPR part lists of each row (lanes TPR r .. TPR r + TPR - 1) and write the result.
+// Merge the TPR part lists of each row (lanes TPR r .. TPR r + TPR - 1) and write the result:
+// the row's output, the split's part list in global memory, or (lists != nullptr) the
+// split's list in this CTA's shared memory for the cluster merge.
 template <int KC, int ROWS>
 __device__ __forceinline__ void tile_finish(const RetrieveArgs& a, int nsplit, int b, int row0,
-                                            int split, Cand (&L)[KC]) {
+                                            int split, Cand (&L)[KC], Cand* lists) {
   constexpr int TPR = kTileThreads / ROWS;
   const int rl = threadIdx.x / TPR, quarter = threadIdx.x % TPR;
   const int i = row0 + rl;
@@ -354,16 +359,96 @@ __device__ __forceinline__ void tile_finish(const RetrieveArgs& a, int nsplit, i
     if (r < kMaxTopk) out[r] = best;
   }
   if (quarter == 0 && i < a.nQ) {
-    if (nsplit == 1) write_row(a, b, i, out);
-    else write_part(a, nsplit, b, i, split, out);
+    if (lists) {
+      for (int r = 0; r < a.topk; ++r) lists[rl * kMaxTopk + r] = out[r];
+    } else if (nsplit == 1) {
+      write_row(a, b, i, out);
+    } else {
+      write_part(a, nsplit, b, i, split, out);
+    }
   }
+}
+
+// ---- thread-block cluster: the nsplit CTAs of one row block (cluster rank = split)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; shared-memory writes before it are visible to
+// the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The Cand at this CTA's shared-memory address p, in CTA `rank` of the cluster.
+__device__ __forceinline__ Cand ld_cand_cluster(const Cand* p, uint32_t rank) {
+  uint32_t ad, k, sc, j;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ad) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(k) : "r"(ad) : "memory");
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(sc) : "r"(ad + 4) : "memory");
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(j) : "r"(ad + 8) : "memory");
+  return Cand{__uint_as_float(k), __uint_as_float(sc), (int)j};
+}
+
+// After tile_finish wrote every split's lists: CTA s merges rows s, s + nsplit, ... of the
+// row block, a warp per row.  Lane l < nsplit copies list l (sorted, best first) from CTA l
+// into registers; each of k rounds takes the best head over the lanes (key descending,
+// index ascending, as everywhere) and the lane that held it moves to its next entry.  The
+// splits' candidate ranges are disjoint, so exactly one lane holds the winning index.
+template <int KC, int ROWS>
+__device__ __forceinline__ void cluster_merge(const RetrieveArgs& a, int nsplit, int b, int row0, const Cand* lists) {
+  cluster_sync();  // every split's lists are in place
+  const uint32_t me = cluster_rank();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int width = 1;
+  while (width < nsplit) width <<= 1;
+  for (int rl = (int)me + nsplit * warp; rl < ROWS; rl += nsplit * (kTileThreads / 32)) {
+    const int i = row0 + rl;
+    if (i >= a.nQ) break;
+    Cand H[KC];
+#pragma unroll
+    for (int k = 0; k < KC; ++k)
+      H[k] = (lane < nsplit && k < a.topk) ? ld_cand_cluster(lists + rl * kMaxTopk + k, (uint32_t)lane) : empty_cand();
+    int32_t* idx = a.idx + ((int64_t)b * a.nQ + i) * a.topk;
+    float* sc = a.scores + ((int64_t)b * a.nQ + i) * a.topk;
+    for (int q = 0; q < a.topk; ++q) {
+      float bk = H[0].key;
+      int bj = H[0].j;
+      for (int m = width >> 1; m >= 1; m >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, m);
+        const int oj = __shfl_xor_sync(0xffffffffu, bj, m);
+        if (ok > bk || (ok == bk && oj < bj)) {
+          bk = ok;
+          bj = oj;
+        }
+      }
+      bj = __shfl_sync(0xffffffffu, bj, 0);
+      if (bj == 0x7fffffff) {  // every list is spent: pad the rest
+        if (lane == 0)
+          for (int t = q; t < a.topk; ++t) {
+            idx[t] = -1;
+            sc[t] = -CUDART_INF_F;
+          }
+        break;
+      }
+      if (lane < nsplit && H[0].j == bj) {
+        idx[q] = bj;
+        sc[q] = H[0].score;
+        list_pop(H);
+      }
+    }
+  }
+  cluster_sync();  // no CTA exits while another still reads its lists
 }
 
 // ROWS query rows per CTA: 64, or 32 (bf16 only) when the problem has too few 64-row
 // blocks to occupy the GPU.
+// cl = 1: launched as clusters of nsplit CTAs along x (bf16 only); the splits merge in the
+// cluster instead of through the part lists.
 template <typename T, int KC, int ROWS>
 __global__ void __launch_bounds__(kTileThreads)
-retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
+retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg, int cl) {
   static_assert(ROWS == 64 || (ROWS == 32 && sizeof(T) == 2), "32-row blocks are bf16 only");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -516,7 +601,12 @@ retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg) {
       }
     }
   }
-  tile_finish<KC, ROWS>(a, nsplit, b, row0, split, L);
+  // The ring is idle here: every step's loads were waited for, and the loop ended on a
+  // barrier after the last reads; the lists reuse its first bytes.
+  Cand* lists = (cl && sizeof(T) == 2) ? reinterpret_cast<Cand*>(smem + (size_t)ROWS * a.D * 2) : nullptr;
+  if (lists) cp_async_wait<0>();
+  tile_finish<KC, ROWS>(a, nsplit, b, row0, split, L, lists);
+  if (lists) cluster_merge<KC, ROWS>(a, nsplit, b, row0, lists);
 }
 
 template <typename F>
@@ -640,6 +730,9 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
     const int rows = r32 ? 32 : 64;
     dim3 grid(p.nsplit, (a.nQ + rows - 1) / rows, a.B);
     const int smem = (int)TileSmem::bytes(a.D, a.bf16 != 0, rows);
+    // bf16 with 2 to 8 splits (the portable cluster size): the splits of a row block
+    // merge in their cluster, and no merge launch follows.
+    bool cl = a.bf16 && p.nsplit >= 2 && p.nsplit <= 8;
     e = with_kc(a.topk, [&](auto kc) -> cudaError_t {
       constexpr int KC = decltype(kc)::value;
       const void* fn = a.bf16 ? (r32 ? (const void*)retrieve_tile_kernel<__nv_bfloat16, KC, 32>
@@ -648,14 +741,37 @@ cudaError_t launch_retrieve(const RetrieveArgs& a, const RetrievePlan& p, cudaSt
       cudaError_t e2 = allow_smem(fn, smem);
       if (e2 != cudaSuccess) return e2;
       launch_begin("retrieve_tile", s);
-      if (a.bf16 && r32)
-        retrieve_tile_kernel<__nv_bfloat16, KC, 32><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
-      else if (a.bf16)
-        retrieve_tile_kernel<__nv_bfloat16, KC, 64><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
-      else
-        retrieve_tile_kernel<float, KC, 64><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg);
+      if (cl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kTileThreads);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = s;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)p.nsplit;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (r32) e2 = cudaLaunchKernelEx(&cfg, retrieve_tile_kernel<__nv_bfloat16, KC, 32>, a, p.nsplit, p.seg, 1);
+        else e2 = cudaLaunchKernelEx(&cfg, retrieve_tile_kernel<__nv_bfloat16, KC, 64>, a, p.nsplit, p.seg, 1);
+        if (e2 == cudaSuccess) return launch_end("retrieve_tile", s);
+        // A cluster launch the device cannot place is refused before anything runs: take
+        // the plain launch and the merge launch instead.
+        (void)cudaGetLastError();
+        cl = false;
+      }
+      if (a.bf16 && r32) {
+        retrieve_tile_kernel<__nv_bfloat16, KC, 32><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg, 0);
+      } else if (a.bf16) {
+        retrieve_tile_kernel<__nv_bfloat16, KC, 64><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg, 0);
+      } else {
+        retrieve_tile_kernel<float, KC, 64><<<grid, kTileThreads, smem, s>>>(a, p.nsplit, p.seg, 0);
+      }
       return launch_end("retrieve_tile", s);
     });
+    if (cl) nsplit = 1;  // merged already
   }
   if (e != cudaSuccess || nsplit == 1) return e;
   const long long rows = (long long)a.B * a.nQ;

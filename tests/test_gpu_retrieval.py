@@ -164,19 +164,36 @@ def test_large_row_blocks_strided_queries_and_shared_keys():
     assert nd > 0.5 * B * nQ  # most rows decidable: the test is not vacuous
 
 
-@pytest.mark.parametrize("nQ,off,K,merge", [(255, 0, 8, "retrieve_merge_block"), (256, 0, 8, "retrieve_merge_heads"),
-                                             (256, 4096, 16, "retrieve_merge_warp"),
-                                             (256, 4096, 8, "retrieve_merge_warp")])
-def test_merge_block_and_warp_paths(nQ, off, K, merge):
-    """Below 256 rows the partial lists of a row are merged by a block, from 256 rows on by
-    a warp: by walking the heads of the row's sorted lists when there are at most 32 lists
-    of at most 128 entries in all, otherwise by re-inserting every entry (here 68 lists per
-    row: 4352 candidates in 64-candidate splits).  Each variant, identified by its launch
-    name, against the oracle."""
+@pytest.mark.parametrize("B,nQ,off,K,merge", [
+    (1, 255, 513, 8, "retrieve_merge_block"),   # 12 splits, fewer than 256 rows
+    (1, 256, 513, 8, "retrieve_merge_heads"),   # 12 splits
+    (1, 256, 300, 8, "retrieve_merge_heads"),   # 9 splits: one past the cluster limit
+    (1, 256, 4096, 16, "retrieve_merge_warp"),
+    (1, 256, 4096, 8, "retrieve_merge_warp"),
+    (1, 129, 0, 8, None),                       # clusters of 2 splits
+    (1, 193, 0, 8, None),                       # 3 splits (butterfly over 4 lanes), ragged block
+    (1, 255, 0, 4, None),                       # 4 splits, k = 4
+    (1, 256, 0, 16, None),                      # 4 splits, k = 16
+    (1, 256, 200, 8, None),                     # 8 splits: the largest cluster
+    (32, 256, 0, 8, None),                      # 64-row blocks (enough CTAs for the GPU)
+])
+def test_merge_paths(B, nQ, off, K, merge):
+    """How the split candidate lists of a row are merged.  bf16 tile problems with 2 to 8
+    splits merge inside the tile kernel: the split CTAs of a row block form a cluster and
+    read each other's lists from shared memory, so no merge launch follows.  Otherwise a
+    merge launch does it: below 256 rows a block per row, from 256 rows on a warp per row,
+    walking the heads of the row's sorted lists when there are at most 32 lists of at most
+    128 entries in all, else re-inserting every entry (here 68 lists per row: 4352
+    candidates in 64-candidate splits).  Each path, identified by its launch names,
+    against the oracle."""
     g = _gca()
     g.profile_begin()
-    _, _, _, nd, _ = run_case(1, nQ, nQ + off, 256, K, "bf16", off=off, gumbel=True, seed=9)
+    _, _, _, nd, _ = run_case(B, nQ, nQ + off, 256, K, "bf16", off=off, gumbel=True, seed=9)
     prof = g.profile_end()
-    assert nd > 0.5 * nQ
-    assert merge in prof, sorted(prof)
-    assert not any(n.startswith("retrieve_merge") and n != merge for n in prof), sorted(prof)
+    assert nd > 0.5 * B * nQ
+    assert "retrieve_tile" in prof, sorted(prof)
+    if merge is None:
+        assert not any(n.startswith("retrieve_merge") for n in prof), sorted(prof)
+    else:
+        assert merge in prof, sorted(prof)
+        assert not any(n.startswith("retrieve_merge") and n != merge for n in prof), sorted(prof)
