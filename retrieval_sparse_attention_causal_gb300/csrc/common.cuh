@@ -77,6 +77,28 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return r;
 }
 
+// ---------------------------------------------------------------- query-tile order
+// Tile t in [0, nQ * H * B) of the persistent forward and query-side kernels, as (query
+// chunk c, head h, sequence b).  The chunks c >= L of every sequence-head come first,
+// head-major with c fastest (the CTAs in flight share that sequence-head's K/V in L2);
+// the first L chunks of each follow.  Under causal retrieval those rows have fewer valid
+// slots (L = min(nQ, shift + topk)), so the tiles that start last are the light ones and
+// the kernels' tails are short.  Any order gives the same results.
+__device__ __forceinline__ void query_tile(int nQ, int H, int B, int L, int t, int& c, int& h, int& b) {
+  const int F = nQ - L, nfull = F * H * B;
+  int hb;
+  if (t < nfull) {
+    hb = t / F;
+    c = L + (t - hb * F);
+  } else {
+    const int u = t - nfull;
+    hb = u / L;
+    c = u - hb * L;
+  }
+  h = hb % H;
+  b = hb / H;
+}
+
 // ---------------------------------------------------------------- splitmix64 noise
 // splitmix64 (Steele, Lea & Flood, 2014): output number n from state `seed`.
 __device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t n) {

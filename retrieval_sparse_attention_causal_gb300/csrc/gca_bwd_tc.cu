@@ -42,8 +42,8 @@ enum { kBarOpReady = 2, kBarEW = 3 };
 
 // ================================================================== query side
 // Persistent: each CTA walks the tiles (query chunk, head, sequence) blockIdx.x,
-// blockIdx.x + gridDim.x, ... (head-major, so the CTAs in flight share K/V in L2), with
-// three warp roles:
+// blockIdx.x + gridDim.x, ... (head-major, so the CTAs in flight share K/V in L2; the
+// light first chunks of every sequence-head last, query_tile), with three warp roles:
 //   * warp 9 (producer): reads each tile's retrieval row (slots and fusion weights) into
 //     a ring of metadata records one tile ahead of its loads; lane 0 streams Q, dO and the
 //     tile's LSE rows (double-buffered) and the K / V tiles of its slots through a ring of
@@ -103,6 +103,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ts = (int64_t)a.H * DH;
   const int ntiles = a.nQ * a.H * a.B;
+  const int qL = min(a.nQ, a.shift + a.topk);  // light chunks per sequence-head (query_tile)
 
   if (warp == kProd && lane == 0) {
     for (int x = 0; x < kMetaBufs; ++x) {
@@ -154,7 +155,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     auto prepare_meta = [&](int k, int t) -> bool {
       const int mb = k % kMetaBufs;
       if (k >= kMetaBufs && !P(&meta_empty[mb], ((k / kMetaBufs) - 1) & 1, 1, k, -1)) return false;
-      const int c = t % a.nQ, b = t / (a.nQ * a.H);
+      int c, h, b;
+      query_tile(a.nQ, a.H, a.B, qL, t, c, h, b);
       const int r = c - a.shift;
       QTileMeta& M = meta[mb];
       if (r >= 0) {
@@ -166,7 +168,7 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
       }
       __syncwarp();
       // The key side takes every consumer's fusion weight from this table (one head writes it).
-      if (r >= 0 && (t / a.nQ) % a.H == 0 && lane < a.topk) a.wrow[((int64_t)b * a.nQ + r) * a.topk + lane] = M.w[lane];
+      if (r >= 0 && h == 0 && lane < a.topk) a.wrow[((int64_t)b * a.nQ + r) * a.topk + lane] = M.w[lane];
       if (lane == 0) {
         int n = 0;
         for (int m = 0; m < a.topk; ++m)
@@ -180,7 +182,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     bool alive = prepare_meta(0, blockIdx.x);
     for (int k = 0, t = blockIdx.x; alive && t < ntiles; ++k, t += gridDim.x) {
       const int buf = k & 1;
-      const int c = t % a.nQ, h = (t / a.nQ) % a.H, b = t / (a.nQ * a.H);
+      int c, h, b;
+      query_tile(a.nQ, a.H, a.B, qL, t, c, h, b);
       if (lane == 0) {  // Q, dO and the LSE rows of tile k
         if (k >= 2 && !P(&qfree[buf], ((k - 2) >> 1) & 1, 2, k, -1)) {
           alive = false;
@@ -317,7 +320,8 @@ gca_bwd_q_tc_kernel(BwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __
     bool alive = true;
     for (int k = 0, t = blockIdx.x; alive && t < ntiles; ++k, t += gridDim.x) {
       const int buf = k & 1;
-      const int c = t % a.nQ, h = (t / a.nQ) % a.H, b = t / (a.nQ * a.H);
+      int c, h, b;
+      query_tile(a.nQ, a.H, a.B, qL, t, c, h, b);
       const int64_t tok0 = ((int64_t)b * a.nQ * 64 + (int64_t)c * 64) * ts + h * DH;
       bf16* dqg = reinterpret_cast<bf16*>(a.dq) + tok0;
       const int64_t rowbase = ((int64_t)b * a.nQ + c) * a.H + h;

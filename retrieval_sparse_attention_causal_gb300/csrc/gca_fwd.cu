@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(128) gca_fwd_mma_kernel(FwdArgs a) {
 // Same decomposition on the 5th-generation tensor cores, warp-specialised and persistent:
 // four CTAs per SM, each walking the tiles (query chunk, head, sequence) blockIdx.x,
 // blockIdx.x + gridDim.x, ... in head-major order (the CTAs in flight share one
-// sequence-head's K/V in L2).  Roles:
+// sequence-head's K/V in L2), the light first chunks of every sequence-head last
+// (query_tile).  Roles:
 //   * warp 6 (metadata): each tile's retrieval row (valid slots, chunks, fusion weights)
 //     into a ring of records, a few tiles ahead;
 //   * warp 5 (producer, lane 0): Q of each tile into one of two buffers, and the K and V
@@ -301,7 +302,8 @@ gca_fwd_tc_kernel(FwdArgs a, const __grid_constant__ CUtensorMap tmQ, const __gr
         }
         break;
       }
-      const int c = t % a.nQ, h = (t / a.nQ) % a.H, b = t / (a.nQ * a.H);
+      int c, h, b;
+      query_tile(a.nQ, a.H, a.B, min(a.nQ, a.shift + a.topk), t, c, h, b);
       const int r = c - a.shift;
       if (r >= 0) {
         row_weights_warp(a.idx + ((int64_t)b * a.nQ + r) * a.topk, a.scores + ((int64_t)b * a.nQ + r) * a.topk,
