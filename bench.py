@@ -193,17 +193,17 @@ KERNEL_SOURCES = {
     "retrieve_tc": ("retrieve_tc.cu", "tc.cuh", "tc_rows.cuh", "common.cuh"),
 }
 KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); profiles/gca_tc_kernels_128m.md
-    "gca_fwd": (3.8188e+08, "241db333501dcbce"),
-    "gca_bwd_q": (5.0978e+08, "56896f4275d0ddf9"),
-    "gca_bwd_kv": (6.9611e+08, "56896f4275d0ddf9"),
+    "gca_fwd": (3.8405e+08, "c215969a10653850"),
+    "gca_bwd_q": (5.1387e+08, "4f625c47e217a1eb"),
+    "gca_bwd_kv": (7.0037e+08, "4f625c47e217a1eb"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (805513984 / 2, "604458e697ccdb3b")
+STREAM_TRAFFIC_PER_SEQ = (805565440 / 2, "ace4f833981931f2")
 
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
 # nothing written back past L2; traffic grows with the number of chunks)
-PREFILL_TRAFFIC_PER_CHUNK = (25217536 / 8192, "11c4cd78c1b2463f")
+PREFILL_TRAFFIC_PER_CHUNK = (25217280 / 8192, "2c1f4177bbce2558")
 
 
 def source_fingerprint(kernel: str) -> str:
