@@ -165,7 +165,7 @@ def algorithmic_bytes(B_, nC, H_, dh, k, esize=2):
 # ----------------------------------------------------------------------------- replicas
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """Slowest rank's time (the job's time).  Works with any initialised backend: NCCL
-    on the GPU machine, gloo in the CPU tests."""
+    on GPUs, gloo in the CPU tests."""
     if world <= 1:
         return ms
     import torch
