@@ -107,6 +107,20 @@ GCA_API gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride, in
                              int B, int nQ, int nC, int D, int topk, int causal_offset,
                              int use_gumbel, uint64_t seed, int group, int32_t* idx,
                              float* scores, void* ws, size_t ws_bytes, gca_stream_t stream);
+/* gca_retrieve_topk_dseed - gca_retrieve_topk with the noise seed in device memory: the
+ * kernels read the one uint64 at `seed` when they run, not when the call is made.  A
+ * captured CUDA graph of a training step can then draw fresh noise on every replay (a
+ * kernel in the graph, or a copy before each replay, writes the next seed).  `seed` is a
+ * device pointer, 8-byte aligned, that the caller keeps alive while the work runs; it is
+ * only read.  Every other argument, the results and the errors are those of
+ * gca_retrieve_topk with that seed value; a NULL or misaligned `seed` returns
+ * GCA_ERR_INVALID_ARG before anything is launched. */
+GCA_API gca_status gca_retrieve_topk_dseed(const void* q_lmk, int64_t q_row_stride,
+                                   int64_t q_batch_stride, const void* k_lmk,
+                                   int64_t k_batch_stride, gca_dtype dtype, int B, int nQ,
+                                   int nC, int D, int topk, int causal_offset, int use_gumbel,
+                                   const uint64_t* seed, int group, int32_t* idx,
+                                   float* scores, void* ws, size_t ws_bytes, gca_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * gca_retrieve_topk_noalloc - gca_retrieve_topk for callers that cannot allocate.

@@ -54,6 +54,7 @@ def _load():
         "gca_last_error_detail": (ctypes.c_char_p, []),
         "gca_retrieve_workspace_size": (SZ, [I, I, I, I, I]),
         "gca_retrieve_topk": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P, SZ, P]),
+        "gca_retrieve_topk_dseed": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, P, I, P, P, P, SZ, P]),
         "gca_retrieve_noalloc_max_scratch": (SZ, []),
         "gca_retrieve_topk_noalloc": (I, [P, I64, I64, P, I64, I, I, I, I, I, I, I, I, U64, I, P, P, P]),
         "gca_retrieve_noalloc_check_error": (I, [P, ctypes.POINTER(I)]),
@@ -92,6 +93,7 @@ def _load():
 LIB = _load()
 EXPORTS = (
     "gca_status_string", "gca_last_error_detail", "gca_retrieve_workspace_size", "gca_retrieve_topk",
+    "gca_retrieve_topk_dseed",
     "gca_retrieve_noalloc_max_scratch", "gca_retrieve_topk_noalloc", "gca_retrieve_noalloc_check_error",
     "gca_retrieve_noalloc_selftest_timeout",
     "gca_forward_workspace_size", "gca_forward", "gca_window_forward", "gca_cca_forward",
@@ -176,11 +178,14 @@ def default_workspace(device) -> Workspace:
 # --------------------------------------------------------------------------- retrieval
 def retrieve_topk(q_lmk: torch.Tensor, k_lmk: torch.Tensor, topk: int, causal_offset: int = 0,
                   use_gumbel: bool = False, seed: int = 0, group: int = 0, ws: Workspace = None,
-                  idx: torch.Tensor = None, scores: torch.Tensor = None, k_shared: bool = False):
+                  idx: torch.Tensor = None, scores: torch.Tensor = None, k_shared: bool = False,
+                  seed_dev: torch.Tensor = None):
     """Causal landmark scoring + top-k (gca_retrieve_topk).
 
     q_lmk [B, nQ, D] (any row/batch strides, unit element stride), k_lmk [B, nC, D]
     (rows contiguous; or [nC, D] shared by all sequences when k_shared).
+    seed_dev: a one-element int64 device tensor; when given, the kernels read the noise
+    seed from it when they run (gca_retrieve_topk_dseed) and `seed` is not used.
     Returns idx [B, nQ, topk] int32 and scores [B, nQ, topk] float32."""
     _cuda(q_lmk, k_lmk)
     B, nQ, D = q_lmk.shape
@@ -201,6 +206,14 @@ def retrieve_topk(q_lmk: torch.Tensor, k_lmk: torch.Tensor, topk: int, causal_of
     ws = ws or default_workspace(dev)
     need = LIB.gca_retrieve_workspace_size(B, nQ, nC, topk, causal_offset)
     buf = ws.get(need)
+    if seed_dev is not None:
+        _cuda(seed_dev)
+        _need(seed_dev.dtype == torch.int64 and seed_dev.numel() == 1, "seed_dev must be a one-element int64 tensor")
+        _check(LIB.gca_retrieve_topk_dseed(_ptr(q_lmk), q_lmk.stride(1), q_lmk.stride(0), _ptr(k_lmk), k_bs,
+                                           _dtype(q_lmk), B, nQ, nC, D, topk, causal_offset, int(bool(use_gumbel)),
+                                           _ptr(seed_dev), group, _ptr(idx), _ptr(scores), _ptr(buf), buf.numel(),
+                                           _stream()))
+        return idx, scores
     _check(LIB.gca_retrieve_topk(_ptr(q_lmk), q_lmk.stride(1), q_lmk.stride(0), _ptr(k_lmk), k_bs,
                                  _dtype(q_lmk), B, nQ, nC, D, topk, causal_offset, int(bool(use_gumbel)),
                                  ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), group, _ptr(idx), _ptr(scores),

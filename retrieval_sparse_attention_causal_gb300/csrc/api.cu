@@ -189,11 +189,11 @@ gca_status gca::check_retrieve_args(const void* q_lmk, int64_t q_row_stride, int
   return GCA_OK;
 }
 
-extern "C" gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
-                                        const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype, int B,
-                                        int nQ, int nC, int D, int topk, int causal_offset, int use_gumbel,
-                                        uint64_t seed, int group, int32_t* idx, float* scores, void* ws,
-                                        size_t ws_bytes, gca_stream_t stream) {
+static gca_status retrieve_topk_impl(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
+                                     const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype, int B, int nQ,
+                                     int nC, int D, int topk, int causal_offset, int use_gumbel, uint64_t seed,
+                                     const uint64_t* seed_dev, int group, int32_t* idx, float* scores, void* ws,
+                                     size_t ws_bytes, gca_stream_t stream) {
   gca_status st = check_retrieve_args(q_lmk, q_row_stride, q_batch_stride, k_lmk, k_batch_stride, dtype, B, nQ,
                                       nC, D, topk, causal_offset, use_gumbel, group, idx, scores);
   if (st != GCA_OK) return st;
@@ -205,13 +205,33 @@ extern "C" gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride,
   a.k = k_lmk; a.k_bs = k_batch_stride;
   a.bf16 = dtype == GCA_BF16;
   a.B = B; a.nQ = nQ; a.nC = nC; a.D = D; a.topk = topk; a.off = causal_offset;
-  a.gumbel = use_gumbel ? 1 : 0; a.seed = seed; a.group = group;
+  a.gumbel = use_gumbel ? 1 : 0; a.seed = seed; a.group = group; a.seed_dev = seed_dev;
   a.idx = idx; a.scores = scores;
   a.err = reinterpret_cast<ErrWord*>(ws);
   a.part = static_cast<unsigned char*>(ws) + kErrBytes;
   cudaError_t e = launch_retrieve(a, p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "gca_retrieve_topk launch");
   return GCA_OK;
+}
+
+extern "C" gca_status gca_retrieve_topk(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
+                                        const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype, int B,
+                                        int nQ, int nC, int D, int topk, int causal_offset, int use_gumbel,
+                                        uint64_t seed, int group, int32_t* idx, float* scores, void* ws,
+                                        size_t ws_bytes, gca_stream_t stream) {
+  return retrieve_topk_impl(q_lmk, q_row_stride, q_batch_stride, k_lmk, k_batch_stride, dtype, B, nQ, nC, D, topk,
+                            causal_offset, use_gumbel, seed, nullptr, group, idx, scores, ws, ws_bytes, stream);
+}
+
+extern "C" gca_status gca_retrieve_topk_dseed(const void* q_lmk, int64_t q_row_stride, int64_t q_batch_stride,
+                                              const void* k_lmk, int64_t k_batch_stride, gca_dtype dtype, int B,
+                                              int nQ, int nC, int D, int topk, int causal_offset, int use_gumbel,
+                                              const uint64_t* seed, int group, int32_t* idx, float* scores,
+                                              void* ws, size_t ws_bytes, gca_stream_t stream) {
+  if (!seed || (reinterpret_cast<uintptr_t>(seed) & 7))
+    return fail(GCA_ERR_INVALID_ARG, "seed must be a non-NULL, 8-byte aligned device pointer");
+  return retrieve_topk_impl(q_lmk, q_row_stride, q_batch_stride, k_lmk, k_batch_stride, dtype, B, nQ, nC, D, topk,
+                            causal_offset, use_gumbel, 0, seed, group, idx, scores, ws, ws_bytes, stream);
 }
 
 // ==================================================================== GCA forward

@@ -56,6 +56,7 @@ struct RetrieveArgs {
   int bf16;
   int B, nQ, nC, D, topk, off;
   int gumbel; uint64_t seed; int group;
+  const uint64_t* seed_dev;  // when set, the kernels take the seed from here at launch
   int32_t* idx; float* scores;
   ErrWord* err;
   void* part;  // partial-candidate buffer (may be null when nsplit == 1)

@@ -90,6 +90,7 @@ __host__ __device__ inline int stream_rows(int D, int elem) {
 template <typename T, int NV, int KC>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 retrieve_stream_kernel(RetrieveArgs a, int nsplit, int seg) {
+  if (a.seed_dev) a.seed = *a.seed_dev;
   constexpr int EPV = 16 / sizeof(T), NST = kStreamStages, NCW = kStreamConsumers;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ Cand red[kStreamThreads / 32];
@@ -449,6 +450,7 @@ __device__ __forceinline__ void cluster_merge(const RetrieveArgs& a, int nsplit,
 template <typename T, int KC, int ROWS>
 __global__ void __launch_bounds__(kTileThreads)
 retrieve_tile_kernel(RetrieveArgs a, int nsplit, int seg, int cl) {
+  if (a.seed_dev) a.seed = *a.seed_dev;
   static_assert(ROWS == 64 || (ROWS == 32 && sizeof(T) == 2), "32-row blocks are bf16 only");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(

@@ -106,6 +106,7 @@ template <int KC, bool kNoise>
 __global__ void __launch_bounds__(kThreads, 1)
 retrieve_tc_kernel(RetrieveArgs a, int ns, int sl, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK) {
+  if (a.seed_dev) a.seed = *a.seed_dev;
   constexpr int NST = kStages;
   constexpr uint32_t kId = tc::idesc_bf16(kBM, kBN, false);
   const int seg = blockIdx.x, mb = gridDim.y - 1 - blockIdx.y, b = blockIdx.z;  // largest row blocks first

@@ -19,8 +19,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (CHUNK, Workspace, default_workspace, gather_chunks, gca_backward, gca_forward, retrieve_topk,
-               scores_backward)
+from . import (CHUNK, Workspace, default_workspace, gather_chunks, gca_backward, gca_forward, launch_count,
+               retrieve_topk, scores_backward)
 
 
 def landmark_view(o: torch.Tensor) -> torch.Tensor:
@@ -94,6 +94,65 @@ def decode_offload(q_new, k_host, v_host, q_lmk_new, k_lmk_store, topk=8, kv_sha
     kd, vd, il = gather_chunks(k_host, v_host, idx, kv_shared=kv_shared, ws=ws, k_dst=kd, v_dst=vd, idx_local=il)
     o, lse = gca_forward(q_new, kd, vd, il, scores, shift=0, ws=ws)
     return dict(idx=idx, scores=scores, o=o, lse=lse, idx_local=il)
+
+
+class TrainGraph:
+    """The training step of one retrieval group (train_step) captured once as a CUDA graph
+    and replayed.
+
+    The step is six launches (retrieval, forward, query side, score gradient, key side,
+    landmark gradients).  Issued one by one, each waits at the GPU's front end for the one
+    before; replayed as one graph, they follow each other with less of that gap.  The
+    noise seed lives in a one-element device tensor (`self.seed`) that the retrieval
+    kernels read when they run, and the graph ends by adding 1 to it: replay number i
+    (counting from 0 after construction or set_seed(s)) draws the noise of seed + i, as
+    train_step(..., seed=seed + i) does.  Replays read the current contents of the input
+    tensors given here (update them in place between steps) and overwrite the tensors of
+    `self.out` (the keys of train_step's result)."""
+
+    def __init__(self, q, k, v, q_lmk, k_lmk, dout, topk=8, seed=0, group=0, use_gumbel=True, ws=None):
+        dev = q.device
+        self.ws = ws or Workspace(dev)
+        B, L, H, dh = q.shape
+        nQ, D = L // CHUNK, q_lmk.shape[2]
+        self.seed = torch.full((1,), int(seed), dtype=torch.int64, device=dev)
+        f32 = torch.float32
+        self.out = dict(idx=torch.empty((B, nQ, topk), dtype=torch.int32, device=dev),
+                        scores=torch.empty((B, nQ, topk), dtype=f32, device=dev),
+                        o=torch.empty_like(q), lse=torch.empty((B, nQ, H, topk, 64), dtype=f32, device=dev),
+                        dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                        dscores=torch.empty((B, nQ, topk), dtype=f32, device=dev),
+                        dq_lmk=torch.empty((B, nQ, D), dtype=f32, device=dev),
+                        dk_lmk=torch.empty((B, k_lmk.shape[1], D), dtype=f32, device=dev))
+        self._in = (q, k, v, q_lmk, k_lmk, dout)
+        self._cfg = (topk, group, use_gumbel)
+        self._step()  # warm-up outside the capture: sizes the workspace, sets kernel attributes
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        n0 = launch_count()
+        with torch.cuda.graph(self.graph):
+            self._step()
+            self.seed.add_(1)
+        self.launches_per_replay = launch_count() - n0  # this library's kernels in one replay
+
+    def _step(self):
+        q, k, v, ql, kl, do = self._in
+        topk, group, use_gumbel = self._cfg
+        o, ws = self.out, self.ws
+        retrieve_topk(ql, kl, topk, 0, use_gumbel, 0, group, ws=ws, idx=o["idx"], scores=o["scores"],
+                      seed_dev=self.seed)
+        gca_forward(q, k, v, o["idx"], o["scores"], shift=1, ws=ws, out=o["o"], lse=o["lse"])
+        gca_backward(q, k, v, o["idx"], o["scores"], do, o["lse"], shift=1, ws=ws, dq=o["dq"], dk=o["dk"],
+                     dv=o["dv"], dscores=o["dscores"])
+        scores_backward(ql, kl, o["idx"], o["dscores"], ws=ws, dq_out=o["dq_lmk"], dk_lmk=o["dk_lmk"])
+
+    def set_seed(self, seed: int):
+        """The next replay draws the noise of `seed` (asynchronous, on the current stream)."""
+        self.seed.fill_(int(seed))
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
 
 
 class DecodeGraph:

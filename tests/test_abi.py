@@ -92,6 +92,20 @@ def _fwd(gca, **kw):
                                a["wsb"], None)
 
 
+def test_retrieve_dseed_rejects_a_bad_seed_pointer(gca):
+    """The device-seed variant checks its seed pointer (NULL, not 8-byte aligned) and
+    otherwise validates like gca_retrieve_topk, all before launching anything."""
+    L = gca.LIB
+
+    def call(seed, q=FAKE):
+        return L.gca_retrieve_topk_dseed(q, 768, 256 * 768, FAKE, 256 * 768, gca.GCA_BF16, 4, 256, 256, 768, 8, 0, 1,
+                                         seed, 0, FAKE, FAKE, FAKE, 1 << 30, None)
+
+    assert call(0) == gca.GCA_ERR_INVALID_ARG
+    assert call(FAKE + 4) == gca.GCA_ERR_INVALID_ARG
+    assert call(FAKE, q=0) == gca.GCA_ERR_INVALID_ARG
+
+
 def test_forward_rejects_bad_arguments(gca):
     assert _fwd(gca, dh=128) == gca.GCA_ERR_UNSUPPORTED
     assert _fwd(gca, shift=2) == gca.GCA_ERR_INVALID_ARG

@@ -227,6 +227,33 @@ def test_decode_graph_replays_the_eager_step():
     g.ws.check()
 
 
+def test_train_graph_replays_the_eager_step():
+    """The training step captured as a CUDA graph (TrainGraph) gives train_step's results
+    bit for bit; replay i draws the noise of seed + i, and set_seed restarts the sequence."""
+    from retrieval_sparse_attention_causal_gb300 import pipeline
+    B, nC, H, dh, D, K = 2, 40, 4, 64, 256, 8
+    x = synth.gca_inputs(63, B, nC, nC, H, dh, 1 / 8, "bf16")
+    lm = synth.landmark_inputs(63, B, nC, nC, D, "bf16")
+    q, k, v, do = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    ql, kl = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
+    g = pipeline.TrainGraph(q, k, v, ql, kl, do, topk=K, seed=100)
+    assert g.launches_per_replay >= 4
+    names = ("idx", "scores", "o", "lse", "dq", "dk", "dv", "dscores", "dq_lmk", "dk_lmk")
+    for s in (100, 101, 102):
+        out = {n: t.clone() for n, t in g.replay().items()}
+        ref = pipeline.train_step(q, k, v, ql, kl, do, topk=K, seed=s)
+        torch.cuda.synchronize()
+        for n in names:
+            assert torch.equal(out[n], ref[n]), (s, n)
+    g.set_seed(101)
+    out = g.replay()
+    ref = pipeline.train_step(q, k, v, ql, kl, do, topk=K, seed=101)
+    torch.cuda.synchronize()
+    assert all(torch.equal(out[n], ref[n]) for n in names)
+    assert not torch.equal(out["idx"], pipeline.train_step(q, k, v, ql, kl, do, topk=K, seed=100)["idx"])
+    g.ws.check()
+
+
 def _near_tie_set_check(idx_g_row, key_o, n_cand, gap, what):
     """The GPU's and the oracle's chosen sets may differ only by candidates whose oracle
     key lies within `gap` of the oracle's k-th key."""

@@ -123,6 +123,31 @@ def test_strided_query_rows_and_shared_keys():
     compare_retrieval(idx_g.cpu().numpy(), host(sc_g), idx_o, sc_o, m, 1e-4, orc=orc, q=qv, k=ko, off=2)
 
 
+@pytest.mark.parametrize("B,nQ,nC,D,off,kernel", [
+    (4, 256, 256, 768, 0, "retrieve_tile"),      # split lists merged in a cluster
+    (2, 3, 5000, 512, 5000, "retrieve_stream"),  # few rows, long rows
+    (4, 4096, 4096, 128, 0, "retrieve_tc"),      # tcgen05 scoring
+])
+def test_device_seed_equals_host_seed(B, nQ, nC, D, off, kernel):
+    """gca_retrieve_topk_dseed with the seed in device memory gives the results of
+    gca_retrieve_topk with that seed, on each retrieval kernel, bit for bit."""
+    g = _gca()
+    lm = synth.landmark_inputs(21, B, nQ, nC, D, "bf16")
+    ql, kl = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
+    sd = torch.tensor([987654321987], dtype=torch.int64, device="cuda")
+    g.profile_begin()
+    i1, s1 = g.retrieve_topk(ql, kl, 8, off, True, 987654321987, 1)
+    p1 = g.profile_end()
+    g.profile_begin()
+    i2, s2 = g.retrieve_topk(ql, kl, 8, off, True, 0, 1, seed_dev=sd)
+    p2 = g.profile_end()
+    torch.cuda.synchronize()
+    assert sorted(p1) == sorted(p2) and kernel in p1, sorted(p1)
+    assert torch.equal(i1, i2) and torch.equal(s1, s2)
+    i3, _ = g.retrieve_topk(ql, kl, 8, off, True, 987654321988, 1)
+    assert not torch.equal(i1, i3)  # the seed matters here
+
+
 def test_deterministic():
     g = _gca()
     lm = synth.landmark_inputs(4, 2, 200, 200, 256, "bf16")
