@@ -300,7 +300,8 @@ def gpu_arm(args):
     # six launches without the front-end gaps between separately issued ones.
     from retrieval_sparse_attention_causal_gb300 import pipeline
     gws = gca.Workspace()
-    graph = pipeline.TrainGraph(q, k, v, ql, kl, do, topk=K, seed=seed, ws=gws)
+    graph = pipeline.TrainGraph(lambda sd: pipeline.train_step(q, k, v, ql, kl, do, topk=K, seed_dev=sd, ws=gws),
+                                seed=seed)
 
     def gstep(i):
         graph.replay()
@@ -692,11 +693,11 @@ def train_350m_leg(args, torch, gca, synth, seed, timed, pk, src, clk_cls):
     o.update({n: torch.empty((b_, nc, d), dtype=f32, device="cuda") for n in ("dq1l", "dk1l", "dk2l")})
     q2l = landmark_view(o["o1"])
 
-    def step(i):
+    def step(i, seed_dev=None):
         last.copy_(last_saved)
-        gca.retrieve_topk(q1l, k1l, k, 0, True, seed + i, 0, ws=ws, idx=o["idx1"], scores=o["s1"])
+        gca.retrieve_topk(q1l, k1l, k, 0, True, seed + i, 0, ws=ws, idx=o["idx1"], scores=o["s1"], seed_dev=seed_dev)
         gca.gca_forward(q1, kk, vv, o["idx1"], o["s1"], shift=1, ws=ws, out=o["o1"], lse=o["lse1"])
-        gca.retrieve_topk(q2l, k2l, k, 0, True, seed + i, 1, ws=ws, idx=o["idx2"], scores=o["s2"])
+        gca.retrieve_topk(q2l, k2l, k, 0, True, seed + i, 1, ws=ws, idx=o["idx2"], scores=o["s2"], seed_dev=seed_dev)
         gca.gca_forward(q2, kk, vv, o["idx2"], o["s2"], shift=1, ws=ws, out=o["o2"], lse=o["lse2"])
         gca.gca_backward(q2, kk, vv, o["idx2"], o["s2"], do2, o["lse2"], shift=1, ws=ws, dq=o["dq2"], dk=o["dk"],
                          dv=o["dv"], dscores=o["ds2"])
@@ -708,11 +709,27 @@ def train_350m_leg(args, torch, gca, synth, seed, timed, pk, src, clk_cls):
     for i in range(args.warmup):
         step(i)
     ws.check()
-    n0 = gca.launch_count()
+    # Timed as one CUDA graph per step (replay i draws the noise of seed + i), as the
+    # 128M step is; the same step issued launch by launch is reported beside it.
+    from retrieval_sparse_attention_causal_gb300 import pipeline
+    graph = pipeline.TrainGraph(lambda sd: step(0, seed_dev=sd), seed=seed)
+
+    def gstep(i):
+        graph.replay()
+
+    for i in range(args.warmup):
+        gstep(i)
     with clk_cls(torch) as clk:
-        reps = timed_repeats(timed, step, args.steps, args.min_seconds)
-    launches = (gca.launch_count() - n0) // len(reps)
+        reps = timed_repeats(timed, gstep, args.steps, args.min_seconds)
+    ws.check()
+    launches = graph.launches_per_replay * args.steps
     ms = statistics.median(reps) / args.steps
+    n0 = gca.launch_count()
+    reps_e = timed_repeats(timed, step, args.steps, args.min_seconds)
+    ms_e = statistics.median(reps_e) / args.steps
+    eager = {"ms_per_step": round(ms_e, 4), "tokens_per_s": round(b_ * wl.L / (ms_e / 1e3), 1),
+             "gpu_launches": int((gca.launch_count() - n0) // len(reps_e))}
+    del graph
     gca.profile_begin()
     timed(step, args.steps)
     prof = gca.profile_end()
@@ -733,6 +750,7 @@ def train_350m_leg(args, torch, gca, synth, seed, timed, pk, src, clk_cls):
                        f"per group, Gumbel noise",
            "tokens_per_s": round(tokens / (ms / 1e3), 1), "ms_per_step": round(ms, 4), "steps": args.steps,
            "timed_repeats": len(reps), "gpu_launches": int(launches), "clocks": clk.summary(),
+           "step_issue": "one CUDA graph per step (pipeline.TrainGraph)", "eager": eager,
            "flops_algorithmic_per_step": step_fl, "tflops_algorithmic": round(tf_step, 1),
            "frac_of_bf16_peak": round(tf_step / pk["bf16_tflops"], 4),
            "peak_source": f"{src} bf16 dense (burst)", "kernels": kern,

@@ -29,10 +29,11 @@ def landmark_view(o: torch.Tensor) -> torch.Tensor:
     return o[:, CHUNK - 1::CHUNK].reshape(B, L // CHUNK, H * dh)
 
 
-def train_step(q, k, v, q_lmk, k_lmk, dout, topk=8, seed=0, group=0, use_gumbel=True, ws=None):
-    """One retrieval group, forward and backward.  Returns a dict of every result."""
+def train_step(q, k, v, q_lmk, k_lmk, dout, topk=8, seed=0, group=0, use_gumbel=True, ws=None, seed_dev=None):
+    """One retrieval group, forward and backward.  Returns a dict of every result.
+    seed_dev (a one-element int64 device tensor) replaces `seed` when given."""
     ws = ws or default_workspace(q.device)
-    idx, scores = retrieve_topk(q_lmk, k_lmk, topk, 0, use_gumbel, seed, group, ws=ws)
+    idx, scores = retrieve_topk(q_lmk, k_lmk, topk, 0, use_gumbel, seed, group, ws=ws, seed_dev=seed_dev)
     o, lse = gca_forward(q, k, v, idx, scores, shift=1, ws=ws)
     dq, dk, dv, ds = gca_backward(q, k, v, idx, scores, dout, lse, shift=1, ws=ws)
     dq_lmk, dk_lmk = scores_backward(q_lmk, k_lmk, idx, ds, ws=ws)
@@ -41,14 +42,15 @@ def train_step(q, k, v, q_lmk, k_lmk, dout, topk=8, seed=0, group=0, use_gumbel=
 
 
 def train_step_two_groups(q1, q2, k, v, q1_lmk, k1_lmk, k2_lmk, dout1, dout2, topk=8, seed=0,
-                          use_gumbel=True, ws=None, dout1_work=None):
+                          use_gumbel=True, ws=None, dout1_work=None, seed_dev=None):
     """Two retrieval groups sharing K/V.  `dout1_work` (optional) is a scratch tensor
-    like dout1 that receives dout1 plus group 2's landmark gradient."""
+    like dout1 that receives dout1 plus group 2's landmark gradient.  seed_dev (a
+    one-element int64 device tensor) replaces `seed` when given."""
     ws = ws or default_workspace(q1.device)
-    idx1, s1 = retrieve_topk(q1_lmk, k1_lmk, topk, 0, use_gumbel, seed, 0, ws=ws)
+    idx1, s1 = retrieve_topk(q1_lmk, k1_lmk, topk, 0, use_gumbel, seed, 0, ws=ws, seed_dev=seed_dev)
     o1, lse1 = gca_forward(q1, k, v, idx1, s1, shift=1, ws=ws)
     q2_lmk = landmark_view(o1)
-    idx2, s2 = retrieve_topk(q2_lmk, k2_lmk, topk, 0, use_gumbel, seed, 1, ws=ws)
+    idx2, s2 = retrieve_topk(q2_lmk, k2_lmk, topk, 0, use_gumbel, seed, 1, ws=ws, seed_dev=seed_dev)
     o2, lse2 = gca_forward(q2, k, v, idx2, s2, shift=1, ws=ws)
     dq2, dk, dv, ds2 = gca_backward(q2, k, v, idx2, s2, dout2, lse2, shift=1, ws=ws)
     if dout1_work is None:
@@ -97,54 +99,32 @@ def decode_offload(q_new, k_host, v_host, q_lmk_new, k_lmk_store, topk=8, kv_sha
 
 
 class TrainGraph:
-    """The training step of one retrieval group (train_step) captured once as a CUDA graph
-    and replayed.
+    """A training step captured once as a CUDA graph and replayed.
 
-    The step is six launches (retrieval, forward, query side, score gradient, key side,
-    landmark gradients).  Issued one by one, each waits at the GPU's front end for the one
-    before; replayed as one graph, they follow each other with less of that gap.  The
-    noise seed lives in a one-element device tensor (`self.seed`) that the retrieval
-    kernels read when they run, and the graph ends by adding 1 to it: replay number i
-    (counting from 0 after construction or set_seed(s)) draws the noise of seed + i, as
-    train_step(..., seed=seed + i) does.  Replays read the current contents of the input
-    tensors given here (update them in place between steps) and overwrite the tensors of
-    `self.out` (the keys of train_step's result)."""
+    `step(seed_dev)` issues one step through this library's calls (train_step or
+    train_step_two_groups with seed_dev=seed_dev, or any such composition), taking the
+    noise seed from the one-element int64 device tensor it is given, and returns its
+    results.  Issued one by one, each of the step's launches waits at the GPU's front end
+    for the one before; replayed as one graph, they follow each other with less of that
+    gap.  The seed lives in `self.seed`, which the retrieval kernels read when they run,
+    and the graph ends by adding 1 to it: replay number i (counting from 0 after
+    construction or set_seed(s)) draws the noise of seed + i, as the eager step with
+    seed + i does.  The step is run once eagerly first (it sizes the workspaces and sets
+    the kernels' attributes).  Replays read the current contents of the step's input
+    tensors (update them in place between steps) and overwrite the tensors of the dict
+    that replay() returns (created during the capture)."""
 
-    def __init__(self, q, k, v, q_lmk, k_lmk, dout, topk=8, seed=0, group=0, use_gumbel=True, ws=None):
-        dev = q.device
-        self.ws = ws or Workspace(dev)
-        B, L, H, dh = q.shape
-        nQ, D = L // CHUNK, q_lmk.shape[2]
+    def __init__(self, step, seed=0, device=None):
+        dev = torch.device(device or "cuda")
         self.seed = torch.full((1,), int(seed), dtype=torch.int64, device=dev)
-        f32 = torch.float32
-        self.out = dict(idx=torch.empty((B, nQ, topk), dtype=torch.int32, device=dev),
-                        scores=torch.empty((B, nQ, topk), dtype=f32, device=dev),
-                        o=torch.empty_like(q), lse=torch.empty((B, nQ, H, topk, 64), dtype=f32, device=dev),
-                        dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
-                        dscores=torch.empty((B, nQ, topk), dtype=f32, device=dev),
-                        dq_lmk=torch.empty((B, nQ, D), dtype=f32, device=dev),
-                        dk_lmk=torch.empty((B, k_lmk.shape[1], D), dtype=f32, device=dev))
-        self._in = (q, k, v, q_lmk, k_lmk, dout)
-        self._cfg = (topk, group, use_gumbel)
-        self._step()  # warm-up outside the capture: sizes the workspace, sets kernel attributes
+        step(self.seed)  # warm-up, outside the capture
         torch.cuda.synchronize(dev)
         self.graph = torch.cuda.CUDAGraph()
         n0 = launch_count()
         with torch.cuda.graph(self.graph):
-            self._step()
+            self.out = step(self.seed)
             self.seed.add_(1)
         self.launches_per_replay = launch_count() - n0  # this library's kernels in one replay
-
-    def _step(self):
-        q, k, v, ql, kl, do = self._in
-        topk, group, use_gumbel = self._cfg
-        o, ws = self.out, self.ws
-        retrieve_topk(ql, kl, topk, 0, use_gumbel, 0, group, ws=ws, idx=o["idx"], scores=o["scores"],
-                      seed_dev=self.seed)
-        gca_forward(q, k, v, o["idx"], o["scores"], shift=1, ws=ws, out=o["o"], lse=o["lse"])
-        gca_backward(q, k, v, o["idx"], o["scores"], do, o["lse"], shift=1, ws=ws, dq=o["dq"], dk=o["dk"],
-                     dv=o["dv"], dscores=o["dscores"])
-        scores_backward(ql, kl, o["idx"], o["dscores"], ws=ws, dq_out=o["dq_lmk"], dk_lmk=o["dk_lmk"])
 
     def set_seed(self, seed: int):
         """The next replay draws the noise of `seed` (asynchronous, on the current stream)."""

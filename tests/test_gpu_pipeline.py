@@ -236,7 +236,8 @@ def test_train_graph_replays_the_eager_step():
     lm = synth.landmark_inputs(63, B, nC, nC, D, "bf16")
     q, k, v, do = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
     ql, kl = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
-    g = pipeline.TrainGraph(q, k, v, ql, kl, do, topk=K, seed=100)
+    ws = pipeline.Workspace()
+    g = pipeline.TrainGraph(lambda sd: pipeline.train_step(q, k, v, ql, kl, do, topk=K, seed_dev=sd, ws=ws), seed=100)
     assert g.launches_per_replay >= 4
     names = ("idx", "scores", "o", "lse", "dq", "dk", "dv", "dscores", "dq_lmk", "dk_lmk")
     for s in (100, 101, 102):
@@ -251,7 +252,34 @@ def test_train_graph_replays_the_eager_step():
     torch.cuda.synchronize()
     assert all(torch.equal(out[n], ref[n]) for n in names)
     assert not torch.equal(out["idx"], pipeline.train_step(q, k, v, ql, kl, do, topk=K, seed=100)["idx"])
-    g.ws.check()
+    ws.check()
+
+
+def test_train_graph_two_groups():
+    """The two-group step captured as a graph: each replay equals train_step_two_groups
+    with the next seed, bit for bit, group 2's landmark gradient pushed into a fresh copy
+    of dO1 every time."""
+    from retrieval_sparse_attention_causal_gb300 import pipeline
+    B, nC, H, dh, K = 1, 24, 4, 64, 4
+    D = H * dh
+    x = synth.gca_inputs(64, B, nC, nC, H, dh, 1 / 8, "bf16")
+    x2 = synth.gca_inputs(65, B, nC, nC, H, dh, 1 / 8, "bf16")
+    q1, k, v, do1 = (dev(x[n], "bf16") for n in ("q", "k", "v", "do"))
+    q2, do2 = dev(x2["q"], "bf16"), dev(x2["do"], "bf16")
+    lm = synth.landmark_inputs(64, B, nC, nC, D, "bf16")
+    q1l, k1l = dev(lm["q_lmk"], "bf16"), dev(lm["k_lmk"], "bf16")
+    k2l = dev(synth.landmark_inputs(66, B, nC, nC, D, "bf16")["k_lmk"], "bf16")
+    ws, work = pipeline.Workspace(), torch.empty_like(do1)
+    g = pipeline.TrainGraph(lambda sd: pipeline.train_step_two_groups(q1, q2, k, v, q1l, k1l, k2l, do1, do2, topk=K,
+                                                                       ws=ws, dout1_work=work, seed_dev=sd), seed=7)
+    for s in (7, 8):
+        out = {n: t.clone() for n, t in g.replay().items()}
+        ref = pipeline.train_step_two_groups(q1, q2, k, v, q1l, k1l, k2l, do1, do2, topk=K, seed=s)
+        torch.cuda.synchronize()
+        for n in ("idx1", "idx2", "o1", "o2", "dq1", "dq2", "dk", "dv", "ds1", "ds2", "dq1_lmk", "dk1_lmk",
+                  "dk2_lmk", "dout1_total"):
+            assert torch.equal(out[n], ref[n]), (s, n)
+    ws.check()
 
 
 def _near_tie_set_check(idx_g_row, key_o, n_cand, gap, what):
