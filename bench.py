@@ -198,12 +198,12 @@ KNOWN_TRAFFIC = {  # kernel: (bytes per launch, source fingerprint at capture); 
     "gca_bwd_kv": (7.0037e+08, "4f625c47e217a1eb"),
 }
 # profiles/retrieve_stream_decode_16m.md (B = 2 capture; traffic grows with the number of sequences)
-STREAM_TRAFFIC_PER_SEQ = (805565440 / 2, "ace4f833981931f2")
+STREAM_TRAFFIC_PER_SEQ = (805500928 / 2, "4efdb061233afa3e")
 
 
 # profiles/retrieve_tc_prefill.md (8192-chunk capture: the two landmark tensors read once,
 # nothing written back past L2; traffic grows with the number of chunks)
-PREFILL_TRAFFIC_PER_CHUNK = (25217280 / 8192, "2c1f4177bbce2558")
+PREFILL_TRAFFIC_PER_CHUNK = (25219328 / 8192, "39d775d958d64b7d")
 
 
 def source_fingerprint(kernel: str) -> str:
